@@ -1,0 +1,204 @@
+/*
+ * skv.h -- C ABI of the GB300 (sm_103a) split-KV decode and attention-state
+ * merge library (libskv.so).
+ *
+ * Pages the operations follow, cited by title and section:
+ *   [F2] "F2 讲解：merge_state，以 2 为底的 LSE 合并"
+ *   [L3] "L3 讲解：split-KV decode 与 LSE 合并"
+ *   [FA] "FlashAttention 的空行 LSE:FA-2 的 +inf 约定与后来的变化"
+ *
+ * Conventions shared by every entry point
+ *   - An attention state is (v, s).  v is the softmax-normalised output over a
+ *     subset of keys; s = log2( sum_j exp(score_j) ) is the BASE-2 log-sum-exp
+ *     of those keys' scores ([F2] §②).  The natural-log form is s * ln 2.
+ *     s is always fp32.  v is fp32, fp16 or bf16 (skv_dtype).
+ *   - An empty state is s = -inf, v = 0 ([F2] §⑤).  Merging two empty states
+ *     gives s = -inf, v = 0, never NaN.  An incoming s that is NaN or +inf is
+ *     read as -inf, i.e. "no weight" ([FA] §2.2).
+ *   - Pointers named v, s, q, *_cache, *_table, ctx, o_*, lse_*, out, workspace
+ *     are DEVICE pointers; `*_host` pointers are host pointers.  The caller
+ *     owns every buffer.  No entry point allocates device or host memory.
+ *   - Every device entry point is asynchronous on `stream` (NULL = the legacy
+ *     default stream) and returns as soon as its kernels are enqueued.
+ *   - Arguments are checked on the host before anything is launched; a failed
+ *     check returns SKV_ERR_INVALID_ARG (bad pointer, size, alignment) or
+ *     SKV_ERR_UNSUPPORTED (a valid shape this build has no kernel for) and
+ *     enqueues nothing.  A launch failure returns SKV_ERR_CUDA.  Errors that
+ *     only the device can see (a page id outside the pool, a ctx larger than
+ *     the page table, a bounded wait that gave up) are recorded in a per-device
+ *     error word read by skv_get_device_error(); the kernel then clamps the
+ *     offending index into range or skips the rest of its work, so it neither
+ *     faults nor hangs, and its outputs are unspecified.
+ *   - The library never aborts, never prints and keeps no state other than the
+ *     per-device error word and cached device attributes.
+ *   - 16-byte alignment is required for every v/q/cache/output pointer and for
+ *     o_part; D * sizeof(element) must be a multiple of 16 bytes.
+ */
+#ifndef SKV_H_
+#define SKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream); NULL is the legacy default stream. */
+typedef struct CUstream_st* skv_stream_t;
+
+typedef enum {
+    SKV_OK = 0,
+    SKV_ERR_INVALID_ARG = 1, /* a pointer, size or alignment check failed         */
+    SKV_ERR_UNSUPPORTED = 2, /* a valid shape or dtype this build has no kernel for */
+    SKV_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed         */
+    SKV_ERR_TIMEOUT = 4      /* a bounded device wait gave up (device error word)   */
+} skv_status;
+
+typedef enum { SKV_F32 = 0, SKV_F16 = 1, SKV_BF16 = 2 } skv_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* skv_status_string(skv_status status);
+
+/* ABI version of this header; bumped on any signature change. */
+int32_t skv_abi_version(void);
+
+/*
+ * Two-state merge ([F2] §③; guards of [F2] §⑤ and [FA] §2.2).
+ * For every row r of R = S*H rows (row r = pos*H + h):
+ *   a = sanitize(s_a[r]), b = sanitize(s_b[r]), m = max(a, b),
+ *   w_x = 2^(x - m) (0 for an empty state), W = w_a + w_b,
+ *   v_out[r, :] = (w_a v_a[r, :] + w_b v_b[r, :]) / W   (0 if W == 0),
+ *   s_out[r]    = m + log2(W)                            (-inf if W == 0).
+ * Layout: v_a, v_b, v_out are [S, H, D] contiguous in `dtype`; s_a, s_b, s_out
+ * are [S, H] contiguous fp32.  Accumulation is fp32; v_out is rounded to
+ * `dtype` (round to nearest even).  The formula is symmetric, so swapping the
+ * two inputs gives bit-identical outputs.  Outputs must not overlap inputs
+ * (use skv_merge_state_in_place for in-place merging).
+ * Limits: S, H >= 0 (S*H == 0 is a no-op), 1 <= D, D*sizeof(dtype) % 16 == 0.
+ */
+skv_status skv_merge_state(const void* v_a, const float* s_a,
+                           const void* v_b, const float* s_b,
+                           void* v_out, float* s_out,
+                           int64_t S, int64_t H, int64_t D,
+                           skv_dtype dtype, skv_stream_t stream);
+
+/*
+ * In-place two-state merge ([F2] §⑦ names merge_state_in_place; the page
+ * gives no body, the reading taken is the unmasked update
+ *   (v, s) <- merge_state((v, s), (v_other, s_other))
+ * with exactly the arithmetic of skv_merge_state, a in the first operand.)
+ * v is [S, H, D] in `dtype` and s is [S, H] fp32, both overwritten; v_other,
+ * s_other are read only and must not overlap v, s.
+ */
+skv_status skv_merge_state_in_place(void* v, float* s,
+                                    const void* v_other, const float* s_other,
+                                    int64_t S, int64_t H, int64_t D,
+                                    skv_dtype dtype, skv_stream_t stream);
+
+/*
+ * Device workspace, in bytes, that skv_merge_states may use for these sizes
+ * (0 when it never needs any).  Few rows with many states are merged in two
+ * levels: several CTAs per row each merge a chunk of the N states into a
+ * partial state kept in the workspace, and the last CTA of the row merges the
+ * partials (exact because merging is associative, [F2] §①).
+ */
+size_t skv_merge_states_workspace_size(int64_t S, int64_t N, int64_t H, int64_t D);
+
+/*
+ * N-state merge in the [S, N, H, D] / [S, N, H] layout ([F2] §④): element
+ * s[pos, n, h] is at offset (pos*N + n)*H + h and v[pos, n, h, :] at that
+ * offset times D.  For every (pos, h):
+ *   m = max_n sanitize(s_n), w_n = 2^(s_n - m) (0 if empty), W = sum_n w_n,
+ *   v_out[pos, h, :] = sum_n w_n v_n / W   (0 if W == 0),
+ *   s_out[pos, h]    = m + log2(W)         (-inf if W == 0).
+ * v_out is [S, H, D] in `dtype`, s_out [S, H] fp32; fp32 accumulation.
+ * Zero-weight states are not read.
+ * workspace: NULL, or a device buffer of workspace_bytes bytes.  If it is at
+ *   least skv_merge_states_workspace_size(S, N, H, D) bytes the two-level
+ *   path may be used; otherwise every row is merged by one CTA (same result
+ *   up to fp32 rounding order).  The workspace MUST be zero-filled before its
+ *   first use; every call that returns SKV_OK and runs to completion leaves it
+ *   zero-filled again, so one buffer can serve consecutive calls on one
+ *   stream.  Calls that share a workspace must not overlap on the GPU.
+ * Limits: S, H >= 0, N >= 1, D as for skv_merge_state.
+ */
+skv_status skv_merge_states(const void* v, const float* s,
+                            void* v_out, float* s_out,
+                            int64_t S, int64_t N, int64_t H, int64_t D,
+                            skv_dtype dtype, void* workspace, size_t workspace_bytes,
+                            skv_stream_t stream);
+
+/*
+ * Page range of one split ([L3] §②), computed on the host with exactly the
+ * integer arithmetic the decode kernel uses:
+ *   num_pages = ceil(ctx / page), pps = ceil(num_pages / num_splits),
+ *   p_start = split * pps, p_end = min(p_start + pps, num_pages).
+ * The raw values are returned (p_end may be <= p_start: the split is empty).
+ * Host only; needs no GPU.  Limits: ctx >= 0, page >= 1, num_splits >= 1,
+ * 0 <= split < num_splits.
+ */
+skv_status skv_split_page_range(int32_t ctx, int32_t page, int32_t num_splits, int32_t split,
+                                int32_t* p_start, int32_t* p_end);
+
+/*
+ * Split count for one decode step ([L3] §⑥): B*Hkv*NS several times the SM
+ * count while every split keeps several pages; no split when B*Hkv already
+ * fills the GPU.  Constants (the page prints none): candidates 1, 4, 16, 64
+ * (the counts the page's sweep measures); NS = 1 if B*Hkv >= 3*sm_count, else
+ * the smallest of 4, 16, 64 reaching 3*sm_count (64 if none does), then
+ * stepped down while ceil(max_pages / NS) < 8.  This reproduces the page's
+ * table exactly (170 SMs: B=1 ctx 32768 -> 64, B=8 ctx 4096 -> 16,
+ * B=64 ctx 1024 -> 1).
+ * ctx_host: host array of B context lengths.  sm_count > 0 is used as given;
+ * sm_count == 0 means the current CUDA device's SM count (needs a GPU).
+ * Result in *num_splits.
+ */
+skv_status skv_splitkv_decode_plan(int32_t B, const int32_t* ctx_host, int32_t Hkv,
+                                   int32_t page, int32_t sm_count, int32_t* num_splits);
+
+/*
+ * Split-KV paged decode attention, Flash-Decoding style ([L3] §① two kernels,
+ * §② ranges, §③ per-split state, §④ empty splits, §⑤ fp32 partials).
+ * Pass 1, one CTA per (b, hkv, split): query heads hq = hkv*G .. hkv*G+G-1
+ * (G = Hq/Hkv, grouped heads are contiguous) attend to the tokens
+ * [p_start*page, min(p_end*page, ctx[b])) of sequence b, with
+ * score = sm_scale * q . k, and write the split-normalised state
+ *   o_part[b, hq, split, :] (fp32) and lse_part[b, hq, split] (fp32, base 2);
+ * an empty split writes o = 0 and lse = -inf.
+ * Pass 2 (only when out != NULL): merges the num_splits states of each
+ * (b, hq) like skv_merge_states and writes out[b, hq, :] in `dtype` and, if
+ * lse_out != NULL, lse_out[b, hq] (fp32, base 2).
+ * Layouts: q [B, Hq, D]; k_cache, v_cache [num_pool_pages, Hkv, page, D]
+ *   (`dtype`); block_table [B, max_pages] int32 pool-page ids, row-major;
+ *   ctx [B] int32 context lengths (device); o_part [B, Hq, num_splits, D];
+ *   lse_part [B, Hq, num_splits]; out [B, Hq, D]; lse_out [B, Hq].
+ * ranges_dbg: NULL, or a device int32 [B, num_splits, 2] receiving the
+ *   (p_start, p_end) each CTA computed.
+ * Supported: dtype SKV_F16, D = 128, page = 16, G in {1, 2, 4, 8},
+ *   1 <= num_splits <= 256.  B = 0 is a no-op.
+ * Device-side checks: a ctx outside [0, max_pages*page] or a page id outside
+ *   [0, num_pool_pages) is clamped into range and flagged in the error word.
+ */
+skv_status skv_splitkv_decode(const void* q, const void* k_cache, const void* v_cache,
+                              int32_t num_pool_pages,
+                              const int32_t* block_table, int32_t max_pages,
+                              const int32_t* ctx,
+                              int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page,
+                              int32_t num_splits, float sm_scale, skv_dtype dtype,
+                              float* o_part, float* lse_part,
+                              void* out, float* lse_out,
+                              int32_t* ranges_dbg, skv_stream_t stream);
+
+/*
+ * Reads and clears the error word of the current CUDA device: *code is 0 or
+ * the skv_status of the first device-side error since the last call, *detail
+ * an index that identifies it (0 if none).  Synchronises the device.
+ */
+skv_status skv_get_device_error(int32_t* code, int32_t* detail);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SKV_H_ */

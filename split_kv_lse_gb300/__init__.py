@@ -1,0 +1,183 @@
+"""GB300 (sm_103a) split-KV decode attention and attention-state merging.
+
+A thin Python binding over the C ABI of libskv.so (include/skv.h): every
+function here only checks tensor metadata, passes device pointers, sizes and
+the current CUDA stream to the library, and returns the output tensors.  All
+arithmetic runs in the library's CUDA kernels; there is no CPU or PyTorch
+fallback, and a missing library raises.
+
+States follow the pages' convention: v is the softmax-normalised output over a
+key subset, s = log2(sum exp(score)) its base-2 log-sum-exp (fp32); an empty
+state is (v = 0, s = -inf).
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _ffi
+from ._ffi import SkvError
+
+__all__ = [
+    "SkvError", "merge_state", "merge_state_in_place", "merge_states",
+    "merge_states_workspace_size", "split_page_range", "splitkv_decode_plan",
+    "splitkv_decode", "get_device_error", "abi_version", "library_path",
+]
+
+_DT = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+
+def library_path() -> str:
+    return _ffi.LIB
+
+
+def abi_version() -> int:
+    return int(_ffi.lib().skv_abi_version())
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def merge_state(v_a, s_a, v_b, s_b, v_out=None, s_out=None):
+    """Two-state merge of [S, H, D] / [S, H] states -> (v, s)."""
+    S, H, D = v_a.shape
+    _need(v_a, "v_a")
+    dt = v_a.dtype
+    _need(v_b, "v_b", dt, (S, H, D))
+    _need(s_a, "s_a", torch.float32, (S, H))
+    _need(s_b, "s_b", torch.float32, (S, H))
+    v_out = torch.empty_like(v_a) if v_out is None else v_out
+    s_out = torch.empty_like(s_a) if s_out is None else s_out
+    _need(v_out, "v_out", dt, (S, H, D))
+    _need(s_out, "s_out", torch.float32, (S, H))
+    _ffi.check("skv_merge_state", _ffi.lib().skv_merge_state(
+        v_a.data_ptr(), s_a.data_ptr(), v_b.data_ptr(), s_b.data_ptr(), v_out.data_ptr(),
+        s_out.data_ptr(), S, H, D, _DT[dt], _stream(v_a)))
+    return v_out, s_out
+
+
+def merge_state_in_place(v, s, v_other, s_other):
+    """(v, s) <- merge_state((v, s), (v_other, s_other)), in place."""
+    S, H, D = v.shape
+    _need(v, "v")
+    _need(v_other, "v_other", v.dtype, (S, H, D))
+    _need(s, "s", torch.float32, (S, H))
+    _need(s_other, "s_other", torch.float32, (S, H))
+    _ffi.check("skv_merge_state_in_place", _ffi.lib().skv_merge_state_in_place(
+        v.data_ptr(), s.data_ptr(), v_other.data_ptr(), s_other.data_ptr(), S, H, D,
+        _DT[v.dtype], _stream(v)))
+    return v, s
+
+
+def merge_states_workspace_size(S: int, N: int, H: int, D: int) -> int:
+    return int(_ffi.lib().skv_merge_states_workspace_size(S, N, H, D))
+
+
+def merge_states(v, s, workspace=None, v_out=None, s_out=None):
+    """N-state merge of v [S, N, H, D], s [S, N, H] -> (v [S, H, D], s [S, H]).
+
+    workspace: optional zero-filled uint8 CUDA tensor of at least
+    merge_states_workspace_size(S, N, H, D) bytes; it is left zero-filled.
+    """
+    S, N, H, D = v.shape
+    _need(v, "v")
+    _need(s, "s", torch.float32, (S, N, H))
+    v_out = torch.empty((S, H, D), dtype=v.dtype, device=v.device) if v_out is None else v_out
+    s_out = torch.empty((S, H), dtype=torch.float32, device=v.device) if s_out is None else s_out
+    _need(v_out, "v_out", v.dtype, (S, H, D))
+    _need(s_out, "s_out", torch.float32, (S, H))
+    ws_bytes = 0
+    if workspace is not None:
+        _need(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _ffi.check("skv_merge_states", _ffi.lib().skv_merge_states(
+        v.data_ptr(), s.data_ptr(), v_out.data_ptr(), s_out.data_ptr(), S, N, H, D,
+        _DT[v.dtype], _ptr(workspace), ws_bytes, _stream(v)))
+    return v_out, s_out
+
+
+def split_page_range(ctx: int, page: int, num_splits: int, split: int):
+    """Raw (p_start, p_end) of one split, computed by the library on the host."""
+    a, b = ctypes.c_int32(), ctypes.c_int32()
+    _ffi.check("skv_split_page_range", _ffi.lib().skv_split_page_range(
+        ctx, page, num_splits, split, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def splitkv_decode_plan(ctx, Hkv: int, page: int = 16, sm_count: int = 0) -> int:
+    """Split count for one decode step (host; sm_count 0 = current device)."""
+    vals = [int(x) for x in (ctx.tolist() if hasattr(ctx, "tolist") else ctx)]
+    arr = (ctypes.c_int32 * max(1, len(vals)))(*vals)
+    ns = ctypes.c_int32()
+    _ffi.check("skv_splitkv_decode_plan", _ffi.lib().skv_splitkv_decode_plan(
+        len(vals), arr, Hkv, page, sm_count, ctypes.byref(ns)))
+    return ns.value
+
+
+def splitkv_decode(q, k_cache, v_cache, block_table, ctx, num_splits: int, sm_scale: float,
+                   o_part=None, lse_part=None, out=None, lse_out=None, combine: bool = True,
+                   ranges_dbg=None):
+    """Split-KV paged decode.
+
+    q [B, Hq, D] fp16; k_cache, v_cache [P, Hkv, page, D] fp16; block_table
+    [B, max_pages] int32; ctx [B] int32 (device).  Returns
+    (out, lse_out, o_part, lse_part); out/lse_out are None when combine=False.
+    """
+    B, Hq, D = q.shape
+    P, Hkv, page, D2 = k_cache.shape
+    _need(q, "q")
+    _need(k_cache, "k_cache", q.dtype)
+    _need(v_cache, "v_cache", q.dtype, tuple(k_cache.shape))
+    _need(block_table, "block_table", torch.int32)
+    _need(ctx, "ctx", torch.int32, (B,))
+    if D2 != D or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("inconsistent decode shapes")
+    dev = q.device
+    if o_part is None:
+        o_part = torch.empty((B, Hq, num_splits, D), dtype=torch.float32, device=dev)
+    if lse_part is None:
+        lse_part = torch.empty((B, Hq, num_splits), dtype=torch.float32, device=dev)
+    _need(o_part, "o_part", torch.float32, (B, Hq, num_splits, D))
+    _need(lse_part, "lse_part", torch.float32, (B, Hq, num_splits))
+    if combine:
+        out = torch.empty((B, Hq, D), dtype=q.dtype, device=dev) if out is None else out
+        lse_out = torch.empty((B, Hq), dtype=torch.float32, device=dev) if lse_out is None else lse_out
+        _need(out, "out", q.dtype, (B, Hq, D))
+        _need(lse_out, "lse_out", torch.float32, (B, Hq))
+    else:
+        out = lse_out = None
+    if ranges_dbg is not None:
+        _need(ranges_dbg, "ranges_dbg", torch.int32, (B, num_splits, 2))
+    _ffi.check("skv_splitkv_decode", _ffi.lib().skv_splitkv_decode(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), P, block_table.data_ptr(),
+        block_table.shape[1], ctx.data_ptr(), B, Hq, Hkv, D, page, num_splits, float(sm_scale),
+        _DT[q.dtype], o_part.data_ptr(), lse_part.data_ptr(), _ptr(out), _ptr(lse_out),
+        _ptr(ranges_dbg), _stream(q)))
+    return out, lse_out, o_part, lse_part
+
+
+def get_device_error():
+    """(code, detail) of the first device-side error since the last call; clears it."""
+    code, detail = ctypes.c_int32(), ctypes.c_int32()
+    _ffi.check("skv_get_device_error", _ffi.lib().skv_get_device_error(
+        ctypes.byref(code), ctypes.byref(detail)))
+    return code.value, detail.value

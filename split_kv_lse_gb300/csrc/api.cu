@@ -1,0 +1,255 @@
+// api.cu -- the extern "C" entry points of libskv (declared in include/skv.h):
+// argument checks on the host, then kernel launches on the caller's stream.
+// Nothing here allocates memory; nothing here prints or aborts.
+//
+// Pages: [F2] "F2 讲解：merge_state，以 2 为底的 LSE 合并",
+// [L3] "L3 讲解：split-KV decode 与 LSE 合并".
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "split_range.h"
+
+namespace skv {
+
+__device__ unsigned long long g_skv_error_word = 0ull;
+
+namespace {
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool valid_dtype(skv_dtype t) { return t == SKV_F32 || t == SKV_F16 || t == SKV_BF16; }
+
+skv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SKV_OK : SKV_ERR_CUDA; }
+
+// Row length checks shared by the merges: D elements of `dt` must be whole
+// 16-byte chunks and at most 32 of them (one chunk per lane of a warp).
+skv_status check_merge_D(int64_t D, skv_dtype dt) {
+    if (!valid_dtype(dt) || D < 1) return SKV_ERR_INVALID_ARG;
+    const int64_t bytes = D * (int64_t)dtype_size(dt);
+    if (bytes % 16 != 0) return SKV_ERR_INVALID_ARG;
+    if (bytes > 512) return SKV_ERR_UNSUPPORTED;
+    return SKV_OK;
+}
+}  // namespace
+
+skv_status current_device(const DeviceInfo** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SKV_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (d.device != dev) {
+        int sms = 0, smem = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SKV_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return SKV_ERR_CUDA;
+        void* word = nullptr;
+        if (cudaGetSymbolAddress(&word, g_skv_error_word) != cudaSuccess) return SKV_ERR_CUDA;
+        d.sm_count = sms;
+        d.max_smem_optin = (size_t)smem;
+        d.err = static_cast<unsigned long long*>(word);
+        d.device = dev;
+    }
+    *out = &d;
+    return SKV_OK;
+}
+
+}  // namespace skv
+
+using namespace skv;
+
+extern "C" {
+
+const char* skv_status_string(skv_status status) {
+    switch (status) {
+        case SKV_OK: return "SKV_OK";
+        case SKV_ERR_INVALID_ARG: return "SKV_ERR_INVALID_ARG";
+        case SKV_ERR_UNSUPPORTED: return "SKV_ERR_UNSUPPORTED";
+        case SKV_ERR_CUDA: return "SKV_ERR_CUDA";
+        case SKV_ERR_TIMEOUT: return "SKV_ERR_TIMEOUT";
+    }
+    return "SKV_UNKNOWN_STATUS";
+}
+
+int32_t skv_abi_version(void) { return 1; }
+
+skv_status skv_merge_state(const void* v_a, const float* s_a, const void* v_b, const float* s_b,
+                           void* v_out, float* s_out, int64_t S, int64_t H, int64_t D,
+                           skv_dtype dtype, skv_stream_t stream) {
+    if (S < 0 || H < 0) return SKV_ERR_INVALID_ARG;
+    skv_status st = check_merge_D(D, dtype);
+    if (st != SKV_OK) return st;
+    if (S * H == 0) return SKV_OK;
+    if (!v_a || !s_a || !v_b || !s_b || !v_out || !s_out) return SKV_ERR_INVALID_ARG;
+    if (!aligned16(v_a) || !aligned16(v_b) || !aligned16(v_out)) return SKV_ERR_INVALID_ARG;
+    if (!aligned4(s_a) || !aligned4(s_b) || !aligned4(s_out)) return SKV_ERR_INVALID_ARG;
+    const DeviceInfo* dev = nullptr;
+    if ((st = current_device(&dev)) != SKV_OK) return st;
+    return from_cuda(launch_merge_state(v_a, s_a, v_b, s_b, v_out, s_out, S * H, D, dtype,
+                                        false, *dev, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+skv_status skv_merge_state_in_place(void* v, float* s, const void* v_other, const float* s_other,
+                                    int64_t S, int64_t H, int64_t D, skv_dtype dtype,
+                                    skv_stream_t stream) {
+    if (S < 0 || H < 0) return SKV_ERR_INVALID_ARG;
+    skv_status st = check_merge_D(D, dtype);
+    if (st != SKV_OK) return st;
+    if (S * H == 0) return SKV_OK;
+    if (!v || !s || !v_other || !s_other) return SKV_ERR_INVALID_ARG;
+    if (!aligned16(v) || !aligned16(v_other) || !aligned4(s) || !aligned4(s_other))
+        return SKV_ERR_INVALID_ARG;
+    const DeviceInfo* dev = nullptr;
+    if ((st = current_device(&dev)) != SKV_OK) return st;
+    return from_cuda(launch_merge_state(v, s, v_other, s_other, v, s, S * H, D, dtype, true,
+                                        *dev, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t skv_merge_states_workspace_size(int64_t S, int64_t N, int64_t H, int64_t D) {
+    if (S <= 0 || H <= 0 || N < 1 || D < 1) return 0;
+    return merge_states_ws_upper_bound(S * H, N, D);
+}
+
+skv_status skv_merge_states(const void* v, const float* s, void* v_out, float* s_out, int64_t S,
+                            int64_t N, int64_t H, int64_t D, skv_dtype dtype, void* workspace,
+                            size_t workspace_bytes, skv_stream_t stream) {
+    if (S < 0 || H < 0 || N < 1) return SKV_ERR_INVALID_ARG;
+    skv_status st = check_merge_D(D, dtype);
+    if (st != SKV_OK) return st;
+    if (S * H == 0) return SKV_OK;
+    if (N > (int64_t)INT32_MAX || S * H > (int64_t)INT32_MAX) return SKV_ERR_UNSUPPORTED;
+    if (!v || !s || !v_out || !s_out) return SKV_ERR_INVALID_ARG;
+    if (!aligned16(v) || !aligned16(v_out) || !aligned4(s) || !aligned4(s_out))
+        return SKV_ERR_INVALID_ARG;
+    if (workspace != nullptr && !aligned16(workspace)) return SKV_ERR_INVALID_ARG;
+    const DeviceInfo* dev = nullptr;
+    if ((st = current_device(&dev)) != SKV_OK) return st;
+    return from_cuda(launch_merge_states(v, s, v_out, s_out, S, N, H, D, dtype, workspace,
+                                         workspace_bytes, *dev,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+skv_status skv_split_page_range(int32_t ctx, int32_t page, int32_t num_splits, int32_t split,
+                                int32_t* p_start, int32_t* p_end) {
+    if (!p_start || !p_end || ctx < 0 || page < 1 || num_splits < 1 || split < 0 ||
+        split >= num_splits)
+        return SKV_ERR_INVALID_ARG;
+    int a = 0, b = 0;
+    split_page_range(ctx, page, num_splits, split, &a, &b);
+    *p_start = a;
+    *p_end = b;
+    return SKV_OK;
+}
+
+skv_status skv_splitkv_decode_plan(int32_t B, const int32_t* ctx_host, int32_t Hkv, int32_t page,
+                                   int32_t sm_count, int32_t* num_splits) {
+    if (B < 0 || Hkv < 1 || page < 1 || sm_count < 0 || !num_splits) return SKV_ERR_INVALID_ARG;
+    if (B > 0 && !ctx_host) return SKV_ERR_INVALID_ARG;
+    if (sm_count == 0) {
+        const DeviceInfo* dev = nullptr;
+        skv_status st = current_device(&dev);
+        if (st != SKV_OK) return st;
+        sm_count = dev->sm_count;
+    }
+    int64_t max_pages = 0;
+    for (int32_t b = 0; b < B; ++b) {
+        if (ctx_host[b] < 0) return SKV_ERR_INVALID_ARG;
+        const int64_t np = ((int64_t)ctx_host[b] + page - 1) / page;
+        if (np > max_pages) max_pages = np;
+    }
+    // [L3] §⑥: no split when B*Hkv programs already fill the GPU several
+    // times over; otherwise the smallest of the page's swept split counts
+    // (4, 16, 64) that does, then fewer while a split would hold < 8 pages.
+    const int64_t programs = (int64_t)B * Hkv;
+    const int64_t target = 3LL * sm_count;
+    int32_t ns = 1;
+    if (programs < target) {
+        ns = 4;
+        while (ns < 64 && programs * ns < target) ns *= 4;
+        while (ns > 1 && (max_pages + ns - 1) / ns < 8) ns /= 4;
+    }
+    *num_splits = ns;
+    return SKV_OK;
+}
+
+skv_status skv_splitkv_decode(const void* q, const void* k_cache, const void* v_cache,
+                              int32_t num_pool_pages, const int32_t* block_table,
+                              int32_t max_pages, const int32_t* ctx, int32_t B, int32_t Hq,
+                              int32_t Hkv, int32_t D, int32_t page, int32_t num_splits,
+                              float sm_scale, skv_dtype dtype, float* o_part, float* lse_part,
+                              void* out, float* lse_out, int32_t* ranges_dbg,
+                              skv_stream_t stream) {
+    if (B < 0 || Hq < 1 || Hkv < 1 || D < 1 || page < 1 || num_splits < 1 || max_pages < 1 ||
+        num_pool_pages < 1 || !valid_dtype(dtype))
+        return SKV_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return SKV_ERR_INVALID_ARG;
+    const int G = Hq / Hkv;
+    if (dtype != SKV_F16 || D != 128 || page != 16 || !(G == 1 || G == 2 || G == 4 || G == 8) ||
+        num_splits > 256 || B > 65535 || Hkv > 65535)
+        return SKV_ERR_UNSUPPORTED;
+    if ((int64_t)max_pages * page > INT32_MAX) return SKV_ERR_UNSUPPORTED;
+    if (B == 0) return SKV_OK;
+    if (!q || !k_cache || !v_cache || !block_table || !ctx || !o_part || !lse_part)
+        return SKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o_part) ||
+        !aligned4(lse_part) || !aligned4(block_table) || !aligned4(ctx))
+        return SKV_ERR_INVALID_ARG;
+    if (out && !aligned16(out)) return SKV_ERR_INVALID_ARG;
+    if (lse_out && !aligned4(lse_out)) return SKV_ERR_INVALID_ARG;
+    if (lse_out && !out) return SKV_ERR_INVALID_ARG;
+    if (ranges_dbg && !aligned4(ranges_dbg)) return SKV_ERR_INVALID_ARG;
+    const DeviceInfo* dev = nullptr;
+    skv_status st = current_device(&dev);
+    if (st != SKV_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    DecodeArgs a;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.num_pool_pages = num_pool_pages;
+    a.block_table = block_table;
+    a.max_pages = max_pages;
+    a.ctx = ctx;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.page = page;
+    a.num_splits = num_splits;
+    a.sm_scale = sm_scale;
+    a.o_part = o_part;
+    a.lse_part = lse_part;
+    a.ranges_dbg = ranges_dbg;
+    cudaError_t e = launch_splitkv_decode(a, *dev, cs);
+    if (e != cudaSuccess) return SKV_ERR_CUDA;
+    if (out != nullptr) {
+        e = launch_combine(o_part, lse_part, (int64_t)B * Hq, num_splits, D, out, dtype, lse_out,
+                           nullptr, nullptr, true, *dev, cs);
+        if (e != cudaSuccess) return SKV_ERR_CUDA;
+    }
+    return SKV_OK;
+}
+
+skv_status skv_get_device_error(int32_t* code, int32_t* detail) {
+    if (!code || !detail) return SKV_ERR_INVALID_ARG;
+    const DeviceInfo* dev = nullptr;
+    skv_status st = current_device(&dev);
+    if (st != SKV_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return SKV_ERR_CUDA;
+    unsigned long long w = 0, zero = 0;
+    if (cudaMemcpy(&w, dev->err, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SKV_ERR_CUDA;
+    if (cudaMemcpy(dev->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+        return SKV_ERR_CUDA;
+    *code = (int32_t)(w & 0xffu);
+    *detail = (int32_t)(w >> 8);
+    return SKV_OK;
+}
+
+}  // extern "C"

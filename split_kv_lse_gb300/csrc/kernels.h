@@ -1,0 +1,71 @@
+// kernels.h -- internal launch interface between the C ABI (api.cu) and the
+// kernel translation units.  Not installed; no torch types anywhere.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/skv.h"
+
+namespace skv {
+
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+    size_t max_smem_optin = 0;
+    unsigned long long* err = nullptr;  // device address of the error word
+};
+// Cached attributes of the current CUDA device (queried once per device).
+skv_status current_device(const DeviceInfo** out);
+
+inline size_t dtype_size(skv_dtype t) { return t == SKV_F32 ? 4 : 2; }
+
+// ---------------------------------------------------------------- merges
+cudaError_t launch_merge_state(const void* va, const float* sa, const void* vb, const float* sb,
+                               void* vo, float* so, int64_t rows, int64_t D, skv_dtype dt,
+                               bool in_place, const DeviceInfo& dev, cudaStream_t st);
+
+// Which N-state merge path a call takes (host logic, shared with the
+// workspace-size query so the two always agree).
+struct MergeStatesPlan {
+    bool team_kernel = false;  // one lane team per row
+    int nsplit = 1;            // CTAs per row on the CTA path (>1 needs workspace)
+    int per_split = 0;         // states per CTA on the CTA path
+    size_t ws_bytes = 0;       // workspace the plan needs
+};
+MergeStatesPlan plan_merge_states(int64_t rows, int64_t N, int64_t D, int sm_count,
+                                  size_t ws_available);
+size_t merge_states_ws_upper_bound(int64_t rows, int64_t N, int64_t D);
+
+cudaError_t launch_merge_states(const void* v, const float* s, void* vo, float* so, int64_t S,
+                                int64_t N, int64_t H, int64_t D, skv_dtype dt, void* ws,
+                                size_t ws_bytes, const DeviceInfo& dev, cudaStream_t st);
+
+// Combine pass of the split-KV decode: merges NS fp32 partial states per row
+// (rows = B*Hq) into `out` (out_dt) and optional lse_out; an optional extra
+// fp32 state per row [rows, D] / [rows] is merged last (cascade prefix).
+// Launched as a programmatic dependent of the preceding kernel on `st`.
+cudaError_t launch_combine(const float* o_part, const float* lse_part, int64_t rows, int NS,
+                           int64_t D, void* out, skv_dtype out_dt, float* lse_out,
+                           const float* extra_v, const float* extra_s, bool pdl,
+                           const DeviceInfo& dev, cudaStream_t st);
+
+// ---------------------------------------------------------------- decode
+struct DecodeArgs {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    int32_t num_pool_pages;
+    const int32_t* block_table;
+    int32_t max_pages;
+    const int32_t* ctx;
+    int32_t B, Hq, Hkv, D, page, num_splits;
+    float sm_scale;
+    float* o_part;
+    float* lse_part;
+    int32_t* ranges_dbg;
+};
+cudaError_t launch_splitkv_decode(const DecodeArgs& a, const DeviceInfo& dev, cudaStream_t st);
+
+}  // namespace skv

@@ -1,0 +1,572 @@
+// merge.cu -- attention-state merge kernels for sm_103a.
+//
+// Pages: [F2] "F2 讲解：merge_state，以 2 为底的 LSE 合并" (§③ two states,
+// §④ N states in the [S, N, H, D] layout, §⑤ empty states, §⑦ the
+// vectorised CUDA kernels and the large-N kernel),
+// [FA] "FlashAttention 的空行 LSE:FA-2 的 +inf 约定与后来的变化" (§2.2
+// sanitize_lse, §4.1 the zero-reciprocal rule for an empty row).
+//
+// All three kernels are HBM-bound streams.  Design (GB300, not the pages'
+// program-per-row Triton): a row's D elements are split into 16-byte chunks
+// and a power-of-two "team" of lanes owns one row, so every load and store is
+// a 128-bit coalesced access; each thread keeps several rows (or states) of
+// loads in flight before it computes; all arithmetic is fp32.
+//   merge_state_kernel        two states, team per row (in-place variant too)
+//   merge_states_team_kernel  N states, team per row: many rows
+//   merge_states_cta_kernel   N states, one CTA (8 warps) per row or per chunk
+//                             of a row's states: few rows, many states; the
+//                             chunks of a row meet in a workspace and the
+//                             last-arriving CTA merges them (associativity,
+//                             [F2] §①) -- never a spin-wait.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace skv {
+namespace {
+
+constexpr int kThreads = 256;
+
+// Lanes of this thread's team inside its warp (teams are aligned powers of 2).
+SKV_DEVINL unsigned team_mask(int tpr) {
+    if (tpr == 32) return 0xffffffffu;
+    unsigned lane = threadIdx.x & 31;
+    return ((1u << tpr) - 1u) << (lane & ~(unsigned)(tpr - 1));
+}
+
+// The two-state formula of [F2] §③ with the guards of [F2] §⑤ / [FA] §2.2.
+// Written symmetrically (separate products, one rounded add) so that
+// swapping the operands gives bit-identical results.
+struct TwoWeights {
+    float wa, wb, inv, s;
+};
+SKV_DEVINL TwoWeights two_weights(float sa, float sb) {
+    float a = sanitize_lse(sa), b = sanitize_lse(sb);
+    float m = fmaxf(a, b);
+    TwoWeights t;
+    t.wa = merge_weight(a, m);
+    t.wb = merge_weight(b, m);
+    float w = __fadd_rn(t.wa, t.wb);
+    t.inv = w > 0.f ? 1.f / w : 0.f;  // [FA] §4.1: empty row -> reciprocal 0
+    t.s = m + log2f(w);               // -inf + log2(0) = -inf for a double-empty row
+    return t;
+}
+SKV_DEVINL float blend(float wa, float xa, float wb, float xb, float inv) {
+    float ta = wa > 0.f ? __fmul_rn(wa, xa) : 0.f;  // a zero-weight state is not read
+    float tb = wb > 0.f ? __fmul_rn(wb, xb) : 0.f;
+    return __fmul_rn(__fadd_rn(ta, tb), inv);
+}
+
+// ---------------------------------------------------------------- two-state merge
+template <typename T, int CPT, int U, bool kInPlace>
+__global__ void __launch_bounds__(kThreads)
+merge_state_kernel(const T* va, const float* sa, const T* __restrict__ vb,
+                   const float* __restrict__ sb, T* vo, float* so, int64_t rows, int chunks,
+                   int tpr_log2) {
+    constexpr int E = Vec<T>::N;
+    const int tpr = 1 << tpr_log2;
+    const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t team = gt >> tpr_log2;
+    const int64_t nteams = ((int64_t)gridDim.x * blockDim.x) >> tpr_log2;
+    const int l = (int)(gt & (tpr - 1));
+    const unsigned tmask = team_mask(tpr);
+    const int64_t row_stride = (int64_t)chunks * 16;  // bytes per row
+
+    for (int64_t r0 = team; r0 < rows; r0 += (int64_t)U * nteams) {
+        float xa[U], xb[U];
+        uint4 ra[U][CPT], rb[U][CPT];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t r = r0 + u * nteams;
+            const bool ok = r < rows;
+            xa[u] = ok ? sa[r] : -INFINITY;
+            xb[u] = ok ? sb[r] : -INFINITY;
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) {
+                const int c = l + k * tpr;
+                if (ok && c < chunks) {
+                    const char* pa = reinterpret_cast<const char*>(va) + r * row_stride + c * 16;
+                    const char* pb = reinterpret_cast<const char*>(vb) + r * row_stride + c * 16;
+                    ra[u][k] = kInPlace ? ld_coherent(pa) : ld_stream(pa);
+                    rb[u][k] = ld_stream(pb);
+                }
+            }
+        }
+        // In place, s_out aliases s_a: every lane of the team has read s_a[r]
+        // before the team's first lane overwrites it.
+        if (kInPlace) __syncwarp(tmask);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t r = r0 + u * nteams;
+            if (r >= rows) continue;
+            const TwoWeights t = two_weights(xa[u], xb[u]);
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) {
+                const int c = l + k * tpr;
+                if (c >= chunks) continue;
+                float fa[E], fb[E], fo[E];
+                to_float<T>(ra[u][k], fa);
+                to_float<T>(rb[u][k], fb);
+#pragma unroll
+                for (int e = 0; e < E; ++e) fo[e] = blend(t.wa, fa[e], t.wb, fb[e], t.inv);
+                char* po = reinterpret_cast<char*>(vo) + r * row_stride + c * 16;
+                st_stream(po, from_float<T>(fo));
+            }
+            if (l == 0) so[r] = t.s;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- N-state, team per row
+// Rows handled by one warp = 32 / tpr; the loop trip count is uniform per
+// warp so that full-warp shuffles are always legal; tail rows are masked.
+template <typename Tin, typename Tout, int CPT, int NB>
+__global__ void __launch_bounds__(kThreads)
+merge_states_team_kernel(const Tin* __restrict__ v, const float* __restrict__ s,
+                         Tout* __restrict__ vo, float* __restrict__ so, int64_t rows, int N,
+                         int64_t H, int chunks, int tpr_log2) {
+    constexpr int E = Vec<Tin>::N;
+    static_assert(Vec<Tin>::N == Vec<Tout>::N, "same element count per 16-byte chunk");
+    const int tpr = 1 << tpr_log2;
+    const int lane = threadIdx.x & 31;
+    const int l = lane & (tpr - 1);
+    const int team_in_warp = lane >> tpr_log2;
+    const int teams_per_warp = 32 >> tpr_log2;
+    const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int src_base = lane & ~(tpr - 1);
+    const int64_t row_bytes = (int64_t)chunks * 16;
+
+    for (int64_t rw = warp_id * teams_per_warp; rw < rows; rw += nwarps * teams_per_warp) {
+        const int64_t r = rw + team_in_warp;
+        const bool ok = r < rows;
+        const int64_t pos = ok ? r / H : 0, h = ok ? r % H : 0;
+        // s[pos, n, h] at (pos*N + n)*H + h ([F2] §④).
+        const float* srow = s + (pos * N) * H + h;
+        float m = -INFINITY;
+        for (int n = l; n < N; n += tpr) m = fmaxf(m, ok ? sanitize_lse(srow[(int64_t)n * H]) : -INFINITY);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)
+            if (o < tpr) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float W = 0.f;
+        for (int n = l; n < N; n += tpr) W += ok ? merge_weight(sanitize_lse(srow[(int64_t)n * H]), m) : 0.f;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)
+            if (o < tpr) W += __shfl_xor_sync(0xffffffffu, W, o);
+
+        float acc[CPT][E];
+#pragma unroll
+        for (int k = 0; k < CPT; ++k)
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[k][e] = 0.f;
+
+        const char* vrow = reinterpret_cast<const char*>(v) + ((pos * N) * H + h) * row_bytes;
+        const int64_t nstride = H * row_bytes;  // bytes between consecutive states
+        const int nb = NB < tpr ? NB : tpr;  // states per batch: one weight per team lane
+        for (int n0 = 0; n0 < N; n0 += nb) {
+            // Lane j < nb of the team computes the weight of state n0 + j.
+            float wmine = 0.f;
+            if (ok && l < nb && n0 + l < N) wmine = merge_weight(sanitize_lse(srow[(int64_t)(n0 + l) * H]), m);
+            float w[NB];
+            uint4 raw[NB][CPT];
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+                w[j] = __shfl_sync(0xffffffffu, wmine, src_base + (j < nb ? j : 0));
+                if (j >= nb) w[j] = 0.f;
+#pragma unroll
+                for (int k = 0; k < CPT; ++k) {
+                    const int c = l + k * tpr;
+                    if (w[j] > 0.f && c < chunks)
+                        raw[j][k] = ld_stream(vrow + (int64_t)(n0 + j) * nstride + c * 16);
+                    else
+                        raw[j][k] = make_uint4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+                if (!(w[j] > 0.f)) continue;
+#pragma unroll
+                for (int k = 0; k < CPT; ++k) {
+                    float f[E];
+                    to_float<Tin>(raw[j][k], f);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[k][e] = fmaf(w[j], f[e], acc[k][e]);
+                }
+            }
+        }
+        if (!ok) continue;
+        const float inv = W > 0.f ? 1.f / W : 0.f;
+        char* orow = reinterpret_cast<char*>(vo) + r * row_bytes;
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+            const int c = l + k * tpr;
+            if (c >= chunks) continue;
+            float f[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) f[e] = acc[k][e] * inv;
+            st_stream(orow + c * 16, from_float<Tout>(f));
+        }
+        if (l == 0) so[r] = m + log2f(W);
+    }
+}
+
+// ---------------------------------------------------------------- N-state, CTA per row
+struct CtaParams {
+    const void* v;        // Tin  [rows_outer.., N, H, D] (see row addressing below)
+    const float* s;       // [S, N, H]
+    void* vo;             // Tout [rows, D]
+    float* so;            // [rows] or nullptr
+    int64_t H;
+    int N;
+    int chunks;           // 16-byte chunks per row of D
+    int tpr_log2;
+    int nsplit;           // CTAs per row
+    int per_split;        // states per CTA
+    float* ws_v;          // [rows, nsplit, D] fp32 partial states (nsplit > 1)
+    float* ws_s;          // [rows, nsplit]
+    unsigned* ws_cnt;     // [rows] arrival tickets, zero between calls
+    const float* extra_v; // [rows, D] fp32 state merged last, or nullptr
+    const float* extra_s; // [rows]
+    int pdl_wait;         // wait for the preceding grid (programmatic launch)
+};
+
+
+
+template <typename T>
+SKV_DEVINL float block_reduce(float x, float* red, bool is_max) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    x = is_max ? warp_max(x) : warp_sum(x);
+    __syncthreads();
+    if (lane == 0) red[w] = x;
+    __syncthreads();
+    float r = red[0];
+    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) r = is_max ? fmaxf(r, red[i]) : r + red[i];
+    return r;
+}
+
+template <typename Tin, typename Tout, int NB>
+__global__ void __launch_bounds__(kThreads)
+merge_states_cta_kernel(CtaParams p) {
+    constexpr int E = Vec<Tin>::N;
+    constexpr int EO = Vec<Tout>::N;
+    __shared__ float red[32];
+    // Team partial sums: nteams * D floats <= (256 / tpr) * (tpr * E) = 256 * E.
+    __shared__ __align__(16) float part[kThreads * E];
+    __shared__ int is_last;
+
+    if (p.pdl_wait) pdl_wait_primary();
+
+    const int64_t row = blockIdx.x;
+    const int split = blockIdx.y;
+    const int64_t pos = row / p.H, h = row % p.H;
+    const int tpr = 1 << p.tpr_log2;
+    const int nteams = kThreads >> p.tpr_log2;
+    const int team = threadIdx.x >> p.tpr_log2;
+    const int l = threadIdx.x & (tpr - 1);
+    const int D = p.chunks * E;
+    const int n_begin = split * p.per_split;
+    const int n_end = min(p.N, n_begin + p.per_split);
+    const float* srow = p.s + (pos * p.N) * p.H + h;
+
+    // Chunk maximum and weight sum over this CTA's states.
+    float m = -INFINITY;
+    for (int n = n_begin + threadIdx.x; n < n_end; n += kThreads)
+        m = fmaxf(m, sanitize_lse(srow[(int64_t)n * p.H]));
+    m = block_reduce<float>(m, red, true);
+    float W = 0.f;
+    for (int n = n_begin + threadIdx.x; n < n_end; n += kThreads)
+        W += merge_weight(sanitize_lse(srow[(int64_t)n * p.H]), m);
+    W = block_reduce<float>(W, red, false);
+
+    // Each team accumulates its states n = n_begin + team + k*nteams.
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    const int64_t row_bytes = (int64_t)p.chunks * 16;
+    const char* vrow = reinterpret_cast<const char*>(p.v) + ((pos * p.N) * p.H + h) * row_bytes;
+    const int64_t nstride = p.H * row_bytes;
+    const bool lane_ok = l < p.chunks;
+    for (int n0 = n_begin + team; n0 < n_end; n0 += NB * nteams) {
+        float w[NB];
+        uint4 raw[NB];
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+            const int n = n0 + j * nteams;
+            w[j] = n < n_end ? merge_weight(sanitize_lse(srow[(int64_t)n * p.H]), m) : 0.f;
+            raw[j] = (w[j] > 0.f && lane_ok)
+                         ? (p.pdl_wait ? ld_cg(vrow + (int64_t)n * nstride + l * 16)
+                                       : ld_stream(vrow + (int64_t)n * nstride + l * 16))
+                         : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+            if (!(w[j] > 0.f)) continue;
+            float f[E];
+            to_float<Tin>(raw[j], f);
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = fmaf(w[j], f[e], acc[e]);
+        }
+    }
+    // Sum the teams' partial vectors through shared memory.
+    if (lane_ok) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) part[team * D + l * E + e] = acc[e];
+    }
+    __syncthreads();
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    const float s_chunk = m + log2f(W);
+    // Thread d (< D) owns output element d.
+    float vd = 0.f;
+    if (threadIdx.x < D) {
+        for (int t = 0; t < nteams; ++t) vd += part[t * D + threadIdx.x];
+        vd *= inv;
+    }
+    float s_fin = s_chunk;
+
+    if (p.nsplit > 1) {
+        // Publish this chunk's partial state, then take a ticket; the CTA that
+        // draws the last ticket of the row merges all partials.
+        if (threadIdx.x < D) p.ws_v[(row * p.nsplit + split) * D + threadIdx.x] = vd;
+        if (threadIdx.x == 0) p.ws_s[row * p.nsplit + split] = s_chunk;
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const unsigned ticket = atomicAdd(&p.ws_cnt[row], 1u);
+            is_last = (ticket == (unsigned)p.nsplit - 1u);
+            if (is_last) p.ws_cnt[row] = 0u;  // every CTA of the row has arrived
+        }
+        __syncthreads();
+        if (!is_last) return;
+        __threadfence();
+        float M = -INFINITY;
+        for (int k = 0; k < p.nsplit; ++k) M = fmaxf(M, ld_cg_f32(&p.ws_s[row * p.nsplit + k]));
+        float WW = 0.f, a = 0.f;
+        for (int k = 0; k < p.nsplit; ++k) {
+            const float wk = merge_weight(ld_cg_f32(&p.ws_s[row * p.nsplit + k]), M);
+            WW += wk;
+            if (threadIdx.x < D && wk > 0.f)
+                a = fmaf(wk, ld_cg_f32(&p.ws_v[(row * p.nsplit + k) * D + threadIdx.x]), a);
+        }
+        vd = WW > 0.f ? a * (1.f / WW) : 0.f;
+        s_fin = M + log2f(WW);
+    }
+
+    if (p.extra_v != nullptr) {
+        // Final two-state merge with the extra state (cascade: prefix state
+        // first, split states second).
+        const TwoWeights t = two_weights(p.extra_s[row], s_fin);
+        const float xe = threadIdx.x < D ? p.extra_v[row * D + threadIdx.x] : 0.f;
+        vd = blend(t.wa, xe, t.wb, vd, t.inv);
+        s_fin = t.s;
+    }
+    // Store: gather to shared memory, then 16-byte stores by `chunks` threads.
+    __syncthreads();
+    if (threadIdx.x < D) part[threadIdx.x] = vd;
+    __syncthreads();
+    if (threadIdx.x < D / EO) {
+        float f[EO];
+#pragma unroll
+        for (int e = 0; e < EO; ++e) f[e] = part[threadIdx.x * EO + e];
+        char* orow = reinterpret_cast<char*>(p.vo) + row * (int64_t)D * sizeof(Tout);
+        st_stream(orow + threadIdx.x * 16, from_float<Tout>(f));
+    }
+    if (threadIdx.x == 0 && p.so != nullptr) p.so[row] = s_fin;
+}
+
+int log2_pow2_at_least(int x) {
+    int l = 0;
+    while ((1 << l) < x) ++l;
+    return l;
+}
+
+template <typename T>
+cudaError_t launch_merge_state_t(const void* va, const float* sa, const void* vb,
+                                 const float* sb, void* vo, float* so, int64_t rows, int chunks,
+                                 bool in_place, const DeviceInfo& dev, cudaStream_t st) {
+    const int tpr_log2 = chunks >= 32 ? 5 : log2_pow2_at_least(chunks);
+    const int tpr = 1 << tpr_log2;
+    const int cpt = (chunks + tpr - 1) / tpr;
+    constexpr int U = 4;
+    const int64_t threads_needed = ((rows + U - 1) / U) * tpr;
+    int64_t blocks = (threads_needed + kThreads - 1) / kThreads;
+    const int64_t cap = (int64_t)dev.sm_count * 64;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    const T* a = static_cast<const T*>(va);
+    const T* b = static_cast<const T*>(vb);
+    T* o = static_cast<T*>(vo);
+#define SKV_MS_LAUNCH(CPT_, UU_)                                                            \
+    do {                                                                                    \
+        if (in_place)                                                                       \
+            merge_state_kernel<T, CPT_, UU_, true><<<(unsigned)blocks, kThreads, 0, st>>>(  \
+                a, sa, b, sb, o, so, rows, chunks, tpr_log2);                               \
+        else                                                                                \
+            merge_state_kernel<T, CPT_, UU_, false><<<(unsigned)blocks, kThreads, 0, st>>>( \
+                a, sa, b, sb, o, so, rows, chunks, tpr_log2);                               \
+    } while (0)
+    if (cpt == 1) SKV_MS_LAUNCH(1, 4);
+    else if (cpt == 2) SKV_MS_LAUNCH(2, 2);
+    else if (cpt <= 4) SKV_MS_LAUNCH(4, 1);
+    else return cudaErrorInvalidValue;
+#undef SKV_MS_LAUNCH
+    return cudaGetLastError();
+}
+
+template <typename Tin, typename Tout>
+cudaError_t launch_cta(const CtaParams& p0, int64_t rows, const DeviceInfo& dev, cudaStream_t st,
+                       bool pdl) {
+    (void)dev;
+    CtaParams p = p0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rows, (unsigned)p.nsplit, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    p.pdl_wait = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, merge_states_cta_kernel<Tin, Tout, 4>, p);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- host entry points
+cudaError_t launch_merge_state(const void* va, const float* sa, const void* vb, const float* sb,
+                               void* vo, float* so, int64_t rows, int64_t D, skv_dtype dt,
+                               bool in_place, const DeviceInfo& dev, cudaStream_t st) {
+    const int chunks = (int)(D * (int64_t)dtype_size(dt) / 16);
+    switch (dt) {
+        case SKV_F32: return launch_merge_state_t<float>(va, sa, vb, sb, vo, so, rows, chunks, in_place, dev, st);
+        case SKV_F16: return launch_merge_state_t<__half>(va, sa, vb, sb, vo, so, rows, chunks, in_place, dev, st);
+        case SKV_BF16: return launch_merge_state_t<__nv_bfloat16>(va, sa, vb, sb, vo, so, rows, chunks, in_place, dev, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+static constexpr int64_t kTeamRows = 4096;  // rows at or above which the team kernel is used
+static constexpr int kMaxSplit = 16;
+
+static int max_split_for(int64_t N) {
+    int64_t m = (N + 7) / 8;  // at least 8 states per CTA
+    if (m > kMaxSplit) m = kMaxSplit;
+    return (int)(m < 1 ? 1 : m);
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static size_t ws_bytes_for(int64_t rows, int nsplit, int64_t D) {
+    if (nsplit <= 1) return 0;
+    return align256((size_t)rows * nsplit * D * 4) + align256((size_t)rows * nsplit * 4) +
+           align256((size_t)rows * 4);
+}
+
+size_t merge_states_ws_upper_bound(int64_t rows, int64_t N, int64_t D) {
+    if (rows <= 0 || rows >= kTeamRows) return 0;
+    return ws_bytes_for(rows, max_split_for(N), D);
+}
+
+MergeStatesPlan plan_merge_states(int64_t rows, int64_t N, int64_t D, int sm_count,
+                                  size_t ws_available) {
+    MergeStatesPlan pl;
+    if (rows >= kTeamRows) {
+        pl.team_kernel = true;
+        return pl;
+    }
+    // Enough CTAs to give every SM about two.
+    int64_t want = (2LL * sm_count + rows - 1) / (rows > 0 ? rows : 1);
+    int nsplit = (int)(want < 1 ? 1 : (want > max_split_for(N) ? max_split_for(N) : want));
+    if (nsplit > 1 && ws_bytes_for(rows, nsplit, D) > ws_available) nsplit = 1;
+    pl.nsplit = nsplit;
+    pl.per_split = (int)((N + nsplit - 1) / nsplit);
+    pl.ws_bytes = ws_bytes_for(rows, nsplit, D);
+    return pl;
+}
+
+cudaError_t launch_merge_states(const void* v, const float* s, void* vo, float* so, int64_t S,
+                                int64_t N, int64_t H, int64_t D, skv_dtype dt, void* ws,
+                                size_t ws_bytes, const DeviceInfo& dev, cudaStream_t st) {
+    const int64_t rows = S * H;
+    const int chunks = (int)(D * (int64_t)dtype_size(dt) / 16);
+    const MergeStatesPlan pl = plan_merge_states(rows, N, D, dev.sm_count, ws ? ws_bytes : 0);
+    if (pl.team_kernel) {
+        const int tpr_log2 = chunks >= 32 ? 5 : log2_pow2_at_least(chunks);
+        const int tpr = 1 << tpr_log2;
+        const int cpt = (chunks + tpr - 1) / tpr;
+        const int64_t warps = (rows + (32 / tpr) - 1) / (32 / tpr);
+        int64_t blocks = (warps * 32 + kThreads - 1) / kThreads;
+        const int64_t cap = (int64_t)dev.sm_count * 32;
+        if (blocks > cap) blocks = cap;
+#define SKV_TEAM(T_, CPT_)                                                                     \
+    merge_states_team_kernel<T_, T_, CPT_, 8><<<(unsigned)blocks, kThreads, 0, st>>>(          \
+        static_cast<const T_*>(v), s, static_cast<T_*>(vo), so, rows, (int)N, H, chunks, tpr_log2)
+#define SKV_TEAM_CPT(T_)                        \
+    do {                                        \
+        if (cpt == 1) SKV_TEAM(T_, 1);          \
+        else if (cpt == 2) SKV_TEAM(T_, 2);     \
+        else if (cpt <= 4) SKV_TEAM(T_, 4);     \
+        else return cudaErrorInvalidValue;      \
+    } while (0)
+        switch (dt) {
+            case SKV_F32: SKV_TEAM_CPT(float); break;
+            case SKV_F16: SKV_TEAM_CPT(__half); break;
+            case SKV_BF16: SKV_TEAM_CPT(__nv_bfloat16); break;
+        }
+#undef SKV_TEAM_CPT
+#undef SKV_TEAM
+        return cudaGetLastError();
+    }
+    CtaParams p = {};
+    p.v = v;
+    p.s = s;
+    p.vo = vo;
+    p.so = so;
+    p.H = H;
+    p.N = (int)N;
+    p.chunks = chunks;
+    p.tpr_log2 = chunks >= 32 ? 5 : log2_pow2_at_least(chunks);
+    p.nsplit = pl.nsplit;
+    p.per_split = pl.per_split;
+    if (pl.nsplit > 1) {
+        char* w = static_cast<char*>(ws);
+        p.ws_v = reinterpret_cast<float*>(w);
+        w += align256((size_t)rows * pl.nsplit * D * 4);
+        p.ws_s = reinterpret_cast<float*>(w);
+        w += align256((size_t)rows * pl.nsplit * 4);
+        p.ws_cnt = reinterpret_cast<unsigned*>(w);
+    }
+    switch (dt) {
+        case SKV_F32: return launch_cta<float, float>(p, rows, dev, st, false);
+        case SKV_F16: return launch_cta<__half, __half>(p, rows, dev, st, false);
+        case SKV_BF16: return launch_cta<__nv_bfloat16, __nv_bfloat16>(p, rows, dev, st, false);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_combine(const float* o_part, const float* lse_part, int64_t rows, int NS,
+                           int64_t D, void* out, skv_dtype out_dt, float* lse_out,
+                           const float* extra_v, const float* extra_s, bool pdl,
+                           const DeviceInfo& dev, cudaStream_t st) {
+    CtaParams p = {};
+    p.v = o_part;
+    p.s = lse_part;
+    p.vo = out;
+    p.so = lse_out;
+    p.H = 1;
+    p.N = NS;
+    p.chunks = (int)(D * 4 / 16);
+    p.tpr_log2 = p.chunks >= 32 ? 5 : log2_pow2_at_least(p.chunks);
+    p.nsplit = 1;
+    p.per_split = NS;
+    p.extra_v = extra_v;
+    p.extra_s = extra_s;
+    switch (out_dt) {
+        case SKV_F32: return launch_cta<float, float>(p, rows, dev, st, pdl);
+        case SKV_F16: return launch_cta<float, __half>(p, rows, dev, st, pdl);
+        case SKV_BF16: return launch_cta<float, __nv_bfloat16>(p, rows, dev, st, pdl);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace skv
