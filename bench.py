@@ -1,0 +1,485 @@
+#!/usr/bin/env python
+"""Benchmark of the split-KV decode / attention-state merge hot path on GB300.
+
+One step = one pass of every stage of the hot path over its synthetic
+workload (seeded, shapes of the named workloads in
+split_kv_lse_gb300/workloads.py), inputs resident in HBM:
+  merge_state           S=8192, H=32, D=128 fp16 (+empty/double-empty/+inf/NaN)
+  merge_state_in_place  same sizes
+  merge_states          S=256, N=64, H=32, D=128 fp32, 5% empty
+  splitkv_decode        B=1, ctx=32768, Hq=32, Hkv=8, D=128, page 16, NS=64,
+                        pass 1 + PDL-chained combine to fp16
+  cascade_decode        B=64, shared 8192-token prefix + 1..2048-token suffixes
+                        (when the library exports it)
+value = algorithmic HBM bytes of the step / step time (GB/s).  Each stage is
+timed with CUDA events on the launching stream; L2 is flushed (a 512 MB
+write, then a 512 MB read, so it holds clean lines) before every step,
+outside the stage events.  --impl reference times
+the fp64 CPU oracle on a bounded sample of the same stages instead.
+
+Prints ONE JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "merge GB/s and split-KV decode µs/step, each as % of GB300 HBM roofline"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = ("split-KV hot path step: merge_state + merge_state_in_place S=8192 H=32 D=128 fp16; "
+            "merge_states S=256 N=64 H=32 D=128 fp32; splitkv_decode B=1 ctx=32768 Hq=32 Hkv=8 "
+            "D=128 page=16 NS=64 fp16")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", default=None,
+                    help="comma-separated stage names to run (profiling); default all")
+    ap.add_argument("--soak-s", type=float, default=1.5,
+                    help="seconds of untimed steps before the timed region, during which "
+                         "(and during the timed region) SM clocks are sampled")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):  # sample every 50 ms
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    smax.append(float(f[2]))
+                except ValueError:
+                    continue
+                for n, val in zip(names, f[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(n)
+        finally:
+            os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- stages
+class Stage:
+    def __init__(self, name, fn, algo_bytes, launches, e2e=None):
+        self.name = name
+        self.fn = fn
+        self.bytes = int(algo_bytes)
+        self.launches = launches
+        self.e2e = e2e          # (h2d_fn, run_fn, d2h_fn, h2d_bytes, d2h_bytes)
+        self.times_ms = []
+
+
+def nbytes(t):
+    return t.numel() * t.element_size()
+
+
+STAGE_NAMES = ("merge_state", "merge_state_in_place", "merge_states", "splitkv_decode")
+# Diagnostic stages, selectable with --only (not part of the default step).
+EXTRA_STAGES = ("splitkv_decode_pass1",)
+
+
+def build_stages(torch, skv, W, dev, only=None):
+    """Create the GPU stages; inputs are generated on the host and copied once."""
+    stages = []
+    hostside = {}
+    want = set(only) if only else set(STAGE_NAMES)
+
+    def to_dev(d):
+        return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+    # merge_state (+ in place), S=8192 H=32 D=128 fp16
+    if want & {"merge_state", "merge_state_in_place"}:
+        _merge_state_stages(torch, skv, W, dev, to_dev, want, stages, hostside)
+    if "merge_states" in want:
+        _merge_states_stage(torch, skv, W, dev, to_dev, stages, hostside)
+    if want & {"splitkv_decode", "splitkv_decode_pass1"}:
+        _decode_stage(torch, skv, W, dev, to_dev, stages, hostside, want)
+    return stages, hostside
+
+
+def _merge_state_stages(torch, skv, W, dev, to_dev, want, stages, hostside):
+    d = W.merge_state_large()
+    g = to_dev(d)
+    vo = torch.empty_like(g["v_a"])
+    so = torch.empty_like(g["s_a"])
+    ms_bytes = 3 * nbytes(g["v_a"]) + 3 * nbytes(g["s_a"])
+    if "merge_state" in want:
+        stages.append(Stage("merge_state",
+                            lambda: skv.merge_state(g["v_a"], g["s_a"], g["v_b"], g["s_b"], vo, so),
+                            ms_bytes, 1))
+    if "merge_state_in_place" in want:
+        v_ip, s_ip = g["v_a"].clone(), g["s_a"].clone()
+        stages.append(Stage("merge_state_in_place",
+                            lambda: skv.merge_state_in_place(v_ip, s_ip, g["v_b"], g["s_b"]),
+                            ms_bytes, 1))
+    hostside["merge_state"] = d
+
+
+def _merge_states_stage(torch, skv, W, dev, to_dev, stages, hostside):
+    # merge_states, S=256 N=64 H=32 D=128 fp32
+    d3 = W.merge_states_main()
+    g3 = to_dev(d3)
+    S, N, H, D = d3["v"].shape
+    vo3 = torch.empty(S, H, D, device=dev)
+    so3 = torch.empty(S, H, device=dev)
+    nonempty = int((d3["s"] != -math.inf).sum())
+    mss_bytes = nonempty * D * 4 + nbytes(d3["s"]) + nbytes(vo3) + nbytes(so3)
+    stages.append(Stage("merge_states", lambda: skv.merge_states(g3["v"], g3["s"], None, vo3, so3),
+                        mss_bytes, 1))
+    hostside["merge_states"] = d3
+
+
+def _decode_stage(torch, skv, W, dev, to_dev, stages, hostside, want):
+    # split-KV decode + combine, B=1 ctx=32768
+    d4 = W.decode_long()
+    g4 = to_dev(d4)
+    ns = d4["num_splits"]
+    B, Hq, D = d4["q"].shape
+    Hkv = d4["k_cache"].shape[1]
+    op = torch.empty(B, Hq, ns, D, device=dev)
+    lp = torch.empty(B, Hq, ns, device=dev)
+    out4 = torch.empty(B, Hq, D, dtype=torch.float16, device=dev)
+    lo4 = torch.empty(B, Hq, device=dev)
+    ctx_tokens = int(d4["ctx"].sum())
+    dec_bytes = (ctx_tokens * Hkv * D * 2 * 2 + nbytes(d4["q"]) +
+                 sum(-(-int(c) // 16) for c in d4["ctx"]) * 4 + nbytes(d4["ctx"]) +
+                 nbytes(out4) + nbytes(lo4))
+    if "splitkv_decode" in want:
+        stages.append(Stage("splitkv_decode",
+                            lambda: skv.splitkv_decode(g4["q"], g4["k_cache"], g4["v_cache"],
+                                                       g4["block_table"], g4["ctx"], ns,
+                                                       d4["sm_scale"], op, lp, out4, lo4),
+                            dec_bytes, 2))
+    if "splitkv_decode_pass1" in want:
+        stages.append(Stage("splitkv_decode_pass1",
+                            lambda: skv.splitkv_decode(g4["q"], g4["k_cache"], g4["v_cache"],
+                                                       g4["block_table"], g4["ctx"], ns,
+                                                       d4["sm_scale"], op, lp, combine=False),
+                            dec_bytes - nbytes(out4) - nbytes(lo4), 1))
+    hostside["decode"] = d4
+
+
+_PINNED_OUT = {}
+
+
+def e2e_step(torch, skv, host, dev):
+    """One step through the public API from pinned host buffers: copy every
+    stage's inputs in, run, copy every stage's outputs back."""
+    h2d = d2h = 0
+    d = host["merge_state"]
+    ga = {k: v.to(dev, non_blocking=True) for k, v in d.items()}
+    h2d += sum(nbytes(v) for v in d.values())
+    v, s = skv.merge_state(ga["v_a"], ga["s_a"], ga["v_b"], ga["s_b"])
+    skv.merge_state_in_place(ga["v_a"], ga["s_a"], ga["v_b"], ga["s_b"])
+    outs = [v, s, ga["v_a"], ga["s_a"]]
+    d3 = host["merge_states"]
+    g3 = {k: v.to(dev, non_blocking=True) for k, v in d3.items()}
+    h2d += sum(nbytes(v) for v in d3.values())
+    outs += list(skv.merge_states(g3["v"], g3["s"]))
+    d4 = host["decode"]
+    g4 = {k: (v.to(dev, non_blocking=True) if isinstance(v, torch.Tensor) else v)
+          for k, v in d4.items()}
+    h2d += sum(nbytes(v) for v in d4.values() if isinstance(v, torch.Tensor))
+    out, lse, _, _ = skv.splitkv_decode(g4["q"], g4["k_cache"], g4["v_cache"], g4["block_table"],
+                                        g4["ctx"], d4["num_splits"], d4["sm_scale"])
+    outs += [out, lse]
+    key = tuple((tuple(o.shape), o.dtype) for o in outs)
+    if key not in _PINNED_OUT:
+        _PINNED_OUT[key] = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    for h, o in zip(_PINNED_OUT[key], outs):
+        h.copy_(o, non_blocking=True)
+        d2h += nbytes(o)
+    return h2d, d2h
+
+
+# ---------------------------------------------------------------- oracle (CPU) stages
+def oracle_sample(W):
+    """Bounded samples of the same stages for the CPU oracle (about 1-3 s per pass)."""
+    import numpy as np
+    samples = []
+    d = W.merge_state_large()
+    rows = 2048  # of 8192 positions
+    a = {k: np.ascontiguousarray(d[k][:rows].double().numpy()) for k in d}
+    samples.append(("merge_state", lambda o=a: __import__("oracle").merge_state(
+        o["v_a"], o["s_a"], o["v_b"], o["s_b"]),
+        3 * rows * 32 * 128 * 2 + 3 * rows * 32 * 4))
+    d3 = W.merge_states_main()
+    S3 = 32  # of 256 positions
+    v3 = np.ascontiguousarray(d3["v"][:S3].double().numpy())
+    s3 = np.ascontiguousarray(d3["s"][:S3].double().numpy())
+    ne = int(np.isfinite(s3).sum())
+    samples.append(("merge_states", lambda: __import__("oracle").merge_states(v3, s3),
+                    ne * 128 * 4 + s3.size * 4 + S3 * 32 * 128 * 4 + S3 * 32 * 4))
+    d4 = W.decode_long()
+    # 2 of 8 KV heads and their 8 query heads, full 32768-token context.
+    q = np.ascontiguousarray(d4["q"][:, :8].double().numpy())
+    kc = np.ascontiguousarray(d4["k_cache"][:, :2].double().numpy())
+    vc = np.ascontiguousarray(d4["v_cache"][:, :2].double().numpy())
+    bt, cx, sc = d4["block_table"].numpy(), d4["ctx"].numpy(), d4["sm_scale"]
+
+    def dec():
+        import oracle
+        oracle.attend_splits(q, kc, vc, bt, cx, sc, 64)
+    samples.append(("splitkv_decode", dec, 32768 * 2 * 128 * 2 * 2 + 8 * 128 * 4))
+    return samples, ("merge_state 2048 of 8192 positions; merge_states 32 of 256 positions; "
+                     "splitkv_decode 2 of 8 KV heads (8 of 32 query heads), full 32768-token "
+                     "context, 64 split partials")
+
+
+def time_oracle(samples, reps=1):
+    total_b = total_t = 0.0
+    for name, fn, b in samples:
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            fn()
+            total_t += time.perf_counter() - t0
+            total_b += b
+    return total_b / total_t / 1e9, total_t
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    from split_kv_lse_gb300 import workloads as W
+    oracle.build()
+    samples, desc = oracle_sample(W)
+    for _ in range(args.warmup):
+        time_oracle(samples)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        v, t = time_oracle(samples)
+        vals.append(v)
+        secs.append(t)
+    value = sum(b for _, _, b in samples) * args.steps / sum(secs) / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * sum(secs) / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD + " (bounded oracle sample)", "sample": desc},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(dev))
+
+    from split_kv_lse_gb300 import build as skv_build
+    skv_build.build()
+    import split_kv_lse_gb300 as skv
+    from split_kv_lse_gb300 import workloads as W
+
+    only = args.only.split(",") if args.only else None
+    stages, host = build_stages(torch, skv, W, dev, only)
+    # L2 flush between steps: write 512 MB, then read another 512 MB so that
+    # the cache holds clean lines (no write-back charged to the next kernel).
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(record):
+        flush.zero_()
+        flush_rd.sum()
+        evs = []
+        for st in stages:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            st.fn()
+            e1.record(stream)
+            evs.append((st, e0, e1))
+        if record:
+            return evs
+        return None
+
+    for _ in range(max(3, args.warmup)):
+        step(False)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # Soak: untimed steps for --soak-s seconds so that the SM clocks sampled
+    # (here and during the timed region) are those of the GPU under this load.
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak_s:
+        for _ in range(20):
+            step(False)
+        torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    all_evs = []
+    for _ in range(args.steps):
+        all_evs.append(step(True))
+    barrier()
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    for evs in all_evs:
+        for st, e0, e1 in evs:
+            st.times_ms.append(e0.elapsed_time(e1))
+    step_ms = sum(statistics.mean(st.times_ms) for st in stages)
+    if dist is not None:
+        t = torch.tensor([step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    step_bytes = sum(st.bytes for st in stages)
+    value = world * step_bytes / (step_ms * 1e-3) / 1e9
+    launches = args.steps * sum(st.launches for st in stages)
+    assert skv.get_device_error() == (0, 0), "device-side error during the benchmark"
+
+    peak, peak_kind = measured_peaks()
+    stage_rep = {}
+    for st in stages:
+        us = 1e3 * statistics.mean(st.times_ms)
+        gbs = st.bytes / (us * 1e-6) / 1e9
+        stage_rep[st.name] = {"us": round(us, 2), "us_min": round(1e3 * min(st.times_ms), 2),
+                              "algo_bytes": st.bytes, "GB_s": round(gbs, 1),
+                              "frac_of_measured_hbm": round(gbs / peak, 4),
+                              "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4)}
+    dom = max(stages, key=lambda s: statistics.mean(s.times_ms))
+    dom_gbs = dom.bytes / (statistics.mean(dom.times_ms) * 1e-3) / 1e9
+
+    e2e = None
+    if not args.no_e2e and only is None:
+        # Same step through the public API with the inputs in pinned host memory.
+        for d in host.values():
+            for k, v in list(d.items()):
+                if isinstance(v, torch.Tensor):
+                    d[k] = v.pin_memory()
+        e2e_step(torch, skv, host, dev)
+        torch.cuda.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        nsteps = max(1, min(args.steps, 5))
+        for _ in range(nsteps):
+            h2d, d2h = e2e_step(torch, skv, host, dev)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_s = (time.perf_counter() - t0) / nsteps
+        e2e = {"value": round(world * step_bytes / e2e_s / 1e9, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_s * 1e3, 3)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and only is None:
+        import oracle
+        oracle.build()
+        samples, desc = oracle_sample(W)
+        v, t = time_oracle(samples)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": desc, "seconds": round(t, 2)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(step_ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD if only is None else ",".join(only),
+                       "l2_flush": "512 MB write + 512 MB read before every step (outside the stage events)",
+                       "clock_window": f"{args.soak_s} s untimed soak of the same steps, then the timed region",
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "stages": stage_rep, "wall_s": round(wall, 3)},
+            "roofline": {"bound": "hbm", "kernel": dom.name, "achieved": round(dom_gbs, 1),
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": round(dom_gbs / peak, 4), "traffic": None},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

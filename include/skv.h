@@ -118,9 +118,10 @@ size_t skv_merge_states_workspace_size(int64_t S, int64_t N, int64_t H, int64_t 
  *   least skv_merge_states_workspace_size(S, N, H, D) bytes the two-level
  *   path may be used; otherwise every row is merged by one CTA (same result
  *   up to fp32 rounding order).  The workspace MUST be zero-filled before its
- *   first use; every call that returns SKV_OK and runs to completion leaves it
- *   zero-filled again, so one buffer can serve consecutive calls on one
- *   stream.  Calls that share a workspace must not overlap on the GPU.
+ *   first use.  It holds per-row arrival counters that every completed call
+ *   returns to zero, so one buffer serves consecutive calls on one stream
+ *   without re-zeroing (zero it again after a call that did not complete).
+ *   Calls that share a workspace must not overlap on the GPU.
  * Limits: S, H >= 0, N >= 1, D as for skv_merge_state.
  */
 skv_status skv_merge_states(const void* v, const float* s,

@@ -90,6 +90,15 @@ SKV_DEVINL uint4 ld_stream(const void* p) {
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
     return r;
 }
+// Read-only load the compiler must keep in registers: volatile asm cannot be
+// re-executed later to rematerialise the value (used for loop-invariant data
+// such as the query of a decode CTA).
+SKV_DEVINL uint4 ld_pinned(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
 // Read of data this kernel may later overwrite (in-place merge): coherent path.
 SKV_DEVINL uint4 ld_coherent(const void* p) {
     uint4 r;

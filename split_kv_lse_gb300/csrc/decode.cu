@@ -1,37 +1,36 @@
-// decode.cu -- split-KV paged decode attention, pass 1, for sm_103a.
+// decode.cu -- split-KV paged decode attention for sm_103a: pass 1 (the
+// per-split states) and pass 2 (their merge, chained with programmatic
+// dependent launch).
 //
 // Page: "L3 讲解：split-KV decode 与 LSE 合并" -- §① the two-pass
 // Flash-Decoding scheme (grid (B, Hkv, NUM_SPLITS), each program walks its
 // own pages and writes a split-normalised o and that split's lse), §② the
 // page ranges, §③ the per-split state o_s = acc/l, lse_s = m + log l (here in
 // base 2: s = m2 + log2 l), §④ empty splits (o = 0, lse = -inf), §⑤ fp32
-// partials.  The combine pass is merge.cu's CTA kernel, chained with
-// programmatic dependent launch.
+// partials.
 //
-// GB300 design (not the page's Triton program):
+// GB300 design of pass 1 (not the page's Triton program):
 //   * One CTA per (b, hkv, split) serves all G = Hq/Hkv query heads of that
 //     KV head, so each K/V byte fetched from HBM feeds G heads.
-//   * W warps per CTA; warp w owns pages p_start + w, + w + W, ... of the
-//     split and streams them through its own ring of R slots.  A slot is the
-//     (page, hkv) tile of K and of V: two contiguous 4 KB blocks copied by the
-//     TMA engine (cp.async.bulk) with completion counted on an mbarrier; the
-//     warp refills a slot right after consuming it, so up to R pages per warp
-//     are in flight.  No cross-warp synchronisation in the main loop.
-//   * Lane (c, th) = (lane % 16, lane / 16) owns dims [8c, 8c+8) and tokens
-//     [8th, 8th+8) of a page: every 16-byte shared-memory read of a warp then
-//     covers two full 256-byte rows, i.e. is bank-conflict free without a
-//     swizzle.  q (pre-scaled by sm_scale*log2 e) and the output accumulators
-//     for the lane's 8 dims of all G heads live in registers.
-//   * Scores: per-lane partial dot products over 8 dims, then a shuffle
-//     reduce-scatter over the 16 dim-lanes leaves each lane complete scores
-//     for 8G/16 (token, head) pairs.  Online softmax in base 2 ([F2] §②
-//     exp2 trick): page max per head by shuffles, p = 2^(x - m), running l
-//     kept per lane and reduced once at the end.  p reaches the PV product
-//     through a per-warp shared-memory buffer.
-//   * CUDA cores only (fp32 FMA): this pass is bound by HBM, not by math.
+//   * W warps; warp w owns the split's pages w, w + W, ... and R/W ring slots.
+//     A slot holds one (page, kv-head) tile: K as two 64-dim boxes copied by
+//     TMA tensor loads with the 128-byte swizzle, V as one contiguous 4 KB
+//     bulk copy, completion counted on the slot's mbarrier.  The warp refills
+//     a slot as soon as it has consumed it.
+//   * QK: lane (g, tg) owns whole dot products -- head g, tokens tg + j*TGN --
+//     over all 128 dims, with q resident in registers, so no cross-lane
+//     reduction; the swizzle makes the lanes' reads of different rows at the
+//     same column bank-conflict free.  fp16 x fp16 -> fp32 FMAs
+//     (fma.rn.f32.f16): the products are exact, no conversions.
+//   * Online softmax in base 2 ([F2] §② exp2 trick) per head; the lanes of
+//     a head hold its running max, so the rescale factor never crosses lanes.
+//     p goes through shared memory as fp16 to the PV product, where lane
+//     (g, dc) owns head g's dims of 16-byte chunks dc, dc + TGN, ....
+//   * CUDA cores only: this pass is bound by HBM, not by math.
 #include "common.cuh"
 #include "kernels.h"
 #include "split_range.h"
+#include "tma.h"
 
 namespace skv {
 namespace {
@@ -44,7 +43,6 @@ constexpr unsigned kFull = 0xffffffffu;
 
 struct DecodeParams {
     const __half* q;
-    const __half* k_cache;
     const __half* v_cache;
     const int32_t* block_table;
     const int32_t* ctx;
@@ -56,62 +54,81 @@ struct DecodeParams {
     float scale_log2;  // sm_scale * log2(e)
 };
 
-// Reduce-scatter of L values over the lanes that differ in bits MASK, MASK/2,
-// ..., 1: at each step a lane keeps the half of its array selected by its
-// lane bit and adds the partner's copy of that half.  After the steps with
-// L >= 2 lane c holds in v[i] the complete sum for original index
-// i + (L_final) * c; once L reaches 1 the remaining steps are plain
-// butterflies (both partners end with the same total).
-template <int L, int MASK>
-SKV_DEVINL void reduce_scatter(float* v, int lane) {
-    if constexpr (MASK >= 1) {
-        if constexpr (L >= 2) {
-            constexpr int H = L / 2;
-            const bool upper = (lane & MASK) != 0;
-#pragma unroll
-            for (int i = 0; i < H; ++i) {
-                const float send = upper ? v[i] : v[i + H];
-                const float keep = upper ? v[i + H] : v[i];
-                v[i] = keep + __shfl_xor_sync(kFull, send, MASK);
-            }
-            reduce_scatter<H, MASK / 2>(v, lane);
-        } else {
-            v[0] += __shfl_xor_sync(kFull, v[0], MASK);
-            reduce_scatter<1, MASK / 2>(v, lane);
-        }
-    }
+// acc += a.lo * b.lo + a.hi * b.hi with fp16 operands and an fp32 accumulator
+// (mixed-precision FMA: the fp16 products are exact in fp32).
+SKV_DEVINL float dot2_h(uint32_t a, uint32_t b, float acc) {
+    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+        "mov.b32 {a0, a1}, %1;\n\t"
+        "mov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
+        "fma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
+        : "+f"(acc) : "r"(a), "r"(b));
+    return acc;
 }
+// (o0, o1) += p * (v.lo, v.hi) where p is the low (HI = false) or high half
+// of `pw`; fp16 operands, fp32 accumulators.
+template <bool HI>
+SKV_DEVINL void axpy2_h(uint32_t pw, uint32_t v, float& o0, float& o1) {
+    if constexpr (HI)
+        asm("{\n\t.reg .f16 v0, v1, p0, p1;\n\t"
+            "mov.b32 {v0, v1}, %2;\n\t"
+            "mov.b32 {p0, p1}, %3;\n\t"
+            "fma.rn.f32.f16 %0, p1, v0, %0;\n\t"
+            "fma.rn.f32.f16 %1, p1, v1, %1;\n\t}"
+            : "+f"(o0), "+f"(o1) : "r"(v), "r"(pw));
+    else
+        asm("{\n\t.reg .f16 v0, v1, p0, p1;\n\t"
+            "mov.b32 {v0, v1}, %2;\n\t"
+            "mov.b32 {p0, p1}, %3;\n\t"
+            "fma.rn.f32.f16 %0, p0, v0, %0;\n\t"
+            "fma.rn.f32.f16 %1, p0, v1, %1;\n\t}"
+            : "+f"(o0), "+f"(o1) : "r"(v), "r"(pw));
+}
+SKV_DEVINL uint16_t to_h(float x) { return __half_as_ushort(__float2half_rn(x)); }
 
-template <int G> struct Layout {
-    static constexpr int NV = 8 * G;                 // partial dots per lane per page
-    static constexpr int LF = NV >= 16 ? NV / 16 : 1;  // complete scores per lane
-    static constexpr int LPH = G == 1 ? 16 : 8 / LF; // dim-lanes sharing one head
+// Lane roles.  G >= 2: lane = g * TGN + x, x in [0, TGN) -- in QK x = tg (the
+// lane's tokens are tg + j*TGN, j < G/2), in PV x = dc (the lane's V chunks
+// are dc + j*TGN, j < G/2).  G == 1: QK lane = dh*16 + t (token t, dims of
+// K box dh, two lanes per token); PV lane = dims [4*lane, 4*lane + 4).
+template <int G> struct Roles {
+    static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group size");
+    static constexpr int TGN = G == 1 ? 32 : 32 / G;  // lanes per head
+    static constexpr int TPL = G == 1 ? 1 : G / 2;    // tokens per lane in QK
+    static constexpr int CPL = G == 1 ? 1 : G / 2;    // V chunks per lane in PV
+    static constexpr int DPL = G == 1 ? 4 : 8 * CPL;  // output dims per lane
 };
+
+constexpr int kBoxBytes = kPage * 128;  // one 16 x 64 fp16 K box (2 KB)
 
 template <int G, int W, int R>
 constexpr size_t smem_bytes() {
-    return (size_t)W * R * kStageBytes + (size_t)W * R * sizeof(uint64_t) +
-           (size_t)W * 2 * 8 * G * sizeof(float);
+    return 1024 /* alignment slack */ + (size_t)R * kStageBytes + (size_t)R * sizeof(uint64_t) +
+           (size_t)W * G * kPage * sizeof(uint16_t);
 }
 
 template <int G, int W, int R>
 __global__ void __launch_bounds__(W * 32)
-splitkv_decode_kernel(const DecodeParams p) {
-    using Lay = Layout<G>;
-    constexpr int NV = Lay::NV, LF = Lay::LF, LPH = Lay::LPH;
-    static_assert(W * R * kStageBytes >= W * G * (kD + 2) * (int)sizeof(float),
+splitkv_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const DecodeParams p) {
+    using Ro = Roles<G>;
+    constexpr int TGN = Ro::TGN, TPL = Ro::TPL, CPL = Ro::CPL, DPL = Ro::DPL;
+    constexpr int SPW = R / W;  // ring slots per warp
+    static_assert(R % W == 0, "each warp owns R/W slots");
+    static_assert(R * kStageBytes >= W * G * (kD + 2) * (int)sizeof(float),
                   "the cross-warp merge buffer reuses the ring");
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t* ring = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + W * R * kStageBytes);
-    float* ps_all = reinterpret_cast<float*>(bars + W * R);
+    extern __shared__ uint8_t smem_raw[];
+    // The swizzled K boxes need 1024-byte alignment.  Offset the shared
+    // pointer itself (an integer round trip would lose the shared address
+    // space and turn every K/V read into a generic load).
+    uint8_t* ring = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + R * kStageBytes);
+    uint16_t* ps_all = reinterpret_cast<uint16_t*>(bars + R);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c = lane & 15, th = lane >> 4;
     const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
 
     // The combine grid may be scheduled now; it waits for this grid to finish.
     pdl_launch_dependents();
+    if (threadIdx.x == 0) tma_prefetch_desc(&tmap_k);
 
     int ctx = p.ctx[b];
     const int cap = p.max_pages * kPage;
@@ -129,31 +146,35 @@ splitkv_decode_kernel(const DecodeParams p) {
     const int nw = npages > warp ? (npages - warp + W - 1) / W : 0;  // this warp's pages
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < W * R; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < R; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
     }
     __syncthreads();
 
-    // q for the lane's 8 dims of every head of the group, scaled so that
-    // scores come out in log2 units.
-    float qf[G][8];
+    // q of this lane's head, all 128 dims, as fp16 pairs (G == 1: the 64
+    // dims of K box dh), pinned in registers for the whole split.
+    const int g_lane = G == 1 ? 0 : lane / TGN;
+    const int x_lane = G == 1 ? lane : lane % TGN;
+    constexpr int QW = G == 1 ? 32 : 64;
+    uint32_t qh[QW];
+    {
+        const __half* qrow = p.q + ((int64_t)b * p.Hq + hkv * G + g_lane) * kD +
+                             (G == 1 ? 64 * (lane >> 4) : 0);
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(
-            p.q + ((int64_t)b * p.Hq + hkv * G + g) * kD + 8 * c);
-        unpack_h(raw, qf[g]);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) qf[g][i] *= p.scale_log2;
+        for (int i = 0; i < QW / 4; ++i) {
+            const uint4 a = ld_pinned(qrow + 8 * i);
+            qh[4 * i + 0] = a.x; qh[4 * i + 1] = a.y; qh[4 * i + 2] = a.z; qh[4 * i + 3] = a.w;
+        }
     }
 
     const int32_t* bt = p.block_table + (int64_t)b * p.max_pages;
     const uint64_t pol = policy_evict_first();
-    uint8_t* my_ring = ring + warp * R * kStageBytes;
-    uint64_t* my_bars = bars + warp * R;
+    uint8_t* my_ring = ring + warp * SPW * kStageBytes;
+    uint64_t* my_bars = bars + warp * SPW;
     // Page ids of this warp's pages k in [kb, kb + 32), one per lane.
     int kb = 0;
     int my_id = (lane < nw) ? bt[p0 + warp + lane * W] : 0;
-    auto issue = [&](int k) {  // warp-uniform
+    auto issue = [&](int k) {  // warp-uniform call; lane 0 issues the copies
         if (k - kb >= 32) {
             kb += 32;
             my_id = (kb + lane < nw) ? bt[p0 + warp + (kb + lane) * W] : 0;
@@ -164,159 +185,183 @@ splitkv_decode_kernel(const DecodeParams p) {
                 record_error(p.err, SKV_ERR_INVALID_ARG, 1 << 20 | b);
                 pid = 0;
             }
-            const int slot = k % R;
+            const int slot = k % SPW;
             uint64_t* bar = &my_bars[slot];
             uint8_t* dst = my_ring + slot * kStageBytes;
-            const int64_t off = ((int64_t)pid * p.Hkv + hkv) * (kPage * kD);
+            const int row = (pid * p.Hkv + hkv) * kPage;  // first row of the tile in [P*Hkv*16, 128]
             mbar_arrive_expect_tx(bar, kStageBytes);
-            bulk_g2s(dst, p.k_cache + off, kTileBytes, bar, pol);
-            bulk_g2s(dst + kTileBytes, p.v_cache + off, kTileBytes, bar, pol);
+            tma_load_2d(dst, &tmap_k, 0, row, bar, pol);
+            tma_load_2d(dst + kBoxBytes, &tmap_k, 64, row, bar, pol);
+            bulk_g2s(dst + kTileBytes, p.v_cache + (int64_t)row * kD, kTileBytes, bar, pol);
         }
     };
 #pragma unroll 1
-    for (int k = 0; k < R && k < nw; ++k) issue(k);
+    for (int k = 0; k < SPW && k < nw; ++k) issue(k);
 
-    float o[G][8];
+    float o[DPL];
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o[g][i] = 0.f;
-    float m_own = -INFINITY;  // running max (log2 units) of this lane's head
-    float l_own = 0.f;        // this lane's share of the running sum
-    const int g_own = G == 1 ? 0 : (LF * c) / 8;
-    float* ps = ps_all + warp * (2 * 8 * G);  // p[th][tl][g]
+    for (int i = 0; i < DPL; ++i) o[i] = 0.f;
+    float m_run = -INFINITY;  // running max (log2 units) of this lane's head
+    float l_run = 0.f;        // this lane's share of the running sum
+    uint16_t* ps = ps_all + warp * (G * kPage);  // p[g][token], fp16
 
 #pragma unroll 1
     for (int k = 0; k < nw; ++k) {
-        const int slot = k % R;
-        const bool ok = mbar_wait(&my_bars[slot], (uint32_t)((k / R) & 1), p.err, 2);
+        const int slot = k % SPW;
+        const bool ok = mbar_wait(&my_bars[slot], (uint32_t)((k / SPW) & 1), p.err, 2);
         if (!__all_sync(kFull, ok)) {
             // A bounded wait gave up (error recorded).  Give the copies this
             // warp still has in flight one more bounded wait each before the
             // ring is reused, then stop.
-            for (int kk = k + 1; kk < nw && kk < k + R; ++kk)
-                mbar_wait(&my_bars[kk % R], (uint32_t)((kk / R) & 1), p.err, 3);
+            for (int kk = k + 1; kk < nw && kk < k + SPW; ++kk)
+                mbar_wait(&my_bars[kk % SPW], (uint32_t)((kk / SPW) & 1), p.err, 3);
             break;
         }
-        const int page_idx = p0 + warp + k * W;
-        const int nvalid = min(kPage, ctx - page_idx * kPage);  // >= 1 inside the range
-        const uint8_t* Ks = my_ring + slot * kStageBytes;
-        const uint8_t* Vs = Ks + kTileBytes;
+        const int nvalid = min(kPage, ctx - (p0 + warp + k * W) * kPage);  // >= 1
+        const uint8_t* Kb = my_ring + slot * kStageBytes;  // two swizzled boxes
+        const uint8_t* Vs = Kb + kTileBytes;
 
-        // Partial scores, head-major: part[g * 8 + tl].
-        float part[NV];
+        // ---- scores of this lane's tokens (log2 units, masked)
+        float x[TPL];
+        if constexpr (G == 1) {
+            const int t = lane & 15, dh = lane >> 4;
+            const uint8_t* rowp = Kb + dh * kBoxBytes + t * 128;
+            const uint32_t sw = (t & 7) << 4;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int tl = 0; tl < 8; ++tl) {
-            const uint4 kr = *reinterpret_cast<const uint4*>(Ks + (8 * th + tl) * (kD * 2) + c * 16);
-            float kf[8];
-            unpack_h(kr, kf);
+            for (int c = 0; c < 8; ++c) {
+                // logical chunk c of row t sits at c ^ (t & 7): lanes reading
+                // different rows at the same logical chunk hit distinct banks
+                const uint4 kv = *reinterpret_cast<const uint4*>(rowp + ((c << 4) ^ sw));
+                acc[c & 3] = dot2_h(qh[4 * c + 0], kv.x, acc[c & 3]);
+                acc[c & 3] = dot2_h(qh[4 * c + 1], kv.y, acc[c & 3]);
+                acc[c & 3] = dot2_h(qh[4 * c + 2], kv.z, acc[c & 3]);
+                acc[c & 3] = dot2_h(qh[4 * c + 3], kv.w, acc[c & 3]);
+            }
+            float sc = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            sc += __shfl_xor_sync(kFull, sc, 16);
+            x[0] = t < nvalid ? sc * p.scale_log2 : -INFINITY;
+        } else {
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float a = qf[g][0] * kf[0];
+            for (int j = 0; j < TPL; ++j) {
+                const int t = x_lane + j * TGN;
+                const uint32_t sw = (t & 7) << 4;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int i = 1; i < 8; ++i) a = fmaf(qf[g][i], kf[i], a);
-                part[g * 8 + tl] = a;
+                for (int h = 0; h < 2; ++h) {
+                    const uint8_t* rowp = Kb + h * kBoxBytes + t * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 kv = *reinterpret_cast<const uint4*>(rowp + ((c << 4) ^ sw));
+                        const int qi = 32 * h + 4 * c;
+                        acc[c & 3] = dot2_h(qh[qi + 0], kv.x, acc[c & 3]);
+                        acc[c & 3] = dot2_h(qh[qi + 1], kv.y, acc[c & 3]);
+                        acc[c & 3] = dot2_h(qh[qi + 2], kv.z, acc[c & 3]);
+                        acc[c & 3] = dot2_h(qh[qi + 3], kv.w, acc[c & 3]);
+                    }
+                }
+                const float sc = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                x[j] = t < nvalid ? sc * p.scale_log2 : -INFINITY;
             }
         }
-        reduce_scatter<NV, 8>(part, lane);
 
-        // Complete scores x[i] for (token 8th + tl_i, head g_own), masked.
-        float x[LF];
-        float mx = -INFINITY;
+        // ---- online softmax of this lane's head (its lanes agree on m)
+        float mx = x[0];
 #pragma unroll
-        for (int i = 0; i < LF; ++i) {
-            const int j = G == 1 ? (c >> 1) : LF * c + i;
-            const int t = 8 * th + (j & 7);
-            x[i] = t < nvalid ? part[i] : -INFINITY;
-            mx = fmaxf(mx, x[i]);
-        }
+        for (int j = 1; j < TPL; ++j) mx = fmaxf(mx, x[j]);
 #pragma unroll
-        for (int mm = 1; mm < LPH; mm <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, mm));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-        const float m_new = fmaxf(m_own, mx);  // finite: token 0 of the page is valid
-        const float alpha_own = exp2f(m_own - m_new);
+        for (int mm = 1; mm < (G == 1 ? 16 : TGN); mm <<= 1)
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, mm));
+        const float m_new = fmaxf(m_run, mx);  // finite: token 0 of the page is valid
+        const float alpha = exp2f(m_run - m_new);
         float psum = 0.f;
 #pragma unroll
-        for (int i = 0; i < LF; ++i) {
-            const float pv = exp2f(x[i] - m_new);
-            psum += pv;
-            const int j = G == 1 ? (c >> 1) : LF * c + i;
-            if (G != 1 || (c & 1) == 0) ps[(th * 8 + (j & 7)) * G + g_own] = pv;
-        }
-        l_own = l_own * alpha_own + psum;
-        m_own = m_new;
-        float alpha[G];
-        bool rescale = false;
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            alpha[g] = __shfl_sync(kFull, alpha_own, g * LPH);
-            rescale |= alpha[g] != 1.f;
-        }
-        __syncwarp();
-        if (__any_sync(kFull, rescale)) {
-#pragma unroll
-            for (int g = 0; g < G; ++g)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) o[g][i] *= alpha[g];
-        }
-        const bool ragged = nvalid < kPage;
-#pragma unroll
-        for (int tl = 0; tl < 8; ++tl) {
-            const int t = 8 * th + tl;
-            const uint4 vr = *reinterpret_cast<const uint4*>(Vs + t * (kD * 2) + c * 16);
-            float vf[8];
-            unpack_h(vr, vf);
-            if (ragged && t >= nvalid) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) vf[i] = 0.f;  // never multiply 0 by a stale value
-            }
-            float pg[G];
-            const float* pp = ps + (th * 8 + tl) * G;
-            if constexpr (G % 4 == 0) {
-#pragma unroll
-                for (int g = 0; g < G; g += 4) {
-                    const float4 t4 = *reinterpret_cast<const float4*>(pp + g);
-                    pg[g] = t4.x; pg[g + 1] = t4.y; pg[g + 2] = t4.z; pg[g + 3] = t4.w;
-                }
-            } else if constexpr (G == 2) {
-                const float2 t2 = *reinterpret_cast<const float2*>(pp);
-                pg[0] = t2.x; pg[1] = t2.y;
+        for (int j = 0; j < TPL; ++j) {
+            const float pj = exp2f(x[j] - m_new);
+            psum += pj;
+            if constexpr (G == 1) {
+                if (lane < 16) ps[lane] = to_h(pj);
             } else {
-                pg[0] = pp[0];
+                ps[g_lane * kPage + x_lane + j * TGN] = to_h(pj);
             }
+        }
+        l_run = fmaf(l_run, alpha, psum);
+        m_run = m_new;
+        __syncwarp();
+
+        // ---- o = alpha * o + p V for this lane's head and dims
+        if (__any_sync(kFull, alpha != 1.f)) {
 #pragma unroll
-            for (int g = 0; g < G; ++g)
+            for (int i = 0; i < DPL; ++i) o[i] *= alpha;
+        }
+        const uint4 pa = *reinterpret_cast<const uint4*>(ps + g_lane * kPage);
+        const uint4 pb = *reinterpret_cast<const uint4*>(ps + g_lane * kPage + 8);
+        const uint32_t pw[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+        auto pv_token = [&](int t) {
+            const uint8_t* vrow = Vs + t * (kD * 2);
+            if constexpr (G == 1) {
+                const uint2 vv = *reinterpret_cast<const uint2*>(vrow + 8 * lane);
+                if (t & 1) {
+                    axpy2_h<true>(pw[t >> 1], vv.x, o[0], o[1]);
+                    axpy2_h<true>(pw[t >> 1], vv.y, o[2], o[3]);
+                } else {
+                    axpy2_h<false>(pw[t >> 1], vv.x, o[0], o[1]);
+                    axpy2_h<false>(pw[t >> 1], vv.y, o[2], o[3]);
+                }
+            } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) o[g][i] = fmaf(pg[g], vf[i], o[g][i]);
+                for (int j = 0; j < CPL; ++j) {
+                    const uint4 vv = *reinterpret_cast<const uint4*>(vrow + (x_lane + j * TGN) * 16);
+                    const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (t & 1)
+                            axpy2_h<true>(pw[t >> 1], w4[i], o[8 * j + 2 * i], o[8 * j + 2 * i + 1]);
+                        else
+                            axpy2_h<false>(pw[t >> 1], w4[i], o[8 * j + 2 * i], o[8 * j + 2 * i + 1]);
+                    }
+                }
+            }
+        };
+        if (nvalid == kPage) {
+#pragma unroll
+            for (int t = 0; t < kPage; ++t) pv_token(t);
+        } else {
+            // Partial last page: tokens past ctx are never read (p = 0 must
+            // not meet a stale value).
+#pragma unroll
+            for (int t = 0; t < kPage; ++t)
+                if (t < nvalid) pv_token(t);
         }
         __syncwarp();  // slot and p buffer fully read
-        if (k + R < nw) issue(k + R);
+        if (k + SPW < nw) issue(k + SPW);
     }
 
-    // Per-head totals of this warp: l over the lanes of the head (each lane
-    // pair of G == 1 holds duplicates), o over the two token halves.
+    // This warp's per-head totals: l over the lanes of the head.
 #pragma unroll
-    for (int mm = (G == 1 ? 2 : 1); mm < LPH; mm <<= 1) l_own += __shfl_xor_sync(kFull, l_own, mm);
-    l_own += __shfl_xor_sync(kFull, l_own, 16);
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o[g][i] += __shfl_xor_sync(kFull, o[g][i], 16);
+    for (int mm = 1; mm < (G == 1 ? 16 : TGN); mm <<= 1) l_run += __shfl_xor_sync(kFull, l_run, mm);
 
     __syncthreads();  // every warp is done with its ring: reuse it
     float* wo = reinterpret_cast<float*>(ring);  // [W][G][kD]
     float* wm = wo + W * G * kD;                 // [W][G]
     float* wl = wm + W * G;                      // [W][G]
-    if (th == 0) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float4* dst = reinterpret_cast<float4*>(wo + (warp * G + g) * kD + 8 * c);
-            dst[0] = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
-            dst[1] = make_float4(o[g][4], o[g][5], o[g][6], o[g][7]);
+    if constexpr (G == 1) {
+        *reinterpret_cast<float4*>(wo + warp * kD + 4 * lane) = make_float4(o[0], o[1], o[2], o[3]);
+        if (lane == 0) {
+            wm[warp] = m_run;
+            wl[warp] = l_run;
         }
-        if (c % LPH == 0) {
-            wm[warp * G + g_own] = m_own;
-            wl[warp * G + g_own] = l_own;
+    } else {
+        float* dst = wo + (warp * G + g_lane) * kD;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            float4* d4 = reinterpret_cast<float4*>(dst + 8 * (x_lane + j * TGN));
+            d4[0] = make_float4(o[8 * j + 0], o[8 * j + 1], o[8 * j + 2], o[8 * j + 3]);
+            d4[1] = make_float4(o[8 * j + 4], o[8 * j + 5], o[8 * j + 6], o[8 * j + 7]);
+        }
+        if (x_lane == 0) {
+            wm[warp * G + g_lane] = m_run;
+            wl[warp * G + g_lane] = l_run;
         }
     }
     __syncthreads();
@@ -346,11 +391,18 @@ splitkv_decode_kernel(const DecodeParams p) {
     }
 }
 
-constexpr int kWarps = 2;
-constexpr int kRing = 3;
+#ifndef SKV_DECODE_WARPS
+#define SKV_DECODE_WARPS 3
+#endif
+#ifndef SKV_DECODE_RING
+#define SKV_DECODE_RING 6
+#endif
+constexpr int kWarps = SKV_DECODE_WARPS;
+constexpr int kRing = SKV_DECODE_RING;
 
 template <int G>
-cudaError_t launch_g(const DecodeParams& p, int B, int Hkv, int NS, cudaStream_t st) {
+cudaError_t launch_g(const CUtensorMap& tk, const DecodeParams& p, int B, int Hkv, int NS,
+                     cudaStream_t st) {
     constexpr size_t smem = smem_bytes<G, kWarps, kRing>();
     auto kern = splitkv_decode_kernel<G, kWarps, kRing>;
     static bool attr_set[64] = {};
@@ -361,16 +413,141 @@ cudaError_t launch_g(const DecodeParams& p, int B, int Hkv, int NS, cudaStream_t
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    kern<<<dim3(NS, Hkv, B), kWarps * 32, smem, st>>>(p);
+    kern<<<dim3(NS, Hkv, B), kWarps * 32, smem, st>>>(tk, p);
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- combine (pass 2)
+// [L3] §③ merge of the split states (base 2), then, for the cascade, a
+// two-state merge with a prefix state ([F2] §⑥).  One CTA per (b, hq) row,
+// 4 warps: warp w takes splits w, w + 4, ...; lane l owns dims [4l, 4l + 4).
+// A warp requests the lse and v chunk of up to kCombBatch splits at once
+// (one L2 round trip for NS <= 4 * kCombBatch), keeps an online (m, W, acc)
+// across batches, and the 4 warp states meet in shared memory.
+constexpr int kCombWarps = 4;
+constexpr int kCombBatch = 16;
+
+struct CombineParams {
+    const float* o_part;   // [rows, NS, D]
+    const float* lse_part; // [rows, NS]
+    void* out;             // [rows, D] Tout
+    float* lse_out;        // [rows] or nullptr
+    const float* extra_v;  // [rows, D] or nullptr
+    const float* extra_s;  // [rows]
+    int NS, D;
+};
+
+template <typename Tout>
+__global__ void __launch_bounds__(kCombWarps * 32)
+combine_kernel(const CombineParams p) {
+    pdl_wait_primary();  // the split states are written by the preceding grid
+    __shared__ float wm[kCombWarps], wW[kCombWarps];
+    __shared__ __align__(16) float wacc[kCombWarps][kD];
+    __shared__ __align__(16) float fin[kD];
+    const int64_t row = blockIdx.x;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool has = 4 * lane < p.D;
+    float m = -INFINITY, W = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int n0 = w; n0 < p.NS; n0 += kCombWarps * kCombBatch) {
+        float lse[kCombBatch];
+        float4 v[kCombBatch];
+#pragma unroll
+        for (int k = 0; k < kCombBatch; ++k) {
+            const int n = n0 + k * kCombWarps;
+            lse[k] = -INFINITY;
+            v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (n < p.NS) {
+                lse[k] = sanitize_lse(ld_cg_f32(p.lse_part + row * p.NS + n));
+                if (has) {
+                    const uint4 r = ld_cg(p.o_part + (row * p.NS + n) * p.D + 4 * lane);
+                    v[k] = make_float4(__uint_as_float(r.x), __uint_as_float(r.y),
+                                       __uint_as_float(r.z), __uint_as_float(r.w));
+                }
+            }
+        }
+        float mb = m;
+#pragma unroll
+        for (int k = 0; k < kCombBatch; ++k) mb = fmaxf(mb, lse[k]);
+        const float sc = merge_weight(m, mb);  // rescale of the running state
+        W *= sc;
+        acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+#pragma unroll
+        for (int k = 0; k < kCombBatch; ++k) {
+            const float wk = merge_weight(lse[k], mb);
+            if (wk > 0.f) {
+                W += wk;
+                acc.x = fmaf(wk, v[k].x, acc.x); acc.y = fmaf(wk, v[k].y, acc.y);
+                acc.z = fmaf(wk, v[k].z, acc.z); acc.w = fmaf(wk, v[k].w, acc.w);
+            }
+        }
+        m = mb;
+    }
+    if (lane == 0) {
+        wm[w] = m;
+        wW[w] = W;
+    }
+    if (has) *reinterpret_cast<float4*>(&wacc[w][4 * lane]) = acc;
+    __syncthreads();
+    if (w == 0 && has) {
+        float M = wm[0];
+#pragma unroll
+        for (int i = 1; i < kCombWarps; ++i) M = fmaxf(M, wm[i]);
+        float WW = 0.f;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < kCombWarps; ++i) {
+            const float sc = merge_weight(wm[i], M);
+            WW = fmaf(sc, wW[i], WW);
+            const float4 t = *reinterpret_cast<const float4*>(&wacc[i][4 * lane]);
+            a.x = fmaf(sc, t.x, a.x); a.y = fmaf(sc, t.y, a.y);
+            a.z = fmaf(sc, t.z, a.z); a.w = fmaf(sc, t.w, a.w);
+        }
+        const float inv = WW > 0.f ? 1.f / WW : 0.f;
+        float vd[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
+        float sd = M + log2f(WW);  // -inf when every split is empty
+        if (p.extra_v != nullptr) {
+            // Cascade: prefix state first, merged split state second.
+            const float se = sanitize_lse(p.extra_s[row]), sb = sanitize_lse(sd);
+            const float mm = fmaxf(se, sb);
+            const float we = merge_weight(se, mm), wb = merge_weight(sb, mm);
+            const float ws = __fadd_rn(we, wb);
+            const float iv = ws > 0.f ? 1.f / ws : 0.f;
+            const float4 xe = *reinterpret_cast<const float4*>(p.extra_v + row * p.D + 4 * lane);
+            const float xs[4] = {xe.x, xe.y, xe.z, xe.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float te = we > 0.f ? __fmul_rn(we, xs[i]) : 0.f;
+                const float tb = wb > 0.f ? __fmul_rn(wb, vd[i]) : 0.f;
+                vd[i] = __fmul_rn(__fadd_rn(te, tb), iv);
+            }
+            sd = mm + log2f(ws);
+        }
+        *reinterpret_cast<float4*>(&fin[4 * lane]) = make_float4(vd[0], vd[1], vd[2], vd[3]);
+        if (lane == 0 && p.lse_out != nullptr) p.lse_out[row] = sd;
+    }
+    __syncthreads();
+    constexpr int EO = Vec<Tout>::N;
+    if ((int)threadIdx.x < p.D / EO) {
+        float f[EO];
+#pragma unroll
+        for (int e = 0; e < EO; ++e) f[e] = fin[threadIdx.x * EO + e];
+        char* orow = reinterpret_cast<char*>(p.out) + row * p.D * (int64_t)sizeof(Tout);
+        st_stream(orow + threadIdx.x * 16, from_float<Tout>(f));
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_splitkv_decode(const DecodeArgs& a, const DeviceInfo& dev, cudaStream_t st) {
+    // K cache viewed as [P * Hkv * page rows, 128 cols] fp16; boxes of
+    // 16 rows x 64 cols (one page tile, half of the head dim), 128-byte swizzle.
+    CUtensorMap tk;
+    cudaError_t e = make_tmap_2d_16bit(&tk, a.k_cache, (uint64_t)a.num_pool_pages * a.Hkv * kPage,
+                                       kD, kD * 2, 64, kPage, true, false);
+    if (e != cudaSuccess) return e;
     DecodeParams p;
     p.q = static_cast<const __half*>(a.q);
-    p.k_cache = static_cast<const __half*>(a.k_cache);
     p.v_cache = static_cast<const __half*>(a.v_cache);
     p.block_table = a.block_table;
     p.ctx = a.ctx;
@@ -385,10 +562,46 @@ cudaError_t launch_splitkv_decode(const DecodeArgs& a, const DeviceInfo& dev, cu
     p.NS = a.num_splits;
     p.scale_log2 = a.sm_scale * 1.4426950408889634f;
     switch (a.Hq / a.Hkv) {
-        case 1: return launch_g<1>(p, a.B, a.Hkv, a.num_splits, st);
-        case 2: return launch_g<2>(p, a.B, a.Hkv, a.num_splits, st);
-        case 4: return launch_g<4>(p, a.B, a.Hkv, a.num_splits, st);
-        case 8: return launch_g<8>(p, a.B, a.Hkv, a.num_splits, st);
+        case 1: return launch_g<1>(tk, p, a.B, a.Hkv, a.num_splits, st);
+        case 2: return launch_g<2>(tk, p, a.B, a.Hkv, a.num_splits, st);
+        case 4: return launch_g<4>(tk, p, a.B, a.Hkv, a.num_splits, st);
+        case 8: return launch_g<8>(tk, p, a.B, a.Hkv, a.num_splits, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace skv
+
+namespace skv {
+
+cudaError_t launch_combine(const float* o_part, const float* lse_part, int64_t rows, int NS,
+                           int64_t D, void* out, skv_dtype out_dt, float* lse_out,
+                           const float* extra_v, const float* extra_s, bool pdl,
+                           const DeviceInfo& dev, cudaStream_t st) {
+    (void)dev;
+    if (D > kD || D % 8 != 0) return cudaErrorInvalidValue;
+    CombineParams p;
+    p.o_part = o_part;
+    p.lse_part = lse_part;
+    p.out = out;
+    p.lse_out = lse_out;
+    p.extra_v = extra_v;
+    p.extra_s = extra_s;
+    p.NS = NS;
+    p.D = (int)D;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rows, 1, 1);
+    cfg.blockDim = dim3(kCombWarps * 32, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    switch (out_dt) {
+        case SKV_F32: return cudaLaunchKernelEx(&cfg, combine_kernel<float>, p);
+        case SKV_F16: return cudaLaunchKernelEx(&cfg, combine_kernel<__half>, p);
+        case SKV_BF16: return cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, p);
     }
     return cudaErrorInvalidValue;
 }

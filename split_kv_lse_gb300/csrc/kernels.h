@@ -34,7 +34,7 @@ struct MergeStatesPlan {
     int per_split = 0;         // states per CTA on the CTA path
     size_t ws_bytes = 0;       // workspace the plan needs
 };
-MergeStatesPlan plan_merge_states(int64_t rows, int64_t N, int64_t D, int sm_count,
+MergeStatesPlan plan_merge_states(int64_t rows, int64_t N, int64_t D, int chunks, int sm_count,
                                   size_t ws_available);
 size_t merge_states_ws_upper_bound(int64_t rows, int64_t N, int64_t D);
 

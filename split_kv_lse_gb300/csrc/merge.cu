@@ -12,7 +12,7 @@
 // a 128-bit coalesced access; each thread keeps several rows (or states) of
 // loads in flight before it computes; all arithmetic is fp32.
 //   merge_state_kernel        two states, team per row (in-place variant too)
-//   merge_states_team_kernel  N states, team per row: many rows
+//   merge_states_bulk_kernel  N states, warp per row, TMA ring: many rows
 //   merge_states_cta_kernel   N states, one CTA (8 warps) per row or per chunk
 //                             of a row's states: few rows, many states; the
 //                             chunks of a row meet in a workspace and the
@@ -24,6 +24,7 @@
 namespace skv {
 namespace {
 
+#define SKV_HOSTDEV_CONST __host__ __device__ constexpr
 constexpr int kThreads = 256;
 
 // Lanes of this thread's team inside its warp (teams are aligned powers of 2).
@@ -57,6 +58,23 @@ SKV_DEVINL float blend(float wa, float xa, float wb, float xb, float inv) {
 }
 
 // ---------------------------------------------------------------- two-state merge
+// Coefficients of the merged row: v = ca * v_a + cb * v_b with
+// ca = w_a / W, cb = w_b / W.  A zero-weight operand's vector is zeroed
+// before use (it is never read into the result, even if not finite).
+struct TwoCoef {
+    float ca, cb, s;
+};
+SKV_DEVINL TwoCoef two_coef(float sa, float sb) {
+    const TwoWeights t = two_weights(sa, sb);
+    TwoCoef c;
+    c.ca = __fmul_rn(t.wa, t.inv);
+    c.cb = __fmul_rn(t.wb, t.inv);
+    c.s = t.s;
+    return c;
+}
+
+// Team of tpr lanes per row, each lane owning CPT 16-byte chunks
+// (c = l + k*tpr); U rows in flight per lane.
 template <typename T, int CPT, int U, bool kInPlace>
 __global__ void __launch_bounds__(kThreads)
 merge_state_kernel(const T* va, const float* sa, const T* __restrict__ vb,
@@ -83,6 +101,7 @@ merge_state_kernel(const T* va, const float* sa, const T* __restrict__ vb,
 #pragma unroll
             for (int k = 0; k < CPT; ++k) {
                 const int c = l + k * tpr;
+                ra[u][k] = rb[u][k] = make_uint4(0, 0, 0, 0);
                 if (ok && c < chunks) {
                     const char* pa = reinterpret_cast<const char*>(va) + r * row_stride + c * 16;
                     const char* pb = reinterpret_cast<const char*>(vb) + r * row_stride + c * 16;
@@ -98,115 +117,142 @@ merge_state_kernel(const T* va, const float* sa, const T* __restrict__ vb,
         for (int u = 0; u < U; ++u) {
             const int64_t r = r0 + u * nteams;
             if (r >= rows) continue;
-            const TwoWeights t = two_weights(xa[u], xb[u]);
+            const TwoCoef cf = two_coef(xa[u], xb[u]);
 #pragma unroll
             for (int k = 0; k < CPT; ++k) {
                 const int c = l + k * tpr;
                 if (c >= chunks) continue;
+                if (!(cf.ca > 0.f)) ra[u][k] = make_uint4(0, 0, 0, 0);
+                if (!(cf.cb > 0.f)) rb[u][k] = make_uint4(0, 0, 0, 0);
                 float fa[E], fb[E], fo[E];
                 to_float<T>(ra[u][k], fa);
                 to_float<T>(rb[u][k], fb);
 #pragma unroll
-                for (int e = 0; e < E; ++e) fo[e] = blend(t.wa, fa[e], t.wb, fb[e], t.inv);
+                for (int e = 0; e < E; ++e)
+                    fo[e] = __fadd_rn(__fmul_rn(cf.ca, fa[e]), __fmul_rn(cf.cb, fb[e]));
                 char* po = reinterpret_cast<char*>(vo) + r * row_stride + c * 16;
                 st_stream(po, from_float<T>(fo));
             }
-            if (l == 0) so[r] = t.s;
+            if (l == 0) so[r] = cf.s;
         }
     }
 }
 
-// ---------------------------------------------------------------- N-state, team per row
-// Rows handled by one warp = 32 / tpr; the loop trip count is uniform per
-// warp so that full-warp shuffles are always legal; tail rows are masked.
-template <typename Tin, typename Tout, int CPT, int NB>
-__global__ void __launch_bounds__(kThreads)
-merge_states_team_kernel(const Tin* __restrict__ v, const float* __restrict__ s,
-                         Tout* __restrict__ vo, float* __restrict__ so, int64_t rows, int N,
-                         int64_t H, int chunks, int tpr_log2) {
-    constexpr int E = Vec<Tin>::N;
-    static_assert(Vec<Tin>::N == Vec<Tout>::N, "same element count per 16-byte chunk");
-    const int tpr = 1 << tpr_log2;
-    const int lane = threadIdx.x & 31;
-    const int l = lane & (tpr - 1);
-    const int team_in_warp = lane >> tpr_log2;
-    const int teams_per_warp = 32 >> tpr_log2;
-    const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int src_base = lane & ~(tpr - 1);
-    const int64_t row_bytes = (int64_t)chunks * 16;
+// ---------------------------------------------------------------- N-state, warp per row
+// One warp per (pos, h) row.  The row's weights are computed once into shared
+// memory; then only the states with non-zero weight are streamed: each
+// state's v row (D contiguous elements) is one TMA bulk copy into a per-warp
+// ring of kBulkRing slots, refilled as soon as it is consumed, so up to
+// kBulkRing rows per warp are in flight without holding registers.
+constexpr int kBulkWarps = 8;
+constexpr int kBulkRing = 8;
+constexpr int kBulkMaxN = 256;
 
-    for (int64_t rw = warp_id * teams_per_warp; rw < rows; rw += nwarps * teams_per_warp) {
-        const int64_t r = rw + team_in_warp;
-        const bool ok = r < rows;
-        const int64_t pos = ok ? r / H : 0, h = ok ? r % H : 0;
-        // s[pos, n, h] at (pos*N + n)*H + h ([F2] §④).
-        const float* srow = s + (pos * N) * H + h;
-        float m = -INFINITY;
-        for (int n = l; n < N; n += tpr) m = fmaxf(m, ok ? sanitize_lse(srow[(int64_t)n * H]) : -INFINITY);
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1)
-            if (o < tpr) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        float W = 0.f;
-        for (int n = l; n < N; n += tpr) W += ok ? merge_weight(sanitize_lse(srow[(int64_t)n * H]), m) : 0.f;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1)
-            if (o < tpr) W += __shfl_xor_sync(0xffffffffu, W, o);
+SKV_HOSTDEV_CONST size_t bulk_smem_bytes(int row_bytes) {
+    return (size_t)kBulkWarps * kBulkRing * row_bytes +                 // rings
+           (size_t)kBulkWarps * kBulkRing * sizeof(uint64_t) +          // mbarriers
+           (size_t)kBulkWarps * kBulkMaxN * sizeof(float) +             // weights
+           (size_t)kBulkWarps * kBulkRing * sizeof(int);                // state of each slot
+}
 
-        float acc[CPT][E];
-#pragma unroll
-        for (int k = 0; k < CPT; ++k)
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc[k][e] = 0.f;
+template <typename T>
+__global__ void __launch_bounds__(kBulkWarps * 32)
+merge_states_bulk_kernel(const T* __restrict__ v, const float* __restrict__ s,
+                         T* __restrict__ vo, float* __restrict__ so, int64_t rows, int N,
+                         int64_t H, int chunks, unsigned long long* err) {
+    constexpr int E = Vec<T>::N;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int row_bytes = chunks * 16;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* ring = smem + (size_t)warp * kBulkRing * row_bytes;
+    uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + (size_t)kBulkWarps * kBulkRing * row_bytes);
+    uint64_t* bars = bars_all + warp * kBulkRing;
+    float* wsm = reinterpret_cast<float*>(bars_all + kBulkWarps * kBulkRing) + warp * kBulkMaxN;
+    int* slot_n = reinterpret_cast<int*>(reinterpret_cast<float*>(bars_all + kBulkWarps * kBulkRing) +
+                                         kBulkWarps * kBulkMaxN) + warp * kBulkRing;
 
-        const char* vrow = reinterpret_cast<const char*>(v) + ((pos * N) * H + h) * row_bytes;
-        const int64_t nstride = H * row_bytes;  // bytes between consecutive states
-        const int nb = NB < tpr ? NB : tpr;  // states per batch: one weight per team lane
-        for (int n0 = 0; n0 < N; n0 += nb) {
-            // Lane j < nb of the team computes the weight of state n0 + j.
-            float wmine = 0.f;
-            if (ok && l < nb && n0 + l < N) wmine = merge_weight(sanitize_lse(srow[(int64_t)(n0 + l) * H]), m);
-            float w[NB];
-            uint4 raw[NB][CPT];
-#pragma unroll
-            for (int j = 0; j < NB; ++j) {
-                w[j] = __shfl_sync(0xffffffffu, wmine, src_base + (j < nb ? j : 0));
-                if (j >= nb) w[j] = 0.f;
-#pragma unroll
-                for (int k = 0; k < CPT; ++k) {
-                    const int c = l + k * tpr;
-                    if (w[j] > 0.f && c < chunks)
-                        raw[j][k] = ld_stream(vrow + (int64_t)(n0 + j) * nstride + c * 16);
-                    else
-                        raw[j][k] = make_uint4(0, 0, 0, 0);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < NB; ++j) {
-                if (!(w[j] > 0.f)) continue;
-#pragma unroll
-                for (int k = 0; k < CPT; ++k) {
-                    float f[E];
-                    to_float<Tin>(raw[j][k], f);
-#pragma unroll
-                    for (int e = 0; e < E; ++e) acc[k][e] = fmaf(w[j], f[e], acc[k][e]);
-                }
-            }
-        }
-        if (!ok) continue;
-        const float inv = W > 0.f ? 1.f / W : 0.f;
-        char* orow = reinterpret_cast<char*>(vo) + r * row_bytes;
-#pragma unroll
-        for (int k = 0; k < CPT; ++k) {
-            const int c = l + k * tpr;
-            if (c >= chunks) continue;
-            float f[E];
-#pragma unroll
-            for (int e = 0; e < E; ++e) f[e] = acc[k][e] * inv;
-            st_stream(orow + c * 16, from_float<Tout>(f));
-        }
-        if (l == 0) so[r] = m + log2f(W);
+    const int64_t r = (int64_t)blockIdx.x * kBulkWarps + warp;
+    if (r >= rows) return;  // whole warp; no block-wide barrier follows
+    if (lane == 0) {
+        for (int i = 0; i < kBulkRing; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
     }
+    const int64_t pos = r / H, h = r % H;
+    // s[pos, n, h] at (pos*N + n)*H + h ([F2] §④).
+    const float* srow = s + (pos * N) * H + h;
+    float m = -INFINITY;
+    for (int n = lane; n < N; n += 32) m = fmaxf(m, sanitize_lse(srow[(int64_t)n * H]));
+    m = warp_max(m);
+    float W = 0.f;
+    for (int n = lane; n < N; n += 32) {
+        const float w = merge_weight(sanitize_lse(srow[(int64_t)n * H]), m);
+        wsm[n] = w;
+        W += w;
+    }
+    W = warp_sum(W);
+    __syncwarp();
+
+    const char* vrow = reinterpret_cast<const char*>(v) + ((pos * N) * H + h) * row_bytes;
+    const int64_t nstride = H * row_bytes;
+    const uint64_t pol = policy_evict_first();
+    int n_next = 0;  // next state to consider for a copy
+    auto next_nonzero = [&](int n) {
+        while (n < N && !(wsm[n] > 0.f)) ++n;
+        return n;
+    };
+    auto issue = [&](int slot, int n) {
+        if (lane == 0) {
+            slot_n[slot] = n;
+            mbar_arrive_expect_tx(&bars[slot], row_bytes);
+            bulk_g2s(ring + slot * row_bytes, vrow + (int64_t)n * nstride, row_bytes, &bars[slot], pol);
+        }
+    };
+    int inflight = 0;
+    for (int i = 0; i < kBulkRing; ++i) {
+        n_next = next_nonzero(n_next);
+        if (n_next >= N) break;
+        issue(i, n_next);
+        ++n_next;
+        ++inflight;
+    }
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    for (int q = 0; inflight > 0; ++q) {
+        const int slot = q % kBulkRing;
+        const bool ok = mbar_wait(&bars[slot], (uint32_t)((q / kBulkRing) & 1), err, 6);
+        if (!__all_sync(0xffffffffu, ok)) {
+            // Bounded wait gave up (error recorded): one more bounded wait per
+            // copy still in flight, then stop.
+            for (int i = 1; i < inflight; ++i)
+                mbar_wait(&bars[(q + i) % kBulkRing], (uint32_t)(((q + i) / kBulkRing) & 1), err, 7);
+            return;
+        }
+        const float w = wsm[slot_n[slot]];
+        if (lane < chunks) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(ring + slot * row_bytes + lane * 16);
+            float f[E];
+            to_float<T>(raw, f);
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = fmaf(w, f[e], acc[e]);
+        }
+        __syncwarp();  // slot (and slot_n) fully read
+        --inflight;
+        n_next = next_nonzero(n_next);
+        if (n_next < N) {
+            issue(slot, n_next);
+            ++n_next;
+            ++inflight;
+        }
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    if (lane < chunks) {
+        float f[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) f[e] = acc[e] * inv;
+        st_stream(reinterpret_cast<char*>(vo) + r * row_bytes + lane * 16, from_float<T>(f));
+    }
+    if (lane == 0) so[r] = m + log2f(W);
 }
 
 // ---------------------------------------------------------------- N-state, CTA per row
@@ -221,8 +267,8 @@ struct CtaParams {
     int tpr_log2;
     int nsplit;           // CTAs per row
     int per_split;        // states per CTA
-    float* ws_v;          // [rows, nsplit, D] fp32 partial states (nsplit > 1)
-    float* ws_s;          // [rows, nsplit]
+    float* ws_v;          // [rows, nsplit, D] fp32 unnormalised chunk sums (nsplit > 1)
+    float* ws_s;          // [rows, nsplit, 2]: chunk max m and weight sum W
     unsigned* ws_cnt;     // [rows] arrival tickets, zero between calls
     const float* extra_v; // [rows, D] fp32 state merged last, or nullptr
     const float* extra_s; // [rows]
@@ -323,10 +369,19 @@ merge_states_cta_kernel(CtaParams p) {
     float s_fin = s_chunk;
 
     if (p.nsplit > 1) {
-        // Publish this chunk's partial state, then take a ticket; the CTA that
-        // draws the last ticket of the row merges all partials.
-        if (threadIdx.x < D) p.ws_v[(row * p.nsplit + split) * D + threadIdx.x] = vd;
-        if (threadIdx.x == 0) p.ws_s[row * p.nsplit + split] = s_chunk;
+        // Publish this chunk's partial state unnormalised -- (m, W, sum w v) --
+        // so the final merge keeps single-pass accuracy (an fp32 s = m +
+        // log2 W of magnitude ~40 would carry ~1e-6 relative weight error).
+        // Then take a ticket; the CTA that draws the row's last ticket merges.
+        if (threadIdx.x < D) {
+            float raw = 0.f;
+            for (int t = 0; t < nteams; ++t) raw += part[t * D + threadIdx.x];
+            p.ws_v[(row * p.nsplit + split) * D + threadIdx.x] = raw;
+        }
+        if (threadIdx.x == 0) {
+            p.ws_s[(row * p.nsplit + split) * 2 + 0] = m;
+            p.ws_s[(row * p.nsplit + split) * 2 + 1] = W;
+        }
         __threadfence();
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -338,13 +393,13 @@ merge_states_cta_kernel(CtaParams p) {
         if (!is_last) return;
         __threadfence();
         float M = -INFINITY;
-        for (int k = 0; k < p.nsplit; ++k) M = fmaxf(M, ld_cg_f32(&p.ws_s[row * p.nsplit + k]));
+        for (int k = 0; k < p.nsplit; ++k) M = fmaxf(M, ld_cg_f32(&p.ws_s[(row * p.nsplit + k) * 2]));
         float WW = 0.f, a = 0.f;
         for (int k = 0; k < p.nsplit; ++k) {
-            const float wk = merge_weight(ld_cg_f32(&p.ws_s[row * p.nsplit + k]), M);
-            WW += wk;
-            if (threadIdx.x < D && wk > 0.f)
-                a = fmaf(wk, ld_cg_f32(&p.ws_v[(row * p.nsplit + k) * D + threadIdx.x]), a);
+            const float sc = merge_weight(ld_cg_f32(&p.ws_s[(row * p.nsplit + k) * 2]), M);
+            if (!(sc > 0.f)) continue;
+            WW = fmaf(sc, ld_cg_f32(&p.ws_s[(row * p.nsplit + k) * 2 + 1]), WW);
+            if (threadIdx.x < D) a = fmaf(sc, ld_cg_f32(&p.ws_v[(row * p.nsplit + k) * D + threadIdx.x]), a);
         }
         vd = WW > 0.f ? a * (1.f / WW) : 0.f;
         s_fin = M + log2f(WW);
@@ -382,32 +437,25 @@ template <typename T>
 cudaError_t launch_merge_state_t(const void* va, const float* sa, const void* vb,
                                  const float* sb, void* vo, float* so, int64_t rows, int chunks,
                                  bool in_place, const DeviceInfo& dev, cudaStream_t st) {
-    const int tpr_log2 = chunks >= 32 ? 5 : log2_pow2_at_least(chunks);
+    // Four 16-byte chunks per lane: a row's weights are computed by
+    // ceil(chunks / 4) lanes, and each lane keeps 2 rows x 8 loads in flight.
+    constexpr int CPT = 4, U = 2;
+    const int tpr_log2 = log2_pow2_at_least((chunks + CPT - 1) / CPT);
     const int tpr = 1 << tpr_log2;
-    const int cpt = (chunks + tpr - 1) / tpr;
-    constexpr int U = 4;
     const int64_t threads_needed = ((rows + U - 1) / U) * tpr;
     int64_t blocks = (threads_needed + kThreads - 1) / kThreads;
-    const int64_t cap = (int64_t)dev.sm_count * 64;
+    const int64_t cap = (int64_t)dev.sm_count * 32;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     const T* a = static_cast<const T*>(va);
     const T* b = static_cast<const T*>(vb);
     T* o = static_cast<T*>(vo);
-#define SKV_MS_LAUNCH(CPT_, UU_)                                                            \
-    do {                                                                                    \
-        if (in_place)                                                                       \
-            merge_state_kernel<T, CPT_, UU_, true><<<(unsigned)blocks, kThreads, 0, st>>>(  \
-                a, sa, b, sb, o, so, rows, chunks, tpr_log2);                               \
-        else                                                                                \
-            merge_state_kernel<T, CPT_, UU_, false><<<(unsigned)blocks, kThreads, 0, st>>>( \
-                a, sa, b, sb, o, so, rows, chunks, tpr_log2);                               \
-    } while (0)
-    if (cpt == 1) SKV_MS_LAUNCH(1, 4);
-    else if (cpt == 2) SKV_MS_LAUNCH(2, 2);
-    else if (cpt <= 4) SKV_MS_LAUNCH(4, 1);
-    else return cudaErrorInvalidValue;
-#undef SKV_MS_LAUNCH
+    if (in_place)
+        merge_state_kernel<T, CPT, U, true><<<(unsigned)blocks, kThreads, 0, st>>>(
+            a, sa, b, sb, o, so, rows, chunks, tpr_log2);
+    else
+        merge_state_kernel<T, CPT, U, false><<<(unsigned)blocks, kThreads, 0, st>>>(
+            a, sa, b, sb, o, so, rows, chunks, tpr_log2);
     return cudaGetLastError();
 }
 
@@ -458,7 +506,7 @@ static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 static size_t ws_bytes_for(int64_t rows, int nsplit, int64_t D) {
     if (nsplit <= 1) return 0;
-    return align256((size_t)rows * nsplit * D * 4) + align256((size_t)rows * nsplit * 4) +
+    return align256((size_t)rows * nsplit * D * 4) + align256((size_t)rows * nsplit * 8) +
            align256((size_t)rows * 4);
 }
 
@@ -467,10 +515,11 @@ size_t merge_states_ws_upper_bound(int64_t rows, int64_t N, int64_t D) {
     return ws_bytes_for(rows, max_split_for(N), D);
 }
 
-MergeStatesPlan plan_merge_states(int64_t rows, int64_t N, int64_t D, int sm_count,
+MergeStatesPlan plan_merge_states(int64_t rows, int64_t N, int64_t D, int chunks, int sm_count,
                                   size_t ws_available) {
+    (void)chunks;
     MergeStatesPlan pl;
-    if (rows >= kTeamRows) {
+    if (rows >= kTeamRows && N <= kBulkMaxN) {
         pl.team_kernel = true;
         return pl;
     }
@@ -489,32 +538,20 @@ cudaError_t launch_merge_states(const void* v, const float* s, void* vo, float* 
                                 size_t ws_bytes, const DeviceInfo& dev, cudaStream_t st) {
     const int64_t rows = S * H;
     const int chunks = (int)(D * (int64_t)dtype_size(dt) / 16);
-    const MergeStatesPlan pl = plan_merge_states(rows, N, D, dev.sm_count, ws ? ws_bytes : 0);
+    const MergeStatesPlan pl = plan_merge_states(rows, N, D, chunks, dev.sm_count, ws ? ws_bytes : 0);
     if (pl.team_kernel) {
-        const int tpr_log2 = chunks >= 32 ? 5 : log2_pow2_at_least(chunks);
-        const int tpr = 1 << tpr_log2;
-        const int cpt = (chunks + tpr - 1) / tpr;
-        const int64_t warps = (rows + (32 / tpr) - 1) / (32 / tpr);
-        int64_t blocks = (warps * 32 + kThreads - 1) / kThreads;
-        const int64_t cap = (int64_t)dev.sm_count * 32;
-        if (blocks > cap) blocks = cap;
-#define SKV_TEAM(T_, CPT_)                                                                     \
-    merge_states_team_kernel<T_, T_, CPT_, 8><<<(unsigned)blocks, kThreads, 0, st>>>(          \
-        static_cast<const T_*>(v), s, static_cast<T_*>(vo), so, rows, (int)N, H, chunks, tpr_log2)
-#define SKV_TEAM_CPT(T_)                        \
-    do {                                        \
-        if (cpt == 1) SKV_TEAM(T_, 1);          \
-        else if (cpt == 2) SKV_TEAM(T_, 2);     \
-        else if (cpt <= 4) SKV_TEAM(T_, 4);     \
-        else return cudaErrorInvalidValue;      \
-    } while (0)
+        const int row_bytes = chunks * 16;
+        const size_t smem = bulk_smem_bytes(row_bytes);
+        const unsigned blocks = (unsigned)((rows + kBulkWarps - 1) / kBulkWarps);
+#define SKV_BULK(T_)                                                                           \
+    merge_states_bulk_kernel<T_><<<blocks, kBulkWarps * 32, smem, st>>>(                      \
+        static_cast<const T_*>(v), s, static_cast<T_*>(vo), so, rows, (int)N, H, chunks, dev.err)
         switch (dt) {
-            case SKV_F32: SKV_TEAM_CPT(float); break;
-            case SKV_F16: SKV_TEAM_CPT(__half); break;
-            case SKV_BF16: SKV_TEAM_CPT(__nv_bfloat16); break;
+            case SKV_F32: SKV_BULK(float); break;
+            case SKV_F16: SKV_BULK(__half); break;
+            case SKV_BF16: SKV_BULK(__nv_bfloat16); break;
         }
-#undef SKV_TEAM_CPT
-#undef SKV_TEAM
+#undef SKV_BULK
         return cudaGetLastError();
     }
     CtaParams p = {};
@@ -533,38 +570,13 @@ cudaError_t launch_merge_states(const void* v, const float* s, void* vo, float* 
         p.ws_v = reinterpret_cast<float*>(w);
         w += align256((size_t)rows * pl.nsplit * D * 4);
         p.ws_s = reinterpret_cast<float*>(w);
-        w += align256((size_t)rows * pl.nsplit * 4);
+        w += align256((size_t)rows * pl.nsplit * 8);
         p.ws_cnt = reinterpret_cast<unsigned*>(w);
     }
     switch (dt) {
         case SKV_F32: return launch_cta<float, float>(p, rows, dev, st, false);
         case SKV_F16: return launch_cta<__half, __half>(p, rows, dev, st, false);
         case SKV_BF16: return launch_cta<__nv_bfloat16, __nv_bfloat16>(p, rows, dev, st, false);
-    }
-    return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_combine(const float* o_part, const float* lse_part, int64_t rows, int NS,
-                           int64_t D, void* out, skv_dtype out_dt, float* lse_out,
-                           const float* extra_v, const float* extra_s, bool pdl,
-                           const DeviceInfo& dev, cudaStream_t st) {
-    CtaParams p = {};
-    p.v = o_part;
-    p.s = lse_part;
-    p.vo = out;
-    p.so = lse_out;
-    p.H = 1;
-    p.N = NS;
-    p.chunks = (int)(D * 4 / 16);
-    p.tpr_log2 = p.chunks >= 32 ? 5 : log2_pow2_at_least(p.chunks);
-    p.nsplit = 1;
-    p.per_split = NS;
-    p.extra_v = extra_v;
-    p.extra_s = extra_s;
-    switch (out_dt) {
-        case SKV_F32: return launch_cta<float, float>(p, rows, dev, st, pdl);
-        case SKV_F16: return launch_cta<float, __half>(p, rows, dev, st, pdl);
-        case SKV_BF16: return launch_cta<float, __nv_bfloat16>(p, rows, dev, st, pdl);
     }
     return cudaErrorInvalidValue;
 }

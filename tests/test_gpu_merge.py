@@ -1,0 +1,188 @@
+"""Parity of the merge kernels (merge_state, merge_state_in_place, merge_states)
+with the fp64 oracle, element by element, on the seeded workloads at full size
+and on edge cases; plus the identities the pages fix, checked on the GPU
+(commutativity and the empty-state identity bit-exact).
+
+Pages: "F2 讲解：merge_state，以 2 为底的 LSE 合并" §①, §③, §④, §⑤;
+"FlashAttention 的空行 LSE:FA-2 的 +inf 约定与后来的变化" §2.2."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import assert_states, np64, require_gpu, skv
+from split_kv_lse_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    require_gpu()
+    return skv()
+
+
+def _cuda(d):
+    return {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+def _check_merge_state(lib, d, dtype):
+    g = _cuda(d)
+    v, s = lib.merge_state(g["v_a"], g["s_a"], g["v_b"], g["s_b"])
+    torch.cuda.synchronize()
+    vr, sr = oracle.merge_state(d["v_a"], d["s_a"], d["v_b"], d["s_b"])
+    assert_states(v, s, vr, sr, dtype)
+    return v, s
+
+
+def test_merge_state_tiny(lib):
+    d = W.merge_state_tiny()
+    v, s = _check_merge_state(lib, d, torch.float32)
+    sf, vf = np64(s).reshape(-1), np64(v).reshape(-1, 64)
+    # Row 3 (a empty) equals b exactly, row 7 (b empty) equals a, row 11 is (0, -inf).
+    assert np.array_equal(vf[3], np64(d["v_b"]).reshape(-1, 64)[3])
+    assert sf[3] == np64(d["s_b"]).reshape(-1)[3]
+    assert np.array_equal(vf[7], np64(d["v_a"]).reshape(-1, 64)[7])
+    assert sf[11] == -math.inf and np.all(vf[11] == 0)
+
+
+def test_merge_state_large_fp16(lib):
+    """S=8192, H=32, D=128 fp16 with empty, double-empty and +inf/NaN inputs."""
+    d = W.merge_state_large()
+    assert torch.isinf(d["s_a"]).any() and torch.isnan(d["s_b"]).any()
+    _check_merge_state(lib, d, torch.float16)
+
+
+def test_merge_state_in_place_large(lib):
+    d = W.merge_state_large()
+    g = _cuda(d)
+    v, s = g["v_a"].clone(), g["s_a"].clone()
+    r = lib.merge_state_in_place(v, s, g["v_b"], g["s_b"])
+    assert r[0].data_ptr() == v.data_ptr()
+    torch.cuda.synchronize()
+    vr, sr = oracle.merge_state(d["v_a"], d["s_a"], d["v_b"], d["s_b"])
+    assert_states(v, s, vr, sr, torch.float16)
+    # Same bits as the out-of-place kernel.
+    vo, so = lib.merge_state(g["v_a"], g["s_a"], g["v_b"], g["s_b"])
+    assert torch.equal(vo, v) and torch.equal(so.isnan(), s.isnan())
+    assert torch.equal(torch.nan_to_num(so), torch.nan_to_num(s))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("S,H,D", [(1, 1, 64), (7, 3, 8 * 4), (33, 5, 96), (129, 2, 128),
+                                   (5, 3, 256)])
+def test_merge_state_shapes(lib, dtype, S, H, D):
+    if D * torch.tensor([], dtype=dtype).element_size() > 512:
+        pytest.skip("rows over 512 bytes are unsupported")
+    d = W.merge_state_inputs(S, H, D, dtype, seed=S * 131 + D, empty_p=0.1,
+                             double_empty_p=0.05, poison_p=0.05)
+    _check_merge_state(lib, d, dtype)
+
+
+def test_merge_state_zero_rows_is_noop(lib):
+    v = torch.zeros(0, 4, 64, device=DEV)
+    s = torch.zeros(0, 4, device=DEV)
+    lib.merge_state(v, s, v, s)
+
+
+def test_merge_state_identities_bit_exact(lib):
+    """Commutative (bit-exact) and empty + x = x (bit-exact) on the GPU."""
+    d = _cuda(W.merge_state_inputs(512, 8, 128, torch.float16, seed=3, empty_p=0.1))
+    v1, s1 = lib.merge_state(d["v_a"], d["s_a"], d["v_b"], d["s_b"])
+    v2, s2 = lib.merge_state(d["v_b"], d["s_b"], d["v_a"], d["s_a"])
+    assert torch.equal(v1, v2) and torch.equal(s1, s2)
+    ve = torch.zeros_like(d["v_a"])
+    se = torch.full_like(d["s_a"], -math.inf)
+    v3, s3 = lib.merge_state(d["v_a"], d["s_a"], ve, se)
+    assert torch.equal(v3, d["v_a"]) and torch.equal(s3, d["s_a"])
+    v4, s4 = lib.merge_state(ve, se, ve, se)
+    assert torch.all(v4 == 0) and torch.all(s4 == -math.inf)
+    # +inf / NaN incoming s behave exactly like an empty state.
+    for bad in (math.inf, math.nan):
+        sb = torch.full_like(d["s_a"], bad)
+        v5, s5 = lib.merge_state(d["v_a"], d["s_a"], d["v_b"], sb)
+        assert torch.equal(v5, d["v_a"]) and torch.equal(s5, d["s_a"])
+
+
+def test_merge_state_printed_selftest(lib):
+    """F2 §⑧ 自测 1 on the GPU: s = 10, 10; v = [1,0], [0,1] -> [0.5, 0.5], 11."""
+    va = torch.zeros(1, 1, 4, device=DEV)
+    vb = torch.zeros(1, 1, 4, device=DEV)
+    va[0, 0, 0] = 1
+    vb[0, 0, 1] = 1
+    s = torch.full((1, 1), 10.0, device=DEV)
+    v, so = lib.merge_state(va, s, vb, s)
+    assert v.cpu().tolist() == [[[0.5, 0.5, 0.0, 0.0]]] and so.item() == 11.0
+
+
+def _check_merge_states(lib, d, dtype, workspace=None):
+    g = _cuda(d)
+    v, s = lib.merge_states(g["v"], g["s"], workspace=workspace)
+    torch.cuda.synchronize()
+    vr, sr = oracle.merge_states(d["v"], d["s"])
+    assert_states(v, s, vr, sr, dtype)
+    return v, s
+
+
+def test_merge_states_main(lib):
+    """S=256, N=64, H=32, D=128 fp32, 5% empty states."""
+    _check_merge_states(lib, W.merge_states_main(), torch.float32)
+
+
+def _ws(lib, S, N, H, D):
+    n = lib.merge_states_workspace_size(S, N, H, D)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=DEV), n
+
+
+@pytest.mark.parametrize("N", W.MERGE_STATES_SWEEP_N)
+@pytest.mark.parametrize("use_ws", [False, True])
+def test_merge_states_sweep(lib, N, use_ws):
+    """S=16, H=8, D=128, N in {1, 2, 3, 128, 1024}: one CTA per row, or the
+    two-level split through a workspace (which must be reusable without
+    re-zeroing: its arrival tickets are reset by the last CTA of each row)."""
+    d = W.merge_states_sweep(N)
+    ws = None
+    if use_ws:
+        ws, need = _ws(lib, 16, N, 8, 128)
+    _check_merge_states(lib, d, torch.float32, ws)
+    if use_ws:
+        # A second call on the same workspace gives the same answer, and the
+        # workspace's ticket counters are back to zero.
+        v1, s1 = lib.merge_states(d["v"].to(DEV), d["s"].to(DEV), workspace=ws)
+        v2, s2 = lib.merge_states(d["v"].to(DEV), d["s"].to(DEV), workspace=ws)
+        assert torch.equal(v1, v2) and torch.equal(s1, s2)
+        torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("S,N,H,D", [(3, 1, 2, 64), (5, 7, 3, 128), (1, 300, 1, 128),
+                                     (2, 33, 4, 64), (4097, 2, 1, 64), (9, 5, 7, 96)])
+def test_merge_states_shapes(lib, dtype, S, N, H, D):
+    d = W.merge_states_inputs(S, N, H, D, dtype, seed=S + N * 7 + D, empty_p=0.2)
+    ws, _ = _ws(lib, S, N, H, D)
+    _check_merge_states(lib, d, dtype, ws)
+    _check_merge_states(lib, d, dtype, None)
+
+
+def test_merge_states_all_empty_and_poisoned(lib):
+    S, N, H, D = 6, 5, 3, 64
+    v = torch.randn(S, N, H, D)
+    s = torch.full((S, N, H), -math.inf)
+    s[0, 2, 1] = 3.0
+    s[1, :, 0] = math.inf
+    s[2, :, 2] = math.nan
+    s[3, 1, 1] = math.nan
+    s[3, 4, 1] = 7.5
+    _check_merge_states(lib, {"v": v, "s": s}, torch.float32)
+
+
+def test_merge_states_two_equals_merge_state(lib):
+    d = _cuda(W.merge_state_inputs(300, 4, 128, torch.float32, seed=9, empty_p=0.2))
+    v2, s2 = lib.merge_state(d["v_a"], d["s_a"], d["v_b"], d["s_b"])
+    vn, sn = lib.merge_states(torch.stack([d["v_a"], d["v_b"]], 1).contiguous(),
+                              torch.stack([d["s_a"], d["s_b"]], 1).contiguous())
+    torch.testing.assert_close(vn, v2, rtol=1e-6, atol=1e-7)
+    torch.testing.assert_close(sn, s2, rtol=0, atol=1e-6)
