@@ -131,6 +131,43 @@ skv_status skv_merge_states(const void* v, const float* s,
                             skv_stream_t stream);
 
 /*
+ * Size of the fixed device scratch array used by skv_merge_states_noalloc
+ * (one array per GPU that loads the library, held until the process exits).
+ */
+#define SKV_MERGE_STATES_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/*
+ * skv_merge_states without a workspace argument, for callers that cannot
+ * allocate device memory.  (The pages have no counterpart: this is a
+ * convenience of this library.)  Some callers have no way to call cudaMalloc:
+ * a plugin inside another runtime that owns every allocation and only hands
+ * over its inputs and outputs, or a latency-critical decode loop that must not
+ * risk the device synchronisation an allocation can cause.  This entry point
+ * computes exactly what skv_merge_states computes, with the same arguments
+ * minus the workspace, and allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library call): when the merge runs in two levels its partial
+ * states live in a file-scope device array of
+ * SKV_MERGE_STATES_NOALLOC_SCRATCH_BYTES bytes inside the library.
+ *   - Sizes whose two-level merge would need more scratch than that are
+ *     rejected with SKV_ERR_UNSUPPORTED (nothing is enqueued).  The two-level
+ *     path is only taken for at most SM-count rows, with at most about
+ *     3 * SM-count partial rows of D fp32 values, so on a GPU with up to 300
+ *     SMs (a GB300 has 152) every supported shape fits.
+ *   - The first call on a device looks up the array's device address with
+ *     cudaGetSymbolAddress (with that device current) and caches it; make that
+ *     first call before any stream capture on the device.
+ *   - Every call shares the one array, which keeps the last call's contents;
+ *     each call clears the part it needs (cudaMemsetAsync on `stream`) before
+ *     using it.  Calls that overlap on the GPU (on different streams, or
+ *     concurrently from several host threads) race on the array and must be
+ *     serialised by the caller.
+ */
+skv_status skv_merge_states_noalloc(const void* v, const float* s,
+                                    void* v_out, float* s_out,
+                                    int64_t S, int64_t N, int64_t H, int64_t D,
+                                    skv_dtype dtype, skv_stream_t stream);
+
+/*
  * Page range of one split ([L3] §②), computed on the host with exactly the
  * integer arithmetic the decode kernel uses:
  *   num_pages = ceil(ctx / page), pps = ceil(num_pages / num_splits),

@@ -36,6 +36,8 @@ SIGNATURES = {
     "skv_merge_states_workspace_size": (size_t, [i64, i64, i64, i64]),
     "skv_merge_states": (i32, [c_void_p, c_void_p, c_void_p, c_void_p, i64, i64, i64, i64, i32,
                                c_void_p, size_t, c_void_p]),
+    "skv_merge_states_noalloc": (i32, [c_void_p, c_void_p, c_void_p, c_void_p, i64, i64, i64,
+                                        i64, i32, c_void_p]),
     "skv_split_page_range": (i32, [i32, i32, i32, i32, c_int32_p, c_int32_p]),
     "skv_splitkv_decode_plan": (i32, [i32, c_int32_p, i32, i32, i32, c_int32_p]),
     "skv_splitkv_decode": (i32, [c_void_p, c_void_p, c_void_p, i32, c_void_p, i32, c_void_p,
