@@ -229,6 +229,51 @@ skv_status skv_splitkv_decode(const void* q, const void* k_cache, const void* v_
                               int32_t* ranges_dbg, skv_stream_t stream);
 
 /*
+ * Device workspace, in bytes, that skv_cascade_decode needs for these sizes
+ * (the per-chunk states of the shared-prefix pass).  sm_count > 0 is used as
+ * given; 0 means the current device's SM count (the chunking depends on it).
+ * Returns 0 for invalid sizes.
+ */
+size_t skv_cascade_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                  int32_t prefix_len, int32_t sm_count);
+
+/*
+ * Two-level cascade decode attention ([F2] §⑥): every request b attends to a
+ * shared prefix of prefix_len tokens (pool pages prefix_pages[0 ..
+ * ceil(prefix_len/page))) followed by its own suffix of ctx[b] tokens (pool
+ * pages block_table[b][..]), as one softmax over prefix || suffix.
+ *   1. Shared-prefix pass on the tensor cores (tcgen05): the prefix KV of each
+ *      kv head is read once for all B*G query rows, as dense QK^T and PV
+ *      products; it writes one state per prefix chunk into `workspace`.
+ *   2. The suffixes run through the split-KV decode (as skv_splitkv_decode
+ *      with `num_splits`), writing o_part / lse_part.
+ *   3. One combine pass merges the prefix chunks into the prefix state
+ *      (o_pre [B, Hq, D] fp32, s_pre [B, Hq] base 2, each written if not
+ *      NULL), the splits into the suffix state, and the two with the
+ *      two-state merge, prefix first, into out [B, Hq, D] (`dtype`) and, if
+ *      not NULL, lse_out [B, Hq] (base 2).
+ * Layouts as for skv_splitkv_decode; prefix_pages is a device int32 array.
+ * prefix_len = 0 gives an empty prefix state (o = 0, s = -inf); ctx[b] = 0 an
+ * empty suffix; both empty give out = 0, lse_out = -inf.
+ * workspace: at least skv_cascade_workspace_size(B, Hq, Hkv, D, prefix_len, 0)
+ *   bytes, 16-byte aligned; no initial contents are needed.
+ * Supported: dtype SKV_F16, D = 128, page = 16, G = Hq/Hkv in {1, 2, 4, 8},
+ *   1 <= num_splits <= 256.  Device-side checks as for skv_splitkv_decode
+ *   (prefix page ids included).
+ */
+skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_cache,
+                              int32_t num_pool_pages,
+                              const int32_t* prefix_pages, int32_t prefix_len,
+                              const int32_t* block_table, int32_t max_pages,
+                              const int32_t* ctx,
+                              int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page,
+                              int32_t num_splits, float sm_scale, skv_dtype dtype,
+                              float* o_pre, float* s_pre,
+                              float* o_part, float* lse_part,
+                              void* out, float* lse_out,
+                              void* workspace, size_t workspace_bytes, skv_stream_t stream);
+
+/*
  * Reads and clears the error word of the current CUDA device: *code is 0 or
  * the skv_status of the first device-side error since the last call, *detail
  * an index that identifies it (0 if none).  Synchronises the device.

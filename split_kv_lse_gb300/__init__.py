@@ -22,7 +22,8 @@ from ._ffi import SkvError
 __all__ = [
     "SkvError", "merge_state", "merge_state_in_place", "merge_states",
     "merge_states_workspace_size", "split_page_range", "splitkv_decode_plan",
-    "splitkv_decode", "get_device_error", "abi_version", "library_path",
+    "splitkv_decode", "cascade_workspace_size", "cascade_decode", "get_device_error",
+    "abi_version", "library_path",
 ]
 
 _DT = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
@@ -173,6 +174,58 @@ def splitkv_decode(q, k_cache, v_cache, block_table, ctx, num_splits: int, sm_sc
         _DT[q.dtype], o_part.data_ptr(), lse_part.data_ptr(), _ptr(out), _ptr(lse_out),
         _ptr(ranges_dbg), _stream(q)))
     return out, lse_out, o_part, lse_part
+
+
+def cascade_workspace_size(B: int, Hq: int, Hkv: int, D: int, prefix_len: int,
+                           sm_count: int = 0) -> int:
+    return int(_ffi.lib().skv_cascade_workspace_size(B, Hq, Hkv, D, prefix_len, sm_count))
+
+
+def cascade_decode(q, k_cache, v_cache, prefix_pages, prefix_len: int, block_table, ctx,
+                   num_splits: int, sm_scale: float, out=None, lse_out=None, o_pre=None,
+                   s_pre=None, o_part=None, lse_part=None, workspace=None):
+    """Two-level cascade decode: shared prefix (tensor cores) + per-request suffix.
+
+    Returns (out, lse_out, o_pre, s_pre, o_part, lse_part).  prefix_pages is a
+    device int32 tensor of the prefix's pool pages.
+    """
+    B, Hq, D = q.shape
+    P, Hkv, page, D2 = k_cache.shape
+    _need(q, "q")
+    _need(k_cache, "k_cache", q.dtype)
+    _need(v_cache, "v_cache", q.dtype, tuple(k_cache.shape))
+    _need(block_table, "block_table", torch.int32)
+    _need(ctx, "ctx", torch.int32, (B,))
+    _need(prefix_pages, "prefix_pages", torch.int32)
+    if D2 != D or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("inconsistent cascade shapes")
+    dev = q.device
+    f32 = torch.float32
+    out = torch.empty((B, Hq, D), dtype=q.dtype, device=dev) if out is None else out
+    lse_out = torch.empty((B, Hq), dtype=f32, device=dev) if lse_out is None else lse_out
+    o_pre = torch.empty((B, Hq, D), dtype=f32, device=dev) if o_pre is None else o_pre
+    s_pre = torch.empty((B, Hq), dtype=f32, device=dev) if s_pre is None else s_pre
+    if o_part is None:
+        o_part = torch.empty((B, Hq, num_splits, D), dtype=f32, device=dev)
+    if lse_part is None:
+        lse_part = torch.empty((B, Hq, num_splits), dtype=f32, device=dev)
+    for t, n, shp in ((out, "out", (B, Hq, D)), (lse_out, "lse_out", (B, Hq)),
+                      (o_pre, "o_pre", (B, Hq, D)), (s_pre, "s_pre", (B, Hq)),
+                      (o_part, "o_part", (B, Hq, num_splits, D)),
+                      (lse_part, "lse_part", (B, Hq, num_splits))):
+        _need(t, n, None, shp)
+    need = cascade_workspace_size(B, Hq, Hkv, D, prefix_len)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _ffi.check("skv_cascade_decode", _ffi.lib().skv_cascade_decode(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), P, prefix_pages.data_ptr(),
+        int(prefix_len), block_table.data_ptr(), block_table.shape[1], ctx.data_ptr(), B, Hq,
+        Hkv, D, page, num_splits, float(sm_scale), _DT[q.dtype], o_pre.data_ptr(),
+        s_pre.data_ptr(), o_part.data_ptr(), lse_part.data_ptr(), out.data_ptr(),
+        lse_out.data_ptr(), workspace.data_ptr(), ws_bytes, _stream(q)))
+    return out, lse_out, o_pre, s_pre, o_part, lse_part
 
 
 def get_device_error():

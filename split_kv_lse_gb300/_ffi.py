@@ -43,6 +43,11 @@ SIGNATURES = {
     "skv_splitkv_decode": (i32, [c_void_p, c_void_p, c_void_p, i32, c_void_p, i32, c_void_p,
                                  i32, i32, i32, i32, i32, i32, f32, i32, c_void_p, c_void_p,
                                  c_void_p, c_void_p, c_void_p, c_void_p]),
+    "skv_cascade_workspace_size": (size_t, [i32, i32, i32, i32, i32, i32]),
+    "skv_cascade_decode": (i32, [c_void_p, c_void_p, c_void_p, i32, c_void_p, i32, c_void_p, i32,
+                                 c_void_p, i32, i32, i32, i32, i32, i32, f32, i32, c_void_p,
+                                 c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                 size_t, c_void_p]),
     "skv_get_device_error": (i32, [c_int32_p, c_int32_p]),
 }
 

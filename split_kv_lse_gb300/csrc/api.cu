@@ -229,10 +229,139 @@ skv_status skv_splitkv_decode(const void* q, const void* k_cache, const void* v_
     cudaError_t e = launch_splitkv_decode(a, *dev, cs);
     if (e != cudaSuccess) return SKV_ERR_CUDA;
     if (out != nullptr) {
-        e = launch_combine(o_part, lse_part, (int64_t)B * Hq, num_splits, D, out, dtype, lse_out,
-                           nullptr, nullptr, true, *dev, cs);
+        CombineArgs c = {};
+        c.o_part = o_part;
+        c.lse_part = lse_part;
+        c.rows = (int64_t)B * Hq;
+        c.NS = num_splits;
+        c.D = D;
+        c.out = out;
+        c.out_dt = dtype;
+        c.lse_out = lse_out;
+        e = launch_combine(c, true, *dev, cs);
         if (e != cudaSuccess) return SKV_ERR_CUDA;
     }
+    return SKV_OK;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static skv_status cascade_chunks(int32_t B, int32_t Hq, int32_t Hkv, int32_t prefix_len,
+                                 int32_t sm_count, int* mtiles, int* bpc, int* nchunks) {
+    if (sm_count == 0) {
+        const DeviceInfo* dev = nullptr;
+        skv_status st = current_device(&dev);
+        if (st != SKV_OK) return st;
+        sm_count = dev->sm_count;
+    }
+    cascade_prefix_geometry(B, Hq / Hkv, Hkv, prefix_len, sm_count, mtiles, bpc, nchunks);
+    return SKV_OK;
+}
+
+size_t skv_cascade_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                  int32_t prefix_len, int32_t sm_count) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 1 || prefix_len < 0 || sm_count < 0)
+        return 0;
+    int mt = 0, bpc = 0, nc = 0;
+    if (cascade_chunks(B, Hq, Hkv, prefix_len, sm_count, &mt, &bpc, &nc) != SKV_OK) return 0;
+    const size_t rows = (size_t)B * Hq;
+    return align256(rows * nc * D * 4) + align256(rows * nc * 4) + 256;
+}
+
+skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_cache,
+                              int32_t num_pool_pages, const int32_t* prefix_pages,
+                              int32_t prefix_len, const int32_t* block_table, int32_t max_pages,
+                              const int32_t* ctx, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                              int32_t page, int32_t num_splits, float sm_scale, skv_dtype dtype,
+                              float* o_pre, float* s_pre, float* o_part, float* lse_part,
+                              void* out, float* lse_out, void* workspace, size_t workspace_bytes,
+                              skv_stream_t stream) {
+    if (B < 0 || Hq < 1 || Hkv < 1 || D < 1 || page < 1 || num_splits < 1 || max_pages < 1 ||
+        num_pool_pages < 1 || prefix_len < 0 || !valid_dtype(dtype))
+        return SKV_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return SKV_ERR_INVALID_ARG;
+    const int G = Hq / Hkv;
+    if (dtype != SKV_F16 || D != 128 || page != 16 || !(G == 1 || G == 2 || G == 4 || G == 8) ||
+        num_splits > 256 || B > 65535 || Hkv > 65535)
+        return SKV_ERR_UNSUPPORTED;
+    if ((int64_t)max_pages * page > INT32_MAX ||
+        (int64_t)num_pool_pages * Hkv * page > INT32_MAX - page)
+        return SKV_ERR_UNSUPPORTED;
+    if (B == 0) return SKV_OK;
+    if (!q || !k_cache || !v_cache || !block_table || !ctx || !o_part || !lse_part || !out ||
+        !workspace)
+        return SKV_ERR_INVALID_ARG;
+    if (prefix_len > 0 && !prefix_pages) return SKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o_part) ||
+        !aligned16(out) || !aligned16(workspace) || !aligned4(lse_part) || !aligned4(block_table) ||
+        !aligned4(ctx) || (prefix_pages && !aligned4(prefix_pages)))
+        return SKV_ERR_INVALID_ARG;
+    if ((o_pre && !aligned16(o_pre)) || (s_pre && !aligned4(s_pre)) ||
+        (lse_out && !aligned4(lse_out)))
+        return SKV_ERR_INVALID_ARG;
+    const DeviceInfo* dev = nullptr;
+    skv_status st = current_device(&dev);
+    if (st != SKV_OK) return st;
+    int mt = 0, bpc = 0, nc = 0;
+    cascade_prefix_geometry(B, G, Hkv, prefix_len, dev->sm_count, &mt, &bpc, &nc);
+    const size_t rows = (size_t)B * Hq;
+    const size_t need = align256(rows * nc * D * 4) + align256(rows * nc * 4) + 256;
+    if (workspace_bytes < need) return SKV_ERR_INVALID_ARG;
+    float* pre_part = static_cast<float*>(workspace);
+    float* pre_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * nc * D * 4));
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    // 1. Shared prefix on the tensor cores: one state per prefix chunk.
+    if (nc > 0) {
+        CascadeArgs ca;
+        ca.q = q;
+        ca.k_cache = k_cache;
+        ca.v_cache = v_cache;
+        ca.num_pool_pages = num_pool_pages;
+        ca.prefix_pages = prefix_pages;
+        ca.prefix_len = prefix_len;
+        ca.B = B;
+        ca.Hq = Hq;
+        ca.Hkv = Hkv;
+        ca.sm_scale = sm_scale;
+        if (launch_cascade_prefix(ca, *dev, pre_part, pre_lse, nc, bpc, mt, cs) != cudaSuccess)
+            return SKV_ERR_CUDA;
+    }
+    // 2. Each request's own suffix through the split-KV decode.
+    DecodeArgs a;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.num_pool_pages = num_pool_pages;
+    a.block_table = block_table;
+    a.max_pages = max_pages;
+    a.ctx = ctx;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.page = page;
+    a.num_splits = num_splits;
+    a.sm_scale = sm_scale;
+    a.o_part = o_part;
+    a.lse_part = lse_part;
+    a.ranges_dbg = nullptr;
+    if (launch_splitkv_decode(a, *dev, cs) != cudaSuccess) return SKV_ERR_CUDA;
+    // 3. Prefix chunks -> prefix state; merge_state(prefix, suffix) -> out.
+    CombineArgs c = {};
+    c.o_part = o_part;
+    c.lse_part = lse_part;
+    c.rows = (int64_t)rows;
+    c.NS = num_splits;
+    c.D = D;
+    c.out = out;
+    c.out_dt = dtype;
+    c.lse_out = lse_out;
+    c.pre_part = pre_part;
+    c.pre_lse = pre_lse;
+    c.C = nc;
+    c.o_pre = o_pre;
+    c.s_pre = s_pre;
+    if (launch_combine(c, true, *dev, cs) != cudaSuccess) return SKV_ERR_CUDA;
     return SKV_OK;
 }
 

@@ -1,0 +1,362 @@
+// cascade.cu -- the shared-prefix pass of two-level cascade decode attention
+// on the 5th-generation tensor cores (tcgen05) of sm_103a.
+//
+// Page: "F2 讲解：merge_state，以 2 为底的 LSE 合并", §⑥: when many requests
+// share one prefix, the prefix KV is read once instead of once per request,
+// and the queries that share it form a dense matrix product that can run on
+// tensor cores; the prefix state is then merged with each request's own
+// suffix state.  The suffix runs through the split-KV decode
+// ("L3 讲解：split-KV decode 与 LSE 合并") and the merges through the combine
+// kernel of decode.cu.
+//
+// One CTA per (kv head, 128-row M tile, chunk of the prefix).  The M tile's
+// rows are (request, group head) pairs -- row = r_local * G + g -- so one KV
+// tile serves 128 query rows.  Per 128-key block:
+//   S = Q K^T        tcgen05.mma kind::f16, Q [128 x 128] and the K block
+//                    [128 keys x 128] K-major in shared memory, S fp32 in TMEM
+//   softmax          4 warps, thread i <-> row i <-> TMEM lane i: base-2
+//                    online max/sum ([F2] §② exp2 trick), P written to shared
+//                    memory as fp16 in the swizzled K-major operand layout
+//   O_blk = P V      tcgen05.mma with V as an MN-major operand, O_blk in TMEM
+//   o = alpha*o + O_blk   accumulated in registers (the rescale stays exact)
+// Q, K and V tiles arrive by TMA tensor loads with the 128-byte swizzle (a
+// page is one 16 x 64 box per half of the head dim); two K and two V blocks
+// are in flight.  Each chunk writes its normalised state (o, s base 2) for
+// the combine kernel, which merges the chunks into the prefix state.
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+#include "tma.h"
+
+namespace skv {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kPage = 16;
+constexpr int kBlockKeys = 128;                      // keys per block (N of QK^T, K of PV)
+constexpr int kPagesPerBlock = kBlockKeys / kPage;   // 8
+constexpr int kM = 128;                              // query rows per CTA
+constexpr int kHalf = 128 * 128;                     // one [128 rows x 64] fp16 swizzled half tile
+constexpr int kTile = 2 * kHalf;                     // one [128 x 128] fp16 operand tile (32 KB)
+constexpr int kStages = 2;                           // K blocks and V blocks in flight
+constexpr int kThreads = 128;
+constexpr uint32_t kTmemCols = 256;                  // S: columns [0, 128), O_blk: [128, 256)
+
+struct PrefixParams {
+    const int32_t* prefix_pages;
+    int32_t prefix_len;
+    int32_t pool_rows;        // rows of the K/V tensor maps: num_pool_pages * Hkv * page
+    int32_t num_pool_pages;
+    int32_t B, Hq, Hkv, G;
+    int32_t blocks_per_chunk, nchunks;
+    float scale_log2;
+    float* pre_part;          // [B*Hq, nchunks, D] split-normalised chunk states
+    float* pre_lse;           // [B*Hq, nchunks] base 2
+    unsigned long long* err;
+};
+
+constexpr size_t kSmemQ = 0;
+constexpr size_t kSmemK = kSmemQ + kTile;
+constexpr size_t kSmemV = kSmemK + (size_t)kStages * kTile;
+constexpr size_t kSmemP = kSmemV + (size_t)kStages * kTile;
+constexpr size_t kSmemBars = kSmemP + kTile;
+constexpr int kNumBars = 2 + 2 * kStages;            // q_full, mma_done, k_full[], v_full[]
+constexpr size_t kSmemTmemSlot = kSmemBars + kNumBars * sizeof(uint64_t);
+constexpr size_t kSmemIds = kSmemTmemSlot + 16;
+
+size_t prefix_smem_bytes(int blocks_per_chunk) {
+    return 1024 + kSmemIds + (size_t)blocks_per_chunk * kPagesPerBlock * sizeof(int);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                      const __grid_constant__ CUtensorMap tv, const PrefixParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint8_t* Qs = sm + kSmemQ;
+    uint8_t* Ks = sm + kSmemK;
+    uint8_t* Vs = sm + kSmemV;
+    uint8_t* Ps = sm + kSmemP;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSmemBars);
+    uint64_t* q_full = bars + 0;
+    uint64_t* mma_done = bars + 1;
+    uint64_t* k_full = bars + 2;
+    uint64_t* v_full = bars + 2 + kStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kSmemTmemSlot);
+    int* ids = reinterpret_cast<int*>(sm + kSmemIds);
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int chunk = blockIdx.x, mtile = blockIdx.y, hkv = blockIdx.z;
+    const int nblocks_total = (p.prefix_len + kBlockKeys - 1) / kBlockKeys;
+    const int blk0 = chunk * p.blocks_per_chunk;
+    const int nb = min(p.blocks_per_chunk, nblocks_total - blk0);  // >= 1 (host sizing)
+    const int npages_prefix = (p.prefix_len + kPage - 1) / kPage;
+
+    // Page ids of this chunk; pages past the prefix are -1 (loaded as zeros).
+    for (int i = tid; i < nb * kPagesPerBlock; i += kThreads) {
+        const int gp = blk0 * kPagesPerBlock + i;
+        int pid = -1;
+        if (gp < npages_prefix) {
+            pid = p.prefix_pages[gp];
+            if ((unsigned)pid >= (unsigned)p.num_pool_pages) {
+                record_error(p.err, SKV_ERR_INVALID_ARG, 2 << 20 | gp);
+                pid = 0;
+            }
+        }
+        ids[i] = pid;
+    }
+    if (tid == 0) {
+        for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+    }
+    if (warp == 0) tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tS = tmem;          // columns [0, 128)
+    const uint32_t tO = tmem + 128;    // columns [128, 256)
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+
+    const uint64_t pol = policy_evict_first();
+    // One thread: copy block j (8 pages x 2 halves) of K or V into a stage.
+    auto load_block = [&](int j, int stage, bool is_v) {
+        uint64_t* bar = is_v ? &v_full[stage] : &k_full[stage];
+        uint8_t* dst = (is_v ? Vs : Ks) + stage * kTile;
+        const CUtensorMap* map = is_v ? &tv : &tk;
+        mbar_arrive_expect_tx(bar, kTile);
+#pragma unroll 1
+        for (int pg = 0; pg < kPagesPerBlock; ++pg) {
+            const int pid = ids[j * kPagesPerBlock + pg];
+            // A page past the prefix is read from the row just past the
+            // tensor: the TMA fills the whole box with zeros.
+            const int row = pid >= 0 ? (pid * p.Hkv + hkv) * kPage : p.pool_rows;
+            tma_load_2d(dst + pg * (kPage * 128), map, 0, row, bar, pol);
+            tma_load_2d(dst + kHalf + pg * (kPage * 128), map, 64, row, bar, pol);
+        }
+    };
+    if (tid == 0) {
+        mbar_arrive_expect_tx(q_full, kTile);
+        const int z = mtile * (kM / p.G);
+        tma_load_3d(Qs, &tq, 0, hkv * p.G, z, q_full);
+        tma_load_3d(Qs + kHalf, &tq, 64, hkv * p.G, z, q_full);
+        for (int s = 0; s < kStages && s < nb; ++s) {
+            load_block(s, s, false);
+            load_block(s, s, true);
+        }
+    }
+
+    constexpr uint32_t idS = tc::idesc_f16_f32(kM, kBlockKeys, false);
+    constexpr uint32_t idPV = tc::idesc_f16_f32(kM, kD, true);
+    float o[kD];
+#pragma unroll
+    for (int i = 0; i < kD; ++i) o[i] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
+    uint32_t mma_phase = 0;
+    bool alive = true;
+
+#pragma unroll 1
+    for (int j = 0; j < nb && alive; ++j) {
+        const int st = j % kStages;
+        const uint32_t par = (uint32_t)((j / kStages) & 1);
+        // ---- S = Q K^T
+        bool ok = true;  // meaningful on the issuing thread
+        if (tid == 0) {
+            if (j == 0) ok = mbar_wait(q_full, 0, p.err, 10);
+            ok = ok && mbar_wait(&k_full[st], par, p.err, 11);
+            if (ok) {
+                tc::fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < kD / 16; ++k) {
+                    const int h = k >> 2, kk = k & 3;
+                    const uint64_t ad = tc::sdesc_sw128(smem_addr(Qs + h * kHalf) + kk * 32, 16, 1024);
+                    const uint64_t bd = tc::sdesc_sw128(smem_addr(Ks + st * kTile + h * kHalf) + kk * 32, 16, 1024);
+                    tc::mma_f16_ss(tS, ad, bd, idS, k > 0);
+                }
+            }
+            tc::mma_commit(mma_done);  // also arrives when nothing was issued
+        }
+        alive = mbar_wait(mma_done, mma_phase, p.err, 12) && ok;
+        mma_phase ^= 1;
+        alive = __syncthreads_and(alive);
+        if (!alive) break;
+        tc::fence_after_sync();
+        if (tid == 0 && j + kStages < nb) load_block(j + kStages, st, false);  // K stage is free
+
+        // ---- softmax of row `tid` over this block (log2 units)
+        const int key0 = (blk0 + j) * kBlockKeys;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float s[32];
+            tc::tmem_ld32(tS + lane_base + 32 * c, s);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (key0 + 32 * c + i < p.prefix_len) mx = fmaxf(mx, s[i] * p.scale_log2);
+        }
+        const float m_new = fmaxf(m_run, mx);  // finite: the block's first key is valid
+        const float alpha = exp2f(m_run - m_new);
+        float psum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float s[32];
+            tc::tmem_ld32(tS + lane_base + 32 * c, s);
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys = one 16-byte chunk of the P row
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i0 = q8 * 8 + 2 * e;
+                    const bool v0 = key0 + 32 * c + i0 < p.prefix_len;
+                    const bool v1 = key0 + 32 * c + i0 + 1 < p.prefix_len;
+                    const float p0 = v0 ? exp2f(s[i0] * p.scale_log2 - m_new) : 0.f;
+                    const float p1 = v1 ? exp2f(s[i0 + 1] * p.scale_log2 - m_new) : 0.f;
+                    psum += p0 + p1;
+                    const __half2 h2 = __floats2half2_rn(p0, p1);
+                    pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                }
+                const int chunk16 = c * 4 + q8;            // logical 16-byte chunk 0..15
+                const int half = chunk16 >> 3;
+                const int pos = (chunk16 & 7) ^ (tid & 7);  // 128-byte swizzle
+                *reinterpret_cast<uint4*>(Ps + half * kHalf + tid * 128 + pos * 16) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+        }
+        l_run = fmaf(l_run, alpha, psum);
+        m_run = m_new;
+        tc::fence_before_sync();
+        tc::fence_proxy_async_smem();
+        __syncthreads();
+
+        // ---- O_blk = P V
+        ok = true;
+        if (tid == 0) {
+            tc::fence_after_sync();
+            ok = mbar_wait(&v_full[st], par, p.err, 13);
+            const int tail = p.prefix_len % kPage;
+            const int last_page = npages_prefix - 1 - (blk0 + j) * kPagesPerBlock;
+            if (ok && tail != 0 && last_page >= 0 && last_page < kPagesPerBlock) {
+                // The prefix ends inside this block's page `last_page`: its
+                // rows past the end hold whatever the pool has there.  P is 0
+                // for them, but 0 times a non-finite value is not 0, so the
+                // rows are zeroed (whole 128-byte rows: the swizzle only
+                // permutes chunks inside a row).
+                for (int t = tail; t < kPage; ++t)
+                    for (int h = 0; h < 2; ++h) {
+                        uint4* row = reinterpret_cast<uint4*>(Vs + st * kTile + h * kHalf +
+                                                              (last_page * kPage + t) * 128);
+                        for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
+                    }
+                tc::fence_proxy_async_smem();
+            }
+            if (ok) {
+#pragma unroll
+                for (int k = 0; k < kBlockKeys / 16; ++k) {
+                    const int h = k >> 2, kk = k & 3;
+                    const uint64_t ad = tc::sdesc_sw128(smem_addr(Ps + h * kHalf) + kk * 32, 16, 1024);
+                    const uint64_t bd = tc::sdesc_sw128(smem_addr(Vs + st * kTile) + k * 2048, kHalf, 1024);
+                    tc::mma_f16_ss(tO, ad, bd, idPV, k > 0);
+                }
+            }
+            tc::mma_commit(mma_done);
+        }
+        alive = mbar_wait(mma_done, mma_phase, p.err, 14) && ok;
+        mma_phase ^= 1;
+        alive = __syncthreads_and(alive);
+        if (!alive) break;
+        tc::fence_after_sync();
+        if (tid == 0 && j + kStages < nb) load_block(j + kStages, st, true);  // V stage is free
+
+        // ---- o = alpha * o + O_blk
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float ob[32];
+            tc::tmem_ld32(tO + lane_base + 32 * c, ob);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[32 * c + i] = fmaf(o[32 * c + i], alpha, ob[i]);
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+    }
+
+    // ---- this chunk's state for row `tid`
+    if (alive) {
+        const int rows_per_req = p.G;
+        const int r = mtile * (kM / rows_per_req) + tid / rows_per_req;
+        const int g = tid % rows_per_req;
+        if (r < p.B) {
+            const int64_t row = (int64_t)r * p.Hq + hkv * p.G + g;
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            float* dst = p.pre_part + (row * p.nchunks + chunk) * kD;
+#pragma unroll
+            for (int i = 0; i < kD; i += 4)
+                *reinterpret_cast<float4*>(dst + i) =
+                    make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+            p.pre_lse[row * p.nchunks + chunk] = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::tmem_free(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+void cascade_prefix_geometry(int B, int G, int Hkv, int prefix_len, int sm_count, int* mtiles,
+                             int* blocks_per_chunk, int* nchunks) {
+    const int nblocks = (prefix_len + kBlockKeys - 1) / kBlockKeys;
+    const int mt = (B * G + kM - 1) / kM;
+    // About one CTA per SM: chunks = SMs / (Hkv * M tiles), at least one block each.
+    int want = sm_count / (Hkv * mt > 0 ? Hkv * mt : 1);
+    if (want < 1) want = 1;
+    if (want > nblocks) want = nblocks;
+    int bpc = nblocks > 0 ? (nblocks + want - 1) / want : 1;
+    *mtiles = mt;
+    *blocks_per_chunk = bpc;
+    *nchunks = nblocks > 0 ? (nblocks + bpc - 1) / bpc : 0;
+}
+
+cudaError_t launch_cascade_prefix(const CascadeArgs& a, const DeviceInfo& dev, float* pre_part,
+                                  float* pre_lse, int nchunks, int blocks_per_chunk, int mtiles,
+                                  cudaStream_t st) {
+    const int G = a.Hq / a.Hkv;
+    CUtensorMap tq, tk, tv;
+    cudaError_t e = make_tmap_3d_16bit(&tq, a.q, kD, a.Hq, a.B, (uint64_t)kD * 2,
+                                       (uint64_t)a.Hq * kD * 2, 64, G, kM / G, true);
+    if (e != cudaSuccess) return e;
+    const uint64_t rows = (uint64_t)a.num_pool_pages * a.Hkv * kPage;
+    if ((e = make_tmap_2d_16bit(&tk, a.k_cache, rows, kD, kD * 2, 64, kPage, true, false)) != cudaSuccess)
+        return e;
+    if ((e = make_tmap_2d_16bit(&tv, a.v_cache, rows, kD, kD * 2, 64, kPage, true, false)) != cudaSuccess)
+        return e;
+    PrefixParams p;
+    p.prefix_pages = a.prefix_pages;
+    p.prefix_len = a.prefix_len;
+    p.pool_rows = (int32_t)rows;
+    p.num_pool_pages = a.num_pool_pages;
+    p.B = a.B;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.G = G;
+    p.blocks_per_chunk = blocks_per_chunk;
+    p.nchunks = nchunks;
+    p.scale_log2 = a.sm_scale * 1.4426950408889634f;
+    p.pre_part = pre_part;
+    p.pre_lse = pre_lse;
+    p.err = dev.err;
+    const size_t smem = prefix_smem_bytes(blocks_per_chunk);
+    if (smem > dev.max_smem_optin) return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(cascade_prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    cascade_prefix_kernel<<<dim3(nchunks, mtiles, a.Hkv), kThreads, smem, st>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace skv

@@ -418,12 +418,14 @@ cudaError_t launch_g(const CUtensorMap& tk, const DecodeParams& p, int B, int Hk
 }
 
 // ---------------------------------------------------------------- combine (pass 2)
-// [L3] §③ merge of the split states (base 2), then, for the cascade, a
-// two-state merge with a prefix state ([F2] §⑥).  One CTA per (b, hq) row,
-// 4 warps: warp w takes splits w, w + 4, ...; lane l owns dims [4l, 4l + 4).
-// A warp requests the lse and v chunk of up to kCombBatch splits at once
-// (one L2 round trip for NS <= 4 * kCombBatch), keeps an online (m, W, acc)
-// across batches, and the 4 warp states meet in shared memory.
+// [L3] §③ merge of the split states (base 2).  For the cascade ([F2] §⑥) the
+// prefix-chunk states are merged first into the prefix state, which is then
+// merged with the merged split state by the two-state formula (prefix first).
+// One CTA per (b, hq) row, 4 warps: warp w takes states w, w + 4, ...; lane l
+// owns dims [4l, 4l + 4).  A warp requests the lse and v chunk of up to
+// kCombBatch states at once (one L2 round trip for N <= 4 * kCombBatch),
+// keeps an online (m, W, acc) across batches, and the 4 warp states meet in
+// shared memory.
 constexpr int kCombWarps = 4;
 constexpr int kCombBatch = 16;
 
@@ -432,98 +434,129 @@ struct CombineParams {
     const float* lse_part; // [rows, NS]
     void* out;             // [rows, D] Tout
     float* lse_out;        // [rows] or nullptr
-    const float* extra_v;  // [rows, D] or nullptr
-    const float* extra_s;  // [rows]
-    int NS, D;
+    const float* pre_part; // [rows, C, D] prefix-chunk states or nullptr
+    const float* pre_lse;  // [rows, C]
+    float* o_pre;          // [rows, D] merged prefix state or nullptr
+    float* s_pre;          // [rows]
+    int NS, C, D;
 };
 
-template <typename Tout>
-__global__ void __launch_bounds__(kCombWarps * 32)
-combine_kernel(const CombineParams p) {
-    pdl_wait_primary();  // the split states are written by the preceding grid
-    __shared__ float wm[kCombWarps], wW[kCombWarps];
-    __shared__ __align__(16) float wacc[kCombWarps][kD];
-    __shared__ __align__(16) float fin[kD];
-    const int64_t row = blockIdx.x;
+struct CombSmem {
+    float wm[kCombWarps], wW[kCombWarps];
+    __align__(16) float wacc[kCombWarps][kD];
+};
+
+// Merge the N states of `row` in (o [rows, N, D], lse [rows, N]); every
+// thread with 4*lane < D receives its 4 output dims in v and the merged s.
+SKV_DEVINL void merge_row(const float* o, const float* lse, int N, int D, int64_t row,
+                          CombSmem& sm, float (&v)[4], float& s_out) {
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool has = 4 * lane < p.D;
+    const bool has = 4 * lane < D;
     float m = -INFINITY, W = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int n0 = w; n0 < p.NS; n0 += kCombWarps * kCombBatch) {
-        float lse[kCombBatch];
-        float4 v[kCombBatch];
+    for (int n0 = w; n0 < N; n0 += kCombWarps * kCombBatch) {
+        float l[kCombBatch];
+        float4 x[kCombBatch];
 #pragma unroll
         for (int k = 0; k < kCombBatch; ++k) {
             const int n = n0 + k * kCombWarps;
-            lse[k] = -INFINITY;
-            v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (n < p.NS) {
-                lse[k] = sanitize_lse(ld_cg_f32(p.lse_part + row * p.NS + n));
+            l[k] = -INFINITY;
+            x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (n < N) {
+                l[k] = sanitize_lse(ld_cg_f32(lse + row * N + n));
                 if (has) {
-                    const uint4 r = ld_cg(p.o_part + (row * p.NS + n) * p.D + 4 * lane);
-                    v[k] = make_float4(__uint_as_float(r.x), __uint_as_float(r.y),
+                    const uint4 r = ld_cg(o + (row * N + n) * D + 4 * lane);
+                    x[k] = make_float4(__uint_as_float(r.x), __uint_as_float(r.y),
                                        __uint_as_float(r.z), __uint_as_float(r.w));
                 }
             }
         }
         float mb = m;
 #pragma unroll
-        for (int k = 0; k < kCombBatch; ++k) mb = fmaxf(mb, lse[k]);
+        for (int k = 0; k < kCombBatch; ++k) mb = fmaxf(mb, l[k]);
         const float sc = merge_weight(m, mb);  // rescale of the running state
         W *= sc;
         acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
 #pragma unroll
         for (int k = 0; k < kCombBatch; ++k) {
-            const float wk = merge_weight(lse[k], mb);
-            if (wk > 0.f) {
+            const float wk = merge_weight(l[k], mb);
+            if (wk > 0.f) {  // a zero-weight state is not read into the result
                 W += wk;
-                acc.x = fmaf(wk, v[k].x, acc.x); acc.y = fmaf(wk, v[k].y, acc.y);
-                acc.z = fmaf(wk, v[k].z, acc.z); acc.w = fmaf(wk, v[k].w, acc.w);
+                acc.x = fmaf(wk, x[k].x, acc.x); acc.y = fmaf(wk, x[k].y, acc.y);
+                acc.z = fmaf(wk, x[k].z, acc.z); acc.w = fmaf(wk, x[k].w, acc.w);
             }
         }
         m = mb;
     }
+    __syncthreads();  // the shared buffers may still be read from a previous merge
     if (lane == 0) {
-        wm[w] = m;
-        wW[w] = W;
+        sm.wm[w] = m;
+        sm.wW[w] = W;
     }
-    if (has) *reinterpret_cast<float4*>(&wacc[w][4 * lane]) = acc;
+    if (has) *reinterpret_cast<float4*>(&sm.wacc[w][4 * lane]) = acc;
     __syncthreads();
-    if (w == 0 && has) {
-        float M = wm[0];
+    float M = sm.wm[0];
 #pragma unroll
-        for (int i = 1; i < kCombWarps; ++i) M = fmaxf(M, wm[i]);
-        float WW = 0.f;
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 1; i < kCombWarps; ++i) M = fmaxf(M, sm.wm[i]);
+    float WW = 0.f;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < kCombWarps; ++i) {
-            const float sc = merge_weight(wm[i], M);
-            WW = fmaf(sc, wW[i], WW);
-            const float4 t = *reinterpret_cast<const float4*>(&wacc[i][4 * lane]);
+    for (int i = 0; i < kCombWarps; ++i) {
+        const float sc = merge_weight(sm.wm[i], M);
+        WW = fmaf(sc, sm.wW[i], WW);
+        if (has) {
+            const float4 t = *reinterpret_cast<const float4*>(&sm.wacc[i][4 * lane]);
             a.x = fmaf(sc, t.x, a.x); a.y = fmaf(sc, t.y, a.y);
             a.z = fmaf(sc, t.z, a.z); a.w = fmaf(sc, t.w, a.w);
         }
-        const float inv = WW > 0.f ? 1.f / WW : 0.f;
-        float vd[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
-        float sd = M + log2f(WW);  // -inf when every split is empty
-        if (p.extra_v != nullptr) {
-            // Cascade: prefix state first, merged split state second.
-            const float se = sanitize_lse(p.extra_s[row]), sb = sanitize_lse(sd);
-            const float mm = fmaxf(se, sb);
-            const float we = merge_weight(se, mm), wb = merge_weight(sb, mm);
-            const float ws = __fadd_rn(we, wb);
-            const float iv = ws > 0.f ? 1.f / ws : 0.f;
-            const float4 xe = *reinterpret_cast<const float4*>(p.extra_v + row * p.D + 4 * lane);
-            const float xs[4] = {xe.x, xe.y, xe.z, xe.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float te = we > 0.f ? __fmul_rn(we, xs[i]) : 0.f;
-                const float tb = wb > 0.f ? __fmul_rn(wb, vd[i]) : 0.f;
-                vd[i] = __fmul_rn(__fadd_rn(te, tb), iv);
-            }
-            sd = mm + log2f(ws);
+    }
+    const float inv = WW > 0.f ? 1.f / WW : 0.f;
+    v[0] = a.x * inv; v[1] = a.y * inv; v[2] = a.z * inv; v[3] = a.w * inv;
+    s_out = M + log2f(WW);  // -inf when every state is empty
+}
+
+template <typename Tout>
+__global__ void __launch_bounds__(kCombWarps * 32)
+combine_kernel(const CombineParams p) {
+    pdl_wait_primary();  // the states are written by the preceding grids
+    __shared__ CombSmem sm;
+    __shared__ __align__(16) float fin[kD];
+    const int64_t row = blockIdx.x;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool has = 4 * lane < p.D;
+    float vs[4], ss;
+    merge_row(p.o_part, p.lse_part, p.NS, p.D, row, sm, vs, ss);
+    float vd[4] = {vs[0], vs[1], vs[2], vs[3]};
+    float sd = ss;
+    if (p.pre_part != nullptr) {
+        float vp[4], sp = -INFINITY;
+        if (p.C > 0) {
+            merge_row(p.pre_part, p.pre_lse, p.C, p.D, row, sm, vp, sp);
+        } else {
+            vp[0] = vp[1] = vp[2] = vp[3] = 0.f;  // empty prefix
         }
-        *reinterpret_cast<float4*>(&fin[4 * lane]) = make_float4(vd[0], vd[1], vd[2], vd[3]);
+        if (w == 0) {
+            if (p.o_pre != nullptr && has)
+                *reinterpret_cast<float4*>(p.o_pre + row * p.D + 4 * lane) =
+                    make_float4(vp[0], vp[1], vp[2], vp[3]);
+            if (p.s_pre != nullptr && lane == 0) p.s_pre[row] = sp;
+        }
+        // Two-state merge, prefix first ([F2] §③, guards of §⑤ and [FA] §2.2).
+        const float se = sanitize_lse(sp), sb = sanitize_lse(sd);
+        const float mm = fmaxf(se, sb);
+        const float we = merge_weight(se, mm), wb = merge_weight(sb, mm);
+        const float ws = __fadd_rn(we, wb);
+        const float iv = ws > 0.f ? 1.f / ws : 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float te = we > 0.f ? __fmul_rn(we, vp[i]) : 0.f;
+            const float tb = wb > 0.f ? __fmul_rn(wb, vd[i]) : 0.f;
+            vd[i] = __fmul_rn(__fadd_rn(te, tb), iv);
+        }
+        sd = mm + log2f(ws);
+    }
+    if (w == 0) {
+        if (has) *reinterpret_cast<float4*>(&fin[4 * lane]) = make_float4(vd[0], vd[1], vd[2], vd[3]);
         if (lane == 0 && p.lse_out != nullptr) p.lse_out[row] = sd;
     }
     __syncthreads();
@@ -574,23 +607,23 @@ cudaError_t launch_splitkv_decode(const DecodeArgs& a, const DeviceInfo& dev, cu
 
 namespace skv {
 
-cudaError_t launch_combine(const float* o_part, const float* lse_part, int64_t rows, int NS,
-                           int64_t D, void* out, skv_dtype out_dt, float* lse_out,
-                           const float* extra_v, const float* extra_s, bool pdl,
-                           const DeviceInfo& dev, cudaStream_t st) {
+cudaError_t launch_combine(const CombineArgs& a, bool pdl, const DeviceInfo& dev, cudaStream_t st) {
     (void)dev;
-    if (D > kD || D % 8 != 0) return cudaErrorInvalidValue;
+    if (a.D > kD || a.D % 8 != 0) return cudaErrorInvalidValue;
     CombineParams p;
-    p.o_part = o_part;
-    p.lse_part = lse_part;
-    p.out = out;
-    p.lse_out = lse_out;
-    p.extra_v = extra_v;
-    p.extra_s = extra_s;
-    p.NS = NS;
-    p.D = (int)D;
+    p.o_part = a.o_part;
+    p.lse_part = a.lse_part;
+    p.out = a.out;
+    p.lse_out = a.lse_out;
+    p.pre_part = a.pre_part;
+    p.pre_lse = a.pre_lse;
+    p.o_pre = a.o_pre;
+    p.s_pre = a.s_pre;
+    p.NS = a.NS;
+    p.C = a.C;
+    p.D = (int)a.D;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)rows, 1, 1);
+    cfg.gridDim = dim3((unsigned)a.rows, 1, 1);
     cfg.blockDim = dim3(kCombWarps * 32, 1, 1);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -598,7 +631,7 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, int64_t r
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    switch (out_dt) {
+    switch (a.out_dt) {
         case SKV_F32: return cudaLaunchKernelEx(&cfg, combine_kernel<float>, p);
         case SKV_F16: return cudaLaunchKernelEx(&cfg, combine_kernel<__half>, p);
         case SKV_BF16: return cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, p);

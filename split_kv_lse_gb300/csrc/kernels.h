@@ -43,13 +43,28 @@ cudaError_t launch_merge_states(const void* v, const float* s, void* vo, float* 
                                 size_t ws_bytes, const DeviceInfo& dev, cudaStream_t st);
 
 // Combine pass of the split-KV decode: merges NS fp32 partial states per row
-// (rows = B*Hq) into `out` (out_dt) and optional lse_out; an optional extra
-// fp32 state per row [rows, D] / [rows] is merged last (cascade prefix).
-// Launched as a programmatic dependent of the preceding kernel on `st`.
-cudaError_t launch_combine(const float* o_part, const float* lse_part, int64_t rows, int NS,
-                           int64_t D, void* out, skv_dtype out_dt, float* lse_out,
-                           const float* extra_v, const float* extra_s, bool pdl,
-                           const DeviceInfo& dev, cudaStream_t st);
+// (rows = B*Hq) into `out` (out_dt) and optional lse_out.  For the cascade,
+// C fp32 prefix-chunk states per row (pre_part [rows, C, D], pre_lse
+// [rows, C]) are first merged into the prefix state -- written to o_pre,
+// s_pre when those are not null -- which is then merged with the split
+// states (prefix first).  Launched as a programmatic dependent of the
+// preceding kernel on `st` when pdl is set.
+struct CombineArgs {
+    const float* o_part;
+    const float* lse_part;
+    int64_t rows;
+    int NS;
+    int64_t D;
+    void* out;
+    skv_dtype out_dt;
+    float* lse_out;
+    const float* pre_part;
+    const float* pre_lse;
+    int C;
+    float* o_pre;
+    float* s_pre;
+};
+cudaError_t launch_combine(const CombineArgs& a, bool pdl, const DeviceInfo& dev, cudaStream_t st);
 
 // ---------------------------------------------------------------- decode
 struct DecodeArgs {
@@ -67,5 +82,24 @@ struct DecodeArgs {
     int32_t* ranges_dbg;
 };
 cudaError_t launch_splitkv_decode(const DecodeArgs& a, const DeviceInfo& dev, cudaStream_t st);
+
+// ---------------------------------------------------------------- cascade
+struct CascadeArgs {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    int32_t num_pool_pages;
+    const int32_t* prefix_pages;
+    int32_t prefix_len;
+    int32_t B, Hq, Hkv;
+    float sm_scale;
+};
+// Grid of the shared-prefix pass: M tiles of 128 query rows, prefix blocks
+// of 128 keys per chunk, number of chunks.
+void cascade_prefix_geometry(int B, int G, int Hkv, int prefix_len, int sm_count, int* mtiles,
+                             int* blocks_per_chunk, int* nchunks);
+cudaError_t launch_cascade_prefix(const CascadeArgs& a, const DeviceInfo& dev, float* pre_part,
+                                  float* pre_lse, int nchunks, int blocks_per_chunk, int mtiles,
+                                  cudaStream_t st);
 
 }  // namespace skv

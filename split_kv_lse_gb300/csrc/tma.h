@@ -21,6 +21,12 @@ cudaError_t make_tmap_2d_16bit(CUtensorMap* map, const void* base, uint64_t rows
                                uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows,
                                bool swizzle128, bool bf16);
 
+// 3-D tiled map over a [d2, d1, d0] array of 16-bit elements (d0 innermost,
+// contiguous), strides in bytes for dims 1 and 2; box b0 x b1 x b2.
+cudaError_t make_tmap_3d_16bit(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1,
+                               uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes,
+                               uint32_t b0, uint32_t b1, uint32_t b2, bool swizzle128);
+
 }  // namespace skv
 
 #ifdef __CUDACC__
@@ -36,6 +42,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         :: "r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
            "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
            "r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar))), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        :: "r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+           "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
+           "r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
         : "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

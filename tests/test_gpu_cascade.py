@@ -1,0 +1,114 @@
+"""Parity of the two-level cascade (tcgen05 shared-prefix pass + split-KV suffix +
+merges) with the fp64 oracle: the prefix state, the suffix split states and the
+merged output, on small and ragged cases, every group size, empty prefixes and
+suffixes, and the full B=64 / 8192-token-prefix workload.
+
+Pages: "F2 讲解：merge_state，以 2 为底的 LSE 合并" §⑥ (cascade);
+"L3 讲解：split-KV decode 与 LSE 合并" §①-④ (the suffix)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import (DEC_LSE_ATOL, DEC_O_ATOL, assert_s_close, assert_v_close,
+                         require_gpu, skv)
+from split_kv_lse_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+H16 = 2.0 ** -11
+
+
+@pytest.fixture(scope="module")
+def lib():
+    require_gpu()
+    return skv()
+
+
+def poison_unused(d):
+    """NaN in every pool slot no request may read: tails of partial last pages
+    (prefix and suffixes) and unused pages."""
+    kc, vc = d["k_cache"], d["v_cache"]
+    used = set()
+    npre = -(-d["prefix_len"] // 16)
+    pre = d["prefix_pages"][:npre].tolist()
+    used.update(pre)
+    if d["prefix_len"] % 16 and npre:
+        kc[pre[-1], :, d["prefix_len"] % 16:] = float("nan")
+        vc[pre[-1], :, d["prefix_len"] % 16:] = float("nan")
+    for b, c in enumerate(d["ctx"].tolist()):
+        n = -(-c // 16)
+        pages = d["block_table"][b, :n].tolist()
+        used.update(pages)
+        if c % 16:
+            kc[pages[-1], :, c % 16:] = float("nan")
+            vc[pages[-1], :, c % 16:] = float("nan")
+    for pid in range(kc.shape[0]):
+        if pid not in used:
+            kc[pid] = float("nan")
+            vc[pid] = float("nan")
+
+
+def run_and_check(lib, d, ns, poison=True):
+    if poison:
+        poison_unused(d)
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    pp = g["prefix_pages"] if g["prefix_pages"].numel() else torch.zeros(1, dtype=torch.int32,
+                                                                       device=DEV)
+    out, lse, o_pre, s_pre, o_part, lse_part = lib.cascade_decode(
+        g["q"], g["k_cache"], g["v_cache"], pp, d["prefix_len"], g["block_table"], g["ctx"], ns,
+        d["sm_scale"])
+    torch.cuda.synchronize()
+    assert lib.get_device_error() == (0, 0)
+    o_r, s_r, op_r, sp_r = oracle.cascade(d["q"], d["k_cache"], d["v_cache"], d["prefix_pages"],
+                                          d["prefix_len"], d["block_table"], d["ctx"],
+                                          d["sm_scale"])
+    assert_s_close(s_pre, sp_r, DEC_LSE_ATOL, "s_pre")
+    assert_v_close(o_pre, op_r, DEC_O_ATOL, 0.0, "o_pre", empty_rows=(sp_r == -math.inf))
+    opr, lpr = oracle.attend_splits(d["q"], d["k_cache"], d["v_cache"], d["block_table"],
+                                    d["ctx"], d["sm_scale"], ns)
+    assert_s_close(lse_part, lpr, DEC_LSE_ATOL, "lse_part")
+    assert_v_close(o_part, opr, DEC_O_ATOL, 0.0, "o_part", empty_rows=(lpr == -math.inf))
+    assert_s_close(lse, s_r, DEC_LSE_ATOL, "lse_out")
+    assert_v_close(out, o_r, DEC_O_ATOL, H16, "out", empty_rows=(s_r == -math.inf))
+    return out, lse, o_pre, s_pre
+
+
+@pytest.mark.parametrize("prefix_len", [128, 200, 1000, 16])
+def test_cascade_small(lib, prefix_len):
+    d = W.cascade_inputs(3, 8, 2, 128, 16, prefix_len, [5, 0, 37], seed=prefix_len)
+    run_and_check(lib, d, 4)
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_cascade_group_sizes(lib, G):
+    # B*G rows spanning two M tiles of 128 rows, the second partial.
+    B = (160 + G - 1) // G
+    ctx = [int(x) for x in np.random.default_rng(G).integers(0, 300, B)]
+    d = W.cascade_inputs(B, 2 * G, 2, 128, 16, 777, ctx, seed=10 + G)
+    run_and_check(lib, d, 8)
+
+
+def test_cascade_empty_prefix(lib):
+    d = W.cascade_inputs(2, 8, 2, 128, 16, 0, [40, 3], seed=20)
+    out, lse, o_pre, s_pre = run_and_check(lib, d, 4)
+    assert torch.all(s_pre.cpu() == -math.inf) and torch.all(o_pre.cpu() == 0)
+
+
+def test_cascade_empty_suffixes(lib):
+    d = W.cascade_inputs(2, 8, 2, 128, 16, 300, [0, 0], seed=21)
+    run_and_check(lib, d, 4)
+
+
+def test_cascade_everything_empty(lib):
+    d = W.cascade_inputs(2, 8, 2, 128, 16, 0, [0, 0], seed=22)
+    out, lse, _, _ = run_and_check(lib, d, 2, poison=False)
+    assert torch.all(lse.cpu() == -math.inf) and torch.all(out.cpu() == 0)
+
+
+def test_cascade_full_workload(lib):
+    """B=64, Hq=32, Hkv=8, an 8192-token shared prefix, suffixes of 1..2048 tokens, NS=16."""
+    d = W.cascade_mixed()
+    run_and_check(lib, d, d["num_splits"], poison=False)
