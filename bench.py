@@ -40,7 +40,8 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 WORKLOAD = ("split-KV hot path step: merge_state + merge_state_in_place S=8192 H=32 D=128 fp16; "
             "merge_states S=256 N=64 H=32 D=128 fp32; splitkv_decode B=1 ctx=32768 Hq=32 Hkv=8 "
-            "D=128 page=16 NS=64 fp16")
+            "D=128 page=16 NS=64 fp16; cascade_decode B=64 Hq=32 Hkv=8 shared prefix 8192 + "
+            "suffixes 1..2048 NS=16 fp16")
 
 
 def parse_args():
@@ -137,7 +138,8 @@ def nbytes(t):
     return t.numel() * t.element_size()
 
 
-STAGE_NAMES = ("merge_state", "merge_state_in_place", "merge_states", "splitkv_decode")
+STAGE_NAMES = ("merge_state", "merge_state_in_place", "merge_states", "splitkv_decode",
+               "cascade_decode")
 # Diagnostic stages, selectable with --only (not part of the default step).
 EXTRA_STAGES = ("splitkv_decode_pass1",)
 
@@ -158,6 +160,8 @@ def build_stages(torch, skv, W, dev, only=None):
         _merge_states_stage(torch, skv, W, dev, to_dev, stages, hostside)
     if want & {"splitkv_decode", "splitkv_decode_pass1"}:
         _decode_stage(torch, skv, W, dev, to_dev, stages, hostside, want)
+    if "cascade_decode" in want:
+        _cascade_stage(torch, skv, W, dev, to_dev, stages, hostside)
     return stages, hostside
 
 
@@ -223,6 +227,34 @@ def _decode_stage(torch, skv, W, dev, to_dev, stages, hostside, want):
     hostside["decode"] = d4
 
 
+def _cascade_stage(torch, skv, W, dev, to_dev, stages, hostside):
+    # Cascade, B=64: shared 8192-token prefix on the tensor cores + suffixes.
+    d5 = W.cascade_mixed()
+    g5 = to_dev(d5)
+    ns = d5["num_splits"]
+    B, Hq, D = d5["q"].shape
+    Hkv = d5["k_cache"].shape[1]
+    f32 = torch.float32
+    bufs = dict(out=torch.empty(B, Hq, D, dtype=torch.float16, device=dev),
+                lse_out=torch.empty(B, Hq, device=dev), o_pre=torch.empty(B, Hq, D, device=dev),
+                s_pre=torch.empty(B, Hq, device=dev),
+                o_part=torch.empty(B, Hq, ns, D, dtype=f32, device=dev),
+                lse_part=torch.empty(B, Hq, ns, dtype=f32, device=dev))
+    ws = torch.empty(max(256, skv.cascade_workspace_size(B, Hq, Hkv, D, d5["prefix_len"])),
+                     dtype=torch.uint8, device=dev)
+    kv_tokens = d5["prefix_len"] + int(d5["ctx"].sum())
+    npages = -(-d5["prefix_len"] // 16) + sum(-(-int(c) // 16) for c in d5["ctx"])
+    cas_bytes = (kv_tokens * Hkv * D * 2 * 2 + nbytes(d5["q"]) + npages * 4 + nbytes(d5["ctx"]) +
+                 nbytes(bufs["out"]) + nbytes(bufs["lse_out"]))
+    stages.append(Stage("cascade_decode",
+                        lambda: skv.cascade_decode(g5["q"], g5["k_cache"], g5["v_cache"],
+                                                   g5["prefix_pages"], d5["prefix_len"],
+                                                   g5["block_table"], g5["ctx"], ns,
+                                                   d5["sm_scale"], workspace=ws, **bufs),
+                        cas_bytes, 3))
+    hostside["cascade"] = d5
+
+
 _PINNED_OUT = {}
 
 
@@ -247,6 +279,15 @@ def e2e_step(torch, skv, host, dev):
     out, lse, _, _ = skv.splitkv_decode(g4["q"], g4["k_cache"], g4["v_cache"], g4["block_table"],
                                         g4["ctx"], d4["num_splits"], d4["sm_scale"])
     outs += [out, lse]
+    d5 = host["cascade"]
+    g5 = {k: (v.to(dev, non_blocking=True) if isinstance(v, torch.Tensor) else v)
+          for k, v in d5.items()}
+    h2d += sum(nbytes(v) for v in d5.values() if isinstance(v, torch.Tensor))
+    out5, lse5, _, _, _, _ = skv.cascade_decode(g5["q"], g5["k_cache"], g5["v_cache"],
+                                                g5["prefix_pages"], d5["prefix_len"],
+                                                g5["block_table"], g5["ctx"], d5["num_splits"],
+                                                d5["sm_scale"])
+    outs += [out5, lse5]
     key = tuple((tuple(o.shape), o.dtype) for o in outs)
     if key not in _PINNED_OUT:
         _PINNED_OUT[key] = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
@@ -285,9 +326,24 @@ def oracle_sample(W):
         import oracle
         oracle.attend_splits(q, kc, vc, bt, cx, sc, 64)
     samples.append(("splitkv_decode", dec, 32768 * 2 * 128 * 2 * 2 + 8 * 128 * 4))
+    d5 = W.cascade_mixed()
+    nb = 4  # of 64 requests, all 32 heads
+    q5 = np.ascontiguousarray(d5["q"][:nb].double().numpy())
+    kc5 = np.ascontiguousarray(d5["k_cache"].double().numpy())
+    vc5 = np.ascontiguousarray(d5["v_cache"].double().numpy())
+    bt5, cx5 = d5["block_table"][:nb].numpy(), d5["ctx"][:nb].numpy()
+    pp5, pl5, sc5 = d5["prefix_pages"].numpy(), d5["prefix_len"], d5["sm_scale"]
+
+    def cas():
+        import oracle
+        oracle.cascade(q5, kc5, vc5, pp5, pl5, bt5, cx5, sc5)
+    # Bytes charged as the GPU stage charges them, scaled to the sampled requests.
+    cas_bytes = (pl5 + int(cx5.sum())) * 8 * 128 * 2 * 2 * nb // 64
+    samples.append(("cascade_decode", cas, cas_bytes))
     return samples, ("merge_state 2048 of 8192 positions; merge_states 32 of 256 positions; "
                      "splitkv_decode 2 of 8 KV heads (8 of 32 query heads), full 32768-token "
-                     "context, 64 split partials")
+                     "context, 64 split partials; cascade 4 of 64 requests, all heads, full "
+                     "prefix and suffixes")
 
 
 def time_oracle(samples, reps=1):

@@ -11,18 +11,29 @@
 //
 // One CTA per (kv head, 128-row M tile, chunk of the prefix).  The M tile's
 // rows are (request, group head) pairs -- row = r_local * G + g -- so one KV
-// tile serves 128 query rows.  Per 128-key block:
-//   S = Q K^T        tcgen05.mma kind::f16, Q [128 x 128] and the K block
-//                    [128 keys x 128] K-major in shared memory, S fp32 in TMEM
+// tile serves 128 query rows.  Per 128-key block j:
+//   S_j = Q K_j^T    tcgen05.mma kind::f16, Q [128 x 128] and the K block
+//                    [128 keys x 128] K-major in shared memory; S fp32 in one
+//                    of two TMEM buffers, so S_{j+1} runs on the tensor core
+//                    while the warps do the softmax of block j
 //   softmax          4 warps, thread i <-> row i <-> TMEM lane i: base-2
-//                    online max/sum ([F2] §② exp2 trick), P written to shared
+//                    online max/sum ([F2] §② exp2 trick); P written to shared
 //                    memory as fp16 in the swizzled K-major operand layout
-//   O_blk = P V      tcgen05.mma with V as an MN-major operand, O_blk in TMEM
-//   o = alpha*o + O_blk   accumulated in registers (the rescale stays exact)
-// Q, K and V tiles arrive by TMA tensor loads with the 128-byte swizzle (a
-// page is one 16 x 64 box per half of the head dim); two K and two V blocks
-// are in flight.  Each chunk writes its normalised state (o, s base 2) for
-// the combine kernel, which merges the chunks into the prefix state.
+//   O += P_j V_j     tcgen05.mma with V as an MN-major operand, O fp32 stays
+//                    in TMEM across blocks
+// Lazy rescale: a row keeps the max it last rescaled to and only rescales
+// O (in TMEM) and its sum when the block max exceeds it by more than 8 (log2
+// units), so p <= 2^8 (exact in fp16 range) and the final normalisation by
+// the same max keeps the result exact.
+// Warp roles: warps 0-3 softmax and epilogue, warp 4 issues the MMAs, warp
+// 5 issues the TMA copies; they meet on mbarriers (S full / free per S
+// buffer, P full, PV done, K and V stage full / empty), so no role waits on
+// another's serial work.  Q, K and V tiles arrive by TMA tensor loads with
+// the 128-byte swizzle (a page is one 16 x 64 box per half of the head dim);
+// two K and two V blocks are in flight.  Every wait is bounded; a wait that
+// gives up raises a shared abort flag that ends every role's loop.  Each
+// chunk writes its normalised state (o, s base 2) for the combine kernel,
+// which merges the chunks into the prefix state.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -39,8 +50,12 @@ constexpr int kM = 128;                              // query rows per CTA
 constexpr int kHalf = 128 * 128;                     // one [128 rows x 64] fp16 swizzled half tile
 constexpr int kTile = 2 * kHalf;                     // one [128 x 128] fp16 operand tile (32 KB)
 constexpr int kStages = 2;                           // K blocks and V blocks in flight
-constexpr int kThreads = 128;
-constexpr uint32_t kTmemCols = 256;                  // S: columns [0, 128), O_blk: [128, 256)
+constexpr int kSoftmaxWarps = 4;                     // one thread per query row
+constexpr int kMmaWarp = 4;
+constexpr int kTmaWarp = 5;
+constexpr int kThreads = 6 * 32;
+constexpr uint32_t kTmemCols = 512;                  // S buffers [0,128), [128,256); O [256,384)
+constexpr float kRescaleThreshold = 8.f;             // log2 units
 
 struct PrefixParams {
     const int32_t* prefix_pages;
@@ -60,12 +75,29 @@ constexpr size_t kSmemK = kSmemQ + kTile;
 constexpr size_t kSmemV = kSmemK + (size_t)kStages * kTile;
 constexpr size_t kSmemP = kSmemV + (size_t)kStages * kTile;
 constexpr size_t kSmemBars = kSmemP + kTile;
-constexpr int kNumBars = 2 + 2 * kStages;            // q_full, mma_done, k_full[], v_full[]
+// q_full, p_full, pv_done, s_full[2], s_free[2], k_full[], k_empty[], v_full[], v_empty[]
+constexpr int kNumBars = 7 + 4 * kStages;
 constexpr size_t kSmemTmemSlot = kSmemBars + kNumBars * sizeof(uint64_t);
-constexpr size_t kSmemIds = kSmemTmemSlot + 16;
+constexpr size_t kSmemIds = kSmemTmemSlot + 16;  // tmem address, abort flag
 
 size_t prefix_smem_bytes(int blocks_per_chunk) {
     return 1024 + kSmemIds + (size_t)blocks_per_chunk * kPagesPerBlock * sizeof(int);
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+SKV_DEVINL bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                              unsigned long long* err, int where) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            record_error(err, SKV_ERR_TIMEOUT, where);
+            *abort_flag = 1;
+            return false;
+        }
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -79,13 +111,19 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     uint8_t* Ps = sm + kSmemP;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSmemBars);
     uint64_t* q_full = bars + 0;
-    uint64_t* mma_done = bars + 1;
-    uint64_t* k_full = bars + 2;
-    uint64_t* v_full = bars + 2 + kStages;
+    uint64_t* p_full = bars + 1;
+    uint64_t* pv_done = bars + 2;
+    uint64_t* s_full = bars + 3;   // [2]
+    uint64_t* s_free = bars + 5;   // [2]
+    uint64_t* k_full = bars + 7;
+    uint64_t* k_empty = k_full + kStages;
+    uint64_t* v_full = k_empty + kStages;
+    uint64_t* v_empty = v_full + kStages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kSmemTmemSlot);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kSmemTmemSlot + 4);
     int* ids = reinterpret_cast<int*>(sm + kSmemIds);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chunk = blockIdx.x, mtile = blockIdx.y, hkv = blockIdx.z;
     const int nblocks_total = (p.prefix_len + kBlockKeys - 1) / kBlockKeys;
     const int blk0 = chunk * p.blocks_per_chunk;
@@ -106,69 +144,118 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         ids[i] = pid;
     }
     if (tid == 0) {
-        for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);
+        mbar_init(q_full, 1);
+        mbar_init(p_full, kSoftmaxWarps);
+        mbar_init(pv_done, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&s_free[b], kSoftmaxWarps);
+        }
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+        }
+        *abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tq);
-        tma_prefetch_desc(&tk);
-        tma_prefetch_desc(&tv);
     }
     if (warp == 0) tc::tmem_alloc(tmem_slot, kTmemCols);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem;          // columns [0, 128)
-    const uint32_t tO = tmem + 128;    // columns [128, 256)
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t tO = tmem + 256;  // columns [256, 384); S buffers at 0 and 128
 
-    const uint64_t pol = policy_evict_first();
-    // One thread: copy block j (8 pages x 2 halves) of K or V into a stage.
-    auto load_block = [&](int j, int stage, bool is_v) {
-        uint64_t* bar = is_v ? &v_full[stage] : &k_full[stage];
-        uint8_t* dst = (is_v ? Vs : Ks) + stage * kTile;
-        const CUtensorMap* map = is_v ? &tv : &tk;
-        mbar_arrive_expect_tx(bar, kTile);
+    if (warp == kTmaWarp) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tq);
+            tma_prefetch_desc(&tk);
+            tma_prefetch_desc(&tv);
+            const uint64_t pol = policy_evict_first();
+            auto load_block = [&](int j, bool is_v) {
+                const int stage = j % kStages;
+                uint64_t* bar = is_v ? &v_full[stage] : &k_full[stage];
+                uint8_t* dst = (is_v ? Vs : Ks) + stage * kTile;
+                const CUtensorMap* map = is_v ? &tv : &tk;
+                mbar_arrive_expect_tx(bar, kTile);
 #pragma unroll 1
-        for (int pg = 0; pg < kPagesPerBlock; ++pg) {
-            const int pid = ids[j * kPagesPerBlock + pg];
-            // A page past the prefix is read from the row just past the
-            // tensor: the TMA fills the whole box with zeros.
-            const int row = pid >= 0 ? (pid * p.Hkv + hkv) * kPage : p.pool_rows;
-            tma_load_2d(dst + pg * (kPage * 128), map, 0, row, bar, pol);
-            tma_load_2d(dst + kHalf + pg * (kPage * 128), map, 64, row, bar, pol);
+                for (int pg = 0; pg < kPagesPerBlock; ++pg) {
+                    const int pid = ids[j * kPagesPerBlock + pg];
+                    // A page past the prefix is read from the row just past
+                    // the tensor: the TMA fills the whole box with zeros.
+                    const int row = pid >= 0 ? (pid * p.Hkv + hkv) * kPage : p.pool_rows;
+                    tma_load_2d(dst + pg * (kPage * 128), map, 0, row, bar, pol);
+                    tma_load_2d(dst + kHalf + pg * (kPage * 128), map, 64, row, bar, pol);
+                }
+            };
+            mbar_arrive_expect_tx(q_full, kTile);
+            const int z = mtile * (kM / p.G);
+            tma_load_3d(Qs, &tq, 0, hkv * p.G, z, q_full);
+            tma_load_3d(Qs + kHalf, &tq, 64, hkv * p.G, z, q_full);
+            for (int j = 0; j < nb; ++j) {
+                if (j >= kStages &&
+                    !wait_or_abort(&k_empty[j % kStages], (uint32_t)((j / kStages - 1) & 1),
+                                   abort_flag, p.err, 20))
+                    break;
+                load_block(j, false);
+                if (j >= kStages &&
+                    !wait_or_abort(&v_empty[j % kStages], (uint32_t)((j / kStages - 1) & 1),
+                                   abort_flag, p.err, 21))
+                    break;
+                load_block(j, true);
+            }
         }
-    };
-    if (tid == 0) {
-        mbar_arrive_expect_tx(q_full, kTile);
-        const int z = mtile * (kM / p.G);
-        tma_load_3d(Qs, &tq, 0, hkv * p.G, z, q_full);
-        tma_load_3d(Qs + kHalf, &tq, 64, hkv * p.G, z, q_full);
-        for (int s = 0; s < kStages && s < nb; ++s) {
-            load_block(s, s, false);
-            load_block(s, s, true);
-        }
-    }
-
-    constexpr uint32_t idS = tc::idesc_f16_f32(kM, kBlockKeys, false);
-    constexpr uint32_t idPV = tc::idesc_f16_f32(kM, kD, true);
-    float o[kD];
-#pragma unroll
-    for (int i = 0; i < kD; ++i) o[i] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
-    uint32_t mma_phase = 0;
-    bool alive = true;
-
-#pragma unroll 1
-    for (int j = 0; j < nb && alive; ++j) {
-        const int st = j % kStages;
-        const uint32_t par = (uint32_t)((j / kStages) & 1);
-        // ---- S = Q K^T
-        bool ok = true;  // meaningful on the issuing thread
-        if (tid == 0) {
-            if (j == 0) ok = mbar_wait(q_full, 0, p.err, 10);
-            ok = ok && mbar_wait(&k_full[st], par, p.err, 11);
-            if (ok) {
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = tc::idesc_f16_f32(kM, kBlockKeys, false);
+            constexpr uint32_t idPV = tc::idesc_f16_f32(kM, kD, true);
+            auto issue_pv = [&](int j) -> bool {  // O += P_j V_j
+                const int st = j % kStages;
+                if (!wait_or_abort(p_full, (uint32_t)(j & 1), abort_flag, p.err, 22)) return false;
+                if (!wait_or_abort(&v_full[st], (uint32_t)((j / kStages) & 1), abort_flag, p.err, 23))
+                    return false;
                 tc::fence_after_sync();
+                const int tail = p.prefix_len % kPage;
+                const int last_page = npages_prefix - 1 - (blk0 + j) * kPagesPerBlock;
+                if (tail != 0 && last_page >= 0 && last_page < kPagesPerBlock) {
+                    // The prefix ends inside this block's page `last_page`:
+                    // its rows past the end hold whatever the pool has there.
+                    // P is 0 for them, but 0 times a non-finite value is not
+                    // 0, so the rows are zeroed (whole 128-byte rows: the
+                    // swizzle only permutes chunks inside a row).
+                    for (int t = tail; t < kPage; ++t)
+                        for (int h = 0; h < 2; ++h) {
+                            uint4* row = reinterpret_cast<uint4*>(Vs + st * kTile + h * kHalf +
+                                                                  (last_page * kPage + t) * 128);
+                            for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
+                        }
+                    tc::fence_proxy_async_smem();
+                }
+#pragma unroll
+                for (int k = 0; k < kBlockKeys / 16; ++k) {
+                    const int h = k >> 2, kk = k & 3;
+                    const uint64_t ad = tc::sdesc_sw128(smem_addr(Ps + h * kHalf) + kk * 32, 16, 1024);
+                    const uint64_t bd = tc::sdesc_sw128(smem_addr(Vs + st * kTile) + k * 2048, kHalf, 1024);
+                    tc::mma_f16_ss(tO, ad, bd, idPV, j > 0 || k > 0);
+                }
+                tc::mma_commit(pv_done);
+                tc::mma_commit(&v_empty[st]);
+                return true;
+            };
+            bool ok = wait_or_abort(q_full, 0, abort_flag, p.err, 24);
+            for (int j = 0; ok && j < nb; ++j) {
+                // S_j = Q K_j^T into S buffer j & 1, then P_{j-1} V_{j-1}: the
+                // tensor core computes S_j while the softmax of block j-1 runs.
+                const int st = j % kStages, b = j & 1;
+                ok = wait_or_abort(&k_full[st], (uint32_t)((j / kStages) & 1), abort_flag, p.err, 25);
+                if (ok && j >= 2)
+                    ok = wait_or_abort(&s_free[b], (uint32_t)(((j >> 1) - 1) & 1), abort_flag, p.err, 26);
+                if (!ok) break;
+                tc::fence_after_sync();
+                const uint32_t tS = tmem + (uint32_t)b * 128;
 #pragma unroll
                 for (int k = 0; k < kD / 16; ++k) {
                     const int h = k >> 2, kk = k & 3;
@@ -176,126 +263,106 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                     const uint64_t bd = tc::sdesc_sw128(smem_addr(Ks + st * kTile + h * kHalf) + kk * 32, 16, 1024);
                     tc::mma_f16_ss(tS, ad, bd, idS, k > 0);
                 }
+                tc::mma_commit(&s_full[b]);
+                tc::mma_commit(&k_empty[st]);
+                if (j >= 1) ok = issue_pv(j - 1);
             }
-            tc::mma_commit(mma_done);  // also arrives when nothing was issued
+            if (ok) issue_pv(nb - 1);
         }
-        alive = mbar_wait(mma_done, mma_phase, p.err, 12) && ok;
-        mma_phase ^= 1;
-        alive = __syncthreads_and(alive);
-        if (!alive) break;
-        tc::fence_after_sync();
-        if (tid == 0 && j + kStages < nb) load_block(j + kStages, st, false);  // K stage is free
-
-        // ---- softmax of row `tid` over this block (log2 units)
-        const int key0 = (blk0 + j) * kBlockKeys;
-        float mx = -INFINITY;
+    } else {
+        // ---------------------------------------------------------------- softmax, row = tid
+        float m_ref = -INFINITY;  // the max this row's O and l are scaled to (log2 units)
+        float l_run = 0.f;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        bool ok = true;
+        for (int j = 0; j < nb; ++j) {
+            const int b = j & 1;
+            ok = wait_or_abort(&s_full[b], (uint32_t)((j >> 1) & 1), abort_flag, p.err, 27);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            float x[kBlockKeys];
+            tc::tmem_ld128(tmem + (uint32_t)b * 128 + lane_base, x);
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[b]);  // S buffer b read by this warp
+            const int key0 = (blk0 + j) * kBlockKeys;
+            float mx = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float s[32];
-            tc::tmem_ld32(tS + lane_base + 32 * c, s);
+            for (int i = 0; i < kBlockKeys; ++i) {
+                x[i] = key0 + i < p.prefix_len ? x[i] * p.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, x[i]);
+            }
+            // PV_{j-1} done: O is stable and the P buffer is free.
+            if (j > 0) {
+                ok = wait_or_abort(pv_done, (uint32_t)((j - 1) & 1), abort_flag, p.err, 28);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+            }
+            if (mx > m_ref + kRescaleThreshold) {  // also the first block (m_ref = -inf)
+                if (j > 0) {
+                    const float alpha = exp2f(m_ref - mx);
+                    l_run *= alpha;
+#pragma unroll 1
+                    for (int c = 0; c < kD / 32; ++c) {  // 32 columns at a time: x[] stays live
+                        float ob[32];
+                        tc::tmem_ld32(tO + lane_base + 32 * c, ob);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (key0 + 32 * c + i < p.prefix_len) mx = fmaxf(mx, s[i] * p.scale_log2);
-        }
-        const float m_new = fmaxf(m_run, mx);  // finite: the block's first key is valid
-        const float alpha = exp2f(m_run - m_new);
-        float psum = 0.f;
+                        for (int i = 0; i < 32; ++i) ob[i] *= alpha;
+                        tc::tmem_st32(tO + lane_base + 32 * c, ob);
+                    }
+                }
+                m_ref = mx;
+            }
+            float psum = 0.f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float s[32];
-            tc::tmem_ld32(tS + lane_base + 32 * c, s);
-#pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys = one 16-byte chunk of the P row
+            for (int chunk16 = 0; chunk16 < 16; ++chunk16) {  // 8 keys = one 16-byte chunk of P
                 uint32_t pk[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int i0 = q8 * 8 + 2 * e;
-                    const bool v0 = key0 + 32 * c + i0 < p.prefix_len;
-                    const bool v1 = key0 + 32 * c + i0 + 1 < p.prefix_len;
-                    const float p0 = v0 ? exp2f(s[i0] * p.scale_log2 - m_new) : 0.f;
-                    const float p1 = v1 ? exp2f(s[i0 + 1] * p.scale_log2 - m_new) : 0.f;
+                    const int i0 = chunk16 * 8 + 2 * e;
+                    const float p0 = exp2f(x[i0] - m_ref);  // masked keys: 2^-inf = 0
+                    const float p1 = exp2f(x[i0 + 1] - m_ref);
                     psum += p0 + p1;
                     const __half2 h2 = __floats2half2_rn(p0, p1);
                     pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
                 }
-                const int chunk16 = c * 4 + q8;            // logical 16-byte chunk 0..15
                 const int half = chunk16 >> 3;
                 const int pos = (chunk16 & 7) ^ (tid & 7);  // 128-byte swizzle
                 *reinterpret_cast<uint4*>(Ps + half * kHalf + tid * 128 + pos * 16) =
                     make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
+            l_run += psum;
+            tc::fence_before_sync();
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);  // P_j (and any O rescale) done by this warp
         }
-        l_run = fmaf(l_run, alpha, psum);
-        m_run = m_new;
-        tc::fence_before_sync();
-        tc::fence_proxy_async_smem();
-        __syncthreads();
-
-        // ---- O_blk = P V
-        ok = true;
-        if (tid == 0) {
+        // ---- this chunk's state for row `tid` (after the last PV)
+        if (ok) ok = wait_or_abort(pv_done, (uint32_t)((nb - 1) & 1), abort_flag, p.err, 29);
+        if (__all_sync(0xffffffffu, ok)) {
             tc::fence_after_sync();
-            ok = mbar_wait(&v_full[st], par, p.err, 13);
-            const int tail = p.prefix_len % kPage;
-            const int last_page = npages_prefix - 1 - (blk0 + j) * kPagesPerBlock;
-            if (ok && tail != 0 && last_page >= 0 && last_page < kPagesPerBlock) {
-                // The prefix ends inside this block's page `last_page`: its
-                // rows past the end hold whatever the pool has there.  P is 0
-                // for them, but 0 times a non-finite value is not 0, so the
-                // rows are zeroed (whole 128-byte rows: the swizzle only
-                // permutes chunks inside a row).
-                for (int t = tail; t < kPage; ++t)
-                    for (int h = 0; h < 2; ++h) {
-                        uint4* row = reinterpret_cast<uint4*>(Vs + st * kTile + h * kHalf +
-                                                              (last_page * kPage + t) * 128);
-                        for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
-                    }
-                tc::fence_proxy_async_smem();
+            const int rows_per_req = p.G;
+            const int r = mtile * (kM / rows_per_req) + tid / rows_per_req;
+            const int g = tid % rows_per_req;
+            float ob[kD];
+            tc::tmem_ld128(tO + lane_base, ob);
+            if (r < p.B) {
+                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                const int64_t row = (int64_t)r * p.Hq + hkv * p.G + g;
+                float* dst = p.pre_part + (row * p.nchunks + chunk) * kD;
+#pragma unroll
+                for (int i = 0; i < kD; i += 4)
+                    *reinterpret_cast<float4*>(dst + i) =
+                        make_float4(ob[i] * inv, ob[i + 1] * inv, ob[i + 2] * inv, ob[i + 3] * inv);
+                p.pre_lse[row * p.nchunks + chunk] =
+                    l_run > 0.f ? m_ref + log2f(l_run) : -INFINITY;
             }
-            if (ok) {
-#pragma unroll
-                for (int k = 0; k < kBlockKeys / 16; ++k) {
-                    const int h = k >> 2, kk = k & 3;
-                    const uint64_t ad = tc::sdesc_sw128(smem_addr(Ps + h * kHalf) + kk * 32, 16, 1024);
-                    const uint64_t bd = tc::sdesc_sw128(smem_addr(Vs + st * kTile) + k * 2048, kHalf, 1024);
-                    tc::mma_f16_ss(tO, ad, bd, idPV, k > 0);
-                }
-            }
-            tc::mma_commit(mma_done);
-        }
-        alive = mbar_wait(mma_done, mma_phase, p.err, 14) && ok;
-        mma_phase ^= 1;
-        alive = __syncthreads_and(alive);
-        if (!alive) break;
-        tc::fence_after_sync();
-        if (tid == 0 && j + kStages < nb) load_block(j + kStages, st, true);  // V stage is free
-
-        // ---- o = alpha * o + O_blk
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float ob[32];
-            tc::tmem_ld32(tO + lane_base + 32 * c, ob);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[32 * c + i] = fmaf(o[32 * c + i], alpha, ob[i]);
-        }
-        tc::fence_before_sync();
-        __syncthreads();
-    }
-
-    // ---- this chunk's state for row `tid`
-    if (alive) {
-        const int rows_per_req = p.G;
-        const int r = mtile * (kM / rows_per_req) + tid / rows_per_req;
-        const int g = tid % rows_per_req;
-        if (r < p.B) {
-            const int64_t row = (int64_t)r * p.Hq + hkv * p.G + g;
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            float* dst = p.pre_part + (row * p.nchunks + chunk) * kD;
-#pragma unroll
-            for (int i = 0; i < kD; i += 4)
-                *reinterpret_cast<float4*>(dst + i) =
-                    make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
-            p.pre_lse[row * p.nchunks + chunk] = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
         }
     }
     tc::fence_before_sync();

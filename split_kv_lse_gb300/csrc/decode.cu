@@ -421,11 +421,11 @@ cudaError_t launch_g(const CUtensorMap& tk, const DecodeParams& p, int B, int Hk
 // [L3] §③ merge of the split states (base 2).  For the cascade ([F2] §⑥) the
 // prefix-chunk states are merged first into the prefix state, which is then
 // merged with the merged split state by the two-state formula (prefix first).
-// One CTA per (b, hq) row, 4 warps: warp w takes states w, w + 4, ...; lane l
-// owns dims [4l, 4l + 4).  A warp requests the lse and v chunk of up to
-// kCombBatch states at once (one L2 round trip for N <= 4 * kCombBatch),
-// keeps an online (m, W, acc) across batches, and the 4 warp states meet in
-// shared memory.
+// WPR warps per (b, hq) row (1 for many rows, 4 for few rows); within a row,
+// warp w takes states w, w + WPR, ...; lane l owns dims [4l, 4l + 4).  A
+// warp requests the lse and v chunk of up to kCombBatch states at once (one
+// L2 round trip per batch), keeps an online (m, W, acc) across batches, and
+// with WPR > 1 the warp states meet in shared memory.
 constexpr int kCombWarps = 4;
 constexpr int kCombBatch = 16;
 
@@ -438,28 +438,28 @@ struct CombineParams {
     const float* pre_lse;  // [rows, C]
     float* o_pre;          // [rows, D] merged prefix state or nullptr
     float* s_pre;          // [rows]
+    int64_t rows;
     int NS, C, D;
 };
 
-struct CombSmem {
-    float wm[kCombWarps], wW[kCombWarps];
-    __align__(16) float wacc[kCombWarps][kD];
+struct WarpState {
+    float m, W;
+    float4 acc;
 };
 
-// Merge the N states of `row` in (o [rows, N, D], lse [rows, N]); every
-// thread with 4*lane < D receives its 4 output dims in v and the merged s.
-SKV_DEVINL void merge_row(const float* o, const float* lse, int N, int D, int64_t row,
-                          CombSmem& sm, float (&v)[4], float& s_out) {
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// This warp's share (states sub, sub + WPR, ...) of the N states of `row`.
+template <int WPR>
+SKV_DEVINL WarpState warp_merge(const float* o, const float* lse, int N, int D, int64_t row,
+                                int sub) {
+    const int lane = threadIdx.x & 31;
     const bool has = 4 * lane < D;
-    float m = -INFINITY, W = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int n0 = w; n0 < N; n0 += kCombWarps * kCombBatch) {
+    WarpState st{-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
+    for (int n0 = sub; n0 < N; n0 += WPR * kCombBatch) {
         float l[kCombBatch];
         float4 x[kCombBatch];
 #pragma unroll
         for (int k = 0; k < kCombBatch; ++k) {
-            const int n = n0 + k * kCombWarps;
+            const int n = n0 + k * WPR;
             l[k] = -INFINITY;
             x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (n < N) {
@@ -471,71 +471,88 @@ SKV_DEVINL void merge_row(const float* o, const float* lse, int N, int D, int64_
                 }
             }
         }
-        float mb = m;
+        float mb = st.m;
 #pragma unroll
         for (int k = 0; k < kCombBatch; ++k) mb = fmaxf(mb, l[k]);
-        const float sc = merge_weight(m, mb);  // rescale of the running state
-        W *= sc;
-        acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+        const float sc = merge_weight(st.m, mb);  // rescale of the running state
+        st.W *= sc;
+        st.acc.x *= sc; st.acc.y *= sc; st.acc.z *= sc; st.acc.w *= sc;
 #pragma unroll
         for (int k = 0; k < kCombBatch; ++k) {
             const float wk = merge_weight(l[k], mb);
             if (wk > 0.f) {  // a zero-weight state is not read into the result
-                W += wk;
-                acc.x = fmaf(wk, x[k].x, acc.x); acc.y = fmaf(wk, x[k].y, acc.y);
-                acc.z = fmaf(wk, x[k].z, acc.z); acc.w = fmaf(wk, x[k].w, acc.w);
+                st.W += wk;
+                st.acc.x = fmaf(wk, x[k].x, st.acc.x); st.acc.y = fmaf(wk, x[k].y, st.acc.y);
+                st.acc.z = fmaf(wk, x[k].z, st.acc.z); st.acc.w = fmaf(wk, x[k].w, st.acc.w);
             }
         }
-        m = mb;
+        st.m = mb;
     }
-    __syncthreads();  // the shared buffers may still be read from a previous merge
-    if (lane == 0) {
-        sm.wm[w] = m;
-        sm.wW[w] = W;
-    }
-    if (has) *reinterpret_cast<float4*>(&sm.wacc[w][4 * lane]) = acc;
-    __syncthreads();
-    float M = sm.wm[0];
-#pragma unroll
-    for (int i = 1; i < kCombWarps; ++i) M = fmaxf(M, sm.wm[i]);
-    float WW = 0.f;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < kCombWarps; ++i) {
-        const float sc = merge_weight(sm.wm[i], M);
-        WW = fmaf(sc, sm.wW[i], WW);
-        if (has) {
-            const float4 t = *reinterpret_cast<const float4*>(&sm.wacc[i][4 * lane]);
-            a.x = fmaf(sc, t.x, a.x); a.y = fmaf(sc, t.y, a.y);
-            a.z = fmaf(sc, t.z, a.z); a.w = fmaf(sc, t.w, a.w);
-        }
-    }
-    const float inv = WW > 0.f ? 1.f / WW : 0.f;
-    v[0] = a.x * inv; v[1] = a.y * inv; v[2] = a.z * inv; v[3] = a.w * inv;
-    s_out = M + log2f(WW);  // -inf when every state is empty
+    return st;
 }
 
-template <typename Tout>
+struct CombSmem {
+    float wm[kCombWarps], wW[kCombWarps];
+    __align__(16) float wacc[kCombWarps][kD];
+};
+
+// Merged state of `row` over N states: v (this lane's 4 dims) and s.  With
+// WPR > 1 every thread of the CTA must call this (block barriers).
+template <int WPR>
+SKV_DEVINL void merge_row(const float* o, const float* lse, int N, int D, int64_t row, int sub,
+                          CombSmem& sm, float (&v)[4], float& s_out) {
+    WarpState st = warp_merge<WPR>(o, lse, N, D, row, sub);
+    if constexpr (WPR > 1) {
+        const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        __syncthreads();  // the buffers may still be read from a previous merge
+        if (lane == 0) {
+            sm.wm[w] = st.m;
+            sm.wW[w] = st.W;
+        }
+        if (4 * lane < D) *reinterpret_cast<float4*>(&sm.wacc[w][4 * lane]) = st.acc;
+        __syncthreads();
+        float M = sm.wm[0];
+#pragma unroll
+        for (int i = 1; i < WPR; ++i) M = fmaxf(M, sm.wm[i]);
+        float WW = 0.f;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < WPR; ++i) {
+            const float sc = merge_weight(sm.wm[i], M);
+            WW = fmaf(sc, sm.wW[i], WW);
+            if (4 * lane < D) {
+                const float4 t = *reinterpret_cast<const float4*>(&sm.wacc[i][4 * lane]);
+                a.x = fmaf(sc, t.x, a.x); a.y = fmaf(sc, t.y, a.y);
+                a.z = fmaf(sc, t.z, a.z); a.w = fmaf(sc, t.w, a.w);
+            }
+        }
+        st.m = M;
+        st.W = WW;
+        st.acc = a;
+    }
+    const float inv = st.W > 0.f ? 1.f / st.W : 0.f;
+    v[0] = st.acc.x * inv; v[1] = st.acc.y * inv; v[2] = st.acc.z * inv; v[3] = st.acc.w * inv;
+    s_out = st.m + log2f(st.W);  // -inf when every state is empty
+}
+
+template <typename Tout, int WPR>
 __global__ void __launch_bounds__(kCombWarps * 32)
 combine_kernel(const CombineParams p) {
     pdl_wait_primary();  // the states are written by the preceding grids
     __shared__ CombSmem sm;
-    __shared__ __align__(16) float fin[kD];
-    const int64_t row = blockIdx.x;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kRowsPerCta = kCombWarps / WPR;
+    const int64_t row_raw = (int64_t)blockIdx.x * kRowsPerCta + w / WPR;
+    const bool row_ok = row_raw < p.rows;
+    const int64_t row = row_ok ? row_raw : p.rows - 1;  // keep every warp on the barriers
+    const int sub = w % WPR;
     const bool has = 4 * lane < p.D;
-    float vs[4], ss;
-    merge_row(p.o_part, p.lse_part, p.NS, p.D, row, sm, vs, ss);
-    float vd[4] = {vs[0], vs[1], vs[2], vs[3]};
-    float sd = ss;
+    float vd[4], sd;
+    merge_row<WPR>(p.o_part, p.lse_part, p.NS, p.D, row, sub, sm, vd, sd);
     if (p.pre_part != nullptr) {
-        float vp[4], sp = -INFINITY;
-        if (p.C > 0) {
-            merge_row(p.pre_part, p.pre_lse, p.C, p.D, row, sm, vp, sp);
-        } else {
-            vp[0] = vp[1] = vp[2] = vp[3] = 0.f;  // empty prefix
-        }
-        if (w == 0) {
+        float vp[4] = {0.f, 0.f, 0.f, 0.f}, sp = -INFINITY;  // empty prefix when C == 0
+        if (p.C > 0) merge_row<WPR>(p.pre_part, p.pre_lse, p.C, p.D, row, sub, sm, vp, sp);
+        if (sub == 0 && row_ok) {
             if (p.o_pre != nullptr && has)
                 *reinterpret_cast<float4*>(p.o_pre + row * p.D + 4 * lane) =
                     make_float4(vp[0], vp[1], vp[2], vp[3]);
@@ -555,18 +572,23 @@ combine_kernel(const CombineParams p) {
         }
         sd = mm + log2f(ws);
     }
-    if (w == 0) {
-        if (has) *reinterpret_cast<float4*>(&fin[4 * lane]) = make_float4(vd[0], vd[1], vd[2], vd[3]);
-        if (lane == 0 && p.lse_out != nullptr) p.lse_out[row] = sd;
-    }
-    __syncthreads();
+    if (sub != 0 || !row_ok) return;
+    if (lane == 0 && p.lse_out != nullptr) p.lse_out[row] = sd;
+    // Lane l holds dims [4l, 4l + 4): write them in the output dtype.
     constexpr int EO = Vec<Tout>::N;
-    if ((int)threadIdx.x < p.D / EO) {
-        float f[EO];
-#pragma unroll
-        for (int e = 0; e < EO; ++e) f[e] = fin[threadIdx.x * EO + e];
-        char* orow = reinterpret_cast<char*>(p.out) + row * p.D * (int64_t)sizeof(Tout);
-        st_stream(orow + threadIdx.x * 16, from_float<Tout>(f));
+    char* orow = reinterpret_cast<char*>(p.out) + row * p.D * (int64_t)sizeof(Tout);
+    if constexpr (EO == 4) {
+        if (has) *reinterpret_cast<float4*>(orow + lane * 16) = make_float4(vd[0], vd[1], vd[2], vd[3]);
+    } else {
+        // Two lanes form one 16-byte chunk of 8 elements.
+        float f[8];
+        const float o0 = __shfl_down_sync(0xffffffffu, vd[0], 1);
+        const float o1 = __shfl_down_sync(0xffffffffu, vd[1], 1);
+        const float o2 = __shfl_down_sync(0xffffffffu, vd[2], 1);
+        const float o3 = __shfl_down_sync(0xffffffffu, vd[3], 1);
+        f[0] = vd[0]; f[1] = vd[1]; f[2] = vd[2]; f[3] = vd[3];
+        f[4] = o0; f[5] = o1; f[6] = o2; f[7] = o3;
+        if ((lane & 1) == 0 && 4 * lane < p.D) st_stream(orow + lane * 8, from_float<Tout>(f));
     }
 }
 
@@ -608,7 +630,6 @@ cudaError_t launch_splitkv_decode(const DecodeArgs& a, const DeviceInfo& dev, cu
 namespace skv {
 
 cudaError_t launch_combine(const CombineArgs& a, bool pdl, const DeviceInfo& dev, cudaStream_t st) {
-    (void)dev;
     if (a.D > kD || a.D % 8 != 0) return cudaErrorInvalidValue;
     CombineParams p;
     p.o_part = a.o_part;
@@ -622,8 +643,11 @@ cudaError_t launch_combine(const CombineArgs& a, bool pdl, const DeviceInfo& dev
     p.NS = a.NS;
     p.C = a.C;
     p.D = (int)a.D;
+    p.rows = a.rows;
+    // Many rows: one warp per row (4 rows per CTA).  Few rows: 4 warps per row.
+    const bool wide = a.rows >= 2LL * dev.sm_count * 4;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.rows, 1, 1);
+    cfg.gridDim = dim3((unsigned)(wide ? (a.rows + kCombWarps - 1) / kCombWarps : a.rows), 1, 1);
     cfg.blockDim = dim3(kCombWarps * 32, 1, 1);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -631,11 +655,15 @@ cudaError_t launch_combine(const CombineArgs& a, bool pdl, const DeviceInfo& dev
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+#define SKV_COMB(T_) \
+    (wide ? cudaLaunchKernelEx(&cfg, combine_kernel<T_, 1>, p) \
+          : cudaLaunchKernelEx(&cfg, combine_kernel<T_, kCombWarps>, p))
     switch (a.out_dt) {
-        case SKV_F32: return cudaLaunchKernelEx(&cfg, combine_kernel<float>, p);
-        case SKV_F16: return cudaLaunchKernelEx(&cfg, combine_kernel<__half>, p);
-        case SKV_BF16: return cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, p);
+        case SKV_F32: return SKV_COMB(float);
+        case SKV_F16: return SKV_COMB(__half);
+        case SKV_BF16: return SKV_COMB(__nv_bfloat16);
     }
+#undef SKV_COMB
     return cudaErrorInvalidValue;
 }
 
