@@ -10,6 +10,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include <stdlib.h>
 #include "split_range.h"
 
 namespace skv {
@@ -178,6 +179,13 @@ skv_status skv_splitkv_decode_plan(int32_t B, const int32_t* ctx_host, int32_t H
     return SKV_OK;
 }
 
+// Pass 1 runs on CUDA cores unless SKV_DECODE_TC=1 selects the tensor-core
+// kernel (decode_tc.cu), which is still being tuned for these shapes.
+static bool use_tc_decode() {
+    const char* v = getenv("SKV_DECODE_TC");
+    return v != nullptr && v[0] == '1';
+}
+
 skv_status skv_splitkv_decode(const void* q, const void* k_cache, const void* v_cache,
                               int32_t num_pool_pages, const int32_t* block_table,
                               int32_t max_pages, const int32_t* ctx, int32_t B, int32_t Hq,
@@ -226,7 +234,8 @@ skv_status skv_splitkv_decode(const void* q, const void* k_cache, const void* v_
     a.o_part = o_part;
     a.lse_part = lse_part;
     a.ranges_dbg = ranges_dbg;
-    cudaError_t e = launch_splitkv_decode(a, *dev, cs);
+    cudaError_t e = use_tc_decode() ? launch_splitkv_decode_tc(a, *dev, cs)
+                                    : launch_splitkv_decode(a, *dev, cs);
     if (e != cudaSuccess) return SKV_ERR_CUDA;
     if (out != nullptr) {
         CombineArgs c = {};
@@ -345,7 +354,9 @@ skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_
     a.o_part = o_part;
     a.lse_part = lse_part;
     a.ranges_dbg = nullptr;
-    if (launch_splitkv_decode(a, *dev, cs) != cudaSuccess) return SKV_ERR_CUDA;
+    if ((use_tc_decode() ? launch_splitkv_decode_tc(a, *dev, cs) : launch_splitkv_decode(a, *dev, cs)) !=
+        cudaSuccess)
+        return SKV_ERR_CUDA;
     // 3. Prefix chunks -> prefix state; merge_state(prefix, suffix) -> out.
     CombineArgs c = {};
     c.o_part = o_part;

@@ -84,22 +84,6 @@ size_t prefix_smem_bytes(int blocks_per_chunk) {
     return 1024 + kSmemIds + (size_t)blocks_per_chunk * kPagesPerBlock * sizeof(int);
 }
 
-// Bounded wait that also gives up as soon as another role has aborted.
-SKV_DEVINL bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                              unsigned long long* err, int where) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            record_error(err, SKV_ERR_TIMEOUT, where);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
 cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const PrefixParams p) {

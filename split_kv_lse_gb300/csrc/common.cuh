@@ -188,6 +188,18 @@ SKV_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
     return ok != 0;
 }
+// As mbar_try_wait, but the thread may be suspended until the phase
+// completes (at most about 20 us), so a waiting warp does not take issue
+// slots from the warps doing the work.
+SKV_DEVINL bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity), "r"(20000u) : "memory");
+    return ok != 0;
+}
 SKV_DEVINL uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -206,6 +218,41 @@ SKV_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned long long* er
             return false;
         }
     }
+}
+// Bounded wait that records nothing: used after an abort, to let copies
+// still in flight land before the CTA ends.
+SKV_DEVINL bool mbar_wait_quiet(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+// Bounded wait that also gives up as soon as another role of the CTA has
+// raised the shared abort flag; a wait that runs out raises it.
+SKV_DEVINL bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                              unsigned long long* err, int where) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            record_error(err, SKV_ERR_TIMEOUT, where);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+// 16-byte asynchronous global -> shared copy (cp.async, bypassing L1), and
+// an arrive on `bar` once every cp.async of this thread so far has landed
+// (the barrier's pending count is raised first, so its expected count is
+// unchanged).
+SKV_DEVINL void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+SKV_DEVINL void cp_async_mbar_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" :: "r"(smem_addr(bar)) : "memory");
 }
 // One contiguous global -> shared copy on the TMA engine, completion counted
 // in bytes on `bar`.  dst, src 16-byte aligned, bytes a multiple of 16.

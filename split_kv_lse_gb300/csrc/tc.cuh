@@ -49,13 +49,27 @@ SKV_DEVINL uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo
     return d;
 }
 
+// Descriptor of an operand without swizzle (K-major core matrices of 8 rows
+// x 16 bytes): LBO = distance between core matrices along K, SBO = along
+// M/N.  Used only for a constant operand whose every element is equal, so
+// the reads stay inside a region of (M/8) * SBO bytes.
+SKV_DEVINL uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
 // Instruction descriptor for kind::f16: fp16 A and B, fp32 accumulator,
-// M x N tile, A K-major, B K-major (b_mn_major = false) or MN-major.
+// M x N tile, A and B each K-major or MN-major.
 //   bits 4-5 D format (1 = f32), 7-9 A format (0 = f16), 10-12 B format,
 //   15 A major, 16 B major (1 = MN), 17-22 N >> 3, 24-28 M >> 4.
-SKV_DEVINL constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major) {
-    return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
+SKV_DEVINL constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major,
+                                             bool a_mn_major = false) {
+    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // ---------------------------------------------------------------- MMA
@@ -138,6 +152,35 @@ SKV_DEVINL void tmem_st32(uint32_t taddr, const float (&v)[32]) {
         : "memory");
 }
 
+// 16 consecutive 32-bit columns of this thread's lane (load + wait; store +
+// wait).
+SKV_DEVINL void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+SKV_DEVINL void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
+        "tcgen05.wait::st.sync.aligned;"
+        :: "r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
+           "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])),
+           "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+           "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+           "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+           "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+        : "memory");
+}
 
 // The 128 consecutive 32-bit columns of this thread's lane in one load (and
 // its wait), as used for a whole S or O row.
