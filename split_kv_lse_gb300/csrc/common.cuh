@@ -208,16 +208,20 @@ SKV_DEVINL uint64_t globaltimer_ns() {
 // Bounded wait: gives up after `limit_ns` of wall time, records
 // SKV_ERR_TIMEOUT with `where` as detail and returns false.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-SKV_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned long long* err, int where) {
-    if (mbar_try_wait(bar, parity)) return true;
-    uint64_t t0 = globaltimer_ns();
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
+                                                    unsigned long long* err, int where) {
+    const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity)) return true;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             record_error(err, SKV_ERR_TIMEOUT, where);
             return false;
         }
     }
+}
+SKV_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned long long* err, int where) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, err, where);
 }
 // Bounded wait that records nothing: used after an abort, to let copies
 // still in flight land before the CTA ends.
@@ -228,10 +232,13 @@ SKV_DEVINL bool mbar_wait_quiet(uint64_t* bar, uint32_t parity) {
     return true;
 }
 // Bounded wait that also gives up as soon as another role of the CTA has
-// raised the shared abort flag; a wait that runs out raises it.
-SKV_DEVINL bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                              unsigned long long* err, int where) {
-    if (mbar_try_wait(bar, parity)) return true;
+// raised the shared abort flag; a wait that runs out raises it.  The first
+// poll is inline; the loop is a call, so the many wait sites of a
+// warp-specialised kernel add little code (its warps run different code
+// and share the instruction cache).
+static __device__ __noinline__ bool wait_or_abort_slow(uint64_t* bar, uint32_t parity,
+                                                 volatile int* abort_flag,
+                                                 unsigned long long* err, int where) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity)) return true;
@@ -242,6 +249,11 @@ SKV_DEVINL bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abor
             return false;
         }
     }
+}
+SKV_DEVINL bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                              unsigned long long* err, int where) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_or_abort_slow(bar, parity, abort_flag, err, where);
 }
 // 16-byte asynchronous global -> shared copy (cp.async, bypassing L1), and
 // an arrive on `bar` once every cp.async of this thread so far has landed

@@ -34,15 +34,16 @@
 // exceeds it by more than 8 (log2 units), then rescales O in TMEM and the
 // sums; p <= 2^8 stays in range for fp16.
 //
-// Persistent CTAs (one per SM): CTA c takes units c, c + grid, ...  Twelve
+// Persistent CTAs (one per SM): CTA c takes units c, c + grid, ...  Fourteen
 // warps:
 //   0-3   softmax (one thread per key row)
 //   4-7   epilogue: per group, o = O / L (thread i <-> dim i <-> TMEM lane i)
 //         and s = m + log2 L, written to the split states
 //   8     issues the S MMAs, 9 issues the PV MMAs
-//   10-11 producers: both walk the same deterministic packing of this CTA's
-//         units into tiles; warp 10 fills the even tiles, warp 11 the odd
-//         ones (q rows by cp.async, K and V as 16 x 64 boxes with the
+//   10-13 producers: all four walk the same deterministic packing of this
+//         CTA's units into tiles; warps 10 and 11 load the K halves, q rows
+//         and descriptors of the even and odd tiles, warps 12 and 13 their V
+//         halves (q rows by cp.async, K and V as 16 x 64 boxes with the
 //         128-byte swizzle, one box per lane)
 // Copies, MMAs and TMEM loads issued one after another by a single thread
 // cannot keep up with HBM, so each of these jobs has its own warp.  Three
@@ -81,8 +82,9 @@ constexpr int kSoftmaxWarps = 4;
 constexpr int kEpiWarp0 = 4;
 constexpr int kQkWarp = 8;
 constexpr int kPvWarp = 9;
-constexpr int kProdWarp0 = 10;
-constexpr int kThreads = 12 * 32;
+constexpr int kProdWarp0 = 10;                    // 10, 11: K + q; 12, 13: V
+constexpr int kProdWarps = 4;
+constexpr int kThreads = 14 * 32;
 constexpr uint32_t kTmemCols = 64;  // S [0,16) [16,32); O [32,48) [48,64)
 constexpr float kRescaleThreshold = 8.f;
 constexpr unsigned kFull = 0xffffffffu;
@@ -134,13 +136,13 @@ constexpr size_t kSmStages = 0;
 constexpr size_t kSmP = kSmStages + (size_t)kStages * kStageBytes;
 constexpr size_t kSmDesc = kSmP + 2 * kPTile;
 constexpr size_t kSmScratch = kSmDesc + kDescs * sizeof(TileDesc);       // one per producer
-constexpr size_t kSmInfo = kSmScratch + 2 * sizeof(TileDesc);
+constexpr size_t kSmInfo = kSmScratch + kProdWarps * sizeof(TileDesc);
 constexpr size_t kSmRed = kSmInfo + 2 * sizeof(GroupInfo);              // [2][8 pages][8] floats
 constexpr size_t kSmBars = kSmRed + 2 * kTilePages * 8 * sizeof(float);
-// k_full[3], v_full[3], k_empty[3], v_empty[3], desc_full[6], s_full[2],
-// s_free[2], p_full[2], pv_done[2], o_full[2], o_free[2], epi_ready[2], red,
-// mma_done[2]
-constexpr int kNumBars = 4 * kStages + kDescs + 17;
+// k_full[3], v_full[3], k_empty[3], v_empty[3], desc_full[6], desc_free[6],
+// s_full[2], s_free[2], p_full[2], pv_done[2], o_full[2], o_free[2],
+// epi_ready[2], red, mma_done[2]
+constexpr int kNumBars = 4 * kStages + 2 * kDescs + 17;
 constexpr size_t kSmMisc = kSmBars + kNumBars * sizeof(uint64_t);  // tmem address, abort flag
 constexpr size_t kSmemBytes = 1024 + kSmMisc + 16;
 
@@ -173,7 +175,8 @@ splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
     // early), a descriptor slot cannot (it is reused only after the PV of its
     // previous tile has been issued).
     uint64_t* desc_full = bars + 4 * kStages;
-    uint64_t* s_full = desc_full + kDescs;
+    uint64_t* desc_free = desc_full + kDescs;  // the PV issuer is done with the slot's descriptor
+    uint64_t* s_full = desc_free + kDescs;
     uint64_t* s_free = s_full + 2;
     uint64_t* p_full = s_free + 2;
     uint64_t* pv_done = p_full + 2;
@@ -197,7 +200,10 @@ splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
             mbar_init(&k_empty[s], 1);
             mbar_init(&v_empty[s], 1);
         }
-        for (int i = 0; i < kDescs; ++i) mbar_init(&desc_full[i], 1);
+        for (int i = 0; i < kDescs; ++i) {
+            mbar_init(&desc_full[i], 1);
+            mbar_init(&desc_free[i], 1);
+        }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
             mbar_init(&s_free[b], kSoftmaxWarps);
@@ -221,6 +227,8 @@ splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
     if (warp >= kProdWarp0) {
         // ------------------------------------------------------------ producers
         const int pw = warp - kProdWarp0;
+        const int par = pw & 1;        // this warp's tiles: tile & 1 == par
+        const bool kprod = pw < 2;     // K half, q rows and descriptor; else the V half
         TileDesc* scratch = reinterpret_cast<TileDesc*>(sm + kSmScratch) + pw;
         if (lane == 0) {
             tma_prefetch_desc(&tk);
@@ -238,7 +246,7 @@ splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
         // Lane l holds unit kb + l of this CTA's list (u = blockIdx.x + k *
         // gridDim.x) and, for a unit of at most 8 pages, the TMA rows of its
         // pages: one round of loads serves 32 units.
-        int kb = 0, bu = -1, bb = 0, bhkv = 0, bp0 = 0, bnp = 0, bctx = 0;
+        int kb = 0, bu = -1, bb = 0, bhkv = 0, bsplit = 0, bp0 = 0, bnp = 0, bctx = 0;
         int brow[kTilePages];
         auto load_batch = [&]() {
             const long long uu = (long long)blockIdx.x + (long long)(kb + lane) * gridDim.x;
@@ -246,8 +254,8 @@ splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
             bnp = 0;
             if (uu < p.units) {
                 bu = (int)uu;
-                int split;
-                decode_unit(p, bu, &bb, &bhkv, &split);
+                decode_unit(p, bu, &bb, &bhkv, &bsplit);
+                const int split = bsplit;
                 int c = p.ctx[bb];
                 if (c < 0 || c > cap) {
                     if (split == 0 && bhkv == 0) record_error(p.err, SKV_ERR_INVALID_ARG, bb);
@@ -320,7 +328,7 @@ splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
                     const int c = __shfl_sync(kFull, bctx, ki);
                     const int b = __shfl_sync(kFull, bb, ki);
                     const int hkv = __shfl_sync(kFull, bhkv, ki);
-                    const int split = (u / p.Hkv) % p.NS;
+                    const int split = __shfl_sync(kFull, bsplit, ki);
                     if (np > kTilePages) {
                         if (nunits == 0) {  // start chunking it
                             lu = u;
@@ -365,8 +373,25 @@ splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
                 if (lnext == lnp) lu = -1;
             }
             const int kind = nunits > 0 ? kTileWork : kTileEnd;
-            if ((tile & 1) != pw) {  // the other producer's tile
+            if ((tile & 1) != par) {  // another pair's tile
                 if (kind == kTileEnd) break;
+                continue;
+            }
+            const int s = tile % kStages;
+            const uint32_t ph_prev = (uint32_t)((tile / kStages - 1) & 1);
+            const int bk = lane >> 1, bh = lane & 1;  // one box per lane: page bk, half bh of the head dim
+            const int rk = __shfl_sync(kFull, my_row, bk & 7);
+            uint8_t* stg = stages + (size_t)s * kStageBytes;
+            if (!kprod) {
+                // ---- the V half, once PV three tiles back is done
+                if (kind == kTileEnd) break;
+                if (tile >= kStages) ok = wait_or_abort(&v_empty[s], ph_prev, abort_flag, p.err, 41);
+                if (!__all_sync(kFull, ok)) break;
+                if (lane == 0) mbar_arrive_expect_tx(&v_full[s], (uint32_t)(npages * kPageBytes / 2));
+                __syncwarp();
+                if (bk < npages)
+                    tma_load_2d(stg + kKVTile + bh * kKVHalf + bk * 2048, &tv, bh * 64, rk, &v_full[s], pol);
+                last_vfill[s] = tile;
                 continue;
             }
             if (lane == 0) {
@@ -377,12 +402,12 @@ splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
                 scratch->partial_mask = (int32_t)partial;
             }
             __syncwarp();
-            // ---- claim the stage's K half.  The descriptor slot of this
-            // tile was last used by tile - 6, whose PV this warp saw done
-            // (V half of tile - 4, its own previous tile) before it got here.
-            const int s = tile % kStages;
-            const uint32_t ph_prev = (uint32_t)((tile / kStages - 1) & 1);
+            // ---- the K half (free once S three tiles back is computed) and
+            // the descriptor slot (free once the PV issuer is done with tile - 6)
             if (tile >= kStages) ok = wait_or_abort(&k_empty[s], ph_prev, abort_flag, p.err, 40);
+            if (ok && tile >= kDescs)
+                ok = wait_or_abort(&desc_free[tile % kDescs], (uint32_t)((tile / kDescs - 1) & 1),
+                                   abort_flag, p.err, 39);
             if (!__all_sync(kFull, ok)) break;
             TileDesc* d = descs + tile % kDescs;
             if (lane < (int)(sizeof(TileDesc) / 16))
@@ -393,7 +418,6 @@ splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
                 if (lane == 0) mbar_arrive(&k_full[s]);
                 break;
             }
-            uint8_t* stg = stages + (size_t)s * kStageBytes;
             // q rows of the slots by cp.async, completion tracked on the stage's
             // barrier: row slot * G + g of Q^T, 16-byte chunk c at its
             // 128-byte-swizzle position (chunk c of a row sits at c ^ (row & 7)).
@@ -408,19 +432,8 @@ splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
             __syncwarp();
             if (lane == 0) mbar_arrive_expect_tx(&k_full[s], (uint32_t)(npages * kPageBytes / 2));
             __syncwarp();
-            // One box per lane: lane 2k + h is page k, half h of the head dim.
-            const int bk = lane >> 1, bh = lane & 1;
-            const int rk = __shfl_sync(kFull, my_row, bk & 7);
             if (bk < npages) tma_load_2d(stg + bh * kKVHalf + bk * 2048, &tk, bh * 64, rk, &k_full[s], pol);
             last_fill[s] = tile;
-            // ---- the V half, once PV three tiles back is done
-            if (tile >= kStages) ok = wait_or_abort(&v_empty[s], ph_prev, abort_flag, p.err, 41);
-            if (!__all_sync(kFull, ok)) break;
-            if (lane == 0) mbar_arrive_expect_tx(&v_full[s], (uint32_t)(npages * kPageBytes / 2));
-            __syncwarp();
-            if (bk < npages)
-                tma_load_2d(stg + kKVTile + bh * kKVHalf + bk * 2048, &tv, bh * 64, rk, &v_full[s], pol);
-            last_vfill[s] = tile;
         }
         // After an abort, copies still in flight land before the CTA ends
         // (without an abort every fill has been consumed, so has completed).
@@ -511,6 +524,7 @@ splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
                 tc::mma_commit(&v_empty[s]);
                 tc::mma_commit(&pv_done[pb]);
                 if (fl & kLast) tc::mma_commit(&o_full[ob]);
+                mbar_arrive(&desc_free[i % kDescs]);  // descriptor no longer read
             }
             __syncwarp();
         }
@@ -741,8 +755,8 @@ splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
                 for (int g = 0; g < G; ++g) {
                     const int c = j * G + g;
                     const int64_t row = (int64_t)(qr + g) * p.NS + split;
-                    p.o_part[row * kD + e] = L[c] > 0.f ? ov[c] * __frcp_rn(L[c]) : 0.f;
-                    if (e == c) p.lse_part[row] = L[c] > 0.f ? gi.m[c] + log2f(L[c]) : -INFINITY;
+                    p.o_part[row * kD + e] = L[c] > 0.f ? __fdividef(ov[c], L[c]) : 0.f;
+                    if (e == c) p.lse_part[row] = L[c] > 0.f ? gi.m[c] + __log2f(L[c]) : -INFINITY;
                 }
             }
             tc::fence_before_sync();
@@ -801,7 +815,11 @@ cudaError_t launch_splitkv_decode_tc(const DecodeArgs& a, const DeviceInfo& dev,
     if (units <= 0 || units > INT32_MAX) return cudaErrorInvalidValue;
     p.units = (int32_t)units;
     p.scale_log2 = a.sm_scale * 1.4426950408889634f;
-    const int grid = (int)(units < dev.sm_count ? units : dev.sm_count);
+    // As few CTAs as give every CTA the same number of units (at most one
+    // per SM): 512 equal units run as 128 CTAs x 4 rather than 152 CTAs of
+    // which 56 take a fourth unit while the rest of the GPU idles.
+    const int64_t per_cta = (units + dev.sm_count - 1) / dev.sm_count;
+    const int grid = (int)((units + per_cta - 1) / per_cta);
     switch (a.Hq / a.Hkv) {
         case 1: return launch_tc_g<1>(tk, tv, p, grid, dev, st);
         case 2: return launch_tc_g<2>(tk, tv, p, grid, dev, st);
