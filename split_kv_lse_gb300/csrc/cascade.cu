@@ -157,39 +157,45 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
             tma_prefetch_desc(&tq);
             tma_prefetch_desc(&tk);
             tma_prefetch_desc(&tv);
-            const uint64_t pol = policy_evict_first();
-            auto load_block = [&](int j, bool is_v) {
-                const int stage = j % kStages;
-                uint64_t* bar = is_v ? &v_full[stage] : &k_full[stage];
-                uint8_t* dst = (is_v ? Vs : Ks) + stage * kTile;
-                const CUtensorMap* map = is_v ? &tv : &tk;
-                mbar_arrive_expect_tx(bar, kTile);
-#pragma unroll 1
-                for (int pg = 0; pg < kPagesPerBlock; ++pg) {
-                    const int pid = ids[j * kPagesPerBlock + pg];
-                    // A page past the prefix is read from the row just past
-                    // the tensor: the TMA fills the whole box with zeros.
-                    const int row = pid >= 0 ? (pid * p.Hkv + hkv) * kPage : p.pool_rows;
-                    tma_load_2d(dst + pg * (kPage * 128), map, 0, row, bar, pol);
-                    tma_load_2d(dst + kHalf + pg * (kPage * 128), map, 64, row, bar, pol);
-                }
-            };
+        }
+        const uint64_t pol = policy_evict_first();
+        // A block's 16 boxes (8 pages x 2 halves of the head dim) go out from
+        // 16 lanes at once: copies issued one after another by one thread
+        // stream at about half the HBM bandwidth.
+        auto load_block = [&](int j, bool is_v) {
+            const int stage = j % kStages;
+            uint64_t* bar = is_v ? &v_full[stage] : &k_full[stage];
+            uint8_t* dst = (is_v ? Vs : Ks) + stage * kTile;
+            const CUtensorMap* map = is_v ? &tv : &tk;
+            if (lane == 0) mbar_arrive_expect_tx(bar, kTile);
+            __syncwarp();
+            const int pg = lane >> 1, h = lane & 1;
+            if (pg < kPagesPerBlock) {
+                const int pid = ids[j * kPagesPerBlock + pg];
+                // A page past the prefix is read from the row just past the
+                // tensor: the TMA fills the whole box with zeros.
+                const int row = pid >= 0 ? (pid * p.Hkv + hkv) * kPage : p.pool_rows;
+                tma_load_2d(dst + h * kHalf + pg * (kPage * 128), map, h * 64, row, bar, pol);
+            }
+        };
+        if (lane == 0) {
             mbar_arrive_expect_tx(q_full, kTile);
             const int z = mtile * (kM / p.G);
             tma_load_3d(Qs, &tq, 0, hkv * p.G, z, q_full);
             tma_load_3d(Qs + kHalf, &tq, 64, hkv * p.G, z, q_full);
-            for (int j = 0; j < nb; ++j) {
-                if (j >= kStages &&
-                    !wait_or_abort(&k_empty[j % kStages], (uint32_t)((j / kStages - 1) & 1),
-                                   abort_flag, p.err, 20))
-                    break;
-                load_block(j, false);
-                if (j >= kStages &&
-                    !wait_or_abort(&v_empty[j % kStages], (uint32_t)((j / kStages - 1) & 1),
-                                   abort_flag, p.err, 21))
-                    break;
-                load_block(j, true);
-            }
+        }
+        for (int j = 0; j < nb; ++j) {
+            bool ok = true;
+            if (j >= kStages)
+                ok = wait_or_abort(&k_empty[j % kStages], (uint32_t)((j / kStages - 1) & 1), abort_flag,
+                                   p.err, 20);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            load_block(j, false);
+            if (j >= kStages)
+                ok = wait_or_abort(&v_empty[j % kStages], (uint32_t)((j / kStages - 1) & 1), abort_flag,
+                                   p.err, 21);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            load_block(j, true);
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
