@@ -134,6 +134,46 @@ class Stage:
         self.times_ms = []
 
 
+# The kernel that dominates the step (largest share of the GPU time in the
+# ncu launch list): pass 1 of the split-KV decode on the cascade suffixes.
+DOMINANT_STAGE = "cascade_suffix_pass1"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dominant_kernel_traffic.json")
+
+
+def decode_kernel_name():
+    return "tensor_cores" if os.environ.get("SKV_DECODE_TC") == "1" else "cuda_cores"
+
+
+def kernel_sources_sha():
+    """Digest of every kernel source: a recorded ncu traffic figure only
+    stands while none of them has changed since the capture."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "split_kv_lse_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(path=TRAFFIC_FILE):
+    """(DRAM bytes per launch, profile summary) of the dominant kernel from
+    the committed ncu capture, or (None, why) when there is none for the
+    current sources."""
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None, "no recorded capture"
+    entry = rec.get(decode_kernel_name())
+    if not entry:
+        return None, "no capture of this kernel"
+    if entry.get("sources_sha") != kernel_sources_sha():
+        return None, "kernel sources changed since the capture"
+    return int(entry["dram_bytes_per_launch"]), entry.get("profile")
+
+
 def nbytes(t):
     return t.numel() * t.element_size()
 
@@ -141,7 +181,7 @@ def nbytes(t):
 STAGE_NAMES = ("merge_state", "merge_state_in_place", "merge_states", "splitkv_decode",
                "cascade_decode")
 # Diagnostic stages, selectable with --only (not part of the default step).
-EXTRA_STAGES = ("splitkv_decode_pass1",)
+EXTRA_STAGES = ("splitkv_decode_pass1", "cascade_suffix_pass1")
 
 
 def build_stages(torch, skv, W, dev, only=None):
@@ -160,8 +200,8 @@ def build_stages(torch, skv, W, dev, only=None):
         _merge_states_stage(torch, skv, W, dev, to_dev, stages, hostside)
     if want & {"splitkv_decode", "splitkv_decode_pass1"}:
         _decode_stage(torch, skv, W, dev, to_dev, stages, hostside, want)
-    if "cascade_decode" in want:
-        _cascade_stage(torch, skv, W, dev, to_dev, stages, hostside)
+    if want & {"cascade_decode", "cascade_suffix_pass1"}:
+        _cascade_stage(torch, skv, W, dev, to_dev, stages, hostside, want)
     return stages, hostside
 
 
@@ -227,7 +267,7 @@ def _decode_stage(torch, skv, W, dev, to_dev, stages, hostside, want):
     hostside["decode"] = d4
 
 
-def _cascade_stage(torch, skv, W, dev, to_dev, stages, hostside):
+def _cascade_stage(torch, skv, W, dev, to_dev, stages, hostside, want):
     # Cascade, B=64: shared 8192-token prefix on the tensor cores + suffixes.
     d5 = W.cascade_mixed()
     g5 = to_dev(d5)
@@ -246,12 +286,24 @@ def _cascade_stage(torch, skv, W, dev, to_dev, stages, hostside):
     npages = -(-d5["prefix_len"] // 16) + sum(-(-int(c) // 16) for c in d5["ctx"])
     cas_bytes = (kv_tokens * Hkv * D * 2 * 2 + nbytes(d5["q"]) + npages * 4 + nbytes(d5["ctx"]) +
                  nbytes(bufs["out"]) + nbytes(bufs["lse_out"]))
-    stages.append(Stage("cascade_decode",
-                        lambda: skv.cascade_decode(g5["q"], g5["k_cache"], g5["v_cache"],
-                                                   g5["prefix_pages"], d5["prefix_len"],
-                                                   g5["block_table"], g5["ctx"], ns,
-                                                   d5["sm_scale"], workspace=ws, **bufs),
-                        cas_bytes, 3))
+    if "cascade_decode" in want:
+        stages.append(Stage("cascade_decode",
+                            lambda: skv.cascade_decode(g5["q"], g5["k_cache"], g5["v_cache"],
+                                                       g5["prefix_pages"], d5["prefix_len"],
+                                                       g5["block_table"], g5["ctx"], ns,
+                                                       d5["sm_scale"], workspace=ws, **bufs),
+                            cas_bytes, 3))
+    if "cascade_suffix_pass1" in want:
+        # The kernel that dominates the step: pass 1 of the split-KV decode on
+        # the cascade's suffixes, launched exactly as cascade_decode launches it.
+        suf_bytes = (int(d5["ctx"].sum()) * Hkv * D * 2 * 2 + nbytes(d5["q"]) +
+                     sum(-(-int(c) // 16) for c in d5["ctx"]) * 4 + nbytes(d5["ctx"]))
+        stages.append(Stage("cascade_suffix_pass1",
+                            lambda: skv.splitkv_decode(g5["q"], g5["k_cache"], g5["v_cache"],
+                                                       g5["block_table"], g5["ctx"], ns,
+                                                       d5["sm_scale"], bufs["o_part"],
+                                                       bufs["lse_part"], combine=False),
+                            suf_bytes, 1))
     hostside["cascade"] = d5
 
 
@@ -387,6 +439,22 @@ def run_reference(args):
     return 0
 
 
+def max_over_ranks(x, dist, device):
+    """The slowest rank's time (replicas run the same workload; the job
+    finishes with the last one)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, step_bytes, step_ms):
+    """Whole-job throughput (GB/s): every replica moves step_bytes per step."""
+    return world * step_bytes / (step_ms * 1e-3) / 1e9
+
+
 def run_ours(args):
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -456,15 +524,33 @@ def run_ours(args):
     for evs in all_evs:
         for st, e0, e1 in evs:
             st.times_ms.append(e0.elapsed_time(e1))
-    step_ms = sum(statistics.mean(st.times_ms) for st in stages)
-    if dist is not None:
-        t = torch.tensor([step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(sum(statistics.mean(st.times_ms) for st in stages), dist, dev)
     step_bytes = sum(st.bytes for st in stages)
-    value = world * step_bytes / (step_ms * 1e-3) / 1e9
+    value = job_value(world, step_bytes, step_ms)
     launches = args.steps * sum(st.launches for st in stages)
     assert skv.get_device_error() == (0, 0), "device-side error during the benchmark"
+
+    # The dominant kernel alone, same launch, same flush between launches.
+    dom_rep = None
+    if only is None:
+        dstages, _ = build_stages(torch, skv, W, dev, [DOMINANT_STAGE])
+        dk = dstages[0]
+        for _ in range(3):
+            dk.fn()
+        evs = []
+        for _ in range(max(10, args.steps)):
+            flush.zero_()
+            flush_rd.sum()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dk.fn()
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+        dom_rep = (dk, ms)
+        assert skv.get_device_error() == (0, 0), "device-side error in the dominant kernel"
 
     peak, peak_kind = measured_peaks()
     stage_rep = {}
@@ -475,8 +561,24 @@ def run_ours(args):
                               "algo_bytes": st.bytes, "GB_s": round(gbs, 1),
                               "frac_of_measured_hbm": round(gbs / peak, 4),
                               "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4)}
-    dom = max(stages, key=lambda s: statistics.mean(s.times_ms))
-    dom_gbs = dom.bytes / (statistics.mean(dom.times_ms) * 1e-3) / 1e9
+    if dom_rep is not None:
+        dk, dms = dom_rep
+        traffic, traffic_src = recorded_traffic()
+        roofline = {"bound": "hbm",
+                    "kernel": f"splitkv_decode pass 1 ({decode_kernel_name()}) on the cascade "
+                              "suffixes: B=64 Hq=32 Hkv=8 D=128, 1..2048 tokens, NS=16",
+                    "achieved": round(dk.bytes / (dms * 1e-3) / 1e9, 1), "peak": None,
+                    "unit": "GB/s", "frac": None, "traffic": traffic,
+                    "traffic_source": traffic_src, "algo_bytes_per_launch": dk.bytes,
+                    "us_per_launch": round(dms * 1e3, 2)}
+    else:
+        dom = max(stages, key=lambda s: statistics.mean(s.times_ms))
+        roofline = {"bound": "hbm", "kernel": f"stage {dom.name}",
+                    "achieved": round(dom.bytes / (statistics.mean(dom.times_ms) * 1e-3) / 1e9, 1),
+                    "peak": None, "unit": "GB/s", "frac": None, "traffic": None}
+    roofline["peak"] = peak
+    roofline["peak_kind"] = peak_kind
+    roofline["frac"] = round(roofline["achieved"] / peak, 4)
 
     e2e = None
     if not args.no_e2e and only is None:
@@ -519,9 +621,7 @@ def run_ours(args):
                        "clock_window": f"{args.soak_s} s untimed soak of the same steps, then the timed region",
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "stages": stage_rep, "wall_s": round(wall, 3)},
-            "roofline": {"bound": "hbm", "kernel": dom.name, "achieved": round(dom_gbs, 1),
-                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": round(dom_gbs / peak, 4), "traffic": None},
+            "roofline": roofline,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
