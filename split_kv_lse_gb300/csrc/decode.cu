@@ -100,9 +100,16 @@ template <int G> struct Roles {
 
 constexpr int kBoxBytes = kPage * 128;  // one 16 x 64 fp16 K box (2 KB)
 
+// The barriers take R words, rounded up to 16 bytes: the p buffer after them
+// is read with 16-byte loads.
+template <int R>
+constexpr size_t bars_bytes() {
+    return ((size_t)R * sizeof(uint64_t) + 15) / 16 * 16;
+}
+
 template <int G, int W, int R>
 constexpr size_t smem_bytes() {
-    return 1024 /* alignment slack */ + (size_t)R * kStageBytes + (size_t)R * sizeof(uint64_t) +
+    return 1024 /* alignment slack */ + (size_t)R * kStageBytes + bars_bytes<R>() +
            (size_t)W * G * kPage * sizeof(uint16_t);
 }
 
@@ -121,7 +128,7 @@ splitkv_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const DecodePa
     // space and turn every K/V read into a generic load).
     uint8_t* ring = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring + R * kStageBytes);
-    uint16_t* ps_all = reinterpret_cast<uint16_t*>(bars + R);
+    uint16_t* ps_all = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(bars) + bars_bytes<R>());
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
@@ -391,20 +398,11 @@ splitkv_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const DecodePa
     }
 }
 
-#ifndef SKV_DECODE_WARPS
-#define SKV_DECODE_WARPS 3
-#endif
-#ifndef SKV_DECODE_RING
-#define SKV_DECODE_RING 6
-#endif
-constexpr int kWarps = SKV_DECODE_WARPS;
-constexpr int kRing = SKV_DECODE_RING;
-
-template <int G>
-cudaError_t launch_g(const CUtensorMap& tk, const DecodeParams& p, int B, int Hkv, int NS,
-                     cudaStream_t st) {
-    constexpr size_t smem = smem_bytes<G, kWarps, kRing>();
-    auto kern = splitkv_decode_kernel<G, kWarps, kRing>;
+template <int G, int W, int R>
+cudaError_t launch_gwr(const CUtensorMap& tk, const DecodeParams& p, int B, int Hkv, int NS,
+                       cudaStream_t st) {
+    constexpr size_t smem = smem_bytes<G, W, R>();
+    auto kern = splitkv_decode_kernel<G, W, R>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -413,8 +411,25 @@ cudaError_t launch_g(const CUtensorMap& tk, const DecodeParams& p, int B, int Hk
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    kern<<<dim3(NS, Hkv, B), kWarps * 32, smem, st>>>(tk, p);
+    kern<<<dim3(NS, Hkv, B), W * 32, smem, st>>>(tk, p);
     return cudaGetLastError();
+}
+
+// Warps per CTA follow the longest possible split (the page table's width
+// over NUM_SPLITS): a CTA of 3 warps with a 6-page ring for long splits; for
+// short splits smaller CTAs, so that many more of them are resident per SM
+// and their fixed latencies (q, page table, first copies) overlap.
+template <int G>
+cudaError_t launch_g(const CUtensorMap& tk, const DecodeParams& p, int B, int Hkv, int NS,
+                     int max_pages, cudaStream_t st) {
+    // Measured on the cascade suffixes (<= 8 pages per split, B=64, NS=16):
+    // pass 1 takes 53 us with 1 warp and a 2-page ring (about 13 CTAs per
+    // SM), 64 us with 2 warps, 72 us with 3; a 4-page ring for the 1-warp
+    // CTA (fewer CTAs per SM) takes 74 us.  Long splits (32 pages) keep 3.
+    const int pps = (max_pages + NS - 1) / NS;
+    if (pps <= 8) return launch_gwr<G, 1, 2>(tk, p, B, Hkv, NS, st);
+    if (pps <= 16) return launch_gwr<G, 2, 4>(tk, p, B, Hkv, NS, st);
+    return launch_gwr<G, 3, 6>(tk, p, B, Hkv, NS, st);
 }
 
 // ---------------------------------------------------------------- combine (pass 2)
@@ -617,10 +632,10 @@ cudaError_t launch_splitkv_decode(const DecodeArgs& a, const DeviceInfo& dev, cu
     p.NS = a.num_splits;
     p.scale_log2 = a.sm_scale * 1.4426950408889634f;
     switch (a.Hq / a.Hkv) {
-        case 1: return launch_g<1>(tk, p, a.B, a.Hkv, a.num_splits, st);
-        case 2: return launch_g<2>(tk, p, a.B, a.Hkv, a.num_splits, st);
-        case 4: return launch_g<4>(tk, p, a.B, a.Hkv, a.num_splits, st);
-        case 8: return launch_g<8>(tk, p, a.B, a.Hkv, a.num_splits, st);
+        case 1: return launch_g<1>(tk, p, a.B, a.Hkv, a.num_splits, a.max_pages, st);
+        case 2: return launch_g<2>(tk, p, a.B, a.Hkv, a.num_splits, a.max_pages, st);
+        case 4: return launch_g<4>(tk, p, a.B, a.Hkv, a.num_splits, a.max_pages, st);
+        case 8: return launch_g<8>(tk, p, a.B, a.Hkv, a.num_splits, a.max_pages, st);
     }
     return cudaErrorInvalidValue;
 }
