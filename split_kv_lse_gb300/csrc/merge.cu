@@ -12,7 +12,7 @@
 // a 128-bit coalesced access; each thread keeps several rows (or states) of
 // loads in flight before it computes; all arithmetic is fp32.
 //   merge_state_kernel        two states, team per row (in-place variant too)
-//   merge_states_bulk_kernel  N states, warp per row, TMA ring: many rows
+//   merge_states_bulk_kernel  N states, warp per row, batches of TMA bulk copies: many rows
 //   merge_states_cta_kernel   N states, one CTA (8 warps) per row or per chunk
 //                             of a row's states: few rows, many states; the
 //                             chunks of a row meet in a workspace and the
@@ -139,24 +139,32 @@ merge_state_kernel(const T* va, const float* sa, const T* __restrict__ vb,
 }
 
 // ---------------------------------------------------------------- N-state, warp per row
-// One warp per (pos, h) row.  The row's weights are computed once into shared
-// memory; then only the states with non-zero weight are streamed: each
-// state's v row (D contiguous elements) is one TMA bulk copy into a per-warp
-// ring of kBulkRing slots, refilled as soon as it is consumed, so up to
-// kBulkRing rows per warp are in flight without holding registers.
-constexpr int kBulkWarps = 8;
-constexpr int kBulkRing = 8;
+// One warp per (pos, h) row.  The row's N LSEs are read once (lane n holds
+// states n, n + 32, ...); the non-empty states are compacted (ballot) into a
+// list of (index, weight) in shared memory -- a zero-weight state is never
+// read, so its v cannot poison the sum.  Their v rows (D contiguous
+// elements) then stream through a per-warp double buffer of two batches of
+// kRowBatch rows: a batch is kRowBatch TMA bulk copies issued by kRowBatch
+// lanes at once and completed on one mbarrier, so the ring bookkeeping is
+// paid once per batch, not once per state.
+#ifndef SKV_ROW_WARPS
+#define SKV_ROW_WARPS 4
+#endif
+#ifndef SKV_ROW_BATCH
+#define SKV_ROW_BATCH 8
+#endif
+constexpr int kRowWarps = SKV_ROW_WARPS;
+constexpr int kRowBatch = SKV_ROW_BATCH;
 constexpr int kBulkMaxN = 256;
 
-SKV_HOSTDEV_CONST size_t bulk_smem_bytes(int row_bytes) {
-    return (size_t)kBulkWarps * kBulkRing * row_bytes +                 // rings
-           (size_t)kBulkWarps * kBulkRing * sizeof(uint64_t) +          // mbarriers
-           (size_t)kBulkWarps * kBulkMaxN * sizeof(float) +             // weights
-           (size_t)kBulkWarps * kBulkRing * sizeof(int);                // state of each slot
+SKV_HOSTDEV_CONST size_t rows_smem_bytes(int row_bytes) {
+    return (size_t)kRowWarps * 2 * kRowBatch * row_bytes +        // double-buffered batches
+           (size_t)kRowWarps * 2 * sizeof(uint64_t) +               // one mbarrier per buffer
+           (size_t)kRowWarps * kBulkMaxN * (sizeof(float) + sizeof(int));  // compacted list
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kBulkWarps * 32)
+__global__ void __launch_bounds__(kRowWarps * 32)
 merge_states_bulk_kernel(const T* __restrict__ v, const float* __restrict__ s,
                          T* __restrict__ vo, float* __restrict__ so, int64_t rows, int N,
                          int64_t H, int chunks, unsigned long long* err) {
@@ -164,86 +172,91 @@ merge_states_bulk_kernel(const T* __restrict__ v, const float* __restrict__ s,
     extern __shared__ __align__(128) uint8_t smem[];
     const int row_bytes = chunks * 16;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint8_t* ring = smem + (size_t)warp * kBulkRing * row_bytes;
-    uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + (size_t)kBulkWarps * kBulkRing * row_bytes);
-    uint64_t* bars = bars_all + warp * kBulkRing;
-    float* wsm = reinterpret_cast<float*>(bars_all + kBulkWarps * kBulkRing) + warp * kBulkMaxN;
-    int* slot_n = reinterpret_cast<int*>(reinterpret_cast<float*>(bars_all + kBulkWarps * kBulkRing) +
-                                         kBulkWarps * kBulkMaxN) + warp * kBulkRing;
+    uint8_t* ring = smem + (size_t)warp * 2 * kRowBatch * row_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kRowWarps * 2 * kRowBatch * row_bytes) +
+                     warp * 2;
+    float* cw = reinterpret_cast<float*>(smem + (size_t)kRowWarps * 2 * kRowBatch * row_bytes +
+                                         (size_t)kRowWarps * 2 * sizeof(uint64_t)) + warp * kBulkMaxN;
+    int* cidx = reinterpret_cast<int*>(cw + (kRowWarps - warp) * kBulkMaxN) + warp * kBulkMaxN;
 
-    const int64_t r = (int64_t)blockIdx.x * kBulkWarps + warp;
+    const int64_t r = (int64_t)blockIdx.x * kRowWarps + warp;
     if (r >= rows) return;  // whole warp; no block-wide barrier follows
     if (lane == 0) {
-        for (int i = 0; i < kBulkRing; ++i) mbar_init(&bars[i], 1);
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
         fence_mbar_init();
     }
     const int64_t pos = r / H, h = r % H;
     // s[pos, n, h] at (pos*N + n)*H + h ([F2] §④).
     const float* srow = s + (pos * N) * H + h;
+    float sv[kBulkMaxN / 32];
     float m = -INFINITY;
-    for (int n = lane; n < N; n += 32) m = fmaxf(m, sanitize_lse(srow[(int64_t)n * H]));
+#pragma unroll
+    for (int k = 0; k < kBulkMaxN / 32; ++k) {
+        const int n = lane + 32 * k;
+        sv[k] = n < N ? sanitize_lse(__ldg(srow + (int64_t)n * H)) : -INFINITY;
+        m = fmaxf(m, sv[k]);
+    }
     m = warp_max(m);
     float W = 0.f;
-    for (int n = lane; n < N; n += 32) {
-        const float w = merge_weight(sanitize_lse(srow[(int64_t)n * H]), m);
-        wsm[n] = w;
+    int nnz = 0;  // non-empty states, in state order
+#pragma unroll
+    for (int k = 0; k < kBulkMaxN / 32; ++k) {
+        const float w = merge_weight(sv[k], m);  // 0 for empty states and n >= N
         W += w;
+        const unsigned live = __ballot_sync(0xffffffffu, w > 0.f);
+        if (w > 0.f) {
+            const int at = nnz + __popc(live & ((1u << lane) - 1u));
+            cidx[at] = lane + 32 * k;
+            cw[at] = w;
+        }
+        nnz += __popc(live);
     }
     W = warp_sum(W);
     __syncwarp();
 
-    const char* vrow = reinterpret_cast<const char*>(v) + ((pos * N) * H + h) * row_bytes;
-    const int64_t nstride = H * row_bytes;
+    const char* vrow = reinterpret_cast<const char*>(v) + ((pos * N) * H + h) * (int64_t)row_bytes;
+    const int64_t nstride = H * (int64_t)row_bytes;
     const uint64_t pol = policy_evict_first();
-    int n_next = 0;  // next state to consider for a copy
-    auto next_nonzero = [&](int n) {
-        while (n < N && !(wsm[n] > 0.f)) ++n;
-        return n;
+    const int nbatch = (nnz + kRowBatch - 1) / kRowBatch;
+    auto issue = [&](int j) {  // batch j into buffer j & 1
+        const int cnt = min(kRowBatch, nnz - j * kRowBatch);
+        uint64_t* bar = &bars[j & 1];
+        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(cnt * row_bytes));
+        __syncwarp();
+        if (lane < cnt)
+            bulk_g2s(ring + ((j & 1) * kRowBatch + lane) * row_bytes,
+                     vrow + (int64_t)cidx[j * kRowBatch + lane] * nstride, row_bytes, bar, pol);
     };
-    auto issue = [&](int slot, int n) {
-        if (lane == 0) {
-            slot_n[slot] = n;
-            mbar_arrive_expect_tx(&bars[slot], row_bytes);
-            bulk_g2s(ring + slot * row_bytes, vrow + (int64_t)n * nstride, row_bytes, &bars[slot], pol);
-        }
-    };
-    int inflight = 0;
-    for (int i = 0; i < kBulkRing; ++i) {
-        n_next = next_nonzero(n_next);
-        if (n_next >= N) break;
-        issue(i, n_next);
-        ++n_next;
-        ++inflight;
-    }
+    if (nbatch > 0) issue(0);
+    if (nbatch > 1) issue(1);
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    for (int q = 0; inflight > 0; ++q) {
-        const int slot = q % kBulkRing;
-        const bool ok = mbar_wait(&bars[slot], (uint32_t)((q / kBulkRing) & 1), err, 6);
+    for (int j = 0; j < nbatch; ++j) {
+        const bool ok = mbar_wait(&bars[j & 1], (uint32_t)((j >> 1) & 1), err, 6);
         if (!__all_sync(0xffffffffu, ok)) {
-            // Bounded wait gave up (error recorded): one more bounded wait per
-            // copy still in flight, then stop.
-            for (int i = 1; i < inflight; ++i)
-                mbar_wait(&bars[(q + i) % kBulkRing], (uint32_t)(((q + i) / kBulkRing) & 1), err, 7);
+            // A bounded wait gave up (error recorded): one more bounded wait
+            // for the other batch in flight, then stop.
+            if (j + 1 < nbatch) mbar_wait(&bars[(j + 1) & 1], (uint32_t)(((j + 1) >> 1) & 1), err, 7);
             return;
         }
-        const float w = wsm[slot_n[slot]];
+        const int cnt = min(kRowBatch, nnz - j * kRowBatch);
         if (lane < chunks) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(ring + slot * row_bytes + lane * 16);
-            float f[E];
-            to_float<T>(raw, f);
+            const uint8_t* buf = ring + (j & 1) * kRowBatch * row_bytes + lane * 16;
 #pragma unroll
-            for (int e = 0; e < E; ++e) acc[e] = fmaf(w, f[e], acc[e]);
+            for (int b = 0; b < kRowBatch; ++b) {
+                if (b < cnt) {
+                    const float w = cw[j * kRowBatch + b];
+                    float f[E];
+                    to_float<T>(*reinterpret_cast<const uint4*>(buf + b * row_bytes), f);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[e] = fmaf(w, f[e], acc[e]);
+                }
+            }
         }
-        __syncwarp();  // slot (and slot_n) fully read
-        --inflight;
-        n_next = next_nonzero(n_next);
-        if (n_next < N) {
-            issue(slot, n_next);
-            ++n_next;
-            ++inflight;
-        }
+        __syncwarp();  // buffer fully read
+        if (j + 2 < nbatch) issue(j + 2);
     }
     const float inv = W > 0.f ? 1.f / W : 0.f;
     if (lane < chunks) {
@@ -533,6 +546,22 @@ MergeStatesPlan plan_merge_states(int64_t rows, int64_t N, int64_t D, int chunks
     return pl;
 }
 
+template <typename T>
+cudaError_t launch_rows(const T* v, const float* s, T* vo, float* so, int64_t rows, int N, int64_t H,
+                        int chunks, unsigned blocks, size_t smem, const DeviceInfo& dev,
+                        cudaStream_t st) {
+    static bool attr_set[64] = {};
+    if (dev.device >= 0 && dev.device < 64 && !attr_set[dev.device]) {
+        cudaError_t e = cudaFuncSetAttribute(merge_states_bulk_kernel<T>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev.device] = true;
+    }
+    merge_states_bulk_kernel<T><<<blocks, kRowWarps * 32, smem, st>>>(v, s, vo, so, rows, N, H, chunks,
+                                                                       dev.err);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_merge_states(const void* v, const float* s, void* vo, float* so, int64_t S,
                                 int64_t N, int64_t H, int64_t D, skv_dtype dt, void* ws,
                                 size_t ws_bytes, const DeviceInfo& dev, cudaStream_t st) {
@@ -541,18 +570,18 @@ cudaError_t launch_merge_states(const void* v, const float* s, void* vo, float* 
     const MergeStatesPlan pl = plan_merge_states(rows, N, D, chunks, dev.sm_count, ws ? ws_bytes : 0);
     if (pl.team_kernel) {
         const int row_bytes = chunks * 16;
-        const size_t smem = bulk_smem_bytes(row_bytes);
-        const unsigned blocks = (unsigned)((rows + kBulkWarps - 1) / kBulkWarps);
-#define SKV_BULK(T_)                                                                           \
-    merge_states_bulk_kernel<T_><<<blocks, kBulkWarps * 32, smem, st>>>(                      \
-        static_cast<const T_*>(v), s, static_cast<T_*>(vo), so, rows, (int)N, H, chunks, dev.err)
+        const size_t smem = rows_smem_bytes(row_bytes);
+        const unsigned blocks = (unsigned)((rows + kRowWarps - 1) / kRowWarps);
+#define SKV_ROWS(T_)                                                                           \
+    launch_rows<T_>(static_cast<const T_*>(v), s, static_cast<T_*>(vo), so, rows, (int)N, H,   \
+                    chunks, blocks, smem, dev, st)
         switch (dt) {
-            case SKV_F32: SKV_BULK(float); break;
-            case SKV_F16: SKV_BULK(__half); break;
-            case SKV_BF16: SKV_BULK(__nv_bfloat16); break;
+            case SKV_F32: return SKV_ROWS(float);
+            case SKV_F16: return SKV_ROWS(__half);
+            case SKV_BF16: return SKV_ROWS(__nv_bfloat16);
         }
-#undef SKV_BULK
-        return cudaGetLastError();
+#undef SKV_ROWS
+        return cudaErrorInvalidValue;
     }
     CtaParams p = {};
     p.v = v;
