@@ -278,12 +278,30 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_free[b]);  // S buffer b read by this warp
+            // Row max in log2 units.  With a positive scale the max of the
+            // raw scores is taken and scaled once, and the scale is folded
+            // into the exponent below (p = 2^(x * sc - m)); only the block
+            // that crosses the end of the prefix is masked.
             const int key0 = (blk0 + j) * kBlockKeys;
-            float mx = -INFINITY;
+            float sc = p.scale_log2, mx;
+            if (sc > 0.f) {
+                if (key0 + kBlockKeys > p.prefix_len) {
 #pragma unroll
-            for (int i = 0; i < kBlockKeys; ++i) {
-                x[i] = key0 + i < p.prefix_len ? x[i] * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, x[i]);
+                    for (int i = 0; i < kBlockKeys; ++i)
+                        if (key0 + i >= p.prefix_len) x[i] = -INFINITY;
+                }
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int i = 0; i < kBlockKeys; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sc;
+            } else {
+                mx = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < kBlockKeys; ++i) {
+                    x[i] = key0 + i < p.prefix_len ? x[i] * sc : -INFINITY;
+                    mx = fmaxf(mx, x[i]);
+                }
+                sc = 1.f;
             }
             // PV_{j-1} done: O is stable and the P buffer is free.
             if (j > 0) {
@@ -309,16 +327,17 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                 }
                 m_ref = mx;
             }
-            float psum = 0.f;
+            float ps4[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
+            const float nm = -m_ref;
 #pragma unroll
             for (int chunk16 = 0; chunk16 < 16; ++chunk16) {  // 8 keys = one 16-byte chunk of P
                 uint32_t pk[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i0 = chunk16 * 8 + 2 * e;
-                    const float p0 = exp2f(x[i0] - m_ref);  // masked keys: 2^-inf = 0
-                    const float p1 = exp2f(x[i0 + 1] - m_ref);
-                    psum += p0 + p1;
+                    const float p0 = fast_exp2(fmaf(x[i0], sc, nm));  // masked keys: 2^-inf = 0
+                    const float p1 = fast_exp2(fmaf(x[i0 + 1], sc, nm));
+                    ps4[e] += p0 + p1;
                     const __half2 h2 = __floats2half2_rn(p0, p1);
                     pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
                 }
@@ -327,7 +346,7 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                 *reinterpret_cast<uint4*>(Ps + half * kHalf + tid * 128 + pos * 16) =
                     make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
-            l_run += psum;
+            l_run += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
             tc::fence_before_sync();
             tc::fence_proxy_async_smem();
             __syncwarp();

@@ -102,7 +102,7 @@ SKV_DEVINL uint4 ld_pinned(const void* p) {
 // Read of data this kernel may later overwrite (in-place merge): coherent path.
 SKV_DEVINL uint4 ld_coherent(const void* p) {
     uint4 r;
-    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p) : "memory");
     return r;
 }
@@ -134,6 +134,15 @@ SKV_DEVINL float sanitize_lse(float s) {
 // (s = m = -inf) get weight 0 instead of NaN.
 SKV_DEVINL float merge_weight(float s, float m) {
     return exp2f(fmaxf(s - m, -INFINITY));
+}
+
+// 2^x by the hardware approximation (ex2.approx, relative error about
+// 2^-22, subnormal results flushed to 0): softmax weights, where that error
+// is far below the fp16 rounding of p.
+SKV_DEVINL float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // ------------------------------------------------------------------ warp helpers
