@@ -51,10 +51,10 @@ constexpr int kHalf = 128 * 128;                     // one [128 rows x 64] fp16
 constexpr int kTile = 2 * kHalf;                     // one [128 x 128] fp16 operand tile (32 KB)
 constexpr int kStages = 2;                           // K blocks and V blocks in flight
 constexpr int kSoftmaxWarps = 4;                     // one thread per query row
-constexpr int kMmaWarp = 4;
-constexpr int kTmaWarp = 5;
-constexpr int kThreads = 6 * 32;
-constexpr uint32_t kTmemCols = 512;                  // S buffers [0,128), [128,256); O [256,384)
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
+constexpr int kThreads = 10 * 32;
+constexpr uint32_t kTmemCols = 512;                  // S_w at 128 w, O_w at 256 + 128 w (w = softmax group)
 constexpr float kRescaleThreshold = 8.f;             // log2 units
 
 struct PrefixParams {
@@ -74,15 +74,14 @@ constexpr size_t kSmemQ = 0;
 constexpr size_t kSmemK = kSmemQ + kTile;
 constexpr size_t kSmemV = kSmemK + (size_t)kStages * kTile;
 constexpr size_t kSmemP = kSmemV + (size_t)kStages * kTile;
-constexpr size_t kSmemBars = kSmemP + kTile;
-// q_full, p_full, pv_done, s_full[2], s_free[2], k_full[], k_empty[], v_full[], v_empty[]
-constexpr int kNumBars = 7 + 4 * kStages;
-constexpr size_t kSmemTmemSlot = kSmemBars + kNumBars * sizeof(uint64_t);
-constexpr size_t kSmemIds = kSmemTmemSlot + 16;  // tmem address, abort flag
+constexpr size_t kSmemBars = kSmemP + 2 * kTile;     // a P buffer per softmax group
+// q_full, p_full[2], pv_done[2], s_full[2], s_free[2], merge, k_full[], k_empty[], v_full[], v_empty[]
+constexpr int kNumBars = 10 + 4 * kStages;
+constexpr size_t kSmemMl = kSmemBars + kNumBars * sizeof(uint64_t);  // group 1's (m, l) per row
+constexpr size_t kSmemTmemSlot = kSmemMl + kM * 2 * sizeof(float);
+constexpr size_t kSmemEnd = kSmemTmemSlot + 16;      // tmem address, abort flag
 
-size_t prefix_smem_bytes(int blocks_per_chunk) {
-    return 1024 + kSmemIds + (size_t)blocks_per_chunk * kPagesPerBlock * sizeof(int);
-}
+size_t prefix_smem_bytes(int) { return 1024 + kSmemEnd; }
 
 __global__ void __launch_bounds__(kThreads, 1)
 cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -95,17 +94,18 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     uint8_t* Ps = sm + kSmemP;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSmemBars);
     uint64_t* q_full = bars + 0;
-    uint64_t* p_full = bars + 1;
-    uint64_t* pv_done = bars + 2;
-    uint64_t* s_full = bars + 3;   // [2]
-    uint64_t* s_free = bars + 5;   // [2]
-    uint64_t* k_full = bars + 7;
+    uint64_t* p_full = bars + 1;   // [2], per softmax group
+    uint64_t* pv_done = bars + 3;  // [2]
+    uint64_t* s_full = bars + 5;   // [2]
+    uint64_t* s_free = bars + 7;   // [2]
+    uint64_t* merge_bar = bars + 9;
+    uint64_t* k_full = bars + 10;
     uint64_t* k_empty = k_full + kStages;
     uint64_t* v_full = k_empty + kStages;
     uint64_t* v_empty = v_full + kStages;
+    float* ml = reinterpret_cast<float*>(sm + kSmemMl);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kSmemTmemSlot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kSmemTmemSlot + 4);
-    int* ids = reinterpret_cast<int*>(sm + kSmemIds);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chunk = blockIdx.x, mtile = blockIdx.y, hkv = blockIdx.z;
@@ -114,27 +114,15 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     const int nb = min(p.blocks_per_chunk, nblocks_total - blk0);  // >= 1 (host sizing)
     const int npages_prefix = (p.prefix_len + kPage - 1) / kPage;
 
-    // Page ids of this chunk; pages past the prefix are -1 (loaded as zeros).
-    for (int i = tid; i < nb * kPagesPerBlock; i += kThreads) {
-        const int gp = blk0 * kPagesPerBlock + i;
-        int pid = -1;
-        if (gp < npages_prefix) {
-            pid = p.prefix_pages[gp];
-            if ((unsigned)pid >= (unsigned)p.num_pool_pages) {
-                record_error(p.err, SKV_ERR_INVALID_ARG, 2 << 20 | gp);
-                pid = 0;
-            }
-        }
-        ids[i] = pid;
-    }
     if (tid == 0) {
         mbar_init(q_full, 1);
-        mbar_init(p_full, kSoftmaxWarps);
-        mbar_init(pv_done, 1);
         for (int b = 0; b < 2; ++b) {
+            mbar_init(&p_full[b], kSoftmaxWarps);
+            mbar_init(&pv_done[b], 1);
             mbar_init(&s_full[b], 1);
             mbar_init(&s_free[b], kSoftmaxWarps);
         }
+        mbar_init(merge_bar, kSoftmaxWarps);
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
@@ -149,7 +137,6 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tO = tmem + 256;  // columns [256, 384); S buffers at 0 and 128
 
     if (warp == kTmaWarp) {
         // ---------------------------------------------------------------- TMA producer
@@ -159,6 +146,7 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
             tma_prefetch_desc(&tv);
         }
         const uint64_t pol = policy_evict_first();
+        int win = -1, wid = -1;  // page-id window of the prefix list, id of page 32 * win + lane
         // A block's 16 boxes (8 pages x 2 halves of the head dim) go out from
         // 16 lanes at once: copies issued one after another by one thread
         // stream at about half the HBM bandwidth.
@@ -170,8 +158,23 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
             if (lane == 0) mbar_arrive_expect_tx(bar, kTile);
             __syncwarp();
             const int pg = lane >> 1, h = lane & 1;
+            // The block's 8 pages lie in one 32-page window of the prefix
+            // page list, held one id per lane (reloaded every 4 blocks).
+            const int g0 = (blk0 + j) * kPagesPerBlock;
+            if ((g0 >> 5) != win) {
+                win = g0 >> 5;
+                const int gl = 32 * win + lane;
+                wid = -1;  // past the prefix: loaded as zeros
+                if (gl < npages_prefix) {
+                    wid = __ldg(p.prefix_pages + gl);
+                    if ((unsigned)wid >= (unsigned)p.num_pool_pages) {
+                        record_error(p.err, SKV_ERR_INVALID_ARG, 2 << 20 | gl);
+                        wid = 0;
+                    }
+                }
+            }
+            const int pid = __shfl_sync(0xffffffffu, wid, (g0 + (pg & 7)) & 31);
             if (pg < kPagesPerBlock) {
-                const int pid = ids[j * kPagesPerBlock + pg];
                 // A page past the prefix is read from the row just past the
                 // tensor: the TMA fills the whole box with zeros.
                 const int row = pid >= 0 ? (pid * p.Hkv + hkv) * kPage : p.pool_rows;
@@ -199,12 +202,14 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
+        // Block j belongs to softmax group w = j & 1: S_w = Q K_j^T, then
+        // O_w += P_j V_j once the group has written P_j.
         if (lane == 0) {
             constexpr uint32_t idS = tc::idesc_f16_f32(kM, kBlockKeys, false);
             constexpr uint32_t idPV = tc::idesc_f16_f32(kM, kD, true);
-            auto issue_pv = [&](int j) -> bool {  // O += P_j V_j
-                const int st = j % kStages;
-                if (!wait_or_abort(p_full, (uint32_t)(j & 1), abort_flag, p.err, 22)) return false;
+            auto issue_pv = [&](int j) -> bool {  // O_w += P_j V_j
+                const int st = j % kStages, w = j & 1;
+                if (!wait_or_abort(&p_full[w], (uint32_t)((j >> 1) & 1), abort_flag, p.err, 22)) return false;
                 if (!wait_or_abort(&v_full[st], (uint32_t)((j / kStages) & 1), abort_flag, p.err, 23))
                     return false;
                 tc::fence_after_sync();
@@ -224,28 +229,30 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                         }
                     tc::fence_proxy_async_smem();
                 }
+                const uint32_t tOw = tmem + 256 + 128 * w;
+                const uint8_t* Pw = Ps + w * kTile;
 #pragma unroll
                 for (int k = 0; k < kBlockKeys / 16; ++k) {
                     const int h = k >> 2, kk = k & 3;
-                    const uint64_t ad = tc::sdesc_sw128(smem_addr(Ps + h * kHalf) + kk * 32, 16, 1024);
+                    const uint64_t ad = tc::sdesc_sw128(smem_addr(Pw + h * kHalf) + kk * 32, 16, 1024);
                     const uint64_t bd = tc::sdesc_sw128(smem_addr(Vs + st * kTile) + k * 2048, kHalf, 1024);
-                    tc::mma_f16_ss(tO, ad, bd, idPV, j > 0 || k > 0);
+                    tc::mma_f16_ss(tOw, ad, bd, idPV, j >= 2 || k > 0);
                 }
-                tc::mma_commit(pv_done);
+                tc::mma_commit(&pv_done[w]);
                 tc::mma_commit(&v_empty[st]);
                 return true;
             };
             bool ok = wait_or_abort(q_full, 0, abort_flag, p.err, 24);
             for (int j = 0; ok && j < nb; ++j) {
-                // S_j = Q K_j^T into S buffer j & 1, then P_{j-1} V_{j-1}: the
+                // S_j into group (j & 1)'s buffer, then P_{j-1} V_{j-1}: the
                 // tensor core computes S_j while the softmax of block j-1 runs.
-                const int st = j % kStages, b = j & 1;
+                const int st = j % kStages, w = j & 1;
                 ok = wait_or_abort(&k_full[st], (uint32_t)((j / kStages) & 1), abort_flag, p.err, 25);
                 if (ok && j >= 2)
-                    ok = wait_or_abort(&s_free[b], (uint32_t)(((j >> 1) - 1) & 1), abort_flag, p.err, 26);
+                    ok = wait_or_abort(&s_free[w], (uint32_t)(((j >> 1) - 1) & 1), abort_flag, p.err, 26);
                 if (!ok) break;
                 tc::fence_after_sync();
-                const uint32_t tS = tmem + (uint32_t)b * 128;
+                const uint32_t tS = tmem + (uint32_t)w * 128;
 #pragma unroll
                 for (int k = 0; k < kD / 16; ++k) {
                     const int h = k >> 2, kk = k & 3;
@@ -253,31 +260,38 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                     const uint64_t bd = tc::sdesc_sw128(smem_addr(Ks + st * kTile + h * kHalf) + kk * 32, 16, 1024);
                     tc::mma_f16_ss(tS, ad, bd, idS, k > 0);
                 }
-                tc::mma_commit(&s_full[b]);
+                tc::mma_commit(&s_full[w]);
                 tc::mma_commit(&k_empty[st]);
                 if (j >= 1) ok = issue_pv(j - 1);
             }
             if (ok) issue_pv(nb - 1);
         }
     } else {
-        // ---------------------------------------------------------------- softmax, row = tid
+        // ---------------------------------------------------------------- softmax, row = tid % 128
+        // Group w (warps 4w .. 4w + 3) takes blocks w, w + 2, ... with its
+        // own S, O and P; the two partial states of a row are merged at the
+        // end, like two splits of the chunk.
+        const int w = warp >> 2, row_t = tid & (kM - 1);
+        const uint32_t tOw = tmem + 256 + 128 * w;
+        uint8_t* Pw = Ps + w * kTile;
         float m_ref = -INFINITY;  // the max this row's O and l are scaled to (log2 units)
         float l_run = 0.f;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         bool ok = true;
-        for (int j = 0; j < nb; ++j) {
-            const int b = j & 1;
-            ok = wait_or_abort(&s_full[b], (uint32_t)((j >> 1) & 1), abort_flag, p.err, 27);
+        int jl = -1;  // this group's last block
+        for (int j = w; j < nb; j += 2) {
+            jl = j;
+            ok = wait_or_abort(&s_full[w], (uint32_t)((j >> 1) & 1), abort_flag, p.err, 27);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
             float x[kBlockKeys];
-            tc::tmem_ld128(tmem + (uint32_t)b * 128 + lane_base, x);
+            tc::tmem_ld128(tmem + (uint32_t)w * 128 + lane_base, x);
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[b]);  // S buffer b read by this warp
+            if (lane == 0) mbar_arrive(&s_free[w]);  // S buffer read by this warp
             // Row max in log2 units.  With a positive scale the max of the
             // raw scores is taken and scaled once, and the scale is folded
             // into the exponent below (p = 2^(x * sc - m)); only the block
@@ -303,9 +317,9 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                 }
                 sc = 1.f;
             }
-            // PV_{j-1} done: O is stable and the P buffer is free.
-            if (j > 0) {
-                ok = wait_or_abort(pv_done, (uint32_t)((j - 1) & 1), abort_flag, p.err, 28);
+            // PV of this group's previous block done: O_w is stable and P_w free.
+            if (j >= 2) {
+                ok = wait_or_abort(&pv_done[w], (uint32_t)(((j - 2) >> 1) & 1), abort_flag, p.err, 28);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
@@ -313,16 +327,16 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                 tc::fence_after_sync();
             }
             if (mx > m_ref + kRescaleThreshold) {  // also the first block (m_ref = -inf)
-                if (j > 0) {
+                if (j >= 2) {
                     const float alpha = exp2f(m_ref - mx);
                     l_run *= alpha;
 #pragma unroll 1
                     for (int c = 0; c < kD / 32; ++c) {  // 32 columns at a time: x[] stays live
                         float ob[32];
-                        tc::tmem_ld32(tO + lane_base + 32 * c, ob);
+                        tc::tmem_ld32(tOw + lane_base + 32 * c, ob);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) ob[i] *= alpha;
-                        tc::tmem_st32(tO + lane_base + 32 * c, ob);
+                        tc::tmem_st32(tOw + lane_base + 32 * c, ob);
                     }
                 }
                 m_ref = mx;
@@ -342,35 +356,62 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                     pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
                 }
                 const int half = chunk16 >> 3;
-                const int pos = (chunk16 & 7) ^ (tid & 7);  // 128-byte swizzle
-                *reinterpret_cast<uint4*>(Ps + half * kHalf + tid * 128 + pos * 16) =
+                const int pos = (chunk16 & 7) ^ (row_t & 7);  // 128-byte swizzle
+                *reinterpret_cast<uint4*>(Pw + half * kHalf + row_t * 128 + pos * 16) =
                     make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
             l_run += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
             tc::fence_before_sync();
             tc::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);  // P_j (and any O rescale) done by this warp
+            if (lane == 0) mbar_arrive(&p_full[w]);  // P_j (and any O rescale) done by this warp
         }
-        // ---- this chunk's state for row `tid` (after the last PV)
-        if (ok) ok = wait_or_abort(pv_done, (uint32_t)((nb - 1) & 1), abort_flag, p.err, 29);
-        if (__all_sync(0xffffffffu, ok)) {
-            tc::fence_after_sync();
-            const int rows_per_req = p.G;
-            const int r = mtile * (kM / rows_per_req) + tid / rows_per_req;
-            const int g = tid % rows_per_req;
-            float ob[kD];
-            tc::tmem_ld128(tO + lane_base, ob);
-            if (r < p.B) {
-                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        // ---- this group's state of row row_t, after its last PV
+        if (ok && jl >= 0) ok = wait_or_abort(&pv_done[w], (uint32_t)((jl >> 1) & 1), abort_flag, p.err, 29);
+        ok = __all_sync(0xffffffffu, ok);
+        if (w == 1) {  // hand (m, l) to group 0 (l = 0: no block, O_1 unused)
+            ml[2 * row_t] = ok ? m_ref : -INFINITY;
+            ml[2 * row_t + 1] = ok ? l_run : 0.f;
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(merge_bar);
+        } else {
+            ok = __all_sync(0xffffffffu, ok && wait_or_abort(merge_bar, 0, abort_flag, p.err, 30));
+            if (ok) {
+                tc::fence_after_sync();
+                const float m1 = ml[2 * row_t], l1 = ml[2 * row_t + 1];
+                // Two-state merge of the groups' states ([F2] §③): weights
+                // relative to the larger max; an empty state weighs 0.
+                const float M = fmaxf(m_ref, m1);
+                const float a0 = l_run > 0.f ? exp2f(m_ref - M) : 0.f;
+                const float a1 = l1 > 0.f ? exp2f(m1 - M) : 0.f;
+                const float L = a0 * l_run + a1 * l1;
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                const float c0 = a0 * inv, c1 = a1 * inv;
+                const int rows_per_req = p.G;
+                const int r = mtile * (kM / rows_per_req) + row_t / rows_per_req;
+                const int g = row_t % rows_per_req;
                 const int64_t row = (int64_t)r * p.Hq + hkv * p.G + g;
                 float* dst = p.pre_part + (row * p.nchunks + chunk) * kD;
+#pragma unroll 1
+                for (int c = 0; c < kD / 32; ++c) {
+                    float o0[32], o1[32];
+                    tc::tmem_ld32(tmem + 256 + lane_base + 32 * c, o0);
+                    if (l1 > 0.f) {
+                        tc::tmem_ld32(tmem + 384 + lane_base + 32 * c, o1);
+                    } else {
 #pragma unroll
-                for (int i = 0; i < kD; i += 4)
-                    *reinterpret_cast<float4*>(dst + i) =
-                        make_float4(ob[i] * inv, ob[i + 1] * inv, ob[i + 2] * inv, ob[i + 3] * inv);
-                p.pre_lse[row * p.nchunks + chunk] =
-                    l_run > 0.f ? m_ref + log2f(l_run) : -INFINITY;
+                        for (int i = 0; i < 32; ++i) o1[i] = 0.f;
+                    }
+                    if (r < p.B) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4*>(dst + 32 * c + i) = make_float4(
+                                c0 * o0[i] + c1 * o1[i], c0 * o0[i + 1] + c1 * o1[i + 1],
+                                c0 * o0[i + 2] + c1 * o1[i + 2], c0 * o0[i + 3] + c1 * o1[i + 3]);
+                    }
+                }
+                if (r < p.B) p.pre_lse[row * p.nchunks + chunk] = L > 0.f ? M + log2f(L) : -INFINITY;
             }
         }
     }
