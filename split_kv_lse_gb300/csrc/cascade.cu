@@ -9,31 +9,33 @@
 // ("L3 讲解：split-KV decode 与 LSE 合并") and the merges through the combine
 // kernel of decode.cu.
 //
-// One CTA per (kv head, 128-row M tile, chunk of the prefix).  The M tile's
-// rows are (request, group head) pairs -- row = r_local * G + g -- so one KV
-// tile serves 128 query rows.  Per 128-key block j:
-//   S_j = Q K_j^T    tcgen05.mma kind::f16, Q [128 x 128] and the K block
-//                    [128 keys x 128] K-major in shared memory; S fp32 in one
-//                    of two TMEM buffers, so S_{j+1} runs on the tensor core
-//                    while the warps do the softmax of block j
-//   softmax          4 warps, thread i <-> row i <-> TMEM lane i: base-2
-//                    online max/sum ([F2] §② exp2 trick); P written to shared
-//                    memory as fp16 in the swizzled K-major operand layout
-//   O += P_j V_j     tcgen05.mma with V as an MN-major operand, O fp32 stays
-//                    in TMEM across blocks
+// One CTA per (kv head, pair of 128-row M tiles, chunk of the prefix).  An M
+// tile's rows are (request, group head) pairs -- row = r_local * G + g -- and
+// the CTA's two M tiles share every K and V block it loads, so each prefix
+// block crosses HBM and the TMA unit once per 256 query rows.  Per 128-key
+// block j and M tile w (softmax group w):
+//   S_w = Q_w K_j^T  tcgen05.mma kind::f16, Q_w [128 x 128] and the K block
+//                    [128 keys x 128] K-major in shared memory, S fp32 in TMEM
+//   softmax          group w, thread i <-> row i <-> TMEM lane i: base-2
+//                    online max/sum ([F2] §② exp2 trick); P = 2^(s - m) as
+//                    fp16 pairs written back into TMEM over S
+//   O_w += P V_j     tcgen05.mma with P from TMEM (A operand) and V an
+//                    MN-major operand in shared memory; O fp32 stays in TMEM
+// The MMAs are issued in the order S_0(j), S_1(j), PV_0(j), S_0(j+1),
+// PV_1(j), S_1(j+1), ...: the tensor core computes one group's S while the
+// other group runs its softmax, and an S MMA never overwrites a P that a
+// PV issued before it has yet to read (tcgen05 MMAs of a thread run in order).
 // Lazy rescale: a row keeps the max it last rescaled to and only rescales
-// O (in TMEM) and its sum when the block max exceeds it by more than 8 (log2
-// units), so p <= 2^8 (exact in fp16 range) and the final normalisation by
-// the same max keeps the result exact.
-// Warp roles: warps 0-3 softmax and epilogue, warp 4 issues the MMAs, warp
-// 5 issues the TMA copies; they meet on mbarriers (S full / free per S
-// buffer, P full, PV done, K and V stage full / empty), so no role waits on
-// another's serial work.  Q, K and V tiles arrive by TMA tensor loads with
-// the 128-byte swizzle (a page is one 16 x 64 box per half of the head dim);
-// two K and two V blocks are in flight.  Every wait is bounded; a wait that
-// gives up raises a shared abort flag that ends every role's loop.  Each
-// chunk writes its normalised state (o, s base 2) for the combine kernel,
-// which merges the chunks into the prefix state.
+// O and its sum when the block max exceeds it by more than 8 (log2 units),
+// so p <= 2^8 (exact in fp16 range); the final normalisation by the same
+// max keeps the result exact.
+// Warp roles: warps 0-3 and 4-7 the two softmax groups (and their
+// epilogues), warp 8 issues the MMAs, warp 9 loads Q and the K blocks,
+// warp 10 the V blocks (16 lanes issue a block's boxes at once).  Two K and
+// two V blocks are in flight.  Every wait is bounded; a wait that gives up
+// raises a shared abort flag that ends every role's loop.  Each chunk writes
+// its normalised state (o, s base 2) per row for the combine kernel, which
+// merges the chunks into the prefix state.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -46,16 +48,18 @@ constexpr int kD = 128;
 constexpr int kPage = 16;
 constexpr int kBlockKeys = 128;                      // keys per block (N of QK^T, K of PV)
 constexpr int kPagesPerBlock = kBlockKeys / kPage;   // 8
-constexpr int kM = 128;                              // query rows per CTA
+constexpr int kM = 128;                              // query rows per M tile
 constexpr int kHalf = 128 * 128;                     // one [128 rows x 64] fp16 swizzled half tile
 constexpr int kTile = 2 * kHalf;                     // one [128 x 128] fp16 operand tile (32 KB)
 constexpr int kStages = 2;                           // K blocks and V blocks in flight
-constexpr int kSoftmaxWarps = 4;                     // one thread per query row
+constexpr int kSoftmaxWarps = 4;                     // per group: one thread per query row
 constexpr int kMmaWarp = 8;
-constexpr int kTmaWarp = 9;
-constexpr int kThreads = 10 * 32;
-constexpr uint32_t kTmemCols = 512;                  // S_w at 128 w, O_w at 256 + 128 w (w = softmax group)
+constexpr int kKWarp = 9;
+constexpr int kVWarp = 10;
+constexpr int kThreads = 11 * 32;
+constexpr uint32_t kTmemCols = 512;                  // group w: S/P at 256 w, O at 256 w + 128
 constexpr float kRescaleThreshold = 8.f;             // log2 units
+constexpr unsigned kFull = 0xffffffffu;
 
 struct PrefixParams {
     const int32_t* prefix_pages;
@@ -70,18 +74,28 @@ struct PrefixParams {
     unsigned long long* err;
 };
 
-constexpr size_t kSmemQ = 0;
-constexpr size_t kSmemK = kSmemQ + kTile;
+constexpr size_t kSmemQ = 0;                                   // Q_0, Q_1
+constexpr size_t kSmemK = kSmemQ + 2 * (size_t)kTile;
 constexpr size_t kSmemV = kSmemK + (size_t)kStages * kTile;
-constexpr size_t kSmemP = kSmemV + (size_t)kStages * kTile;
-constexpr size_t kSmemBars = kSmemP + 2 * kTile;     // a P buffer per softmax group
-// q_full, p_full[2], pv_done[2], s_full[2], s_free[2], merge, k_full[], k_empty[], v_full[], v_empty[]
-constexpr int kNumBars = 10 + 4 * kStages;
-constexpr size_t kSmemMl = kSmemBars + kNumBars * sizeof(uint64_t);  // group 1's (m, l) per row
-constexpr size_t kSmemTmemSlot = kSmemMl + kM * 2 * sizeof(float);
+constexpr size_t kSmemBars = kSmemV + (size_t)kStages * kTile;
+// q_full, s_full[2], p_full[2], pv_done[2], k_full[], k_empty[], v_full[], v_empty[]
+constexpr int kNumBars = 7 + 4 * kStages;
+constexpr size_t kSmemTmemSlot = kSmemBars + kNumBars * sizeof(uint64_t);
 constexpr size_t kSmemEnd = kSmemTmemSlot + 16;      // tmem address, abort flag
 
 size_t prefix_smem_bytes(int) { return 1024 + kSmemEnd; }
+
+// D[tmem] (+)= A[tmem] * B[smem]^T: the A operand (M rows = TMEM lanes, K
+// 16-bit elements packed two per 32-bit column) is read from tensor memory.
+SKV_DEVINL void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                           bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -91,24 +105,20 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     uint8_t* Qs = sm + kSmemQ;
     uint8_t* Ks = sm + kSmemK;
     uint8_t* Vs = sm + kSmemV;
-    uint8_t* Ps = sm + kSmemP;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSmemBars);
     uint64_t* q_full = bars + 0;
-    uint64_t* p_full = bars + 1;   // [2], per softmax group
-    uint64_t* pv_done = bars + 3;  // [2]
-    uint64_t* s_full = bars + 5;   // [2]
-    uint64_t* s_free = bars + 7;   // [2]
-    uint64_t* merge_bar = bars + 9;
-    uint64_t* k_full = bars + 10;
+    uint64_t* s_full = bars + 1;   // [2] per group
+    uint64_t* p_full = bars + 3;   // [2]
+    uint64_t* pv_done = bars + 5;  // [2]
+    uint64_t* k_full = bars + 7;
     uint64_t* k_empty = k_full + kStages;
     uint64_t* v_full = k_empty + kStages;
     uint64_t* v_empty = v_full + kStages;
-    float* ml = reinterpret_cast<float*>(sm + kSmemMl);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kSmemTmemSlot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kSmemTmemSlot + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int chunk = blockIdx.x, mtile = blockIdx.y, hkv = blockIdx.z;
+    const int chunk = blockIdx.x, mpair = blockIdx.y, hkv = blockIdx.z;
     const int nblocks_total = (p.prefix_len + kBlockKeys - 1) / kBlockKeys;
     const int blk0 = chunk * p.blocks_per_chunk;
     const int nb = min(p.blocks_per_chunk, nblocks_total - blk0);  // >= 1 (host sizing)
@@ -116,13 +126,11 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
 
     if (tid == 0) {
         mbar_init(q_full, 1);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&p_full[b], kSoftmaxWarps);
-            mbar_init(&pv_done[b], 1);
-            mbar_init(&s_full[b], 1);
-            mbar_init(&s_free[b], kSoftmaxWarps);
+        for (int w = 0; w < 2; ++w) {
+            mbar_init(&s_full[w], 1);
+            mbar_init(&p_full[w], kSoftmaxWarps);
+            mbar_init(&pv_done[w], 1);
         }
-        mbar_init(merge_bar, kSoftmaxWarps);
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
@@ -138,28 +146,28 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kTmaWarp) {
-        // ---------------------------------------------------------------- TMA producer
+    if (warp == kKWarp || warp == kVWarp) {
+        // ---------------------------------------------------------------- TMA producers
+        const bool isk = warp == kKWarp;
         if (lane == 0) {
-            tma_prefetch_desc(&tq);
-            tma_prefetch_desc(&tk);
-            tma_prefetch_desc(&tv);
+            if (isk) tma_prefetch_desc(&tq);
+            tma_prefetch_desc(isk ? &tk : &tv);
         }
         const uint64_t pol = policy_evict_first();
-        int win = -1, wid = -1;  // page-id window of the prefix list, id of page 32 * win + lane
+        int win = -1, wid = -1;  // page-id window of the prefix list: id of page 32 * win + lane
         // A block's 16 boxes (8 pages x 2 halves of the head dim) go out from
         // 16 lanes at once: copies issued one after another by one thread
         // stream at about half the HBM bandwidth.
-        auto load_block = [&](int j, bool is_v) {
+        auto load_block = [&](int j) {
             const int stage = j % kStages;
-            uint64_t* bar = is_v ? &v_full[stage] : &k_full[stage];
-            uint8_t* dst = (is_v ? Vs : Ks) + stage * kTile;
-            const CUtensorMap* map = is_v ? &tv : &tk;
+            uint64_t* bar = isk ? &k_full[stage] : &v_full[stage];
+            uint8_t* dst = (isk ? Ks : Vs) + stage * kTile;
+            const CUtensorMap* map = isk ? &tk : &tv;
             if (lane == 0) mbar_arrive_expect_tx(bar, kTile);
             __syncwarp();
             const int pg = lane >> 1, h = lane & 1;
-            // The block's 8 pages lie in one 32-page window of the prefix
-            // page list, held one id per lane (reloaded every 4 blocks).
+            // The block's 8 pages lie in one 32-page window of the prefix page
+            // list, held one id per lane (reloaded every 4 blocks).
             const int g0 = (blk0 + j) * kPagesPerBlock;
             if ((g0 >> 5) != win) {
                 win = g0 >> 5;
@@ -173,7 +181,7 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                     }
                 }
             }
-            const int pid = __shfl_sync(0xffffffffu, wid, (g0 + (pg & 7)) & 31);
+            const int pid = __shfl_sync(kFull, wid, (g0 + (pg & 7)) & 31);
             if (pg < kPagesPerBlock) {
                 // A page past the prefix is read from the row just past the
                 // tensor: the TMA fills the whole box with zeros.
@@ -181,38 +189,66 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                 tma_load_2d(dst + h * kHalf + pg * (kPage * 128), map, h * 64, row, bar, pol);
             }
         };
-        if (lane == 0) {
-            mbar_arrive_expect_tx(q_full, kTile);
-            const int z = mtile * (kM / p.G);
-            tma_load_3d(Qs, &tq, 0, hkv * p.G, z, q_full);
-            tma_load_3d(Qs + kHalf, &tq, 64, hkv * p.G, z, q_full);
+        if (isk && lane == 0) {  // both M tiles' queries (a tile past B reads zeros)
+            mbar_arrive_expect_tx(q_full, 2 * kTile);
+            for (int w = 0; w < 2; ++w) {
+                const int z = (2 * mpair + w) * (kM / p.G);
+                tma_load_3d(Qs + w * kTile, &tq, 0, hkv * p.G, z, q_full);
+                tma_load_3d(Qs + w * kTile + kHalf, &tq, 64, hkv * p.G, z, q_full);
+            }
         }
+        uint64_t* empty = isk ? k_empty : v_empty;
         for (int j = 0; j < nb; ++j) {
             bool ok = true;
             if (j >= kStages)
-                ok = wait_or_abort(&k_empty[j % kStages], (uint32_t)((j / kStages - 1) & 1), abort_flag,
-                                   p.err, 20);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            load_block(j, false);
-            if (j >= kStages)
-                ok = wait_or_abort(&v_empty[j % kStages], (uint32_t)((j / kStages - 1) & 1), abort_flag,
-                                   p.err, 21);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            load_block(j, true);
+                ok = wait_or_abort(&empty[j % kStages], (uint32_t)((j / kStages - 1) & 1), abort_flag,
+                                   p.err, isk ? 20 : 21);
+            if (!__all_sync(kFull, ok)) break;
+            load_block(j);
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
-        // Block j belongs to softmax group w = j & 1: S_w = Q K_j^T, then
-        // O_w += P_j V_j once the group has written P_j.
         if (lane == 0) {
             constexpr uint32_t idS = tc::idesc_f16_f32(kM, kBlockKeys, false);
-            constexpr uint32_t idPV = tc::idesc_f16_f32(kM, kD, true);
-            auto issue_pv = [&](int j) -> bool {  // O_w += P_j V_j
-                const int st = j % kStages, w = j & 1;
-                if (!wait_or_abort(&p_full[w], (uint32_t)((j >> 1) & 1), abort_flag, p.err, 22)) return false;
-                if (!wait_or_abort(&v_full[st], (uint32_t)((j / kStages) & 1), abort_flag, p.err, 23))
-                    return false;
+            constexpr uint32_t idPV = tc::idesc_f16_f32(kM, kD, true);  // A (P) from TMEM, B (V) MN-major
+            auto qk = [&](int j, int w) {  // S_w = Q_w K_j^T
+                const int st = j % kStages;
+                const uint8_t* Qw = Qs + w * kTile;
+#pragma unroll
+                for (int k = 0; k < kD / 16; ++k) {
+                    const int h = k >> 2, kk = k & 3;
+                    const uint64_t ad = tc::sdesc_sw128(smem_addr(Qw + h * kHalf) + kk * 32, 16, 1024);
+                    const uint64_t bd = tc::sdesc_sw128(smem_addr(Ks + st * kTile + h * kHalf) + kk * 32, 16, 1024);
+                    tc::mma_f16_ss(tmem + 256 * w, ad, bd, idS, k > 0);
+                }
+                tc::mma_commit(&s_full[w]);
+            };
+            auto pv = [&](int j, int w) -> bool {  // O_w += P_w V_j
+                if (!wait_or_abort(&p_full[w], (uint32_t)(j & 1), abort_flag, p.err, 22)) return false;
                 tc::fence_after_sync();
+                const int st = j % kStages;
+#pragma unroll
+                for (int k = 0; k < kBlockKeys / 16; ++k) {
+                    const uint64_t bd = tc::sdesc_sw128(smem_addr(Vs + st * kTile) + k * 2048, kHalf, 1024);
+                    mma_f16_ts(tmem + 256 * w + 128, tmem + 256 * w + 8 * k, bd, idPV, j > 0 || k > 0);
+                }
+                tc::mma_commit(&pv_done[w]);
+                return true;
+            };
+            bool ok = wait_or_abort(q_full, 0, abort_flag, p.err, 24);
+            ok = ok && wait_or_abort(&k_full[0], 0, abort_flag, p.err, 25);
+            if (ok) {
+                tc::fence_after_sync();
+                qk(0, 0);
+                qk(0, 1);
+                tc::mma_commit(&k_empty[0]);
+            }
+            // S_0(j+1) goes in after PV_0(j) and S_1(j+1) after PV_1(j): a PV
+            // reads its P from the TMEM columns that the next S overwrites.
+            for (int j = 0; ok && j < nb; ++j) {
+                const int st = j % kStages;
+                ok = wait_or_abort(&v_full[st], (uint32_t)((j / kStages) & 1), abort_flag, p.err, 23);
+                if (!ok) break;
                 const int tail = p.prefix_len % kPage;
                 const int last_page = npages_prefix - 1 - (blk0 + j) * kPagesPerBlock;
                 if (tail != 0 && last_page >= 0 && last_page < kPagesPerBlock) {
@@ -229,69 +265,43 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                         }
                     tc::fence_proxy_async_smem();
                 }
-                const uint32_t tOw = tmem + 256 + 128 * w;
-                const uint8_t* Pw = Ps + w * kTile;
-#pragma unroll
-                for (int k = 0; k < kBlockKeys / 16; ++k) {
-                    const int h = k >> 2, kk = k & 3;
-                    const uint64_t ad = tc::sdesc_sw128(smem_addr(Pw + h * kHalf) + kk * 32, 16, 1024);
-                    const uint64_t bd = tc::sdesc_sw128(smem_addr(Vs + st * kTile) + k * 2048, kHalf, 1024);
-                    tc::mma_f16_ss(tOw, ad, bd, idPV, j >= 2 || k > 0);
+                if (!(ok = pv(j, 0))) break;
+                const bool more = j + 1 < nb;
+                if (more) {
+                    ok = wait_or_abort(&k_full[(j + 1) % kStages], (uint32_t)(((j + 1) / kStages) & 1),
+                                       abort_flag, p.err, 25);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    qk(j + 1, 0);
                 }
-                tc::mma_commit(&pv_done[w]);
+                if (!(ok = pv(j, 1))) break;
                 tc::mma_commit(&v_empty[st]);
-                return true;
-            };
-            bool ok = wait_or_abort(q_full, 0, abort_flag, p.err, 24);
-            for (int j = 0; ok && j < nb; ++j) {
-                // S_j into group (j & 1)'s buffer, then P_{j-1} V_{j-1}: the
-                // tensor core computes S_j while the softmax of block j-1 runs.
-                const int st = j % kStages, w = j & 1;
-                ok = wait_or_abort(&k_full[st], (uint32_t)((j / kStages) & 1), abort_flag, p.err, 25);
-                if (ok && j >= 2)
-                    ok = wait_or_abort(&s_free[w], (uint32_t)(((j >> 1) - 1) & 1), abort_flag, p.err, 26);
-                if (!ok) break;
-                tc::fence_after_sync();
-                const uint32_t tS = tmem + (uint32_t)w * 128;
-#pragma unroll
-                for (int k = 0; k < kD / 16; ++k) {
-                    const int h = k >> 2, kk = k & 3;
-                    const uint64_t ad = tc::sdesc_sw128(smem_addr(Qs + h * kHalf) + kk * 32, 16, 1024);
-                    const uint64_t bd = tc::sdesc_sw128(smem_addr(Ks + st * kTile + h * kHalf) + kk * 32, 16, 1024);
-                    tc::mma_f16_ss(tS, ad, bd, idS, k > 0);
+                if (more) {
+                    qk(j + 1, 1);
+                    tc::mma_commit(&k_empty[(j + 1) % kStages]);
                 }
-                tc::mma_commit(&s_full[w]);
-                tc::mma_commit(&k_empty[st]);
-                if (j >= 1) ok = issue_pv(j - 1);
             }
-            if (ok) issue_pv(nb - 1);
         }
     } else {
-        // ---------------------------------------------------------------- softmax, row = tid % 128
-        // Group w (warps 4w .. 4w + 3) takes blocks w, w + 2, ... with its
-        // own S, O and P; the two partial states of a row are merged at the
-        // end, like two splits of the chunk.
+        // ---------------------------------------------------------------- softmax group w, row = tid % 128
         const int w = warp >> 2, row_t = tid & (kM - 1);
-        const uint32_t tOw = tmem + 256 + 128 * w;
-        uint8_t* Pw = Ps + w * kTile;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + 256 * w + lane_base;        // S, then P over it
+        const uint32_t tO = tmem + 256 * w + 128 + lane_base;
         float m_ref = -INFINITY;  // the max this row's O and l are scaled to (log2 units)
         float l_run = 0.f;
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         bool ok = true;
-        int jl = -1;  // this group's last block
-        for (int j = w; j < nb; j += 2) {
-            jl = j;
-            ok = wait_or_abort(&s_full[w], (uint32_t)((j >> 1) & 1), abort_flag, p.err, 27);
-            if (!__all_sync(0xffffffffu, ok)) {
+        for (int j = 0; j < nb; ++j) {
+            // S_w(j) is complete; so is every MMA issued before it, PV_w(j-1)
+            // included: O_w is stable and P_w's columns may be rewritten.
+            ok = wait_or_abort(&s_full[w], (uint32_t)(j & 1), abort_flag, p.err, 27);
+            if (!__all_sync(kFull, ok)) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
             float x[kBlockKeys];
-            tc::tmem_ld128(tmem + (uint32_t)w * 128 + lane_base, x);
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[w]);  // S buffer read by this warp
+            tc::tmem_ld128(tS, x);
             // Row max in log2 units.  With a positive scale the max of the
             // raw scores is taken and scaled once, and the scale is folded
             // into the exponent below (p = 2^(x * sc - m)); only the block
@@ -317,101 +327,86 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                 }
                 sc = 1.f;
             }
-            // PV of this group's previous block done: O_w is stable and P_w free.
-            if (j >= 2) {
-                ok = wait_or_abort(&pv_done[w], (uint32_t)(((j - 2) >> 1) & 1), abort_flag, p.err, 28);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after_sync();
-            }
             if (mx > m_ref + kRescaleThreshold) {  // also the first block (m_ref = -inf)
-                if (j >= 2) {
+                if (j > 0) {
                     const float alpha = exp2f(m_ref - mx);
                     l_run *= alpha;
 #pragma unroll 1
                     for (int c = 0; c < kD / 32; ++c) {  // 32 columns at a time: x[] stays live
                         float ob[32];
-                        tc::tmem_ld32(tOw + lane_base + 32 * c, ob);
+                        tc::tmem_ld32(tO + 32 * c, ob);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) ob[i] *= alpha;
-                        tc::tmem_st32(tOw + lane_base + 32 * c, ob);
+                        tc::tmem_st32(tO + 32 * c, ob);
                     }
                 }
                 m_ref = mx;
             }
+            // P as fp16 pairs, key 2c in the low half of column c, written
+            // over S (this thread's own TMEM lane, already read).
             float ps4[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
             const float nm = -m_ref;
 #pragma unroll
-            for (int chunk16 = 0; chunk16 < 16; ++chunk16) {  // 8 keys = one 16-byte chunk of P
-                uint32_t pk[4];
+            for (int hh = 0; hh < 2; ++hh) {
+                float pk[32];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i0 = chunk16 * 8 + 2 * e;
+                for (int c = 0; c < 32; ++c) {
+                    const int i0 = 64 * hh + 2 * c;
                     const float p0 = fast_exp2(fmaf(x[i0], sc, nm));  // masked keys: 2^-inf = 0
                     const float p1 = fast_exp2(fmaf(x[i0 + 1], sc, nm));
-                    ps4[e] += p0 + p1;
+                    ps4[c & 3] += p0 + p1;
                     const __half2 h2 = __floats2half2_rn(p0, p1);
-                    pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                    pk[c] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h2));
                 }
-                const int half = chunk16 >> 3;
-                const int pos = (chunk16 & 7) ^ (row_t & 7);  // 128-byte swizzle
-                *reinterpret_cast<uint4*>(Pw + half * kHalf + row_t * 128 + pos * 16) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                tc::tmem_st32(tS + 32 * hh, pk);
             }
             l_run += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
             tc::fence_before_sync();
-            tc::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[w]);  // P_j (and any O rescale) done by this warp
+            if (lane == 0) mbar_arrive(&p_full[w]);  // P_w(j) (and any O rescale) done by this warp
         }
-        // ---- this group's state of row row_t, after its last PV
-        if (ok && jl >= 0) ok = wait_or_abort(&pv_done[w], (uint32_t)((jl >> 1) & 1), abort_flag, p.err, 29);
-        ok = __all_sync(0xffffffffu, ok);
-        if (w == 1) {  // hand (m, l) to group 0 (l = 0: no block, O_1 unused)
-            ml[2 * row_t] = ok ? m_ref : -INFINITY;
-            ml[2 * row_t + 1] = ok ? l_run : 0.f;
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(merge_bar);
-        } else {
-            ok = __all_sync(0xffffffffu, ok && wait_or_abort(merge_bar, 0, abort_flag, p.err, 30));
-            if (ok) {
-                tc::fence_after_sync();
-                const float m1 = ml[2 * row_t], l1 = ml[2 * row_t + 1];
-                // Two-state merge of the groups' states ([F2] §③): weights
-                // relative to the larger max; an empty state weighs 0.
-                const float M = fmaxf(m_ref, m1);
-                const float a0 = l_run > 0.f ? exp2f(m_ref - M) : 0.f;
-                const float a1 = l1 > 0.f ? exp2f(m1 - M) : 0.f;
-                const float L = a0 * l_run + a1 * l1;
-                const float inv = L > 0.f ? 1.f / L : 0.f;
-                const float c0 = a0 * inv, c1 = a1 * inv;
-                const int rows_per_req = p.G;
-                const int r = mtile * (kM / rows_per_req) + row_t / rows_per_req;
-                const int g = row_t % rows_per_req;
-                const int64_t row = (int64_t)r * p.Hq + hkv * p.G + g;
-                float* dst = p.pre_part + (row * p.nchunks + chunk) * kD;
+        // ---- this chunk's state of row row_t of M tile w, after its last PV.
+        // Every MMA of the CTA is complete once both groups' last PVs are,
+        // and the last S MMAs were issued before them: Q_w and K stage w
+        // (64 KB) are free and stage this group's 128 normalised rows, which
+        // each warp then stores row by row with coalesced 512-byte writes
+        // (one thread per row would write 16-byte pieces of 32 rows at once).
+        if (ok) ok = wait_or_abort(&pv_done[w], (uint32_t)((nb - 1) & 1), abort_flag, p.err, 29);
+        if (__all_sync(kFull, ok)) {
+            tc::fence_after_sync();
+            auto stage_row = [&](int r) -> uint8_t* {  // 512 bytes per row, chunks XOR-swizzled by row
+                return r < 64 ? Qs + w * kTile + r * 512 : Ks + w * kTile + (r - 64) * 512;
+            };
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            uint8_t* mine = stage_row(row_t);
 #pragma unroll 1
-                for (int c = 0; c < kD / 32; ++c) {
-                    float o0[32], o1[32];
-                    tc::tmem_ld32(tmem + 256 + lane_base + 32 * c, o0);
-                    if (l1 > 0.f) {
-                        tc::tmem_ld32(tmem + 384 + lane_base + 32 * c, o1);
-                    } else {
+            for (int c = 0; c < kD / 32; ++c) {
+                float ob[32];
+                tc::tmem_ld32(tO + 32 * c, ob);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o1[i] = 0.f;
-                    }
-                    if (r < p.B) {
-#pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4*>(dst + 32 * c + i) = make_float4(
-                                c0 * o0[i] + c1 * o1[i], c0 * o0[i + 1] + c1 * o1[i + 1],
-                                c0 * o0[i + 2] + c1 * o1[i + 2], c0 * o0[i + 3] + c1 * o1[i + 3]);
-                    }
+                for (int q = 0; q < 8; ++q)
+                    *reinterpret_cast<float4*>(mine + (((8 * c + q) ^ (row_t & 31)) << 4)) =
+                        make_float4(ob[4 * q] * inv, ob[4 * q + 1] * inv, ob[4 * q + 2] * inv,
+                                    ob[4 * q + 3] * inv);
+            }
+            const int rows_per_req = p.G;
+            const int req0 = (2 * mpair + w) * (kM / rows_per_req);
+            {
+                const int r = req0 + row_t / rows_per_req, g = row_t % rows_per_req;
+                if (r < p.B)
+                    p.pre_lse[((int64_t)r * p.Hq + hkv * p.G + g) * p.nchunks + chunk] =
+                        l_run > 0.f ? m_ref + log2f(l_run) : -INFINITY;
+            }
+            __syncwarp();  // this warp's 32 rows are staged
+#pragma unroll 4
+            for (int i = 0; i < 32; ++i) {
+                const int rt = (warp & 3) * 32 + i;
+                const int r = req0 + rt / rows_per_req, g = rt % rows_per_req;
+                if (r < p.B) {
+                    const float4 v = *reinterpret_cast<const float4*>(stage_row(rt) + ((lane ^ (rt & 31)) << 4));
+                    float* dst = p.pre_part + (((int64_t)r * p.Hq + hkv * p.G + g) * p.nchunks + chunk) * kD;
+                    *reinterpret_cast<float4*>(dst + 4 * lane) = v;
                 }
-                if (r < p.B) p.pre_lse[row * p.nchunks + chunk] = L > 0.f ? M + log2f(L) : -INFINITY;
             }
         }
     }
@@ -429,8 +424,9 @@ void cascade_prefix_geometry(int B, int G, int Hkv, int prefix_len, int sm_count
                              int* blocks_per_chunk, int* nchunks) {
     const int nblocks = (prefix_len + kBlockKeys - 1) / kBlockKeys;
     const int mt = (B * G + kM - 1) / kM;
-    // About one CTA per SM: chunks = SMs / (Hkv * M tiles), at least one block each.
-    int want = sm_count / (Hkv * mt > 0 ? Hkv * mt : 1);
+    const int pairs = (mt + 1) / 2;  // a CTA takes two M tiles
+    // About one CTA per SM: chunks = SMs / (Hkv * pairs), at least one block each.
+    int want = sm_count / (Hkv * pairs > 0 ? Hkv * pairs : 1);
     if (want < 1) want = 1;
     if (want > nblocks) want = nblocks;
     int bpc = nblocks > 0 ? (nblocks + want - 1) / want : 1;
@@ -472,7 +468,7 @@ cudaError_t launch_cascade_prefix(const CascadeArgs& a, const DeviceInfo& dev, f
     e = cudaFuncSetAttribute(cascade_prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    cascade_prefix_kernel<<<dim3(nchunks, mtiles, a.Hkv), kThreads, smem, st>>>(tq, tk, tv, p);
+    cascade_prefix_kernel<<<dim3(nchunks, (mtiles + 1) / 2, a.Hkv), kThreads, smem, st>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 

@@ -607,6 +607,73 @@ combine_kernel(const CombineParams p) {
     }
 }
 
+// Cascade combine with many rows: two warps per row, so that the row's two
+// lists are read at once -- warp 0 merges the suffix's split states, warp 1
+// the prefix chunks' states into the prefix state (written to o_pre/s_pre)
+// -- and they meet in shared memory for the two-state merge, prefix first.
+template <typename Tout>
+__global__ void __launch_bounds__(kCombWarps * 32)
+cascade_combine_kernel(const CombineParams p) {
+    pdl_wait_primary();  // the states are written by the preceding grids
+    __shared__ CombSmem sm;  // unused by merge_row<1>
+    __shared__ __align__(16) float pre_v[kCombWarps / 2][kD];
+    __shared__ float pre_s[kCombWarps / 2];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = w & 1, slot = w >> 1;
+    const int64_t row_raw = (int64_t)blockIdx.x * (kCombWarps / 2) + slot;
+    const bool row_ok = row_raw < p.rows;
+    const int64_t row = row_ok ? row_raw : p.rows - 1;  // every warp reaches the barrier
+    const bool has = 4 * lane < p.D;
+    float v[4] = {0.f, 0.f, 0.f, 0.f}, s = -INFINITY;
+    if (sub == 0) {
+        merge_row<1>(p.o_part, p.lse_part, p.NS, p.D, row, 0, sm, v, s);
+    } else {
+        if (p.C > 0) merge_row<1>(p.pre_part, p.pre_lse, p.C, p.D, row, 0, sm, v, s);
+        if (row_ok) {
+            if (p.o_pre != nullptr && has)
+                *reinterpret_cast<float4*>(p.o_pre + row * p.D + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
+            if (p.s_pre != nullptr && lane == 0) p.s_pre[row] = s;
+        }
+        if (has) *reinterpret_cast<float4*>(&pre_v[slot][4 * lane]) = make_float4(v[0], v[1], v[2], v[3]);
+        if (lane == 0) pre_s[slot] = s;
+    }
+    __syncthreads();
+    if (sub != 0 || !row_ok) return;
+    float vp[4] = {0.f, 0.f, 0.f, 0.f};
+    if (has) {
+        const float4 t = *reinterpret_cast<const float4*>(&pre_v[slot][4 * lane]);
+        vp[0] = t.x; vp[1] = t.y; vp[2] = t.z; vp[3] = t.w;
+    }
+    // Two-state merge, prefix first ([F2] §③, guards of §⑤ and [FA] §2.2).
+    const float se = sanitize_lse(pre_s[slot]), sb = sanitize_lse(s);
+    const float mm = fmaxf(se, sb);
+    const float we = merge_weight(se, mm), wb = merge_weight(sb, mm);
+    const float ws = __fadd_rn(we, wb);
+    const float iv = ws > 0.f ? 1.f / ws : 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float te = we > 0.f ? __fmul_rn(we, vp[i]) : 0.f;
+        const float tb = wb > 0.f ? __fmul_rn(wb, v[i]) : 0.f;
+        v[i] = __fmul_rn(__fadd_rn(te, tb), iv);
+    }
+    const float so = mm + log2f(ws);
+    if (lane == 0 && p.lse_out != nullptr) p.lse_out[row] = so;
+    constexpr int EO = Vec<Tout>::N;
+    char* orow = reinterpret_cast<char*>(p.out) + row * p.D * (int64_t)sizeof(Tout);
+    if constexpr (EO == 4) {
+        if (has) *reinterpret_cast<float4*>(orow + lane * 16) = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+        float f[8];
+        const float o0 = __shfl_down_sync(0xffffffffu, v[0], 1);
+        const float o1 = __shfl_down_sync(0xffffffffu, v[1], 1);
+        const float o2 = __shfl_down_sync(0xffffffffu, v[2], 1);
+        const float o3 = __shfl_down_sync(0xffffffffu, v[3], 1);
+        f[0] = v[0]; f[1] = v[1]; f[2] = v[2]; f[3] = v[3];
+        f[4] = o0; f[5] = o1; f[6] = o2; f[7] = o3;
+        if ((lane & 1) == 0 && 4 * lane < p.D) st_stream(orow + lane * 8, from_float<Tout>(f));
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_splitkv_decode(const DecodeArgs& a, const DeviceInfo& dev, cudaStream_t st) {
@@ -661,8 +728,11 @@ cudaError_t launch_combine(const CombineArgs& a, bool pdl, const DeviceInfo& dev
     p.rows = a.rows;
     // Many rows: one warp per row (4 rows per CTA).  Few rows: 4 warps per row.
     const bool wide = a.rows >= 2LL * dev.sm_count * 4;
+    const bool cascade = wide && a.pre_part != nullptr && a.NS <= kCombBatch && a.C <= kCombBatch;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(wide ? (a.rows + kCombWarps - 1) / kCombWarps : a.rows), 1, 1);
+    cfg.gridDim = dim3((unsigned)(cascade ? (a.rows + kCombWarps / 2 - 1) / (kCombWarps / 2)
+                                          : (wide ? (a.rows + kCombWarps - 1) / kCombWarps : a.rows)),
+                       1, 1);
     cfg.blockDim = dim3(kCombWarps * 32, 1, 1);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -671,8 +741,9 @@ cudaError_t launch_combine(const CombineArgs& a, bool pdl, const DeviceInfo& dev
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
 #define SKV_COMB(T_) \
-    (wide ? cudaLaunchKernelEx(&cfg, combine_kernel<T_, 1>, p) \
-          : cudaLaunchKernelEx(&cfg, combine_kernel<T_, kCombWarps>, p))
+    (cascade ? cudaLaunchKernelEx(&cfg, cascade_combine_kernel<T_>, p) \
+             : (wide ? cudaLaunchKernelEx(&cfg, combine_kernel<T_, 1>, p) \
+                     : cudaLaunchKernelEx(&cfg, combine_kernel<T_, kCombWarps>, p)))
     switch (a.out_dt) {
         case SKV_F32: return SKV_COMB(float);
         case SKV_F16: return SKV_COMB(__half);
