@@ -65,6 +65,23 @@ SKV_DEVINL float dot2_h(uint32_t a, uint32_t b, float acc) {
         : "+f"(acc) : "r"(a), "r"(b));
     return acc;
 }
+// acc += a.lo * b.lo (HI = false) or a.hi * b.hi, fp16 operands, fp32 sum.
+template <bool HI>
+SKV_DEVINL float fma_h(uint32_t a, uint32_t b, float acc) {
+    if constexpr (HI)
+        asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+            "mov.b32 {a0, a1}, %1;\n\t"
+            "mov.b32 {b0, b1}, %2;\n\t"
+            "fma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
+            : "+f"(acc) : "r"(a), "r"(b));
+    else
+        asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+            "mov.b32 {a0, a1}, %1;\n\t"
+            "mov.b32 {b0, b1}, %2;\n\t"
+            "fma.rn.f32.f16 %0, a0, b0, %0;\n\t}"
+            : "+f"(acc) : "r"(a), "r"(b));
+    return acc;
+}
 // (o0, o1) += p * (v.lo, v.hi) where p is the low (HI = false) or high half
 // of `pw`; fp16 operands, fp32 accumulators.
 template <bool HI>
@@ -249,25 +266,42 @@ splitkv_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const DecodePa
             sc += __shfl_xor_sync(kFull, sc, 16);
             x[0] = t < nvalid ? sc * p.scale_log2 : -INFINITY;
         } else {
+            // The lane's TPL tokens side by side, and the low and high fp16
+            // halves of each word into separate sums: 8 * TPL independent
+            // FMA chains, each advanced once per 16-byte chunk of K.
+            float acc[TPL][8];
+#pragma unroll
+            for (int j = 0; j < TPL; ++j)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[j][i] = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 kv[TPL];
+#pragma unroll
+                    for (int j = 0; j < TPL; ++j) {
+                        const int t = x_lane + j * TGN;
+                        kv[j] = *reinterpret_cast<const uint4*>(Kb + h * kBoxBytes + t * 128 +
+                                                                ((c << 4) ^ ((t & 7) << 4)));
+                    }
+                    const int qi = 32 * h + 4 * c;
+#pragma unroll
+                    for (int j = 0; j < TPL; ++j) {
+                        const uint32_t kw[4] = {kv[j].x, kv[j].y, kv[j].z, kv[j].w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            acc[j][2 * i] = fma_h<false>(qh[qi + i], kw[i], acc[j][2 * i]);
+                            acc[j][2 * i + 1] = fma_h<true>(qh[qi + i], kw[i], acc[j][2 * i + 1]);
+                        }
+                    }
+                }
+            }
 #pragma unroll
             for (int j = 0; j < TPL; ++j) {
                 const int t = x_lane + j * TGN;
-                const uint32_t sw = (t & 7) << 4;
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint8_t* rowp = Kb + h * kBoxBytes + t * 128;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 kv = *reinterpret_cast<const uint4*>(rowp + ((c << 4) ^ sw));
-                        const int qi = 32 * h + 4 * c;
-                        acc[c & 3] = dot2_h(qh[qi + 0], kv.x, acc[c & 3]);
-                        acc[c & 3] = dot2_h(qh[qi + 1], kv.y, acc[c & 3]);
-                        acc[c & 3] = dot2_h(qh[qi + 2], kv.z, acc[c & 3]);
-                        acc[c & 3] = dot2_h(qh[qi + 3], kv.w, acc[c & 3]);
-                    }
-                }
-                const float sc = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                const float sc = ((acc[j][0] + acc[j][1]) + (acc[j][2] + acc[j][3])) +
+                                 ((acc[j][4] + acc[j][5]) + (acc[j][6] + acc[j][7]));
                 x[j] = t < nvalid ? sc * p.scale_log2 : -INFINITY;
             }
         }
@@ -463,42 +497,44 @@ struct WarpState {
 };
 
 // This warp's share (states sub, sub + WPR, ...) of the N states of `row`.
+// Per batch of kCombBatch states: lane k (and lane k + 16) reads state k's
+// lse and computes its weight, the batch max and weight sum go through
+// shuffles, and every lane then accumulates its 4 dims of the batch's v rows
+// with the weights broadcast from their lanes.
 template <int WPR>
 SKV_DEVINL WarpState warp_merge(const float* o, const float* lse, int N, int D, int64_t row,
                                 int sub) {
+    static_assert(kCombBatch == 16, "two lanes per state in a batch");
     const int lane = threadIdx.x & 31;
     const bool has = 4 * lane < D;
     WarpState st{-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
     for (int n0 = sub; n0 < N; n0 += WPR * kCombBatch) {
-        float l[kCombBatch];
+        const int nk = n0 + (lane & 15) * WPR;
+        const float lk = nk < N ? sanitize_lse(__ldcg(lse + row * N + nk)) : -INFINITY;
         float4 x[kCombBatch];
 #pragma unroll
         for (int k = 0; k < kCombBatch; ++k) {
             const int n = n0 + k * WPR;
-            l[k] = -INFINITY;
-            x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (n < N) {
-                l[k] = sanitize_lse(ld_cg_f32(lse + row * N + n));
-                if (has) {
-                    const uint4 r = ld_cg(o + (row * N + n) * D + 4 * lane);
-                    x[k] = make_float4(__uint_as_float(r.x), __uint_as_float(r.y),
-                                       __uint_as_float(r.z), __uint_as_float(r.w));
-                }
-            }
+            x[k] = (n < N && has) ? __ldcg(reinterpret_cast<const float4*>(o + (row * N + n) * D) + lane)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        float mb = st.m;
+        float mb = lk;
 #pragma unroll
-        for (int k = 0; k < kCombBatch; ++k) mb = fmaxf(mb, l[k]);
+        for (int mm = 1; mm < 16; mm <<= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, mm));
+        mb = fmaxf(mb, st.m);
+        const float wk = merge_weight(lk, mb);
+        float ws = wk;
+#pragma unroll
+        for (int mm = 1; mm < 16; mm <<= 1) ws += __shfl_xor_sync(kFull, ws, mm);
         const float sc = merge_weight(st.m, mb);  // rescale of the running state
-        st.W *= sc;
+        st.W = fmaf(st.W, sc, ws);
         st.acc.x *= sc; st.acc.y *= sc; st.acc.z *= sc; st.acc.w *= sc;
 #pragma unroll
         for (int k = 0; k < kCombBatch; ++k) {
-            const float wk = merge_weight(l[k], mb);
-            if (wk > 0.f) {  // a zero-weight state is not read into the result
-                st.W += wk;
-                st.acc.x = fmaf(wk, x[k].x, st.acc.x); st.acc.y = fmaf(wk, x[k].y, st.acc.y);
-                st.acc.z = fmaf(wk, x[k].z, st.acc.z); st.acc.w = fmaf(wk, x[k].w, st.acc.w);
+            const float w = __shfl_sync(kFull, wk, k);
+            if (w > 0.f) {  // a zero-weight state is not read into the result
+                st.acc.x = fmaf(w, x[k].x, st.acc.x); st.acc.y = fmaf(w, x[k].y, st.acc.y);
+                st.acc.z = fmaf(w, x[k].z, st.acc.z); st.acc.w = fmaf(w, x[k].w, st.acc.w);
             }
         }
         st.m = mb;
