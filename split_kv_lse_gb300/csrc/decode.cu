@@ -13,24 +13,24 @@
 //   * One CTA per (b, hkv, split) serves all G = Hq/Hkv query heads of that
 //     KV head, so each K/V byte fetched from HBM feeds G heads.
 //   * W warps; warp w owns the split's pages w, w + W, ... and R/W ring slots.
-//     A slot holds one (page, kv-head) tile: K as two 64-dim boxes copied by
-//     TMA tensor loads with the 128-byte swizzle, V as one contiguous 4 KB
-//     bulk copy, completion counted on the slot's mbarrier.  The warp refills
-//     a slot as soon as it has consumed it.
+//     A slot holds one (page, kv-head) tile: K and V, each one contiguous
+//     4 KB run of its cache, copied by two bulk copies (TMA engine) that two
+//     lanes issue in one instruction, completion counted on the slot's
+//     mbarrier.  The warp refills a slot as soon as it has consumed it.
 //   * QK: lane (g, tg) owns whole dot products -- head g, tokens tg + j*TGN --
 //     over all 128 dims, with q resident in registers, so no cross-lane
-//     reduction; the swizzle makes the lanes' reads of different rows at the
-//     same column bank-conflict free.  fp16 x fp16 -> fp32 FMAs
-//     (fma.rn.f32.f16): the products are exact, no conversions.
+//     reduction.  A lane walks the 16-byte chunks of its rows in an order
+//     rotated by its token (q is held rotated the same way), so the lanes'
+//     reads of different rows fall in different banks.  fp16 x fp16 -> fp32
+//     FMAs (fma.rn.f32.f16): the products are exact, no conversions.
 //   * Online softmax in base 2 ([F2] §② exp2 trick) per head; the lanes of
 //     a head hold its running max, so the rescale factor never crosses lanes.
 //     p goes through shared memory as fp16 to the PV product, where lane
 //     (g, dc) owns head g's dims of 16-byte chunks dc, dc + TGN, ....
-//   * CUDA cores only: this pass is bound by HBM, not by math.
+//   * CUDA cores only (the pages put tensor cores in the shared-prefix pass).
 #include "common.cuh"
 #include "kernels.h"
 #include "split_range.h"
-#include "tma.h"
 
 namespace skv {
 namespace {
@@ -43,6 +43,7 @@ constexpr unsigned kFull = 0xffffffffu;
 
 struct DecodeParams {
     const __half* q;
+    const __half* k_cache;
     const __half* v_cache;
     const int32_t* block_table;
     const int32_t* ctx;
@@ -115,7 +116,6 @@ template <int G> struct Roles {
     static constexpr int DPL = G == 1 ? 4 : 8 * CPL;  // output dims per lane
 };
 
-constexpr int kBoxBytes = kPage * 128;  // one 16 x 64 fp16 K box (2 KB)
 
 // The barriers take R words, rounded up to 16 bytes: the p buffer after them
 // is read with 16-byte loads.
@@ -132,7 +132,7 @@ constexpr size_t smem_bytes() {
 
 template <int G, int W, int R>
 __global__ void __launch_bounds__(W * 32)
-splitkv_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const DecodeParams p) {
+splitkv_decode_kernel(const DecodeParams p) {
     using Ro = Roles<G>;
     constexpr int TGN = Ro::TGN, TPL = Ro::TPL, CPL = Ro::CPL, DPL = Ro::DPL;
     constexpr int SPW = R / W;  // ring slots per warp
@@ -152,7 +152,6 @@ splitkv_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const DecodePa
 
     // The combine grid may be scheduled now; it waits for this grid to finish.
     pdl_launch_dependents();
-    if (threadIdx.x == 0) tma_prefetch_desc(&tmap_k);
 
     int ctx = p.ctx[b];
     const int cap = p.max_pages * kPage;
@@ -182,11 +181,15 @@ splitkv_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const DecodePa
     constexpr int QW = G == 1 ? 32 : 64;
     uint32_t qh[QW];
     {
+        // Rotated: register chunk i holds q chunk (i + r) mod n, r = the
+        // lane's token (G == 1: within its half of the head dim).
         const __half* qrow = p.q + ((int64_t)b * p.Hq + hkv * G + g_lane) * kD +
                              (G == 1 ? 64 * (lane >> 4) : 0);
+        constexpr int nq = QW / 4;
+        const int r = G == 1 ? (lane & 15) : x_lane;
 #pragma unroll
-        for (int i = 0; i < QW / 4; ++i) {
-            const uint4 a = ld_pinned(qrow + 8 * i);
+        for (int i = 0; i < nq; ++i) {
+            const uint4 a = ld_pinned(qrow + 8 * ((i + r) & (nq - 1)));
             qh[4 * i + 0] = a.x; qh[4 * i + 1] = a.y; qh[4 * i + 2] = a.z; qh[4 * i + 3] = a.w;
         }
     }
@@ -198,26 +201,28 @@ splitkv_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const DecodePa
     // Page ids of this warp's pages k in [kb, kb + 32), one per lane.
     int kb = 0;
     int my_id = (lane < nw) ? bt[p0 + warp + lane * W] : 0;
-    auto issue = [&](int k) {  // warp-uniform call; lane 0 issues the copies
+    auto issue = [&](int k) {  // warp-uniform call; lanes 0 and 1 issue the copies
         if (k - kb >= 32) {
             kb += 32;
             my_id = (kb + lane < nw) ? bt[p0 + warp + (kb + lane) * W] : 0;
         }
         int pid = __shfl_sync(kFull, my_id, k - kb);
-        if (lane == 0) {
-            if ((unsigned)pid >= (unsigned)p.num_pool_pages) {
-                record_error(p.err, SKV_ERR_INVALID_ARG, 1 << 20 | b);
-                pid = 0;
-            }
-            const int slot = k % SPW;
-            uint64_t* bar = &my_bars[slot];
-            uint8_t* dst = my_ring + slot * kStageBytes;
-            const int row = (pid * p.Hkv + hkv) * kPage;  // first row of the tile in [P*Hkv*16, 128]
-            mbar_arrive_expect_tx(bar, kStageBytes);
-            tma_load_2d(dst, &tmap_k, 0, row, bar, pol);
-            tma_load_2d(dst + kBoxBytes, &tmap_k, 64, row, bar, pol);
-            bulk_g2s(dst + kTileBytes, p.v_cache + (int64_t)row * kD, kTileBytes, bar, pol);
+        if ((unsigned)pid >= (unsigned)p.num_pool_pages) {
+            if (lane == 0) record_error(p.err, SKV_ERR_INVALID_ARG, 1 << 20 | b);
+            pid = 0;
         }
+        const int slot = k % SPW;
+        uint64_t* bar = &my_bars[slot];
+        uint8_t* dst = my_ring + slot * kStageBytes;
+        const int64_t row = ((int64_t)pid * p.Hkv + hkv) * kPage;  // first row of the tile
+        if (lane == 0) mbar_arrive_expect_tx(bar, kStageBytes);
+        __syncwarp();
+        // The K and V tiles are each one contiguous 4 KB run of the cache:
+        // two bulk copies, issued by two lanes in one instruction (one thread
+        // issuing its copies back to back is held up by the copy engine).
+        if (lane < 2)
+            bulk_g2s(dst + lane * kTileBytes, (lane == 0 ? p.k_cache : p.v_cache) + row * kD,
+                     kTileBytes, bar, pol);
     };
 #pragma unroll 1
     for (int k = 0; k < SPW && k < nw; ++k) issue(k);
@@ -249,14 +254,14 @@ splitkv_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const DecodePa
         float x[TPL];
         if constexpr (G == 1) {
             const int t = lane & 15, dh = lane >> 4;
-            const uint8_t* rowp = Kb + dh * kBoxBytes + t * 128;
-            const uint32_t sw = (t & 7) << 4;
+            const uint8_t* rowp = Kb + t * (kD * 2) + dh * 128;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                // logical chunk c of row t sits at c ^ (t & 7): lanes reading
-                // different rows at the same logical chunk hit distinct banks
-                const uint4 kv = *reinterpret_cast<const uint4*>(rowp + ((c << 4) ^ sw));
+                // Step c reads chunk (c + t) & 7 of the lane's half row (q is
+                // held rotated to match), so lanes of different rows read
+                // different banks.
+                const uint4 kv = *reinterpret_cast<const uint4*>(rowp + (((c + t) & 7) << 4));
                 acc[c & 3] = dot2_h(qh[4 * c + 0], kv.x, acc[c & 3]);
                 acc[c & 3] = dot2_h(qh[4 * c + 1], kv.y, acc[c & 3]);
                 acc[c & 3] = dot2_h(qh[4 * c + 2], kv.z, acc[c & 3]);
@@ -274,26 +279,25 @@ splitkv_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const DecodePa
             for (int j = 0; j < TPL; ++j)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) acc[j][i] = 0.f;
+            // Step c reads chunk (c + t) & 15 of row t: the lanes of a head
+            // read different banks.  The lane's q is held rotated by x_lane,
+            // so token t = x_lane + j * TGN meets q chunk (c + j * TGN) & 15.
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int c = 0; c < 16; ++c) {
+                uint4 kv[TPL];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint4 kv[TPL];
+                for (int j = 0; j < TPL; ++j) {
+                    const int t = x_lane + j * TGN;
+                    kv[j] = *reinterpret_cast<const uint4*>(Kb + t * (kD * 2) + (((c + t) & 15) << 4));
+                }
 #pragma unroll
-                    for (int j = 0; j < TPL; ++j) {
-                        const int t = x_lane + j * TGN;
-                        kv[j] = *reinterpret_cast<const uint4*>(Kb + h * kBoxBytes + t * 128 +
-                                                                ((c << 4) ^ ((t & 7) << 4)));
-                    }
-                    const int qi = 32 * h + 4 * c;
+                for (int j = 0; j < TPL; ++j) {
+                    const int qi = 4 * ((c + j * TGN) & 15);
+                    const uint32_t kw[4] = {kv[j].x, kv[j].y, kv[j].z, kv[j].w};
 #pragma unroll
-                    for (int j = 0; j < TPL; ++j) {
-                        const uint32_t kw[4] = {kv[j].x, kv[j].y, kv[j].z, kv[j].w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            acc[j][2 * i] = fma_h<false>(qh[qi + i], kw[i], acc[j][2 * i]);
-                            acc[j][2 * i + 1] = fma_h<true>(qh[qi + i], kw[i], acc[j][2 * i + 1]);
-                        }
+                    for (int i = 0; i < 4; ++i) {
+                        acc[j][2 * i] = fma_h<false>(qh[qi + i], kw[i], acc[j][2 * i]);
+                        acc[j][2 * i + 1] = fma_h<true>(qh[qi + i], kw[i], acc[j][2 * i + 1]);
                     }
                 }
             }
@@ -433,7 +437,7 @@ splitkv_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const DecodePa
 }
 
 template <int G, int W, int R>
-cudaError_t launch_gwr(const CUtensorMap& tk, const DecodeParams& p, int B, int Hkv, int NS,
+cudaError_t launch_gwr(const DecodeParams& p, int B, int Hkv, int NS,
                        cudaStream_t st) {
     constexpr size_t smem = smem_bytes<G, W, R>();
     auto kern = splitkv_decode_kernel<G, W, R>;
@@ -445,7 +449,7 @@ cudaError_t launch_gwr(const CUtensorMap& tk, const DecodeParams& p, int B, int 
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    kern<<<dim3(NS, Hkv, B), W * 32, smem, st>>>(tk, p);
+    kern<<<dim3(NS, Hkv, B), W * 32, smem, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -454,16 +458,16 @@ cudaError_t launch_gwr(const CUtensorMap& tk, const DecodeParams& p, int B, int 
 // short splits smaller CTAs, so that many more of them are resident per SM
 // and their fixed latencies (q, page table, first copies) overlap.
 template <int G>
-cudaError_t launch_g(const CUtensorMap& tk, const DecodeParams& p, int B, int Hkv, int NS,
+cudaError_t launch_g(const DecodeParams& p, int B, int Hkv, int NS,
                      int max_pages, cudaStream_t st) {
     // Measured on the cascade suffixes (<= 8 pages per split, B=64, NS=16):
     // pass 1 takes 53 us with 1 warp and a 2-page ring (about 13 CTAs per
     // SM), 64 us with 2 warps, 72 us with 3; a 4-page ring for the 1-warp
     // CTA (fewer CTAs per SM) takes 74 us.  Long splits (32 pages) keep 3.
     const int pps = (max_pages + NS - 1) / NS;
-    if (pps <= 8) return launch_gwr<G, 1, 2>(tk, p, B, Hkv, NS, st);
-    if (pps <= 16) return launch_gwr<G, 2, 4>(tk, p, B, Hkv, NS, st);
-    return launch_gwr<G, 3, 6>(tk, p, B, Hkv, NS, st);
+    if (pps <= 8) return launch_gwr<G, 1, 2>(p, B, Hkv, NS, st);
+    if (pps <= 16) return launch_gwr<G, 2, 4>(p, B, Hkv, NS, st);
+    return launch_gwr<G, 3, 6>(p, B, Hkv, NS, st);
 }
 
 // ---------------------------------------------------------------- combine (pass 2)
@@ -713,14 +717,9 @@ cascade_combine_kernel(const CombineParams p) {
 }  // namespace
 
 cudaError_t launch_splitkv_decode(const DecodeArgs& a, const DeviceInfo& dev, cudaStream_t st) {
-    // K cache viewed as [P * Hkv * page rows, 128 cols] fp16; boxes of
-    // 16 rows x 64 cols (one page tile, half of the head dim), 128-byte swizzle.
-    CUtensorMap tk;
-    cudaError_t e = make_tmap_2d_16bit(&tk, a.k_cache, (uint64_t)a.num_pool_pages * a.Hkv * kPage,
-                                       kD, kD * 2, 64, kPage, true, false);
-    if (e != cudaSuccess) return e;
     DecodeParams p;
     p.q = static_cast<const __half*>(a.q);
+    p.k_cache = static_cast<const __half*>(a.k_cache);
     p.v_cache = static_cast<const __half*>(a.v_cache);
     p.block_table = a.block_table;
     p.ctx = a.ctx;
@@ -735,10 +734,10 @@ cudaError_t launch_splitkv_decode(const DecodeArgs& a, const DeviceInfo& dev, cu
     p.NS = a.num_splits;
     p.scale_log2 = a.sm_scale * 1.4426950408889634f;
     switch (a.Hq / a.Hkv) {
-        case 1: return launch_g<1>(tk, p, a.B, a.Hkv, a.num_splits, a.max_pages, st);
-        case 2: return launch_g<2>(tk, p, a.B, a.Hkv, a.num_splits, a.max_pages, st);
-        case 4: return launch_g<4>(tk, p, a.B, a.Hkv, a.num_splits, a.max_pages, st);
-        case 8: return launch_g<8>(tk, p, a.B, a.Hkv, a.num_splits, a.max_pages, st);
+        case 1: return launch_g<1>(p, a.B, a.Hkv, a.num_splits, a.max_pages, st);
+        case 2: return launch_g<2>(p, a.B, a.Hkv, a.num_splits, a.max_pages, st);
+        case 4: return launch_g<4>(p, a.B, a.Hkv, a.num_splits, a.max_pages, st);
+        case 8: return launch_g<8>(p, a.B, a.Hkv, a.num_splits, a.max_pages, st);
     }
     return cudaErrorInvalidValue;
 }

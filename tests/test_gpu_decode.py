@@ -149,3 +149,23 @@ def test_decode_partials_only(lib):
     _, _, op2, lp2 = lib.splitkv_decode(g["q"], g["k_cache"], g["v_cache"], g["block_table"],
                                         g["ctx"], 8, d["sm_scale"])
     assert torch.equal(op, op2) and torch.equal(lp, lp2)
+
+
+def test_decode_many_short_splits(lib):
+    """Far more (request, kv head, split) units than resident CTAs, with short
+    ragged contexts, empty splits and ctx = 0: the short-split kernel's CTAs
+    each walk a run of units through one ring."""
+    rng = np.random.default_rng(11)
+    ctx = rng.integers(0, 130, size=300).tolist()
+    ctx[5], ctx[17], ctx[18] = 0, 128, 129
+    d = W.decode_inputs(len(ctx), 32, 8, 128, 16, ctx, seed=11, pool_extra=2)
+    check_decode(lib, d, 16, nan_tail=True)
+
+
+def test_decode_short_splits_many_requests(lib):
+    """More requests than the short-split kernel keeps in shared memory: the
+    one-CTA-per-split kernel serves them."""
+    rng = np.random.default_rng(12)
+    ctx = rng.integers(0, 40, size=1100).tolist()
+    d = W.decode_inputs(len(ctx), 2, 1, 128, 16, ctx, seed=12)
+    check_decode(lib, d, 4)
