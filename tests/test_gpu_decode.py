@@ -152,9 +152,8 @@ def test_decode_partials_only(lib):
 
 
 def test_decode_many_short_splits(lib):
-    """Far more (request, kv head, split) units than resident CTAs, with short
-    ragged contexts, empty splits and ctx = 0: the short-split kernel's CTAs
-    each walk a run of units through one ring."""
+    """Far more (request, kv head, split) CTAs than fit on the GPU at once
+    (several waves), with short ragged contexts, empty splits and ctx = 0."""
     rng = np.random.default_rng(11)
     ctx = rng.integers(0, 130, size=300).tolist()
     ctx[5], ctx[17], ctx[18] = 0, 128, 129
@@ -163,8 +162,8 @@ def test_decode_many_short_splits(lib):
 
 
 def test_decode_short_splits_many_requests(lib):
-    """More requests than the short-split kernel keeps in shared memory: the
-    one-CTA-per-split kernel serves them."""
+    """Over a thousand requests (the grid's request dimension) with contexts
+    of 0 to 39 tokens."""
     rng = np.random.default_rng(12)
     ctx = rng.integers(0, 40, size=1100).tolist()
     d = W.decode_inputs(len(ctx), 2, 1, 128, 16, ctx, seed=12)
