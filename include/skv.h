@@ -213,8 +213,9 @@ skv_status skv_splitkv_decode_plan(int32_t B, const int32_t* ctx_host, int32_t H
  *   lse_part [B, Hq, num_splits]; out [B, Hq, D]; lse_out [B, Hq].
  * ranges_dbg: NULL, or a device int32 [B, num_splits, 2] receiving the
  *   (p_start, p_end) each CTA computed.
- * Supported: dtype SKV_F16, D = 128, page = 16, G in {1, 2, 4, 8},
- *   1 <= num_splits <= 256.  B = 0 is a no-op.
+ * Supported: dtype SKV_F16 or SKV_BF16 (q, K, V and out; the products are
+ *   exact in fp32, p enters P.V rounded to the dtype), D = 128, page = 16,
+ *   G in {1, 2, 4, 8}, 1 <= num_splits <= 256.  B = 0 is a no-op.
  * Device-side checks: a ctx outside [0, max_pages*page] or a page id outside
  *   [0, num_pool_pages) is clamped into range and flagged in the error word.
  */
@@ -257,7 +258,8 @@ size_t skv_cascade_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
  * empty suffix; both empty give out = 0, lse_out = -inf.
  * workspace: at least skv_cascade_workspace_size(B, Hq, Hkv, D, prefix_len, 0)
  *   bytes, 16-byte aligned; no initial contents are needed.
- * Supported: dtype SKV_F16, D = 128, page = 16, G = Hq/Hkv in {1, 2, 4, 8},
+ * Supported: dtype SKV_F16 or SKV_BF16 (the tensor-core products in the
+ *   same type), D = 128, page = 16, G = Hq/Hkv in {1, 2, 4, 8},
  *   1 <= num_splits <= 256.  Device-side checks as for skv_splitkv_decode
  *   (prefix page ids included).
  */

@@ -198,8 +198,8 @@ skv_status skv_splitkv_decode(const void* q, const void* k_cache, const void* v_
         return SKV_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return SKV_ERR_INVALID_ARG;
     const int G = Hq / Hkv;
-    if (dtype != SKV_F16 || D != 128 || page != 16 || !(G == 1 || G == 2 || G == 4 || G == 8) ||
-        num_splits > 256 || B > 65535 || Hkv > 65535)
+    if ((dtype != SKV_F16 && dtype != SKV_BF16) || D != 128 || page != 16 ||
+        !(G == 1 || G == 2 || G == 4 || G == 8) || num_splits > 256 || B > 65535 || Hkv > 65535)
         return SKV_ERR_UNSUPPORTED;
     if ((int64_t)max_pages * page > INT32_MAX) return SKV_ERR_UNSUPPORTED;
     if (B == 0) return SKV_OK;
@@ -234,6 +234,7 @@ skv_status skv_splitkv_decode(const void* q, const void* k_cache, const void* v_
     a.o_part = o_part;
     a.lse_part = lse_part;
     a.ranges_dbg = ranges_dbg;
+    a.bf16 = dtype == SKV_BF16;
     cudaError_t e = use_tc_decode() ? launch_splitkv_decode_tc(a, *dev, cs)
                                     : launch_splitkv_decode(a, *dev, cs);
     if (e != cudaSuccess) return SKV_ERR_CUDA;
@@ -290,8 +291,8 @@ skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_
         return SKV_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return SKV_ERR_INVALID_ARG;
     const int G = Hq / Hkv;
-    if (dtype != SKV_F16 || D != 128 || page != 16 || !(G == 1 || G == 2 || G == 4 || G == 8) ||
-        num_splits > 256 || B > 65535 || Hkv > 65535)
+    if ((dtype != SKV_F16 && dtype != SKV_BF16) || D != 128 || page != 16 ||
+        !(G == 1 || G == 2 || G == 4 || G == 8) || num_splits > 256 || B > 65535 || Hkv > 65535)
         return SKV_ERR_UNSUPPORTED;
     if ((int64_t)max_pages * page > INT32_MAX ||
         (int64_t)num_pool_pages * Hkv * page > INT32_MAX - page)
@@ -331,6 +332,7 @@ skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_
         ca.B = B;
         ca.Hq = Hq;
         ca.Hkv = Hkv;
+        ca.bf16 = dtype == SKV_BF16;
         ca.sm_scale = sm_scale;
         if (launch_cascade_prefix(ca, *dev, pre_part, pre_lse, nc, bpc, mt, cs) != cudaSuccess)
             return SKV_ERR_CUDA;
@@ -354,6 +356,7 @@ skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_
     a.o_part = o_part;
     a.lse_part = lse_part;
     a.ranges_dbg = nullptr;
+    a.bf16 = dtype == SKV_BF16;
     if ((use_tc_decode() ? launch_splitkv_decode_tc(a, *dev, cs) : launch_splitkv_decode(a, *dev, cs)) !=
         cudaSuccess)
         return SKV_ERR_CUDA;

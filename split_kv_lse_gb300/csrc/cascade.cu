@@ -97,6 +97,7 @@ SKV_DEVINL void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, ui
         : "memory");
 }
 
+template <bool BF>  // q, K, V (and so P) bf16, else fp16
 __global__ void __launch_bounds__(kThreads, 1)
 cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const PrefixParams p) {
@@ -209,8 +210,9 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idS = tc::idesc_f16_f32(kM, kBlockKeys, false);
-            constexpr uint32_t idPV = tc::idesc_f16_f32(kM, kD, true);  // A (P) from TMEM, B (V) MN-major
+            constexpr uint32_t idS = tc::idesc_f16_f32(kM, kBlockKeys, false, false, BF);
+            // A (P) from TMEM, B (V) MN-major
+            constexpr uint32_t idPV = tc::idesc_f16_f32(kM, kD, true, false, BF);
             auto qk = [&](int j, int w) {  // S_w = Q_w K_j^T
                 const int st = j % kStages;
                 const uint8_t* Qw = Qs + w * kTile;
@@ -355,8 +357,15 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                     const float p0 = fast_exp2(fmaf(x[i0], sc, nm));  // masked keys: 2^-inf = 0
                     const float p1 = fast_exp2(fmaf(x[i0 + 1], sc, nm));
                     ps4[c & 3] += p0 + p1;
-                    const __half2 h2 = __floats2half2_rn(p0, p1);
-                    pk[c] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h2));
+                    uint32_t h2;  // (p0, p1) in the operand type, nearest even
+                    if constexpr (BF) {
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+                        h2 = *reinterpret_cast<const uint32_t*>(&b2);
+                    } else {
+                        const __half2 f2 = __floats2half2_rn(p0, p1);
+                        h2 = *reinterpret_cast<const uint32_t*>(&f2);
+                    }
+                    pk[c] = __uint_as_float(h2);
                 }
                 tc::tmem_st32(tS + 32 * hh, pk);
             }
@@ -440,13 +449,15 @@ cudaError_t launch_cascade_prefix(const CascadeArgs& a, const DeviceInfo& dev, f
                                   cudaStream_t st) {
     const int G = a.Hq / a.Hkv;
     CUtensorMap tq, tk, tv;
+    // (fp16 element type for bf16 q too: the copies are bitwise and the
+    // out-of-range fill, zero bits, is +0 in both.)
     cudaError_t e = make_tmap_3d_16bit(&tq, a.q, kD, a.Hq, a.B, (uint64_t)kD * 2,
                                        (uint64_t)a.Hq * kD * 2, 64, G, kM / G, true);
     if (e != cudaSuccess) return e;
     const uint64_t rows = (uint64_t)a.num_pool_pages * a.Hkv * kPage;
-    if ((e = make_tmap_2d_16bit(&tk, a.k_cache, rows, kD, kD * 2, 64, kPage, true, false)) != cudaSuccess)
+    if ((e = make_tmap_2d_16bit(&tk, a.k_cache, rows, kD, kD * 2, 64, kPage, true, a.bf16)) != cudaSuccess)
         return e;
-    if ((e = make_tmap_2d_16bit(&tv, a.v_cache, rows, kD, kD * 2, 64, kPage, true, false)) != cudaSuccess)
+    if ((e = make_tmap_2d_16bit(&tv, a.v_cache, rows, kD, kD * 2, 64, kPage, true, a.bf16)) != cudaSuccess)
         return e;
     PrefixParams p;
     p.prefix_pages = a.prefix_pages;
@@ -465,10 +476,10 @@ cudaError_t launch_cascade_prefix(const CascadeArgs& a, const DeviceInfo& dev, f
     p.err = dev.err;
     const size_t smem = prefix_smem_bytes(blocks_per_chunk);
     if (smem > dev.max_smem_optin) return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(cascade_prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
+    auto kern = a.bf16 ? cascade_prefix_kernel<true> : cascade_prefix_kernel<false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    cascade_prefix_kernel<<<dim3(nchunks, (mtiles + 1) / 2, a.Hkv), kThreads, smem, st>>>(tq, tk, tv, p);
+    kern<<<dim3(nchunks, (mtiles + 1) / 2, a.Hkv), kThreads, smem, st>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 

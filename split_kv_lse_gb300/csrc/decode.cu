@@ -42,9 +42,9 @@ constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
 constexpr unsigned kFull = 0xffffffffu;
 
 struct DecodeParams {
-    const __half* q;
-    const __half* k_cache;
-    const __half* v_cache;
+    const uint16_t* q;  // fp16 or bf16 bit patterns
+    const uint16_t* k_cache;
+    const uint16_t* v_cache;
     const int32_t* block_table;
     const int32_t* ctx;
     float* o_part;
@@ -55,54 +55,61 @@ struct DecodeParams {
     float scale_log2;  // sm_scale * log2(e)
 };
 
-// acc += a.lo * b.lo + a.hi * b.hi with fp16 operands and an fp32 accumulator
-// (mixed-precision FMA: the fp16 products are exact in fp32).
+// Mixed-precision FMAs on 16-bit operand pairs: fp16 (BF = false) or bf16
+// (BF = true) products, exact in fp32, added into fp32 accumulators.
+#define SKV_MIXED_FMA(TY) "fma.rn.f32." TY
+// acc += a.lo * b.lo + a.hi * b.hi.
+template <bool BF>
 SKV_DEVINL float dot2_h(uint32_t a, uint32_t b, float acc) {
-    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
-        "mov.b32 {a0, a1}, %1;\n\t"
-        "mov.b32 {b0, b1}, %2;\n\t"
-        "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
-        "fma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
-        : "+f"(acc) : "r"(a), "r"(b));
+#define SKV_DOT2(TY)                                                  \
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\t"                         \
+        "mov.b32 {a0, a1}, %1;\n\t"                                   \
+        "mov.b32 {b0, b1}, %2;\n\t" SKV_MIXED_FMA(TY) " %0, a0, b0, %0;\n\t" \
+        SKV_MIXED_FMA(TY) " %0, a1, b1, %0;\n\t}"                     \
+        : "+f"(acc) : "r"(a), "r"(b))
+    if constexpr (BF) SKV_DOT2("bf16");
+    else SKV_DOT2("f16");
+#undef SKV_DOT2
     return acc;
 }
-// acc += a.lo * b.lo (HI = false) or a.hi * b.hi, fp16 operands, fp32 sum.
-template <bool HI>
+// acc += a.lo * b.lo (HI = false) or a.hi * b.hi.
+template <bool BF, bool HI>
 SKV_DEVINL float fma_h(uint32_t a, uint32_t b, float acc) {
-    if constexpr (HI)
-        asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
-            "mov.b32 {a0, a1}, %1;\n\t"
-            "mov.b32 {b0, b1}, %2;\n\t"
-            "fma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
-            : "+f"(acc) : "r"(a), "r"(b));
-    else
-        asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
-            "mov.b32 {a0, a1}, %1;\n\t"
-            "mov.b32 {b0, b1}, %2;\n\t"
-            "fma.rn.f32.f16 %0, a0, b0, %0;\n\t}"
-            : "+f"(acc) : "r"(a), "r"(b));
+#define SKV_FMA1(TY, X, Y)                                            \
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\t"                         \
+        "mov.b32 {a0, a1}, %1;\n\t"                                   \
+        "mov.b32 {b0, b1}, %2;\n\t" SKV_MIXED_FMA(TY) " %0, " X ", " Y ", %0;\n\t}" \
+        : "+f"(acc) : "r"(a), "r"(b))
+    if constexpr (BF && HI) SKV_FMA1("bf16", "a1", "b1");
+    else if constexpr (BF) SKV_FMA1("bf16", "a0", "b0");
+    else if constexpr (HI) SKV_FMA1("f16", "a1", "b1");
+    else SKV_FMA1("f16", "a0", "b0");
+#undef SKV_FMA1
     return acc;
 }
 // (o0, o1) += p * (v.lo, v.hi) where p is the low (HI = false) or high half
-// of `pw`; fp16 operands, fp32 accumulators.
-template <bool HI>
+// of `pw`.
+template <bool BF, bool HI>
 SKV_DEVINL void axpy2_h(uint32_t pw, uint32_t v, float& o0, float& o1) {
-    if constexpr (HI)
-        asm("{\n\t.reg .f16 v0, v1, p0, p1;\n\t"
-            "mov.b32 {v0, v1}, %2;\n\t"
-            "mov.b32 {p0, p1}, %3;\n\t"
-            "fma.rn.f32.f16 %0, p1, v0, %0;\n\t"
-            "fma.rn.f32.f16 %1, p1, v1, %1;\n\t}"
-            : "+f"(o0), "+f"(o1) : "r"(v), "r"(pw));
-    else
-        asm("{\n\t.reg .f16 v0, v1, p0, p1;\n\t"
-            "mov.b32 {v0, v1}, %2;\n\t"
-            "mov.b32 {p0, p1}, %3;\n\t"
-            "fma.rn.f32.f16 %0, p0, v0, %0;\n\t"
-            "fma.rn.f32.f16 %1, p0, v1, %1;\n\t}"
-            : "+f"(o0), "+f"(o1) : "r"(v), "r"(pw));
+#define SKV_AXPY2(TY, P)                                              \
+    asm("{\n\t.reg .b16 v0, v1, p0, p1;\n\t"                         \
+        "mov.b32 {v0, v1}, %2;\n\t"                                   \
+        "mov.b32 {p0, p1}, %3;\n\t" SKV_MIXED_FMA(TY) " %0, " P ", v0, %0;\n\t" \
+        SKV_MIXED_FMA(TY) " %1, " P ", v1, %1;\n\t}"                  \
+        : "+f"(o0), "+f"(o1) : "r"(v), "r"(pw))
+    if constexpr (BF && HI) SKV_AXPY2("bf16", "p1");
+    else if constexpr (BF) SKV_AXPY2("bf16", "p0");
+    else if constexpr (HI) SKV_AXPY2("f16", "p1");
+    else SKV_AXPY2("f16", "p0");
+#undef SKV_AXPY2
 }
-SKV_DEVINL uint16_t to_h(float x) { return __half_as_ushort(__float2half_rn(x)); }
+#undef SKV_MIXED_FMA
+// p rounded to the operand type (nearest even).
+template <bool BF>
+SKV_DEVINL uint16_t to_p(float x) {
+    if constexpr (BF) return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+    else return __half_as_ushort(__float2half_rn(x));
+}
 
 // Lane roles.  G >= 2: lane = g * TGN + x, x in [0, TGN) -- in QK x = tg (the
 // lane's tokens are tg + j*TGN, j < G/2), in PV x = dc (the lane's V chunks
@@ -130,7 +137,7 @@ constexpr size_t smem_bytes() {
            (size_t)W * G * kPage * sizeof(uint16_t);
 }
 
-template <int G, int W, int R>
+template <int G, int W, int R, bool BF>
 __global__ void __launch_bounds__(W * 32)
 splitkv_decode_kernel(const DecodeParams p) {
     using Ro = Roles<G>;
@@ -183,7 +190,7 @@ splitkv_decode_kernel(const DecodeParams p) {
     {
         // Rotated: register chunk i holds q chunk (i + r) mod n, r = the
         // lane's token (G == 1: within its half of the head dim).
-        const __half* qrow = p.q + ((int64_t)b * p.Hq + hkv * G + g_lane) * kD +
+        const uint16_t* qrow = p.q + ((int64_t)b * p.Hq + hkv * G + g_lane) * kD +
                              (G == 1 ? 64 * (lane >> 4) : 0);
         constexpr int nq = QW / 4;
         const int r = G == 1 ? (lane & 15) : x_lane;
@@ -262,10 +269,10 @@ splitkv_decode_kernel(const DecodeParams p) {
                 // held rotated to match), so lanes of different rows read
                 // different banks.
                 const uint4 kv = *reinterpret_cast<const uint4*>(rowp + (((c + t) & 7) << 4));
-                acc[c & 3] = dot2_h(qh[4 * c + 0], kv.x, acc[c & 3]);
-                acc[c & 3] = dot2_h(qh[4 * c + 1], kv.y, acc[c & 3]);
-                acc[c & 3] = dot2_h(qh[4 * c + 2], kv.z, acc[c & 3]);
-                acc[c & 3] = dot2_h(qh[4 * c + 3], kv.w, acc[c & 3]);
+                acc[c & 3] = dot2_h<BF>(qh[4 * c + 0], kv.x, acc[c & 3]);
+                acc[c & 3] = dot2_h<BF>(qh[4 * c + 1], kv.y, acc[c & 3]);
+                acc[c & 3] = dot2_h<BF>(qh[4 * c + 2], kv.z, acc[c & 3]);
+                acc[c & 3] = dot2_h<BF>(qh[4 * c + 3], kv.w, acc[c & 3]);
             }
             float sc = (acc[0] + acc[1]) + (acc[2] + acc[3]);
             sc += __shfl_xor_sync(kFull, sc, 16);
@@ -296,8 +303,8 @@ splitkv_decode_kernel(const DecodeParams p) {
                     const uint32_t kw[4] = {kv[j].x, kv[j].y, kv[j].z, kv[j].w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        acc[j][2 * i] = fma_h<false>(qh[qi + i], kw[i], acc[j][2 * i]);
-                        acc[j][2 * i + 1] = fma_h<true>(qh[qi + i], kw[i], acc[j][2 * i + 1]);
+                        acc[j][2 * i] = fma_h<BF, false>(qh[qi + i], kw[i], acc[j][2 * i]);
+                        acc[j][2 * i + 1] = fma_h<BF, true>(qh[qi + i], kw[i], acc[j][2 * i + 1]);
                     }
                 }
             }
@@ -325,9 +332,9 @@ splitkv_decode_kernel(const DecodeParams p) {
             const float pj = exp2f(x[j] - m_new);
             psum += pj;
             if constexpr (G == 1) {
-                if (lane < 16) ps[lane] = to_h(pj);
+                if (lane < 16) ps[lane] = to_p<BF>(pj);
             } else {
-                ps[g_lane * kPage + x_lane + j * TGN] = to_h(pj);
+                ps[g_lane * kPage + x_lane + j * TGN] = to_p<BF>(pj);
             }
         }
         l_run = fmaf(l_run, alpha, psum);
@@ -347,11 +354,11 @@ splitkv_decode_kernel(const DecodeParams p) {
             if constexpr (G == 1) {
                 const uint2 vv = *reinterpret_cast<const uint2*>(vrow + 8 * lane);
                 if (t & 1) {
-                    axpy2_h<true>(pw[t >> 1], vv.x, o[0], o[1]);
-                    axpy2_h<true>(pw[t >> 1], vv.y, o[2], o[3]);
+                    axpy2_h<BF, true>(pw[t >> 1], vv.x, o[0], o[1]);
+                    axpy2_h<BF, true>(pw[t >> 1], vv.y, o[2], o[3]);
                 } else {
-                    axpy2_h<false>(pw[t >> 1], vv.x, o[0], o[1]);
-                    axpy2_h<false>(pw[t >> 1], vv.y, o[2], o[3]);
+                    axpy2_h<BF, false>(pw[t >> 1], vv.x, o[0], o[1]);
+                    axpy2_h<BF, false>(pw[t >> 1], vv.y, o[2], o[3]);
                 }
             } else {
 #pragma unroll
@@ -361,9 +368,9 @@ splitkv_decode_kernel(const DecodeParams p) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         if (t & 1)
-                            axpy2_h<true>(pw[t >> 1], w4[i], o[8 * j + 2 * i], o[8 * j + 2 * i + 1]);
+                            axpy2_h<BF, true>(pw[t >> 1], w4[i], o[8 * j + 2 * i], o[8 * j + 2 * i + 1]);
                         else
-                            axpy2_h<false>(pw[t >> 1], w4[i], o[8 * j + 2 * i], o[8 * j + 2 * i + 1]);
+                            axpy2_h<BF, false>(pw[t >> 1], w4[i], o[8 * j + 2 * i], o[8 * j + 2 * i + 1]);
                     }
                 }
             }
@@ -436,11 +443,11 @@ splitkv_decode_kernel(const DecodeParams p) {
     }
 }
 
-template <int G, int W, int R>
+template <int G, int W, int R, bool BF>
 cudaError_t launch_gwr(const DecodeParams& p, int B, int Hkv, int NS,
                        cudaStream_t st) {
     constexpr size_t smem = smem_bytes<G, W, R>();
-    auto kern = splitkv_decode_kernel<G, W, R>;
+    auto kern = splitkv_decode_kernel<G, W, R, BF>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -457,7 +464,7 @@ cudaError_t launch_gwr(const DecodeParams& p, int B, int Hkv, int NS,
 // over NUM_SPLITS): a CTA of 3 warps with a 6-page ring for long splits; for
 // short splits smaller CTAs, so that many more of them are resident per SM
 // and their fixed latencies (q, page table, first copies) overlap.
-template <int G>
+template <int G, bool BF>
 cudaError_t launch_g(const DecodeParams& p, int B, int Hkv, int NS,
                      int max_pages, cudaStream_t st) {
     // Measured on the cascade suffixes (<= 8 pages per split, B=64, NS=16):
@@ -465,9 +472,9 @@ cudaError_t launch_g(const DecodeParams& p, int B, int Hkv, int NS,
     // SM), 64 us with 2 warps, 72 us with 3; a 4-page ring for the 1-warp
     // CTA (fewer CTAs per SM) takes 74 us.  Long splits (32 pages) keep 3.
     const int pps = (max_pages + NS - 1) / NS;
-    if (pps <= 8) return launch_gwr<G, 1, 2>(p, B, Hkv, NS, st);
-    if (pps <= 16) return launch_gwr<G, 2, 4>(p, B, Hkv, NS, st);
-    return launch_gwr<G, 3, 6>(p, B, Hkv, NS, st);
+    if (pps <= 8) return launch_gwr<G, 1, 2, BF>(p, B, Hkv, NS, st);
+    if (pps <= 16) return launch_gwr<G, 2, 4, BF>(p, B, Hkv, NS, st);
+    return launch_gwr<G, 3, 6, BF>(p, B, Hkv, NS, st);
 }
 
 // ---------------------------------------------------------------- combine (pass 2)
@@ -718,9 +725,9 @@ cascade_combine_kernel(const CombineParams p) {
 
 cudaError_t launch_splitkv_decode(const DecodeArgs& a, const DeviceInfo& dev, cudaStream_t st) {
     DecodeParams p;
-    p.q = static_cast<const __half*>(a.q);
-    p.k_cache = static_cast<const __half*>(a.k_cache);
-    p.v_cache = static_cast<const __half*>(a.v_cache);
+    p.q = static_cast<const uint16_t*>(a.q);
+    p.k_cache = static_cast<const uint16_t*>(a.k_cache);
+    p.v_cache = static_cast<const uint16_t*>(a.v_cache);
     p.block_table = a.block_table;
     p.ctx = a.ctx;
     p.o_part = a.o_part;
@@ -733,12 +740,15 @@ cudaError_t launch_splitkv_decode(const DecodeArgs& a, const DeviceInfo& dev, cu
     p.Hkv = a.Hkv;
     p.NS = a.num_splits;
     p.scale_log2 = a.sm_scale * 1.4426950408889634f;
-    switch (a.Hq / a.Hkv) {
-        case 1: return launch_g<1>(p, a.B, a.Hkv, a.num_splits, a.max_pages, st);
-        case 2: return launch_g<2>(p, a.B, a.Hkv, a.num_splits, a.max_pages, st);
-        case 4: return launch_g<4>(p, a.B, a.Hkv, a.num_splits, a.max_pages, st);
-        case 8: return launch_g<8>(p, a.B, a.Hkv, a.num_splits, a.max_pages, st);
+#define SKV_LAUNCH_G(BF_)                                                             \
+    switch (a.Hq / a.Hkv) {                                                           \
+        case 1: return launch_g<1, BF_>(p, a.B, a.Hkv, a.num_splits, a.max_pages, st); \
+        case 2: return launch_g<2, BF_>(p, a.B, a.Hkv, a.num_splits, a.max_pages, st); \
+        case 4: return launch_g<4, BF_>(p, a.B, a.Hkv, a.num_splits, a.max_pages, st); \
+        case 8: return launch_g<8, BF_>(p, a.B, a.Hkv, a.num_splits, a.max_pages, st); \
     }
+    if (a.bf16) SKV_LAUNCH_G(true) else SKV_LAUNCH_G(false)
+#undef SKV_LAUNCH_G
     return cudaErrorInvalidValue;
 }
 

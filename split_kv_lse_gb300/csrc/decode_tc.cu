@@ -120,7 +120,7 @@ struct __align__(16) GroupInfo {
 };
 
 struct TcParams {
-    const __half* q;
+    const uint16_t* q;  // fp16 or bf16 bit patterns
     const int32_t* block_table;
     const int32_t* ctx;
     float* o_part;
@@ -153,7 +153,7 @@ SKV_DEVINL void decode_unit(const TcParams& p, int u, int* b, int* hkv, int* spl
     *b = r / p.NS;
 }
 
-template <int G>
+template <int G, bool BF>
 __global__ void __launch_bounds__(kThreads, 1)
 splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
                          const __grid_constant__ CUtensorMap tv, const TcParams p) {
@@ -444,7 +444,7 @@ splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
             }
     } else if (warp == kQkWarp) {
         // ------------------------------------------------------------ S = K Q^T issuer
-        constexpr uint32_t idQK = tc::idesc_f16_f32(kM, kN, false, false);
+        constexpr uint32_t idQK = tc::idesc_f16_f32(kM, kN, false, false, BF);
         for (int i = 0;; ++i) {
             const int s = i % kStages, sb = i & 1;
             bool ok = wait_or_abort(&k_full[s], (uint32_t)((i / kStages) & 1), abort_flag, p.err, 44);
@@ -480,7 +480,7 @@ splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
         __syncwarp();
     } else if (warp == kPvWarp) {
         // ------------------------------------------------------------ O^T += V^T P^T issuer
-        constexpr uint32_t idPV = tc::idesc_f16_f32(kM, kN, false, true);
+        constexpr uint32_t idPV = tc::idesc_f16_f32(kM, kN, false, true, BF);
         int gcount = 0;
         for (int i = 0;; ++i) {
             const int s = i % kStages, pb = i & 1;
@@ -670,19 +670,20 @@ splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
             if (i >= 2 &&
                 !wait_or_abort(&pv_done[pb], (uint32_t)(((i - 2) >> 1) & 1), abort_flag, p.err, 51))
                 break;
-            __half ph[G];
+            uint16_t ph[G];  // p in the operand type (fp16 or bf16, nearest even)
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const float pf = valid ? exp2f(v[g] - m[g]) : 0.f;
                 l[g] += pf;
-                ph[g] = __float2half_rn(pf);
+                ph[g] = BF ? __bfloat16_as_ushort(__float2bfloat16_rn(pf))
+                           : __half_as_ushort(__float2half_rn(pf));
             }
             uint8_t* P = Ps + pb * kPTile + (t >> 6) * kPHalf + (t & 7) * 2;
             const int tq = (t & 63) >> 3;
-            const __half hz = __float2half_rn(0.f);
 #pragma unroll
-            for (int c = 0; c < kN; ++c)
-                *reinterpret_cast<__half*>(P + c * 128 + ((tq ^ (c & 7)) << 4)) = (c / G == cslot) ? ph[c % G] : hz;
+            for (int c = 0; c < kN; ++c)  // +0 is all zero bits in both types
+                *reinterpret_cast<uint16_t*>(P + c * 128 + ((tq ^ (c & 7)) << 4)) =
+                    (c / G == cslot) ? ph[c % G] : (uint16_t)0;
             tc::fence_proxy_async_smem();
             tc::fence_before_sync();
             __syncwarp();
@@ -772,10 +773,10 @@ splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
     }
 }
 
-template <int G>
+template <int G, bool BF>
 cudaError_t launch_tc_g(const CUtensorMap& tk, const CUtensorMap& tv, const TcParams& p, int grid,
                         const DeviceInfo& dev, cudaStream_t st) {
-    auto kern = splitkv_decode_tc_kernel<G>;
+    auto kern = splitkv_decode_tc_kernel<G, BF>;
     static bool attr_set[64] = {};
     if (dev.device >= 0 && dev.device < 64 && !attr_set[dev.device]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -793,12 +794,12 @@ cudaError_t launch_splitkv_decode_tc(const DecodeArgs& a, const DeviceInfo& dev,
     if (kSmemBytes > dev.max_smem_optin) return cudaErrorInvalidValue;
     const uint64_t rows = (uint64_t)a.num_pool_pages * a.Hkv * kPage;
     CUtensorMap tk, tv;
-    cudaError_t e = make_tmap_2d_16bit(&tk, a.k_cache, rows, kD, kD * 2, 64, kPage, true, false);
+    cudaError_t e = make_tmap_2d_16bit(&tk, a.k_cache, rows, kD, kD * 2, 64, kPage, true, a.bf16);
     if (e != cudaSuccess) return e;
-    if ((e = make_tmap_2d_16bit(&tv, a.v_cache, rows, kD, kD * 2, 64, kPage, true, false)) != cudaSuccess)
+    if ((e = make_tmap_2d_16bit(&tv, a.v_cache, rows, kD, kD * 2, 64, kPage, true, a.bf16)) != cudaSuccess)
         return e;
     TcParams p;
-    p.q = static_cast<const __half*>(a.q);
+    p.q = static_cast<const uint16_t*>(a.q);
     p.block_table = a.block_table;
     p.ctx = a.ctx;
     p.o_part = a.o_part;
@@ -820,12 +821,15 @@ cudaError_t launch_splitkv_decode_tc(const DecodeArgs& a, const DeviceInfo& dev,
     // which 56 take a fourth unit while the rest of the GPU idles.
     const int64_t per_cta = (units + dev.sm_count - 1) / dev.sm_count;
     const int grid = (int)((units + per_cta - 1) / per_cta);
-    switch (a.Hq / a.Hkv) {
-        case 1: return launch_tc_g<1>(tk, tv, p, grid, dev, st);
-        case 2: return launch_tc_g<2>(tk, tv, p, grid, dev, st);
-        case 4: return launch_tc_g<4>(tk, tv, p, grid, dev, st);
-        case 8: return launch_tc_g<8>(tk, tv, p, grid, dev, st);
+#define SKV_LAUNCH_TC(BF_)                                            \
+    switch (a.Hq / a.Hkv) {                                           \
+        case 1: return launch_tc_g<1, BF_>(tk, tv, p, grid, dev, st); \
+        case 2: return launch_tc_g<2, BF_>(tk, tv, p, grid, dev, st); \
+        case 4: return launch_tc_g<4, BF_>(tk, tv, p, grid, dev, st); \
+        case 8: return launch_tc_g<8, BF_>(tk, tv, p, grid, dev, st); \
     }
+    if (a.bf16) SKV_LAUNCH_TC(true) else SKV_LAUNCH_TC(false)
+#undef SKV_LAUNCH_TC
     return cudaErrorInvalidValue;
 }
 

@@ -80,6 +80,7 @@ struct DecodeArgs {
     float* o_part;
     float* lse_part;
     int32_t* ranges_dbg;
+    bool bf16;  // q, K, V are bf16 (else fp16)
 };
 cudaError_t launch_splitkv_decode(const DecodeArgs& a, const DeviceInfo& dev, cudaStream_t st);
 // The same pass on the tensor cores (persistent CTAs, packed short splits).
@@ -95,6 +96,7 @@ struct CascadeArgs {
     int32_t prefix_len;
     int32_t B, Hq, Hkv;
     float sm_scale;
+    bool bf16;  // q, K, V are bf16 (else fp16)
 };
 // Grid of the shared-prefix pass: M tiles of 128 query rows, prefix blocks
 // of 128 keys per chunk, number of chunks.

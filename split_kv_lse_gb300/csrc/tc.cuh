@@ -62,14 +62,16 @@ SKV_DEVINL uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo
     return d;
 }
 
-// Instruction descriptor for kind::f16: fp16 A and B, fp32 accumulator,
-// M x N tile, A and B each K-major or MN-major.
-//   bits 4-5 D format (1 = f32), 7-9 A format (0 = f16), 10-12 B format,
+// Instruction descriptor for kind::f16: fp16 or bf16 A and B, fp32
+// accumulator, M x N tile, A and B each K-major or MN-major.
+//   bits 4-5 D format (1 = f32), 7-9 A format (0 = f16, 1 = bf16), 10-12 B format,
 //   15 A major, 16 B major (1 = MN), 17-22 N >> 3, 24-28 M >> 4.
 SKV_DEVINL constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major,
-                                             bool a_mn_major = false) {
-    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+                                             bool a_mn_major = false, bool bf16 = false) {
+    // A and B formats (bits 7-9, 10-12): 0 = fp16, 1 = bf16, always the same
+    // for both operands.
+    return (1u << 4) | (bf16 ? (1u << 7) | (1u << 10) : 0u) | ((a_mn_major ? 1u : 0u) << 15) |
+           ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // ---------------------------------------------------------------- MMA

@@ -12,13 +12,12 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import (DECODE_KERNELS, select_decode_kernel, DEC_LSE_ATOL, DEC_O_ATOL, assert_s_close, assert_v_close,
+from gpu_helpers import (DECODE_KERNELS, select_decode_kernel, DEC_LSE_ATOL, DEC_O_TOL, assert_s_close, assert_v_close,
                          require_gpu, skv)
 from split_kv_lse_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
-H16 = 2.0 ** -11
 
 
 @pytest.fixture(params=DECODE_KERNELS, autouse=True)
@@ -73,14 +72,16 @@ def run_and_check(lib, d, ns, poison=True):
     o_r, s_r, op_r, sp_r = oracle.cascade(d["q"], d["k_cache"], d["v_cache"], d["prefix_pages"],
                                           d["prefix_len"], d["block_table"], d["ctx"],
                                           d["sm_scale"])
+    atol, rtol_part, rtol_out = DEC_O_TOL[d["q"].dtype]
+    assert out.dtype == d["q"].dtype
     assert_s_close(s_pre, sp_r, DEC_LSE_ATOL, "s_pre")
-    assert_v_close(o_pre, op_r, DEC_O_ATOL, 0.0, "o_pre", empty_rows=(sp_r == -math.inf))
+    assert_v_close(o_pre, op_r, atol, rtol_part, "o_pre", empty_rows=(sp_r == -math.inf))
     opr, lpr = oracle.attend_splits(d["q"], d["k_cache"], d["v_cache"], d["block_table"],
                                     d["ctx"], d["sm_scale"], ns)
     assert_s_close(lse_part, lpr, DEC_LSE_ATOL, "lse_part")
-    assert_v_close(o_part, opr, DEC_O_ATOL, 0.0, "o_part", empty_rows=(lpr == -math.inf))
+    assert_v_close(o_part, opr, atol, rtol_part, "o_part", empty_rows=(lpr == -math.inf))
     assert_s_close(lse, s_r, DEC_LSE_ATOL, "lse_out")
-    assert_v_close(out, o_r, DEC_O_ATOL, H16, "out", empty_rows=(s_r == -math.inf))
+    assert_v_close(out, o_r, atol, rtol_out, "out", empty_rows=(s_r == -math.inf))
     return out, lse, o_pre, s_pre
 
 
@@ -120,3 +121,21 @@ def test_cascade_full_workload(lib):
     """B=64, Hq=32, Hkv=8, an 8192-token shared prefix, suffixes of 1..2048 tokens, NS=16."""
     d = W.cascade_mixed()
     run_and_check(lib, d, d["num_splits"], poison=False)
+
+
+@pytest.mark.parametrize("G", [1, 4])
+def test_cascade_bf16(lib, G):
+    """bf16 q/K/V: the prefix pass on the tensor cores with bf16 operands (P in
+    bf16), bf16 suffix decode, bf16 output."""
+    B = (160 + G - 1) // G
+    ctx = [int(x) for x in np.random.default_rng(30 + G).integers(0, 300, B)]
+    d = W.cascade_inputs(B, 2 * G, 2, 128, 16, 777, ctx, seed=30 + G, dtype=torch.bfloat16)
+    run_and_check(lib, d, 8)
+
+
+def test_cascade_bf16_full_workload(lib):
+    """The B=64 cascade workload in bf16."""
+    fp16 = W.cascade_mixed()
+    suffix = fp16["ctx"].tolist()  # the same suffix lengths as the fp16 workload
+    d = W.cascade_inputs(64, 32, 8, 128, 16, 8192, suffix, 0, dtype=torch.bfloat16)
+    run_and_check(lib, d, 16, poison=False)

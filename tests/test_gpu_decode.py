@@ -11,13 +11,12 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import (DECODE_KERNELS, select_decode_kernel, DEC_LSE_ATOL, DEC_O_ATOL, assert_s_close, assert_v_close, np64,
+from gpu_helpers import (DECODE_KERNELS, select_decode_kernel, DEC_LSE_ATOL, DEC_O_TOL, assert_s_close, assert_v_close, np64,
                          require_gpu, skv)
 from split_kv_lse_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
-H16 = 2.0 ** -11  # fp16 output rounding (relative)
 
 
 @pytest.fixture(params=DECODE_KERNELS, autouse=True)
@@ -67,10 +66,12 @@ def check_decode(lib, d, ns, nan_tail=False):
     op_r, lp_r = oracle.attend_splits(*args, ns)
     o_r, s_r = oracle.attend_full(*args)
     empty = lp_r == -math.inf
+    atol, rtol_part, rtol_out = DEC_O_TOL[d["q"].dtype]
+    assert out.dtype == d["q"].dtype
     assert_s_close(lse_part, lp_r, DEC_LSE_ATOL, "lse_part")
-    assert_v_close(o_part, op_r, DEC_O_ATOL, 0.0, "o_part", empty_rows=empty)
+    assert_v_close(o_part, op_r, atol, rtol_part, "o_part", empty_rows=empty)
     assert_s_close(lse, s_r, DEC_LSE_ATOL, "lse_out")
-    assert_v_close(out, o_r, DEC_O_ATOL, H16, "out", empty_rows=(s_r == -math.inf))
+    assert_v_close(out, o_r, atol, rtol_out, "out", empty_rows=(s_r == -math.inf))
     # Page ranges, bit-exact against the oracle's integer formula.
     ranges = rd.cpu().numpy()
     for b, c in enumerate(d["ctx"].tolist()):
@@ -168,3 +169,20 @@ def test_decode_short_splits_many_requests(lib):
     ctx = rng.integers(0, 40, size=1100).tolist()
     d = W.decode_inputs(len(ctx), 2, 1, 128, 16, ctx, seed=12)
     check_decode(lib, d, 4)
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("ns", [3, 64])
+def test_decode_bf16_small(lib, G, ns):
+    """bf16 q/K/V end to end: bf16 x bf16 -> fp32 products, bf16 output."""
+    ctx = [1, 15, 16, 17, 37, 100, 1000, 0]
+    Hkv = 2
+    d = W.decode_inputs(len(ctx), Hkv * G, Hkv, 128, 16, ctx, seed=G * 100 + ns + 7,
+                        dtype=torch.bfloat16, pool_extra=3)
+    check_decode(lib, d, ns, nan_tail=True)
+
+
+def test_decode_bf16_long_context(lib):
+    """The long-context workload (B=1, ctx=32768, Hq=32, Hkv=8, NS=64) in bf16."""
+    d = W.decode_inputs(1, 32, 8, 128, 16, [32768], seed=0, dtype=torch.bfloat16)
+    check_decode(lib, d, 64)
