@@ -13,8 +13,9 @@ split_kv_lse_gb300/workloads.py), inputs resident in HBM:
                         (when the library exports it)
 value = algorithmic HBM bytes of the step / step time (GB/s).  Each stage is
 timed with CUDA events on the launching stream; L2 is flushed (a 512 MB
-write, then a 512 MB read, so it holds clean lines) before every step,
-outside the stage events.  --impl reference times
+write, then a 512 MB read, so it holds clean lines) before every stage,
+outside the stage events, so each stage starts cold and is not charged for
+the write-back of the previous stage's output.  --impl reference times
 the fp64 CPU oracle on a bounded sample of the same stages instead.
 
 Prints ONE JSON line (rank 0).
@@ -488,17 +489,19 @@ def run_ours(args):
 
     only = args.only.split(",") if args.only else None
     stages, host = build_stages(torch, skv, W, dev, only)
-    # L2 flush between steps: write 512 MB, then read another 512 MB so that
-    # the cache holds clean lines (no write-back charged to the next kernel).
+    # L2 flush before every stage: write 512 MB, then read another 512 MB so
+    # that the cache holds clean lines (no write-back charged to the next kernel).
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     flush_rd = torch.ones(128 * 1024 * 1024, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
     def step(record):
-        flush.zero_()
-        flush_rd.sum()
         evs = []
         for st in stages:
+            # Every stage starts from a flushed L2 holding clean lines: no stage
+            # is charged for the write-back of the previous stage's output.
+            flush.zero_()
+            flush_rd.sum()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -631,7 +634,7 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": WORKLOAD if only is None else ",".join(only),
-                       "l2_flush": "512 MB write + 512 MB read before every step (outside the stage events)",
+                       "l2_flush": "512 MB write + 512 MB read before every stage of every step (outside the stage events)",
                        "clock_window": f"{args.soak_s} s untimed soak of the same steps, then the timed region",
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "stages": stage_rep, "wall_s": round(wall, 3)},
