@@ -22,6 +22,21 @@ constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
+// The cascade's shared-prefix pass runs on a library-owned stream beside the
+// caller's, forked from and joined back into it with events, so that it
+// overlaps the suffix pass.  One stream and one pair of events per device,
+// created on first use; the fork/join sequence is serialised per device.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    std::mutex mu;
+};
+SideStream g_side[kMaxDevices];
+
+// Share of the SMs the prefix pass is sized for (its CTAs hold a whole SM
+// each); the suffix pass fills the rest of the GPU meanwhile.
+constexpr int kPrefixSmNum = 1, kPrefixSmDen = 4;
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 bool valid_dtype(skv_dtype t) { return t == SKV_F32 || t == SKV_F16 || t == SKV_BF16; }
@@ -264,7 +279,29 @@ static skv_status cascade_chunks(int32_t B, int32_t Hq, int32_t Hkv, int32_t pre
         if (st != SKV_OK) return st;
         sm_count = dev->sm_count;
     }
-    cascade_prefix_geometry(B, Hq / Hkv, Hkv, prefix_len, sm_count, mtiles, bpc, nchunks);
+    const int budget = sm_count * kPrefixSmNum / kPrefixSmDen;
+    cascade_prefix_geometry(B, Hq / Hkv, Hkv, prefix_len, budget > 0 ? budget : 1, mtiles, bpc,
+                            nchunks);
+    return SKV_OK;
+}
+
+// The device's side stream (highest priority) and fork/join events.
+static skv_status side_stream(int device, SideStream** out) {
+    if (device < 0 || device >= kMaxDevices) return SKV_ERR_CUDA;
+    SideStream& s = g_side[device];
+    std::lock_guard<std::mutex> lk(s.mu);
+    if (s.stream == nullptr) {
+        int lo = 0, hi = 0;
+        if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return SKV_ERR_CUDA;
+        cudaStream_t st = nullptr;
+        if (cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, hi) != cudaSuccess)
+            return SKV_ERR_CUDA;
+        if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess)
+            return SKV_ERR_CUDA;
+        s.stream = st;
+    }
+    *out = &s;
     return SKV_OK;
 }
 
@@ -313,15 +350,25 @@ skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_
     skv_status st = current_device(&dev);
     if (st != SKV_OK) return st;
     int mt = 0, bpc = 0, nc = 0;
-    cascade_prefix_geometry(B, G, Hkv, prefix_len, dev->sm_count, &mt, &bpc, &nc);
+    if ((st = cascade_chunks(B, Hq, Hkv, prefix_len, dev->sm_count, &mt, &bpc, &nc)) != SKV_OK)
+        return st;
     const size_t rows = (size_t)B * Hq;
     const size_t need = align256(rows * nc * D * 4) + align256(rows * nc * 4) + 256;
     if (workspace_bytes < need) return SKV_ERR_INVALID_ARG;
     float* pre_part = static_cast<float*>(workspace);
     float* pre_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * nc * D * 4));
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    // 1. Shared prefix on the tensor cores: one state per prefix chunk.
+    SideStream* side = nullptr;
+    if (nc > 0 && (st = side_stream(dev->device, &side)) != SKV_OK) return st;
+    std::unique_lock<std::mutex> side_lk;
+    // 1. Shared prefix on the tensor cores, one state per prefix chunk, on the
+    // side stream: forked after everything the caller queued before this call,
+    // joined back before the combine.
     if (nc > 0) {
+        side_lk = std::unique_lock<std::mutex>(side->mu);
+        if (cudaEventRecord(side->fork, cs) != cudaSuccess ||
+            cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
+            return SKV_ERR_CUDA;
         CascadeArgs ca;
         ca.q = q;
         ca.k_cache = k_cache;
@@ -334,7 +381,9 @@ skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_
         ca.Hkv = Hkv;
         ca.bf16 = dtype == SKV_BF16;
         ca.sm_scale = sm_scale;
-        if (launch_cascade_prefix(ca, *dev, pre_part, pre_lse, nc, bpc, mt, cs) != cudaSuccess)
+        if (launch_cascade_prefix(ca, *dev, pre_part, pre_lse, nc, bpc, mt, side->stream) !=
+                cudaSuccess ||
+            cudaEventRecord(side->join, side->stream) != cudaSuccess)
             return SKV_ERR_CUDA;
     }
     // 2. Each request's own suffix through the split-KV decode.
@@ -360,6 +409,7 @@ skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_
     if ((use_tc_decode() ? launch_splitkv_decode_tc(a, *dev, cs) : launch_splitkv_decode(a, *dev, cs)) !=
         cudaSuccess)
         return SKV_ERR_CUDA;
+    if (nc > 0 && cudaStreamWaitEvent(cs, side->join, 0) != cudaSuccess) return SKV_ERR_CUDA;
     // 3. Prefix chunks -> prefix state; merge_state(prefix, suffix) -> out.
     CombineArgs c = {};
     c.o_part = o_part;
@@ -375,7 +425,9 @@ skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_
     c.C = nc;
     c.o_pre = o_pre;
     c.s_pre = s_pre;
-    if (launch_combine(c, true, *dev, cs) != cudaSuccess) return SKV_ERR_CUDA;
+    // Without a prefix the combine follows pass 1 directly (programmatic
+    // dependent launch); after the join it waits for both in stream order.
+    if (launch_combine(c, nc == 0, *dev, cs) != cudaSuccess) return SKV_ERR_CUDA;
     return SKV_OK;
 }
 
