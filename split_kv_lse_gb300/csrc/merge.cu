@@ -151,7 +151,7 @@ merge_state_kernel(const T* va, const float* sa, const T* __restrict__ vb,
 #define SKV_ROW_WARPS 4
 #endif
 #ifndef SKV_ROW_BATCH
-#define SKV_ROW_BATCH 8
+#define SKV_ROW_BATCH 4
 #endif
 constexpr int kRowWarps = SKV_ROW_WARPS;
 constexpr int kRowBatch = SKV_ROW_BATCH;
