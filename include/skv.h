@@ -276,6 +276,59 @@ skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_
                               void* workspace, size_t workspace_bytes, skv_stream_t stream);
 
 /*
+ * One shared level of a multi-level cascade: the requests are cut into
+ * num_groups contiguous groups, group g = requests [group_start[g],
+ * group_start[g+1]), whose members all attend to the same group_len[g]
+ * tokens on the pool pages group_pages[g][0 .. ceil(group_len[g]/page)).
+ *   group_start: host int32 [num_groups + 1], non-decreasing, from 0 to B.
+ *   group_len:   host int32 [num_groups], >= 0 (0: the group shares nothing
+ *                at this level).
+ *   group_pages: host array of num_groups device pointers (int32, 4-byte
+ *                aligned; may be NULL where group_len is 0).
+ */
+typedef struct {
+    int32_t num_groups;
+    const int32_t* group_start;
+    const int32_t* group_len;
+    const int32_t* const* group_pages;
+} skv_cascade_level;
+
+/*
+ * Device workspace, in bytes, that skv_cascade_decode_multilevel needs for
+ * these levels and sizes (the prefix-chunk states of every level).  sm_count
+ * as for skv_cascade_workspace_size.  Returns 0 for invalid arguments.
+ */
+size_t skv_cascade_multilevel_workspace_size(int32_t num_levels, const skv_cascade_level* levels,
+                                             int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                             int32_t sm_count);
+
+/*
+ * Multi-level cascade decode attention ([F2] §⑥: attention level by level,
+ * then merge): request b attends, as one softmax, to the concatenation of
+ * its group's shared tokens at level 0, 1, ..., num_levels - 1 and then its
+ * own suffix of ctx[b] tokens (block_table[b][..]).  Each group's shared
+ * tokens go through the tensor-core prefix pass for the group's requests
+ * only (their K/V read once for the group); the suffixes through the
+ * split-KV decode; one combine merges every level's chunk states into the
+ * prefix state (o_pre, s_pre: over all shared levels) and that with the
+ * suffix state into out and lse_out.  With one level of one group this is
+ * skv_cascade_decode.  Arguments, layouts, workspace rules (sized by
+ * skv_cascade_multilevel_workspace_size), support and device-side checks as
+ * for skv_cascade_decode; a level list that does not cover [0, B) in order
+ * returns SKV_ERR_INVALID_ARG.
+ */
+skv_status skv_cascade_decode_multilevel(const void* q, const void* k_cache, const void* v_cache,
+                                         int32_t num_pool_pages, int32_t num_levels,
+                                         const skv_cascade_level* levels,
+                                         const int32_t* block_table, int32_t max_pages,
+                                         const int32_t* ctx, int32_t B, int32_t Hq, int32_t Hkv,
+                                         int32_t D, int32_t page, int32_t num_splits,
+                                         float sm_scale, skv_dtype dtype, float* o_pre,
+                                         float* s_pre, float* o_part, float* lse_part, void* out,
+                                         float* lse_out, void* workspace, size_t workspace_bytes,
+                                         skv_stream_t stream);
+
+/*
  * Reads and clears the error word of the current CUDA device: *code is 0 or
  * the skv_status of the first device-side error since the last call, *detail
  * an index that identifies it (0 if none).  Synchronises the device.

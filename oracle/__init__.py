@@ -98,6 +98,10 @@ class Oracle:
         lib.oracle_cascade.argtypes = common + [_ip, _i32, _ip, _i32, _ip, ctypes.c_double,
                                                 _dp, _dp, _dp, _dp]
         lib.oracle_cascade.restype = None
+        lib.oracle_cascade_multilevel.argtypes = common + [
+            _i32, _ip, ctypes.POINTER(ctypes.c_int64), _ip, _ip, _i32, _ip, ctypes.c_double,
+            _dp, _dp, _dp, _dp]
+        lib.oracle_cascade_multilevel.restype = None
         self.lib = lib
         self.path = path
 
@@ -189,6 +193,38 @@ class Oracle:
         return out, s, o_pre, s_pre
 
 
+    def cascade_multilevel(self, q, k_cache, v_cache, levels, block_table, ctx,
+                           sm_scale: float):
+        """Multi-level cascade ([F2] §⑥) -> (out, s, o_pre, s_pre).  levels[l] is a
+        list of groups (r0, r1, pages, length): requests [r0, r1) share `length`
+        tokens on the page list `pages` at level l."""
+        q, kc, vc, bt, cx, B, Hq, Hkv, D, page = self._decode_args(
+            q, k_cache, v_cache, block_table, ctx)
+        L = len(levels)
+        lens = np.zeros((B, max(L, 1)), dtype=np.int32)
+        offs = np.zeros((B, max(L, 1)), dtype=np.int64)
+        chunks = [np.zeros(1, dtype=np.int32)]
+        at = 1
+        for li, groups in enumerate(levels):
+            for r0, r1, pages, length in groups:
+                pg = _i32a(pages).reshape(-1) if pages is not None else np.zeros(0, np.int32)
+                for b in range(int(r0), int(r1)):
+                    lens[b, li] = int(length)
+                    offs[b, li] = at
+                chunks.append(pg)
+                at += pg.size
+        segp = np.ascontiguousarray(np.concatenate(chunks).astype(np.int32))
+        out = np.empty((B, Hq, D))
+        s = np.empty((B, Hq))
+        o_pre = np.empty((B, Hq, D))
+        s_pre = np.empty((B, Hq))
+        self.lib.oracle_cascade_multilevel(
+            B, Hq, Hkv, D, page, _p(q), _p(kc), _p(vc), L, _pi(segp),
+            offs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), _pi(lens), _pi(bt), bt.shape[1],
+            _pi(cx), float(sm_scale), _p(out), _p(s), _p(o_pre), _p(s_pre))
+        return out, s, o_pre, s_pre
+
+
 def default() -> Oracle:
     """The oracle built from the committed oracle.c."""
     global _default
@@ -224,3 +260,7 @@ def attend_splits(*a, **k):
 
 def cascade(*a, **k):
     return default().cascade(*a, **k)
+
+
+def cascade_multilevel(*a, **k):
+    return default().cascade_multilevel(*a, **k)

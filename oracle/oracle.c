@@ -328,3 +328,52 @@ void oracle_cascade(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page,
     free(kr);
     free(vr);
 }
+
+/*
+ * Multi-level cascade ([F2] §⑥: attention level by level, then merge): as
+ * oracle_cascade, with L shared segments before each request's suffix.
+ * Request b's keys are, in order, seg_len[b*L + l] tokens on the pages
+ * seg_pages + seg_page_off[b*L + l] for l = 0 .. L-1 (its group's shared
+ * tokens at level l), then its ctx[b] suffix tokens.  out/s_out: one softmax
+ * over all of them (the plain definition); o_pre/s_pre: one softmax over the
+ * shared tokens only (the prefix state the merge combines with the suffix).
+ */
+void oracle_cascade_multilevel(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page,
+                               const double* q, const double* k_cache, const double* v_cache,
+                               int32_t L, const int32_t* seg_pages, const int64_t* seg_page_off,
+                               const int32_t* seg_len, const int32_t* block_table,
+                               int32_t max_pages, const int32_t* ctx, double sm_scale,
+                               double* out, double* s_out, double* o_pre, double* s_pre) {
+    int32_t G = Hq / Hkv;
+    int64_t cap = 1;
+    for (int32_t b = 0; b < B; ++b) {
+        int64_t n = ctx[b];
+        for (int32_t l = 0; l < L; ++l) n += seg_len[(int64_t)b * L + l];
+        if (n > cap) cap = n;
+    }
+    const double** kr = (const double**)malloc(sizeof(double*) * (size_t)cap);
+    const double** vr = (const double**)malloc(sizeof(double*) * (size_t)cap);
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t* sfx = block_table + (int64_t)b * max_pages;  /* the suffix's pages */
+        for (int32_t hq = 0; hq < Hq; ++hq) {
+            int32_t hk = hq / G;
+            int32_t n = 0;
+            for (int32_t l = 0; l < L; ++l) {
+                const int32_t* sp = seg_pages + seg_page_off[(int64_t)b * L + l];
+                for (int32_t t = 0; t < seg_len[(int64_t)b * L + l]; ++t, ++n) {
+                    kr[n] = token_row(k_cache, sp, t, Hkv, hk, page, D);
+                    vr[n] = token_row(v_cache, sp, t, Hkv, hk, page, D);
+                }
+            }
+            int64_t row = (int64_t)b * Hq + hq;
+            attend_rows(D, q + row * D, n, kr, vr, sm_scale, o_pre + row * D, s_pre + row);
+            for (int32_t t = 0; t < ctx[b]; ++t, ++n) {
+                kr[n] = token_row(k_cache, sfx, t, Hkv, hk, page, D);
+                vr[n] = token_row(v_cache, sfx, t, Hkv, hk, page, D);
+            }
+            attend_rows(D, q + row * D, n, kr, vr, sm_scale, out + row * D, s_out + row);
+        }
+    }
+    free(kr);
+    free(vr);
+}

@@ -228,6 +228,92 @@ def cascade_decode(q, k_cache, v_cache, prefix_pages, prefix_len: int, block_tab
     return out, lse_out, o_pre, s_pre, o_part, lse_part
 
 
+def _levels_struct(levels, B):
+    """ctypes array of skv_cascade_level for levels = [[(r0, r1, pages, length), ...], ...]
+    (pages: device int32 tensor or None); returns it with the buffers it points into."""
+    keep = []
+    arr = (_ffi.CascadeLevel * max(1, len(levels)))()
+    for li, groups in enumerate(levels):
+        n = len(groups)
+        starts = (ctypes.c_int32 * (n + 1))()
+        lens = (ctypes.c_int32 * n)()
+        pages = (ctypes.c_void_p * n)()
+        for gi, (r0, r1, pg, length) in enumerate(groups):
+            if gi == 0 and r0 != 0:
+                raise ValueError("level groups must start at request 0")
+            if gi > 0 and r0 != groups[gi - 1][1]:
+                raise ValueError("level groups must be contiguous")
+            starts[gi] = int(r0)
+            lens[gi] = int(length)
+            if pg is not None:
+                _need(pg, "group pages", torch.int32)
+                pages[gi] = pg.data_ptr()
+        starts[n] = int(groups[-1][1]) if n else 0
+        if n and starts[n] != B:
+            raise ValueError("level groups must end at request B")
+        arr[li].num_groups = n
+        arr[li].group_start = ctypes.cast(starts, ctypes.POINTER(ctypes.c_int32))
+        arr[li].group_len = ctypes.cast(lens, ctypes.POINTER(ctypes.c_int32))
+        arr[li].group_pages = ctypes.cast(pages, ctypes.POINTER(ctypes.c_void_p))
+        keep += [starts, lens, pages]
+    return arr, keep
+
+
+def cascade_multilevel_workspace_size(levels, B: int, Hq: int, Hkv: int, D: int,
+                                      sm_count: int = 0) -> int:
+    arr, _keep = _levels_struct(levels, B)
+    return int(_ffi.lib().skv_cascade_multilevel_workspace_size(
+        len(levels), ctypes.cast(arr, ctypes.c_void_p), B, Hq, Hkv, D, sm_count))
+
+
+def cascade_decode_multilevel(q, k_cache, v_cache, levels, block_table, ctx, num_splits: int,
+                              sm_scale: float, out=None, lse_out=None, o_pre=None, s_pre=None,
+                              o_part=None, lse_part=None, workspace=None):
+    """Multi-level cascade decode.  levels[l] is a list of groups (r0, r1, pages, length):
+    requests [r0, r1) share `length` tokens on the device int32 page list `pages` at level l
+    (the groups of a level cover 0..B in order).  Returns
+    (out, lse_out, o_pre, s_pre, o_part, lse_part)."""
+    B, Hq, D = q.shape
+    P, Hkv, page, D2 = k_cache.shape
+    _need(q, "q")
+    _need(k_cache, "k_cache", q.dtype)
+    _need(v_cache, "v_cache", q.dtype, tuple(k_cache.shape))
+    _need(block_table, "block_table", torch.int32)
+    _need(ctx, "ctx", torch.int32, (B,))
+    if D2 != D or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("inconsistent cascade shapes")
+    dev = q.device
+    f32 = torch.float32
+    out = torch.empty((B, Hq, D), dtype=q.dtype, device=dev) if out is None else out
+    lse_out = torch.empty((B, Hq), dtype=f32, device=dev) if lse_out is None else lse_out
+    o_pre = torch.empty((B, Hq, D), dtype=f32, device=dev) if o_pre is None else o_pre
+    s_pre = torch.empty((B, Hq), dtype=f32, device=dev) if s_pre is None else s_pre
+    if o_part is None:
+        o_part = torch.empty((B, Hq, num_splits, D), dtype=f32, device=dev)
+    if lse_part is None:
+        lse_part = torch.empty((B, Hq, num_splits), dtype=f32, device=dev)
+    for t, n, shp in ((out, "out", (B, Hq, D)), (lse_out, "lse_out", (B, Hq)),
+                      (o_pre, "o_pre", (B, Hq, D)), (s_pre, "s_pre", (B, Hq)),
+                      (o_part, "o_part", (B, Hq, num_splits, D)),
+                      (lse_part, "lse_part", (B, Hq, num_splits))):
+        _need(t, n, None, shp)
+    arr, keep = _levels_struct(levels, B)
+    need = int(_ffi.lib().skv_cascade_multilevel_workspace_size(
+        len(levels), ctypes.cast(arr, ctypes.c_void_p), B, Hq, Hkv, D, 0))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _ffi.check("skv_cascade_decode_multilevel", _ffi.lib().skv_cascade_decode_multilevel(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), P, len(levels),
+        ctypes.cast(arr, ctypes.c_void_p), block_table.data_ptr(), block_table.shape[1],
+        ctx.data_ptr(), B, Hq, Hkv, D, page, num_splits, float(sm_scale), _DT[q.dtype],
+        o_pre.data_ptr(), s_pre.data_ptr(), o_part.data_ptr(), lse_part.data_ptr(),
+        out.data_ptr(), lse_out.data_ptr(), workspace.data_ptr(), ws_bytes, _stream(q)))
+    del keep
+    return out, lse_out, o_pre, s_pre, o_part, lse_part
+
+
 def get_device_error():
     """(code, detail) of the first device-side error since the last call; clears it."""
     code, detail = ctypes.c_int32(), ctypes.c_int32()

@@ -48,8 +48,19 @@ SIGNATURES = {
                                  c_void_p, i32, i32, i32, i32, i32, i32, f32, i32, c_void_p,
                                  c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                  size_t, c_void_p]),
+    "skv_cascade_multilevel_workspace_size": (size_t, [i32, c_void_p, i32, i32, i32, i32, i32]),
+    "skv_cascade_decode_multilevel": (i32, [c_void_p, c_void_p, c_void_p, i32, i32, c_void_p,
+                                            c_void_p, i32, c_void_p, i32, i32, i32, i32, i32, i32,
+                                            f32, i32, c_void_p, c_void_p, c_void_p, c_void_p,
+                                            c_void_p, c_void_p, c_void_p, size_t, c_void_p]),
     "skv_get_device_error": (i32, [c_int32_p, c_int32_p]),
 }
+
+
+class CascadeLevel(ctypes.Structure):
+    """skv_cascade_level: host arrays (group_start, group_len, group_pages)."""
+    _fields_ = [("num_groups", i32), ("group_start", c_int32_p), ("group_len", c_int32_p),
+                ("group_pages", ctypes.POINTER(c_void_p))]
 
 
 class SkvError(RuntimeError):

@@ -6,7 +6,9 @@
 // [L3] "L3 讲解：split-KV decode 与 LSE 合并".
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -305,26 +307,86 @@ static skv_status side_stream(int device, SideStream** out) {
     return SKV_OK;
 }
 
-size_t skv_cascade_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
-                                  int32_t prefix_len, int32_t sm_count) {
-    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 1 || prefix_len < 0 || sm_count < 0)
-        return 0;
-    int mt = 0, bpc = 0, nc = 0;
-    if (cascade_chunks(B, Hq, Hkv, prefix_len, sm_count, &mt, &bpc, &nc) != SKV_OK) return 0;
-    const size_t rows = (size_t)B * Hq;
-    return align256(rows * nc * D * 4) + align256(rows * nc * 4) + 256;
+}  // extern "C"
+
+namespace {
+
+// One group of a cascade level: requests [r0, r1) share `len` tokens on the
+// pool pages `pages`.
+struct CascadeGroup {
+    int32_t r0, r1;
+    const int32_t* pages;
+    int32_t len;
+};
+using CascadeLevels = std::vector<std::vector<CascadeGroup>>;
+
+// Chunk-state slots per row: each level gets as many as the most chunks any
+// of its groups' prefixes needs.
+struct LevelPlan {
+    int slots = 0, offset = 0;
+    std::vector<int> mt, bpc;
+};
+
+skv_status cascade_plan(const CascadeLevels& levels, int32_t Hq, int32_t Hkv, int32_t sm_count,
+                        std::vector<LevelPlan>* plan, int* total_slots) {
+    plan->assign(levels.size(), LevelPlan());
+    int total = 0;
+    for (size_t l = 0; l < levels.size(); ++l) {
+        LevelPlan& lp = (*plan)[l];
+        for (const CascadeGroup& g : levels[l]) {
+            int mt = 0, bpc = 0, nc = 0;
+            skv_status st = cascade_chunks(g.r1 - g.r0, Hq, Hkv, g.len, sm_count, &mt, &bpc, &nc);
+            if (st != SKV_OK) return st;
+            lp.mt.push_back(mt);
+            lp.bpc.push_back(bpc);
+            lp.slots = std::max(lp.slots, nc);
+        }
+        lp.offset = total;
+        total += lp.slots;
+    }
+    *total_slots = total;
+    return SKV_OK;
 }
 
-skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_cache,
-                              int32_t num_pool_pages, const int32_t* prefix_pages,
-                              int32_t prefix_len, const int32_t* block_table, int32_t max_pages,
-                              const int32_t* ctx, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
-                              int32_t page, int32_t num_splits, float sm_scale, skv_dtype dtype,
-                              float* o_pre, float* s_pre, float* o_part, float* lse_part,
-                              void* out, float* lse_out, void* workspace, size_t workspace_bytes,
-                              skv_stream_t stream) {
+size_t cascade_ws_bytes(size_t rows, int slots, int32_t D) {
+    return align256(rows * slots * D * 4) + align256(rows * slots * 4) + 256;
+}
+
+// Converts the public level descriptions, checking them.
+skv_status read_levels(int32_t num_levels, const skv_cascade_level* levels, int32_t B,
+                       CascadeLevels* out) {
+    if (num_levels < 0 || (num_levels > 0 && !levels)) return SKV_ERR_INVALID_ARG;
+    out->assign((size_t)num_levels, {});
+    for (int32_t l = 0; l < num_levels; ++l) {
+        const skv_cascade_level& lv = levels[l];
+        if (lv.num_groups < 1 || !lv.group_start || !lv.group_len || !lv.group_pages)
+            return SKV_ERR_INVALID_ARG;
+        if (lv.group_start[0] != 0 || lv.group_start[lv.num_groups] != B) return SKV_ERR_INVALID_ARG;
+        for (int32_t g = 0; g < lv.num_groups; ++g) {
+            const int32_t r0 = lv.group_start[g], r1 = lv.group_start[g + 1], len = lv.group_len[g];
+            const int32_t* pages = lv.group_pages[g];
+            if (r1 < r0 || len < 0) return SKV_ERR_INVALID_ARG;
+            if (len > 0 && (!pages || !aligned4(pages))) return SKV_ERR_INVALID_ARG;
+            if (r1 > r0) (*out)[l].push_back(CascadeGroup{r0, r1, pages, len});
+        }
+    }
+    return SKV_OK;
+}
+
+// The cascade for any number of shared levels ([F2] §⑥ and the multi-level
+// wrapper it names): each group's prefix pass writes its chunk states into
+// its level's slots of every row it covers (on the side stream), the
+// suffixes run through the split-KV decode, and one combine merges all
+// slots into the prefix state and that with the suffix splits.
+skv_status cascade_run(const void* q, const void* k_cache, const void* v_cache,
+                       int32_t num_pool_pages, const CascadeLevels& levels,
+                       const int32_t* block_table, int32_t max_pages, const int32_t* ctx,
+                       int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page,
+                       int32_t num_splits, float sm_scale, skv_dtype dtype, float* o_pre,
+                       float* s_pre, float* o_part, float* lse_part, void* out, float* lse_out,
+                       void* workspace, size_t workspace_bytes, skv_stream_t stream) {
     if (B < 0 || Hq < 1 || Hkv < 1 || D < 1 || page < 1 || num_splits < 1 || max_pages < 1 ||
-        num_pool_pages < 1 || prefix_len < 0 || !valid_dtype(dtype))
+        num_pool_pages < 1 || !valid_dtype(dtype))
         return SKV_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return SKV_ERR_INVALID_ARG;
     const int G = Hq / Hkv;
@@ -338,10 +400,9 @@ skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_
     if (!q || !k_cache || !v_cache || !block_table || !ctx || !o_part || !lse_part || !out ||
         !workspace)
         return SKV_ERR_INVALID_ARG;
-    if (prefix_len > 0 && !prefix_pages) return SKV_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o_part) ||
         !aligned16(out) || !aligned16(workspace) || !aligned4(lse_part) || !aligned4(block_table) ||
-        !aligned4(ctx) || (prefix_pages && !aligned4(prefix_pages)))
+        !aligned4(ctx))
         return SKV_ERR_INVALID_ARG;
     if ((o_pre && !aligned16(o_pre)) || (s_pre && !aligned4(s_pre)) ||
         (lse_out && !aligned4(lse_out)))
@@ -349,42 +410,52 @@ skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_
     const DeviceInfo* dev = nullptr;
     skv_status st = current_device(&dev);
     if (st != SKV_OK) return st;
-    int mt = 0, bpc = 0, nc = 0;
-    if ((st = cascade_chunks(B, Hq, Hkv, prefix_len, dev->sm_count, &mt, &bpc, &nc)) != SKV_OK)
-        return st;
+    std::vector<LevelPlan> plan;
+    int slots = 0;
+    if ((st = cascade_plan(levels, Hq, Hkv, dev->sm_count, &plan, &slots)) != SKV_OK) return st;
     const size_t rows = (size_t)B * Hq;
-    const size_t need = align256(rows * nc * D * 4) + align256(rows * nc * 4) + 256;
-    if (workspace_bytes < need) return SKV_ERR_INVALID_ARG;
+    if (workspace_bytes < cascade_ws_bytes(rows, slots, D)) return SKV_ERR_INVALID_ARG;
     float* pre_part = static_cast<float*>(workspace);
-    float* pre_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * nc * D * 4));
+    float* pre_lse =
+        reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * slots * D * 4));
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     SideStream* side = nullptr;
-    if (nc > 0 && (st = side_stream(dev->device, &side)) != SKV_OK) return st;
+    if (slots > 0 && (st = side_stream(dev->device, &side)) != SKV_OK) return st;
     std::unique_lock<std::mutex> side_lk;
-    // 1. Shared prefix on the tensor cores, one state per prefix chunk, on the
-    // side stream: forked after everything the caller queued before this call,
-    // joined back before the combine.
-    if (nc > 0) {
+    // 1. Shared prefixes on the tensor cores, one state per prefix chunk, on
+    // the side stream: forked after everything the caller queued before this
+    // call, joined back before the combine.
+    if (slots > 0) {
         side_lk = std::unique_lock<std::mutex>(side->mu);
         if (cudaEventRecord(side->fork, cs) != cudaSuccess ||
             cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
             return SKV_ERR_CUDA;
-        CascadeArgs ca;
-        ca.q = q;
-        ca.k_cache = k_cache;
-        ca.v_cache = v_cache;
-        ca.num_pool_pages = num_pool_pages;
-        ca.prefix_pages = prefix_pages;
-        ca.prefix_len = prefix_len;
-        ca.B = B;
-        ca.Hq = Hq;
-        ca.Hkv = Hkv;
-        ca.bf16 = dtype == SKV_BF16;
-        ca.sm_scale = sm_scale;
-        if (launch_cascade_prefix(ca, *dev, pre_part, pre_lse, nc, bpc, mt, side->stream) !=
-                cudaSuccess ||
-            cudaEventRecord(side->join, side->stream) != cudaSuccess)
-            return SKV_ERR_CUDA;
+        const size_t elt = 2;  // fp16 / bf16
+        for (size_t l = 0; l < levels.size(); ++l) {
+            const LevelPlan& lp = plan[l];
+            if (lp.slots == 0) continue;
+            for (size_t gi = 0; gi < levels[l].size(); ++gi) {
+                const CascadeGroup& g = levels[l][gi];
+                CascadeArgs ca;
+                ca.q = static_cast<const char*>(q) + (size_t)g.r0 * Hq * D * elt;
+                ca.k_cache = k_cache;
+                ca.v_cache = v_cache;
+                ca.num_pool_pages = num_pool_pages;
+                ca.prefix_pages = g.pages;
+                ca.prefix_len = g.len;
+                ca.B = g.r1 - g.r0;
+                ca.Hq = Hq;
+                ca.Hkv = Hkv;
+                ca.bf16 = dtype == SKV_BF16;
+                ca.sm_scale = sm_scale;
+                const size_t row0 = (size_t)g.r0 * Hq;
+                if (launch_cascade_prefix(ca, *dev, pre_part + row0 * slots * D, pre_lse + row0 * slots,
+                                          lp.slots, lp.bpc[gi], lp.mt[gi], slots, lp.offset,
+                                          side->stream) != cudaSuccess)
+                    return SKV_ERR_CUDA;
+            }
+        }
+        if (cudaEventRecord(side->join, side->stream) != cudaSuccess) return SKV_ERR_CUDA;
     }
     // 2. Each request's own suffix through the split-KV decode.
     DecodeArgs a;
@@ -409,8 +480,9 @@ skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_
     if ((use_tc_decode() ? launch_splitkv_decode_tc(a, *dev, cs) : launch_splitkv_decode(a, *dev, cs)) !=
         cudaSuccess)
         return SKV_ERR_CUDA;
-    if (nc > 0 && cudaStreamWaitEvent(cs, side->join, 0) != cudaSuccess) return SKV_ERR_CUDA;
-    // 3. Prefix chunks -> prefix state; merge_state(prefix, suffix) -> out.
+    if (slots > 0 && cudaStreamWaitEvent(cs, side->join, 0) != cudaSuccess) return SKV_ERR_CUDA;
+    // 3. Prefix chunks of every level -> prefix state; merge_state(prefix,
+    // suffix) -> out.
     CombineArgs c = {};
     c.o_part = o_part;
     c.lse_part = lse_part;
@@ -422,13 +494,80 @@ skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_
     c.lse_out = lse_out;
     c.pre_part = pre_part;
     c.pre_lse = pre_lse;
-    c.C = nc;
+    c.C = slots;
     c.o_pre = o_pre;
     c.s_pre = s_pre;
     // Without a prefix the combine follows pass 1 directly (programmatic
     // dependent launch); after the join it waits for both in stream order.
-    if (launch_combine(c, nc == 0, *dev, cs) != cudaSuccess) return SKV_ERR_CUDA;
+    if (launch_combine(c, slots == 0, *dev, cs) != cudaSuccess) return SKV_ERR_CUDA;
     return SKV_OK;
+}
+
+CascadeLevels two_level(int32_t B, const int32_t* prefix_pages, int32_t prefix_len) {
+    CascadeLevels lv(1);
+    if (B > 0) lv[0].push_back(CascadeGroup{0, B, prefix_pages, prefix_len});
+    return lv;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t skv_cascade_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                  int32_t prefix_len, int32_t sm_count) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 1 || prefix_len < 0 || sm_count < 0)
+        return 0;
+    std::vector<LevelPlan> plan;
+    int slots = 0;
+    if (cascade_plan(two_level(B, nullptr, prefix_len), Hq, Hkv, sm_count, &plan, &slots) != SKV_OK)
+        return 0;
+    return cascade_ws_bytes((size_t)B * Hq, slots, D);
+}
+
+skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_cache,
+                              int32_t num_pool_pages, const int32_t* prefix_pages,
+                              int32_t prefix_len, const int32_t* block_table, int32_t max_pages,
+                              const int32_t* ctx, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                              int32_t page, int32_t num_splits, float sm_scale, skv_dtype dtype,
+                              float* o_pre, float* s_pre, float* o_part, float* lse_part,
+                              void* out, float* lse_out, void* workspace, size_t workspace_bytes,
+                              skv_stream_t stream) {
+    if (prefix_len < 0) return SKV_ERR_INVALID_ARG;
+    if (prefix_len > 0 && (!prefix_pages || !aligned4(prefix_pages))) return SKV_ERR_INVALID_ARG;
+    return cascade_run(q, k_cache, v_cache, num_pool_pages, two_level(B, prefix_pages, prefix_len),
+                       block_table, max_pages, ctx, B, Hq, Hkv, D, page, num_splits, sm_scale, dtype,
+                       o_pre, s_pre, o_part, lse_part, out, lse_out, workspace, workspace_bytes,
+                       stream);
+}
+
+size_t skv_cascade_multilevel_workspace_size(int32_t num_levels, const skv_cascade_level* levels,
+                                             int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                             int32_t sm_count) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 1 || sm_count < 0) return 0;
+    CascadeLevels lv;
+    if (read_levels(num_levels, levels, B, &lv) != SKV_OK) return 0;
+    std::vector<LevelPlan> plan;
+    int slots = 0;
+    if (cascade_plan(lv, Hq, Hkv, sm_count, &plan, &slots) != SKV_OK) return 0;
+    return cascade_ws_bytes((size_t)B * Hq, slots, D);
+}
+
+skv_status skv_cascade_decode_multilevel(const void* q, const void* k_cache, const void* v_cache,
+                                         int32_t num_pool_pages, int32_t num_levels,
+                                         const skv_cascade_level* levels,
+                                         const int32_t* block_table, int32_t max_pages,
+                                         const int32_t* ctx, int32_t B, int32_t Hq, int32_t Hkv,
+                                         int32_t D, int32_t page, int32_t num_splits,
+                                         float sm_scale, skv_dtype dtype, float* o_pre,
+                                         float* s_pre, float* o_part, float* lse_part, void* out,
+                                         float* lse_out, void* workspace, size_t workspace_bytes,
+                                         skv_stream_t stream) {
+    CascadeLevels lv;
+    skv_status st = read_levels(num_levels, levels, B, &lv);
+    if (st != SKV_OK) return st;
+    return cascade_run(q, k_cache, v_cache, num_pool_pages, lv, block_table, max_pages, ctx, B, Hq,
+                       Hkv, D, page, num_splits, sm_scale, dtype, o_pre, s_pre, o_part, lse_part,
+                       out, lse_out, workspace, workspace_bytes, stream);
 }
 
 skv_status skv_get_device_error(int32_t* code, int32_t* detail) {

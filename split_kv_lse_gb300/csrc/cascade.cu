@@ -67,10 +67,12 @@ struct PrefixParams {
     int32_t pool_rows;        // rows of the K/V tensor maps: num_pool_pages * Hkv * page
     int32_t num_pool_pages;
     int32_t B, Hq, Hkv, G;
-    int32_t blocks_per_chunk, nchunks;
+    int32_t blocks_per_chunk;
+    int32_t chunk_stride;     // chunk-state slots per row in pre_part / pre_lse
+    int32_t chunk_offset;     // slot of this launch's chunk 0
     float scale_log2;
-    float* pre_part;          // [B*Hq, nchunks, D] split-normalised chunk states
-    float* pre_lse;           // [B*Hq, nchunks] base 2
+    float* pre_part;          // [B*Hq, chunk_stride, D] split-normalised chunk states
+    float* pre_lse;           // [B*Hq, chunk_stride] base 2
     unsigned long long* err;
 };
 
@@ -122,8 +124,21 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     const int chunk = blockIdx.x, mpair = blockIdx.y, hkv = blockIdx.z;
     const int nblocks_total = (p.prefix_len + kBlockKeys - 1) / kBlockKeys;
     const int blk0 = chunk * p.blocks_per_chunk;
-    const int nb = min(p.blocks_per_chunk, nblocks_total - blk0);  // >= 1 (host sizing)
+    const int nb = min(p.blocks_per_chunk, nblocks_total - blk0);
     const int npages_prefix = (p.prefix_len + kPage - 1) / kPage;
+    if (nb <= 0) {
+        // A slot past this prefix's last block (the grid covers the most
+        // chunks any prefix of its level has): an empty state, s = -inf, for
+        // each of the CTA's rows (a zero-weight state's v is never read).
+        for (int i = tid; i < 2 * kM; i += kThreads) {
+            const int r = i / p.G, g = i % p.G;  // row i of the M pair: request, group head
+            const int req = 2 * mpair * (kM / p.G) + r;
+            if (req < p.B)
+                p.pre_lse[((int64_t)req * p.Hq + hkv * p.G + g) * p.chunk_stride + p.chunk_offset +
+                          chunk] = -INFINITY;
+        }
+        return;
+    }
 
     if (tid == 0) {
         mbar_init(q_full, 1);
@@ -403,7 +418,7 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
             {
                 const int r = req0 + row_t / rows_per_req, g = row_t % rows_per_req;
                 if (r < p.B)
-                    p.pre_lse[((int64_t)r * p.Hq + hkv * p.G + g) * p.nchunks + chunk] =
+                    p.pre_lse[((int64_t)r * p.Hq + hkv * p.G + g) * p.chunk_stride + p.chunk_offset + chunk] =
                         l_run > 0.f ? m_ref + log2f(l_run) : -INFINITY;
             }
             __syncwarp();  // this warp's 32 rows are staged
@@ -413,7 +428,8 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                 const int r = req0 + rt / rows_per_req, g = rt % rows_per_req;
                 if (r < p.B) {
                     const float4 v = *reinterpret_cast<const float4*>(stage_row(rt) + ((lane ^ (rt & 31)) << 4));
-                    float* dst = p.pre_part + (((int64_t)r * p.Hq + hkv * p.G + g) * p.nchunks + chunk) * kD;
+                    float* dst = p.pre_part +
+                                 (((int64_t)r * p.Hq + hkv * p.G + g) * p.chunk_stride + p.chunk_offset + chunk) * kD;
                     *reinterpret_cast<float4*>(dst + 4 * lane) = v;
                 }
             }
@@ -446,7 +462,7 @@ void cascade_prefix_geometry(int B, int G, int Hkv, int prefix_len, int sm_count
 
 cudaError_t launch_cascade_prefix(const CascadeArgs& a, const DeviceInfo& dev, float* pre_part,
                                   float* pre_lse, int nchunks, int blocks_per_chunk, int mtiles,
-                                  cudaStream_t st) {
+                                  int chunk_stride, int chunk_offset, cudaStream_t st) {
     const int G = a.Hq / a.Hkv;
     CUtensorMap tq, tk, tv;
     // (fp16 element type for bf16 q too: the copies are bitwise and the
@@ -469,7 +485,8 @@ cudaError_t launch_cascade_prefix(const CascadeArgs& a, const DeviceInfo& dev, f
     p.Hkv = a.Hkv;
     p.G = G;
     p.blocks_per_chunk = blocks_per_chunk;
-    p.nchunks = nchunks;
+    p.chunk_stride = chunk_stride;
+    p.chunk_offset = chunk_offset;
     p.scale_log2 = a.sm_scale * 1.4426950408889634f;
     p.pre_part = pre_part;
     p.pre_lse = pre_lse;

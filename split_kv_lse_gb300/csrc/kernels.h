@@ -102,8 +102,11 @@ struct CascadeArgs {
 // of 128 keys per chunk, number of chunks.
 void cascade_prefix_geometry(int B, int G, int Hkv, int prefix_len, int sm_count, int* mtiles,
                              int* blocks_per_chunk, int* nchunks);
+// Launches nchunks chunk CTAs per (M-tile pair, kv head); chunk c writes
+// slot chunk_offset + c of chunk_stride slots per row (slots past the
+// prefix's last block get an empty state).
 cudaError_t launch_cascade_prefix(const CascadeArgs& a, const DeviceInfo& dev, float* pre_part,
                                   float* pre_lse, int nchunks, int blocks_per_chunk, int mtiles,
-                                  cudaStream_t st);
+                                  int chunk_stride, int chunk_offset, cudaStream_t st);
 
 }  // namespace skv

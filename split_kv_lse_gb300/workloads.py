@@ -174,6 +174,40 @@ def cascade_inputs(B, Hq, Hkv, D, page, prefix_len, suffix_ctx, seed=0, dtype=to
             "page": page}
 
 
+def cascade_multilevel_inputs(B, Hq, Hkv, D, page, levels, suffix_ctx, seed=0,
+                              dtype=torch.float16):
+    """Shared tokens at several levels plus a per-request suffix.  levels[l] is a
+    list of groups (r0, r1, length): requests [r0, r1) share `length` tokens at
+    level l.  Every group's tokens and every suffix get their own pool pages, in
+    one random permutation of the pool.  Returns the cascade inputs with
+    "levels" = [[(r0, r1, pages int32 tensor, length), ...], ...]."""
+    g = _gen(seed)
+    sizes = [math.ceil(length / page) for groups in levels for (_, _, length) in groups]
+    need = [math.ceil(c / page) for c in suffix_ctx]
+    P = max(1, sum(sizes) + sum(need))
+    perm = torch.randperm(P, generator=g).to(torch.int32)
+    at = 0
+    out_levels = []
+    for groups in levels:
+        lv = []
+        for (r0, r1, length) in groups:
+            n = math.ceil(length / page)
+            lv.append((r0, r1, perm[at:at + n].clone(), length))
+            at += n
+        out_levels.append(lv)
+    mp = max(1, max(need) if need else 1)
+    table = torch.zeros(B, mp, dtype=torch.int32)
+    for b, n in enumerate(need):
+        table[b, :n] = perm[at:at + n]
+        at += n
+    q = torch.randn(B, Hq, D, generator=g, dtype=torch.float32).to(dtype)
+    kc = torch.randn(P, Hkv, page, D, generator=g, dtype=torch.float32).to(dtype)
+    vc = torch.randn(P, Hkv, page, D, generator=g, dtype=torch.float32).to(dtype)
+    return {"q": q, "k_cache": kc, "v_cache": vc, "levels": out_levels, "block_table": table,
+            "ctx": torch.tensor(suffix_ctx, dtype=torch.int32), "sm_scale": 1.0 / math.sqrt(D),
+            "page": page}
+
+
 def cascade_mixed(seed=0):
     """B=64 requests sharing an 8192-token prefix; suffix lengths uniform in
     [1, 2048] (so some have fewer tokens than page*NS and get empty splits);

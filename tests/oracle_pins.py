@@ -464,4 +464,82 @@ def pin_cascade(orc):
         assert np.allclose(ms.reshape(s.shape)[fin], s[fin], rtol=0, atol=1e-12)
 
 
+def pin_cascade_multilevel(orc):
+    """[F2] §⑥ (attention level by level, then merge): shared tokens at several
+    levels, then the suffix, equal one softmax over their concatenation; one
+    level of one group is the two-level cascade; the prefix state is the merge
+    of the levels' own states."""
+    rng = np.random.default_rng(17)
+    B, Hq, Hkv, D, page = 5, 4, 2, 8, 4
+    ctx = [5, 0, 9, 3, 6]
+    # levels[l] = groups (r0, r1, length); pages drawn after the suffix pages.
+    for spec in (
+            [[(0, 5, 12)]],                                    # one level, one group
+            [[(0, 5, 8)], [(0, 2, 4), (2, 5, 12)], [(0, 3, 0), (3, 5, 8)]],   # whole pages
+            [[(0, 5, 7)], [(0, 1, 5), (1, 4, 0), (4, 5, 10)]],  # partial pages, an empty group
+    ):
+        npg = sum(-(-ln // page) for lv in spec for (_, _, ln) in lv)
+        q, kc, vc, bt, cx = _rand_decode(rng, B, Hq, Hkv, D, page, ctx, pool_extra=npg + 1)
+        used = set(bt.reshape(-1).tolist()) if max(ctx) > 0 else set()
+        free = [p for p in range(kc.shape[0]) if p not in used]
+        levels, at = [], 0
+        for lv in spec:
+            groups = []
+            for (r0, r1, ln) in lv:
+                n = -(-ln // page)
+                groups.append((r0, r1, np.array(free[at:at + n], np.int32), ln))
+                at += n
+            levels.append(groups)
+        out, s, o_pre, s_pre = orc.cascade_multilevel(q, kc, vc, levels, bt, cx, 0.4)
+        if len(spec) == 1 and len(spec[0]) == 1:
+            o2, s2, op2, sp2 = orc.cascade(q, kc, vc, levels[0][0][2], spec[0][0][2], bt, cx, 0.4)
+            assert np.allclose(out, o2, rtol=1e-13, atol=1e-14)
+            assert np.allclose(s, s2, rtol=0, atol=1e-12)
+            assert np.allclose(o_pre, op2, rtol=1e-13, atol=1e-14)
+            assert np.allclose(s_pre, sp2, rtol=0, atol=1e-12)
+        if all(ln % page == 0 for lv in spec for (_, _, ln) in lv):
+            # Whole pages: one block table per request, shared pages first.
+            rows, lens = [], []
+            for b in range(B):
+                pg, n = [], 0
+                for groups in levels:
+                    for (r0, r1, pages, ln) in groups:
+                        if r0 <= b < r1:
+                            pg += pages.tolist()
+                            n += ln
+                pg += bt[b, :-(-int(cx[b]) // page)].tolist() if cx[b] else []
+                rows.append(pg)
+                lens.append(n + int(cx[b]))
+            cat = np.zeros((B, max(1, max(len(r) for r in rows))), np.int32)
+            for b, r in enumerate(rows):
+                cat[b, :len(r)] = r
+            of, sf = orc.attend_full(q, kc, vc, cat, np.array(lens, np.int32), 0.4)
+            assert np.allclose(out, of, rtol=1e-13, atol=1e-14)
+            fin = np.isfinite(sf)
+            assert np.array_equal(np.isfinite(s), fin)
+            assert np.allclose(s[fin], sf[fin], rtol=0, atol=1e-12)
+        # The prefix state is the merge of each level's own state (each
+        # group's tokens alone, through the unsplit definition), and out is
+        # that merged with the suffix state.
+        acc_v = np.zeros((B * Hq, D))
+        acc_s = np.full(B * Hq, -np.inf)
+        for groups in levels:
+            lv_v = np.zeros((B, Hq, D))
+            lv_s = np.full((B, Hq), -np.inf)
+            for (r0, r1, pages, ln) in groups:
+                nb = r1 - r0
+                tab = np.repeat(pages[None], nb, 0) if pages.size else np.zeros((nb, 1), np.int32)
+                ov, sv = orc.attend_full(q[r0:r1], kc, vc, tab, np.full(nb, ln, np.int32), 0.4)
+                lv_v[r0:r1], lv_s[r0:r1] = ov, sv
+            acc_v, acc_s = orc.merge_state(acc_v, acc_s, lv_v.reshape(-1, D), lv_s.reshape(-1))
+        assert np.allclose(acc_v.reshape(o_pre.shape), o_pre, rtol=1e-12, atol=1e-13)
+        fin = np.isfinite(s_pre)
+        assert np.array_equal(np.isfinite(acc_s.reshape(s_pre.shape)), fin)
+        assert np.allclose(acc_s.reshape(s_pre.shape)[fin], s_pre[fin], rtol=0, atol=1e-12)
+        ov, sv = orc.attend_full(q, kc, vc, bt, cx, 0.4)
+        mv, ms = orc.merge_state(o_pre.reshape(-1, D), s_pre.reshape(-1), ov.reshape(-1, D),
+                                 sv.reshape(-1))
+        assert np.allclose(mv.reshape(out.shape), out, rtol=1e-12, atol=1e-13)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -170,6 +170,40 @@ def test_merge_states_workspace_size(lib):
     assert f(0, 4, 4, 64) == 0 and f(4, 0, 4, 64) == 0
 
 
+def _level(starts, lens):
+    from split_kv_lse_gb300 import _ffi
+    n = len(lens)
+    s = (ctypes.c_int32 * (n + 1))(*starts)
+    ln = (ctypes.c_int32 * n)(*lens)
+    pg = (ctypes.c_void_p * n)(*[16 if x > 0 else None for x in lens])  # never dereferenced here
+    lv = _ffi.CascadeLevel(n, ctypes.cast(s, ctypes.POINTER(ctypes.c_int32)),
+                           ctypes.cast(ln, ctypes.POINTER(ctypes.c_int32)),
+                           ctypes.cast(pg, ctypes.POINTER(ctypes.c_void_p)))
+    return lv, (s, ln, pg)
+
+
+def test_cascade_multilevel_workspace_size(lib):
+    """One level of one group needs what the two-level cascade needs; more
+    levels add their chunk-state slots; a level that does not cover 0..B in
+    order is rejected (size 0)."""
+    from split_kv_lse_gb300 import _ffi
+    two = lib.skv_cascade_workspace_size(64, 32, 8, 128, 8192, 152)
+    lv, keep = _level([0, 64], [8192])
+    arr = (_ffi.CascadeLevel * 1)(lv)
+    assert lib.skv_cascade_multilevel_workspace_size(1, arr, 64, 32, 8, 128, 152) == two
+    lv1, k1 = _level([0, 30, 64], [1000, 0])
+    arr2 = (_ffi.CascadeLevel * 2)(lv, lv1)
+    assert lib.skv_cascade_multilevel_workspace_size(2, arr2, 64, 32, 8, 128, 152) > two
+    bad, kb = _level([0, 40, 30, 64], [5, 5, 5])     # decreasing boundary
+    assert lib.skv_cascade_multilevel_workspace_size(1, (_ffi.CascadeLevel * 1)(bad), 64, 32, 8,
+                                                     128, 152) == 0
+    short, ks = _level([0, 60], [5])                 # does not reach B
+    assert lib.skv_cascade_multilevel_workspace_size(1, (_ffi.CascadeLevel * 1)(short), 64, 32,
+                                                     8, 128, 152) == 0
+    # No shared level: the suffix alone, no slots.
+    assert lib.skv_cascade_multilevel_workspace_size(0, None, 64, 32, 8, 128, 152) > 0
+
+
 def test_product_path_never_imports_the_oracle():
     """The library package must not reference the oracle in any form."""
     pkg = os.path.join(ROOT, "split_kv_lse_gb300")

@@ -139,3 +139,102 @@ def test_cascade_bf16_full_workload(lib):
     suffix = fp16["ctx"].tolist()  # the same suffix lengths as the fp16 workload
     d = W.cascade_inputs(64, 32, 8, 128, 16, 8192, suffix, 0, dtype=torch.bfloat16)
     run_and_check(lib, d, 16, poison=False)
+
+
+# ---------------------------------------------------------------- multi-level cascade
+def poison_multilevel(d):
+    """NaN into every cache slot no request may read: the tails of partial last
+    pages of every shared list and suffix, and unused pool pages."""
+    kc, vc = d["k_cache"], d["v_cache"]
+    used = set()
+    segs = [(pages.tolist(), length) for groups in d["levels"] for (_, _, pages, length) in groups]
+    segs += [(d["block_table"][b].tolist(), c) for b, c in enumerate(d["ctx"].tolist())]
+    for pages, length in segs:
+        n = -(-length // 16)
+        used.update(pages[:n])
+        if length % 16:
+            kc[pages[n - 1], :, length % 16:] = float("nan")
+            vc[pages[n - 1], :, length % 16:] = float("nan")
+    for pid in range(kc.shape[0]):
+        if pid not in used:
+            kc[pid] = float("nan")
+            vc[pid] = float("nan")
+
+
+def run_multilevel(lib, d, ns, poison=True):
+    if poison:
+        poison_multilevel(d)
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    levels = [[(r0, r1, pages.to(DEV) if pages.numel() else None, length)
+               for (r0, r1, pages, length) in groups] for groups in d["levels"]]
+    res = lib.cascade_decode_multilevel(g["q"], g["k_cache"], g["v_cache"], levels,
+                                        g["block_table"], g["ctx"], ns, d["sm_scale"])
+    torch.cuda.synchronize()
+    assert lib.get_device_error() == (0, 0)
+    out, lse, o_pre, s_pre, o_part, lse_part = res
+    o_r, s_r, op_r, sp_r = oracle.cascade_multilevel(d["q"], d["k_cache"], d["v_cache"],
+                                                     d["levels"], d["block_table"], d["ctx"],
+                                                     d["sm_scale"])
+    atol, rtol_part, rtol_out = DEC_O_TOL[d["q"].dtype]
+    assert out.dtype == d["q"].dtype
+    assert_s_close(s_pre, sp_r, DEC_LSE_ATOL, "s_pre")
+    assert_v_close(o_pre, op_r, atol, rtol_part, "o_pre", empty_rows=(sp_r == -math.inf))
+    opr, lpr = oracle.attend_splits(d["q"], d["k_cache"], d["v_cache"], d["block_table"],
+                                    d["ctx"], d["sm_scale"], ns)
+    assert_s_close(lse_part, lpr, DEC_LSE_ATOL, "lse_part")
+    assert_v_close(o_part, opr, atol, rtol_part, "o_part", empty_rows=(lpr == -math.inf))
+    assert_s_close(lse, s_r, DEC_LSE_ATOL, "lse_out")
+    assert_v_close(out, o_r, atol, rtol_out, "out", empty_rows=(s_r == -math.inf))
+    return res
+
+
+THREE_LEVELS = [[(0, 12, 1000)], [(0, 5, 300), (5, 9, 0), (9, 12, 77)],
+                [(0, 3, 16), (3, 12, 200)]]
+
+
+def test_cascade_multilevel_three_levels(lib):
+    """A level shared by all 12 requests, a level of three groups (one sharing
+    nothing), a third level of two groups, ragged suffixes (one empty)."""
+    ctx = [5, 0, 37, 100, 16, 1, 250, 17, 64, 3, 90, 31]
+    d = W.cascade_multilevel_inputs(12, 16, 4, 128, 16, THREE_LEVELS, ctx, seed=40)
+    run_multilevel(lib, d, 4)
+
+
+@pytest.mark.parametrize("G", [1, 8])
+def test_cascade_multilevel_group_sizes_bf16(lib, G):
+    ctx = [int(x) for x in np.random.default_rng(41 + G).integers(0, 200, 12)]
+    d = W.cascade_multilevel_inputs(12, 2 * G, 2, 128, 16, THREE_LEVELS, ctx, seed=41 + G,
+                                    dtype=torch.bfloat16)
+    run_multilevel(lib, d, 8)
+
+
+def test_cascade_multilevel_no_shared_level(lib):
+    """No shared level: the prefix state is empty and out is the suffix alone."""
+    d = W.cascade_multilevel_inputs(3, 8, 2, 128, 16, [], [40, 0, 7], seed=43)
+    out, lse, o_pre, s_pre, _, _ = run_multilevel(lib, d, 4)
+    assert torch.all(s_pre.cpu() == -math.inf) and torch.all(o_pre.cpu() == 0)
+
+
+def test_cascade_multilevel_one_level_is_the_two_level_cascade(lib):
+    """One level of one group runs exactly the two-level cascade: equal bits."""
+    d = W.cascade_multilevel_inputs(6, 16, 4, 128, 16, [[(0, 6, 777)]], [9, 0, 33, 200, 1, 64],
+                                    seed=44)
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    r0, r1, pages, length = d["levels"][0][0]
+    a = lib.cascade_decode_multilevel(g["q"], g["k_cache"], g["v_cache"],
+                                      [[(r0, r1, pages.to(DEV), length)]], g["block_table"],
+                                      g["ctx"], 4, d["sm_scale"])
+    b = lib.cascade_decode(g["q"], g["k_cache"], g["v_cache"], pages.to(DEV), length,
+                           g["block_table"], g["ctx"], 4, d["sm_scale"])
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_cascade_multilevel_full_size(lib):
+    """B=64: an 8192-token level shared by all, then eight groups of eight
+    requests sharing 512 tokens each, then suffixes of 1..2048 tokens."""
+    suffix = W.cascade_mixed()["ctx"].tolist()
+    levels = [[(0, 64, 8192)], [(8 * i, 8 * i + 8, 512) for i in range(8)]]
+    d = W.cascade_multilevel_inputs(64, 32, 8, 128, 16, levels, suffix, seed=45)
+    run_multilevel(lib, d, 16, poison=False)

@@ -48,6 +48,25 @@ MUTANTS = [
      "            for (int32_t t = 0; t < ctx[b]; ++t, ++n) {\n                kr[n] = token_row(k_cache, pages, t, Hkv, hk, page, D);",
      "            for (int32_t t = 0; t < ctx[b]; ++t, ++n) {\n                kr[n] = token_row(k_cache, prefix_pages, t, Hkv, hk, page, D);"),
     ("transposed_v_token", "o[d] += p * vrows[j][d];", "o[d] += p * vrows[n - 1 - j][d];"),
+    # multi-level cascade: every level reads level 0's length; the prefix
+    # state taken after the suffix; the suffix read from the last shared list
+    ("multilevel_level0_length",
+     "for (int32_t t = 0; t < seg_len[(int64_t)b * L + l]; ++t, ++n) {",
+     "for (int32_t t = 0; t < seg_len[(int64_t)b * L]; ++t, ++n) {"),
+    ("multilevel_prefix_state_after_suffix",
+     "            attend_rows(D, q + row * D, n, kr, vr, sm_scale, o_pre + row * D, s_pre + row);\n"
+     "            for (int32_t t = 0; t < ctx[b]; ++t, ++n) {\n"
+     "                kr[n] = token_row(k_cache, sfx, t, Hkv, hk, page, D);\n"
+     "                vr[n] = token_row(v_cache, sfx, t, Hkv, hk, page, D);\n"
+     "            }\n",
+     "            for (int32_t t = 0; t < ctx[b]; ++t, ++n) {\n"
+     "                kr[n] = token_row(k_cache, sfx, t, Hkv, hk, page, D);\n"
+     "                vr[n] = token_row(v_cache, sfx, t, Hkv, hk, page, D);\n"
+     "            }\n"
+     "            attend_rows(D, q + row * D, n, kr, vr, sm_scale, o_pre + row * D, s_pre + row);\n"),
+    ("multilevel_suffix_from_shared_pages",
+     "kr[n] = token_row(k_cache, sfx, t, Hkv, hk, page, D);",
+     "kr[n] = token_row(k_cache, seg_pages, t, Hkv, hk, page, D);"),
 ]
 
 
