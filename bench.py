@@ -184,7 +184,7 @@ def nbytes(t):
 STAGE_NAMES = ("merge_state", "merge_state_in_place", "merge_states", "splitkv_decode",
                "cascade_decode")
 # Diagnostic stages, selectable with --only (not part of the default step).
-EXTRA_STAGES = ("splitkv_decode_pass1", "cascade_suffix_pass1")
+EXTRA_STAGES = ("splitkv_decode_pass1", "cascade_suffix_pass1", "cascade_multilevel")
 
 
 def build_stages(torch, skv, W, dev, only=None):
@@ -205,6 +205,8 @@ def build_stages(torch, skv, W, dev, only=None):
         _decode_stage(torch, skv, W, dev, to_dev, stages, hostside, want)
     if want & {"cascade_decode", "cascade_suffix_pass1"}:
         _cascade_stage(torch, skv, W, dev, to_dev, stages, hostside, want)
+    if "cascade_multilevel" in want:
+        _multilevel_stage(torch, skv, W, dev, to_dev, stages)
     return stages, hostside
 
 
@@ -308,6 +310,40 @@ def _cascade_stage(torch, skv, W, dev, to_dev, stages, hostside, want):
                                                        bufs["lse_part"], combine=False),
                             suf_bytes, 1))
     hostside["cascade"] = d5
+
+
+def _multilevel_stage(torch, skv, W, dev, to_dev, stages):
+    # Three-level cascade, B=64: an 8192-token level shared by all requests,
+    # eight groups of eight sharing 512 tokens each, then the suffixes of the
+    # cascade workload (1..2048 tokens), NS=16.
+    suffix = W.cascade_mixed()["ctx"].tolist()
+    spec = [[(0, 64, 8192)], [(8 * i, 8 * i + 8, 512) for i in range(8)]]
+    d = W.cascade_multilevel_inputs(64, 32, 8, 128, 16, spec, suffix, seed=45)
+    g = to_dev({k: v for k, v in d.items() if k != "levels"})
+    levels = [[(r0, r1, pages.to(dev), ln) for (r0, r1, pages, ln) in groups]
+              for groups in d["levels"]]
+    B, Hq, D = d["q"].shape
+    Hkv = d["k_cache"].shape[1]
+    f32 = torch.float32
+    bufs = dict(out=torch.empty(B, Hq, D, dtype=torch.float16, device=dev),
+                lse_out=torch.empty(B, Hq, device=dev), o_pre=torch.empty(B, Hq, D, device=dev),
+                s_pre=torch.empty(B, Hq, device=dev),
+                o_part=torch.empty(B, Hq, 16, D, dtype=f32, device=dev),
+                lse_part=torch.empty(B, Hq, 16, dtype=f32, device=dev))
+    ws = torch.empty(max(256, skv.cascade_multilevel_workspace_size(levels, B, Hq, Hkv, D)),
+                     dtype=torch.uint8, device=dev)
+    shared = sum(ln * (r1 - r0 > 0) for groups in d["levels"] for (r0, r1, _, ln) in groups)
+    npages = sum(-(-ln // 16) for groups in d["levels"] for (_, _, _, ln) in groups)
+    npages += sum(-(-int(c) // 16) for c in d["ctx"])
+    kv_tokens = shared + int(d["ctx"].sum())
+    nbytes_ = (kv_tokens * Hkv * D * 2 * 2 + nbytes(d["q"]) + npages * 4 + nbytes(d["ctx"]) +
+               nbytes(bufs["out"]) + nbytes(bufs["lse_out"]))
+    launches = 1 + len(levels[1]) + 2  # level-0 prefix, one prefix pass per group, pass 1, combine
+    stages.append(Stage("cascade_multilevel",
+                        lambda: skv.cascade_decode_multilevel(
+                            g["q"], g["k_cache"], g["v_cache"], levels, g["block_table"],
+                            g["ctx"], 16, d["sm_scale"], workspace=ws, **bufs),
+                        nbytes_, launches))
 
 
 _PINNED_OUT = {}

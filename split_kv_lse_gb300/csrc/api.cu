@@ -24,13 +24,15 @@ constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
-// The cascade's shared-prefix pass runs on a library-owned stream beside the
-// caller's, forked from and joined back into it with events, so that it
-// overlaps the suffix pass.  One stream and one pair of events per device,
-// created on first use; the fork/join sequence is serialised per device.
+// The cascade's shared-prefix passes run on library-owned streams beside the
+// caller's, forked from and joined back into it with events, so that they
+// overlap the suffix pass and each other (the groups of a level).  kSides
+// streams and their events per device, created on first use; the fork/join
+// sequence is serialised per device.
+constexpr int kSides = 8;
 struct SideStream {
-    cudaStream_t stream = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaStream_t stream[kSides] = {};
+    cudaEvent_t fork = nullptr, join[kSides] = {};
     std::mutex mu;
 };
 SideStream g_side[kMaxDevices];
@@ -292,16 +294,19 @@ static skv_status side_stream(int device, SideStream** out) {
     if (device < 0 || device >= kMaxDevices) return SKV_ERR_CUDA;
     SideStream& s = g_side[device];
     std::lock_guard<std::mutex> lk(s.mu);
-    if (s.stream == nullptr) {
+    if (s.stream[kSides - 1] == nullptr) {
         int lo = 0, hi = 0;
         if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return SKV_ERR_CUDA;
-        cudaStream_t st = nullptr;
-        if (cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, hi) != cudaSuccess)
+        if (s.fork == nullptr && cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess)
             return SKV_ERR_CUDA;
-        if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess)
-            return SKV_ERR_CUDA;
-        s.stream = st;
+        for (int i = 0; i < kSides; ++i) {
+            if (s.stream[i] != nullptr) continue;
+            cudaStream_t st = nullptr;
+            if (cudaEventCreateWithFlags(&s.join[i], cudaEventDisableTiming) != cudaSuccess ||
+                cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, hi) != cudaSuccess)
+                return SKV_ERR_CUDA;
+            s.stream[i] = st;
+        }
     }
     *out = &s;
     return SKV_OK;
@@ -330,12 +335,21 @@ struct LevelPlan {
 skv_status cascade_plan(const CascadeLevels& levels, int32_t Hq, int32_t Hkv, int32_t sm_count,
                         std::vector<LevelPlan>* plan, int* total_slots) {
     plan->assign(levels.size(), LevelPlan());
+    if (sm_count == 0) {  // the current device's
+        const DeviceInfo* dev = nullptr;
+        skv_status st = current_device(&dev);
+        if (st != SKV_OK) return st;
+        sm_count = dev->sm_count;
+    }
     int total = 0;
     for (size_t l = 0; l < levels.size(); ++l) {
         LevelPlan& lp = (*plan)[l];
+        // The groups of a level run side by side: each is sized for its
+        // share of the prefix pass's SMs.
+        const int share = std::max(1, sm_count / std::max(1, (int)levels[l].size()));
         for (const CascadeGroup& g : levels[l]) {
             int mt = 0, bpc = 0, nc = 0;
-            skv_status st = cascade_chunks(g.r1 - g.r0, Hq, Hkv, g.len, sm_count, &mt, &bpc, &nc);
+            skv_status st = cascade_chunks(g.r1 - g.r0, Hq, Hkv, g.len, share, &mt, &bpc, &nc);
             if (st != SKV_OK) return st;
             lp.mt.push_back(mt);
             lp.bpc.push_back(bpc);
@@ -422,15 +436,22 @@ skv_status cascade_run(const void* q, const void* k_cache, const void* v_cache,
     SideStream* side = nullptr;
     if (slots > 0 && (st = side_stream(dev->device, &side)) != SKV_OK) return st;
     std::unique_lock<std::mutex> side_lk;
+    int nsides = 0;  // side streams used by this call
     // 1. Shared prefixes on the tensor cores, one state per prefix chunk, on
     // the side stream: forked after everything the caller queued before this
     // call, joined back before the combine.
     if (slots > 0) {
+        int ngroups = 0;
+        for (size_t l = 0; l < levels.size(); ++l)
+            if (plan[l].slots > 0) ngroups += (int)levels[l].size();
+        nsides = std::min(ngroups, kSides);
         side_lk = std::unique_lock<std::mutex>(side->mu);
-        if (cudaEventRecord(side->fork, cs) != cudaSuccess ||
-            cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
-            return SKV_ERR_CUDA;
+        if (cudaEventRecord(side->fork, cs) != cudaSuccess) return SKV_ERR_CUDA;
+        for (int i = 0; i < nsides; ++i)
+            if (cudaStreamWaitEvent(side->stream[i], side->fork, 0) != cudaSuccess)
+                return SKV_ERR_CUDA;
         const size_t elt = 2;  // fp16 / bf16
+        int launched = 0;  // group launches, spread over the side streams in turn
         for (size_t l = 0; l < levels.size(); ++l) {
             const LevelPlan& lp = plan[l];
             if (lp.slots == 0) continue;
@@ -451,11 +472,13 @@ skv_status cascade_run(const void* q, const void* k_cache, const void* v_cache,
                 const size_t row0 = (size_t)g.r0 * Hq;
                 if (launch_cascade_prefix(ca, *dev, pre_part + row0 * slots * D, pre_lse + row0 * slots,
                                           lp.slots, lp.bpc[gi], lp.mt[gi], slots, lp.offset,
-                                          side->stream) != cudaSuccess)
+                                          side->stream[launched % nsides]) != cudaSuccess)
                     return SKV_ERR_CUDA;
+                ++launched;
             }
         }
-        if (cudaEventRecord(side->join, side->stream) != cudaSuccess) return SKV_ERR_CUDA;
+        for (int i = 0; i < nsides; ++i)
+            if (cudaEventRecord(side->join[i], side->stream[i]) != cudaSuccess) return SKV_ERR_CUDA;
     }
     // 2. Each request's own suffix through the split-KV decode.
     DecodeArgs a;
@@ -480,7 +503,8 @@ skv_status cascade_run(const void* q, const void* k_cache, const void* v_cache,
     if ((use_tc_decode() ? launch_splitkv_decode_tc(a, *dev, cs) : launch_splitkv_decode(a, *dev, cs)) !=
         cudaSuccess)
         return SKV_ERR_CUDA;
-    if (slots > 0 && cudaStreamWaitEvent(cs, side->join, 0) != cudaSuccess) return SKV_ERR_CUDA;
+    for (int i = 0; i < nsides; ++i)
+        if (cudaStreamWaitEvent(cs, side->join[i], 0) != cudaSuccess) return SKV_ERR_CUDA;
     // 3. Prefix chunks of every level -> prefix state; merge_state(prefix,
     // suffix) -> out.
     CombineArgs c = {};
