@@ -17,16 +17,19 @@
 //     4 KB run of its cache, copied by two bulk copies (TMA engine) that two
 //     lanes issue in one instruction, completion counted on the slot's
 //     mbarrier.  The warp refills a slot as soon as it has consumed it.
-//   * QK: lane (g, tg) owns whole dot products -- head g, tokens tg + j*TGN --
-//     over all 128 dims, with q resident in registers, so no cross-lane
-//     reduction.  A lane walks the 16-byte chunks of its rows in an order
-//     rotated by its token (q is held rotated the same way), so the lanes'
-//     reads of different rows fall in different banks.  fp16 x fp16 -> fp32
-//     FMAs (fma.rn.f32.f16): the products are exact, no conversions.
-//   * Online softmax in base 2 ([F2] §② exp2 trick) per head; the lanes of
-//     a head hold its running max, so the rescale factor never crosses lanes.
-//     p goes through shared memory as fp16 to the PV product, where lane
-//     (g, dc) owns head g's dims of 16-byte chunks dc, dc + TGN, ....
+//   * QK: lane (tg, dq) owns tokens tg + j*TG and part dq of the head dim
+//     for all G heads, with q resident in registers; each K row is read
+//     from shared memory once, and the G lanes of a token group sum their
+//     partial dot products by a butterfly reduce-scatter that leaves head
+//     dq's scores on lane dq.  The lanes of a quarter-warp walk their row
+//     parts in rotated orders (q held rotated the same way), so they read
+//     different banks.  fp16 x fp16 -> fp32 FMAs (fma.rn.f32.f16): the
+//     products are exact, no conversions.
+//   * Online softmax in base 2 ([F2] §② exp2 trick) per head, rescaled
+//     lazily (only when a page's max passes the running max by 8); p goes
+//     through shared memory as [token][head] 16-bit values to the PV
+//     product, where lane l owns dims [4l, 4l + 4) of every head, so each V
+//     row is read once.
 //   * CUDA cores only (the pages put tensor cores in the shared-prefix pass).
 #include "common.cuh"
 #include "kernels.h"
@@ -111,18 +114,31 @@ SKV_DEVINL uint16_t to_p(float x) {
     else return __half_as_ushort(__float2half_rn(x));
 }
 
-// Lane roles.  G >= 2: lane = g * TGN + x, x in [0, TGN) -- in QK x = tg (the
-// lane's tokens are tg + j*TGN, j < G/2), in PV x = dc (the lane's V chunks
-// are dc + j*TGN, j < G/2).  G == 1: QK lane = dh*16 + t (token t, dims of
-// K box dh, two lanes per token); PV lane = dims [4*lane, 4*lane + 4).
+// Lane roles.  G >= 2: lane = tg * G + dq.  In QK the lane owns the tokens
+// tg + j*TG (j < TPL) and, for all G heads, the dims of part dq of the head
+// dim (128/G dims: P chunks of 16 bytes), so each K row is read from shared
+// memory once, by the G lanes of its token group; the group's partial dot
+// products are summed by a butterfly reduce-scatter that leaves head dq's
+// scores on lane dq.  In PV the lane owns dims [4*lane, 4*lane + 4) of all G
+// heads, so each V row is read once, by the whole warp.  G == 1: QK lane =
+// dh*16 + t (token t, half dh of the head dim); PV as for G >= 2.
 template <int G> struct Roles {
     static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group size");
-    static constexpr int TGN = G == 1 ? 32 : 32 / G;  // lanes per head
-    static constexpr int TPL = G == 1 ? 1 : G / 2;    // tokens per lane in QK
-    static constexpr int CPL = G == 1 ? 1 : G / 2;    // V chunks per lane in PV
-    static constexpr int DPL = G == 1 ? 4 : 8 * CPL;  // output dims per lane
+    static constexpr int TG = G == 1 ? 16 : 32 / G;  // token groups in QK
+    static constexpr int TPL = G == 1 ? 1 : G / 2;   // tokens per lane in QK
+    static constexpr int P = G == 1 ? 8 : 16 / G;    // 16-byte chunks of the lane's K row part
+    static constexpr int NC = G == 2 ? 4 : (G == 4 ? 2 : 1);  // FMA chains per (token, head)
+    static constexpr int QW = G == 1 ? 32 : 64;      // q registers (16-bit pairs)
 };
 
+// Lazy rescale ([F2] §② exp2 form): the running max moves only when a page's
+// max exceeds it by more than this many log2 units, so p = 2^(x - m) <= 2^8
+// (exact in fp16 and bf16 range) and the accumulators are rescaled rarely.
+constexpr float kLazyRescale = 8.f;
+
+// Registers per lane for the page ids loaded before ctx is known (up to
+// 32 * kSpecRegs table entries per warp).
+constexpr int kSpecRegs = 4;
 
 // The barriers take R words, rounded up to 16 bytes: the p buffer after them
 // is read with 16-byte loads.
@@ -133,7 +149,7 @@ constexpr size_t bars_bytes() {
 
 template <int G, int W, int R>
 constexpr size_t smem_bytes() {
-    return 1024 /* alignment slack */ + (size_t)R * kStageBytes + bars_bytes<R>() +
+    return 128 /* alignment slack */ + (size_t)R * kStageBytes + bars_bytes<R>() +
            (size_t)W * G * kPage * sizeof(uint16_t);
 }
 
@@ -141,16 +157,16 @@ template <int G, int W, int R, bool BF>
 __global__ void __launch_bounds__(W * 32)
 splitkv_decode_kernel(const DecodeParams p) {
     using Ro = Roles<G>;
-    constexpr int TGN = Ro::TGN, TPL = Ro::TPL, CPL = Ro::CPL, DPL = Ro::DPL;
+    constexpr int TG = Ro::TG, TPL = Ro::TPL, P = Ro::P, NC = Ro::NC, QW = Ro::QW;
     constexpr int SPW = R / W;  // ring slots per warp
     static_assert(R % W == 0, "each warp owns R/W slots");
     static_assert(R * kStageBytes >= W * G * (kD + 2) * (int)sizeof(float),
                   "the cross-warp merge buffer reuses the ring");
     extern __shared__ uint8_t smem_raw[];
-    // The swizzled K boxes need 1024-byte alignment.  Offset the shared
-    // pointer itself (an integer round trip would lose the shared address
-    // space and turn every K/V read into a generic load).
-    uint8_t* ring = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    // The ring starts on a 128-byte boundary (bulk copies need 16).  Offset
+    // the shared pointer itself (an integer round trip would lose the shared
+    // address space and turn every K/V read into a generic load).
+    uint8_t* ring = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring + R * kStageBytes);
     uint16_t* ps_all = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(bars) + bars_bytes<R>());
 
@@ -159,6 +175,24 @@ splitkv_decode_kernel(const DecodeParams p) {
 
     // The combine grid may be scheduled now; it waits for this grid to finish.
     pdl_launch_dependents();
+
+    // Page ids are loaded before ctx is known, so that the two loads overlap
+    // instead of following one another.  The split's first page is split *
+    // pps with 1 <= pps <= pps_max (pps_max: a full page table).  When the
+    // entries [split, (split + 1) * pps_max) that any ctx could select are
+    // few, they are all loaded (lane l holds entry split + l + 32 i);
+    // otherwise the ids of a full table's split are, and reloaded if ctx
+    // turns out shorter.
+    const int32_t* bt = p.block_table + (int64_t)b * p.max_pages;
+    const int pps_max = (p.max_pages + p.NS - 1) / p.NS;
+    const int ulo = split, uhi = min((split + 1) * pps_max, p.max_pages);
+    const bool spec_union = uhi - ulo <= 32 * kSpecRegs;
+    int spec[kSpecRegs];
+#pragma unroll
+    for (int i = 0; i < kSpecRegs; ++i) {
+        const int e = spec_union ? ulo + lane + 32 * i : (i == 0 ? split * pps_max + warp + lane * W : -1);
+        spec[i] = (e >= 0 && e < uhi) ? bt[e] : 0;
+    }
 
     int ctx = p.ctx[b];
     const int cap = p.max_pages * kPage;
@@ -181,33 +215,30 @@ splitkv_decode_kernel(const DecodeParams p) {
     }
     __syncthreads();
 
-    // q of this lane's head, all 128 dims, as fp16 pairs (G == 1: the 64
-    // dims of K box dh), pinned in registers for the whole split.
-    const int g_lane = G == 1 ? 0 : lane / TGN;
-    const int x_lane = G == 1 ? lane : lane % TGN;
-    constexpr int QW = G == 1 ? 32 : 64;
-    uint32_t qh[QW];
-    {
-        // Rotated: register chunk i holds q chunk (i + r) mod n, r = the
-        // lane's token (G == 1: within its half of the head dim).
-        const uint16_t* qrow = p.q + ((int64_t)b * p.Hq + hkv * G + g_lane) * kD +
-                             (G == 1 ? 64 * (lane >> 4) : 0);
-        constexpr int nq = QW / 4;
-        const int r = G == 1 ? (lane & 15) : x_lane;
-#pragma unroll
-        for (int i = 0; i < nq; ++i) {
-            const uint4 a = ld_pinned(qrow + 8 * ((i + r) & (nq - 1)));
-            qh[4 * i + 0] = a.x; qh[4 * i + 1] = a.y; qh[4 * i + 2] = a.z; qh[4 * i + 3] = a.w;
-        }
-    }
-
-    const int32_t* bt = p.block_table + (int64_t)b * p.max_pages;
     const uint64_t pol = policy_evict_first();
     uint8_t* my_ring = ring + warp * SPW * kStageBytes;
     uint64_t* my_bars = bars + warp * SPW;
-    // Page ids of this warp's pages k in [kb, kb + 32), one per lane.
+    // Page ids of this warp's pages k in [kb, kb + 32), one per lane: entry
+    // p0 + warp + lane * W of the table row, from the speculative loads when
+    // they hold it.
     int kb = 0;
-    int my_id = (lane < nw) ? bt[p0 + warp + lane * W] : 0;
+    int my_id = 0;
+    {
+        const int e = p0 + warp + lane * W;
+        if (spec_union) {
+            // e lies in [ulo, uhi) for lane < nw (p0 >= split, e < p1).
+            const int off = lane < nw ? e - ulo : 0;
+#pragma unroll
+            for (int i = 0; i < kSpecRegs; ++i) {
+                const int v = __shfl_sync(kFull, spec[i], off & 31);
+                my_id = (off >> 5) == i ? v : my_id;
+            }
+        } else if (p0 == split * pps_max) {
+            my_id = spec[0];
+        } else if (lane < nw) {
+            my_id = bt[e];
+        }
+    }
     auto issue = [&](int k) {  // warp-uniform call; lanes 0 and 1 issue the copies
         if (k - kb >= 32) {
             kb += 32;
@@ -234,12 +265,39 @@ splitkv_decode_kernel(const DecodeParams p) {
 #pragma unroll 1
     for (int k = 0; k < SPW && k < nw; ++k) issue(k);
 
-    float o[DPL];
+    // q pinned in registers for the whole split, as 16-bit pairs, loaded
+    // while the first pages are in flight.  G == 1: the 64 dims of the
+    // lane's half dh, 16-byte chunk i in register chunk (i - r) mod 8, r =
+    // the lane's token.  G >= 2: for each head h the P chunks of part dq,
+    // chunk c of the part in register chunk (c - r) mod P, r the lane's
+    // rotation (below).
+    const int tg = G == 1 ? (lane & 15) : lane / G;
+    const int dq = G == 1 ? (lane >> 4) : lane % G;
+    // Rotation of the lane's walk over its K row part: the 8 lanes of a
+    // quarter-warp then read 8 different 16-byte bank groups.
+    const int rot = G == 1 ? (lane & 7) : (lane / (G / 2)) % P;
+    uint32_t qh[QW];
+    {
+        const uint16_t* qbase = p.q + ((int64_t)b * p.Hq + hkv * G) * kD;
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) o[i] = 0.f;
-    float m_run = -INFINITY;  // running max (log2 units) of this lane's head
-    float l_run = 0.f;        // this lane's share of the running sum
-    uint16_t* ps = ps_all + warp * (G * kPage);  // p[g][token], fp16
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int i = 0; i < P; ++i) {
+                const int c = (i + rot) & (P - 1);
+                const uint4 a = ld_pinned(qbase + h * kD + dq * (kD / (G == 1 ? 2 : G)) + 8 * c);
+                qh[(h * P + i) * 4 + 0] = a.x; qh[(h * P + i) * 4 + 1] = a.y;
+                qh[(h * P + i) * 4 + 2] = a.z; qh[(h * P + i) * 4 + 3] = a.w;
+            }
+    }
+
+    float o[G][4];  // PV: head h, dims [4*lane, 4*lane + 4)
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[h][i] = 0.f;
+    float m_run = -INFINITY;  // running max (log2 units) of the lane's QK head
+    float l_run = 0.f;        // the lane's share of that head's running sum
+    uint16_t* ps = ps_all + warp * (kPage * G);  // p[token][head], 16-bit
 
 #pragma unroll 1
     for (int k = 0; k < nw; ++k) {
@@ -254,21 +312,17 @@ splitkv_decode_kernel(const DecodeParams p) {
             break;
         }
         const int nvalid = min(kPage, ctx - (p0 + warp + k * W) * kPage);  // >= 1
-        const uint8_t* Kb = my_ring + slot * kStageBytes;  // two swizzled boxes
+        const uint8_t* Kb = my_ring + slot * kStageBytes;
         const uint8_t* Vs = Kb + kTileBytes;
 
-        // ---- scores of this lane's tokens (log2 units, masked)
+        // ---- scores of the lane's tokens for its QK head (log2 units, masked)
         float x[TPL];
         if constexpr (G == 1) {
-            const int t = lane & 15, dh = lane >> 4;
-            const uint8_t* rowp = Kb + t * (kD * 2) + dh * 128;
+            const uint8_t* rowp = Kb + tg * (kD * 2) + dq * 128;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                // Step c reads chunk (c + t) & 7 of the lane's half row (q is
-                // held rotated to match), so lanes of different rows read
-                // different banks.
-                const uint4 kv = *reinterpret_cast<const uint4*>(rowp + (((c + t) & 7) << 4));
+                const uint4 kv = *reinterpret_cast<const uint4*>(rowp + (((c + rot) & 7) << 4));
                 acc[c & 3] = dot2_h<BF>(qh[4 * c + 0], kv.x, acc[c & 3]);
                 acc[c & 3] = dot2_h<BF>(qh[4 * c + 1], kv.y, acc[c & 3]);
                 acc[c & 3] = dot2_h<BF>(qh[4 * c + 2], kv.z, acc[c & 3]);
@@ -276,56 +330,79 @@ splitkv_decode_kernel(const DecodeParams p) {
             }
             float sc = (acc[0] + acc[1]) + (acc[2] + acc[3]);
             sc += __shfl_xor_sync(kFull, sc, 16);
-            x[0] = t < nvalid ? sc * p.scale_log2 : -INFINITY;
+            x[0] = tg < nvalid ? sc * p.scale_log2 : -INFINITY;
         } else {
-            // The lane's TPL tokens side by side, and the low and high fp16
-            // halves of each word into separate sums: 8 * TPL independent
-            // FMA chains, each advanced once per 16-byte chunk of K.
-            float acc[TPL][8];
+            // Partial dot products over part dq for every (token j, head h),
+            // NC independent FMA chains each (low and high 16-bit halves,
+            // and for G = 2 even and odd words, apart).
+            float acc[TPL][G][NC];
 #pragma unroll
             for (int j = 0; j < TPL; ++j)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[j][i] = 0.f;
-            // Step c reads chunk (c + t) & 15 of row t: the lanes of a head
-            // read different banks.  The lane's q is held rotated by x_lane,
-            // so token t = x_lane + j * TGN meets q chunk (c + j * TGN) & 15.
+                for (int h = 0; h < G; ++h)
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
+                    for (int c = 0; c < NC; ++c) acc[j][h][c] = 0.f;
+#pragma unroll
+            for (int i = 0; i < P; ++i) {
                 uint4 kv[TPL];
 #pragma unroll
-                for (int j = 0; j < TPL; ++j) {
-                    const int t = x_lane + j * TGN;
-                    kv[j] = *reinterpret_cast<const uint4*>(Kb + t * (kD * 2) + (((c + t) & 15) << 4));
-                }
+                for (int j = 0; j < TPL; ++j)
+                    kv[j] = *reinterpret_cast<const uint4*>(
+                        Kb + (tg + j * TG) * (kD * 2) + ((dq * P + ((i + rot) & (P - 1))) << 4));
 #pragma unroll
                 for (int j = 0; j < TPL; ++j) {
-                    const int qi = 4 * ((c + j * TGN) & 15);
                     const uint32_t kw[4] = {kv[j].x, kv[j].y, kv[j].z, kv[j].w};
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        acc[j][2 * i] = fma_h<BF, false>(qh[qi + i], kw[i], acc[j][2 * i]);
-                        acc[j][2 * i + 1] = fma_h<BF, true>(qh[qi + i], kw[i], acc[j][2 * i + 1]);
-                    }
+                    for (int h = 0; h < G; ++h)
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const uint32_t qw = qh[(h * P + i) * 4 + w];
+                            float& a0 = acc[j][h][(2 * w) % NC];
+                            a0 = fma_h<BF, false>(qw, kw[w], a0);
+                            float& a1 = acc[j][h][(2 * w + 1) % NC];
+                            a1 = fma_h<BF, true>(qw, kw[w], a1);
+                        }
                 }
             }
 #pragma unroll
             for (int j = 0; j < TPL; ++j) {
-                const int t = x_lane + j * TGN;
-                const float sc = ((acc[j][0] + acc[j][1]) + (acc[j][2] + acc[j][3])) +
-                                 ((acc[j][4] + acc[j][5]) + (acc[j][6] + acc[j][7]));
-                x[j] = t < nvalid ? sc * p.scale_log2 : -INFINITY;
+                float cur[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    float s = acc[j][h][0];
+#pragma unroll
+                    for (int c = 1; c < NC; ++c) s += acc[j][h][c];
+                    cur[h] = s;
+                }
+                // Reduce-scatter over the G lanes of the token group: at step
+                // m the lane keeps the half of its heads whose bit m matches
+                // its own and sends the other half to lane ^ m.
+#pragma unroll
+                for (int m = G / 2; m >= 1; m >>= 1) {
+                    const bool up = (dq & m) != 0;
+#pragma unroll
+                    for (int kk = 0; kk < m; ++kk) {
+                        const float send = up ? cur[kk] : cur[kk + m];
+                        const float keep = up ? cur[kk + m] : cur[kk];
+                        cur[kk] = keep + __shfl_xor_sync(kFull, send, m);
+                    }
+                }
+                x[j] = tg + j * TG < nvalid ? cur[0] * p.scale_log2 : -INFINITY;
             }
         }
 
-        // ---- online softmax of this lane's head (its lanes agree on m)
+        // ---- online softmax of the lane's QK head (its lanes agree on m),
+        // lazily rescaled
+        constexpr int MLO = G == 1 ? 1 : G, MHI = G == 1 ? 16 : 32;  // lanes of one head
         float mx = x[0];
 #pragma unroll
         for (int j = 1; j < TPL; ++j) mx = fmaxf(mx, x[j]);
 #pragma unroll
-        for (int mm = 1; mm < (G == 1 ? 16 : TGN); mm <<= 1)
-            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, mm));
-        const float m_new = fmaxf(m_run, mx);  // finite: token 0 of the page is valid
-        const float alpha = exp2f(m_run - m_new);
+        for (int mm = MLO; mm < MHI; mm <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, mm));
+        // mx is finite: token 0 of the page is valid.
+        const bool need = mx > m_run + kLazyRescale;
+        const float m_new = need ? mx : m_run;
+        const float alpha = need ? exp2f(m_run - m_new) : 1.f;
         float psum = 0.f;
 #pragma unroll
         for (int j = 0; j < TPL; ++j) {
@@ -334,44 +411,44 @@ splitkv_decode_kernel(const DecodeParams p) {
             if constexpr (G == 1) {
                 if (lane < 16) ps[lane] = to_p<BF>(pj);
             } else {
-                ps[g_lane * kPage + x_lane + j * TGN] = to_p<BF>(pj);
+                ps[(tg + j * TG) * G + dq] = to_p<BF>(pj);
             }
         }
         l_run = fmaf(l_run, alpha, psum);
         m_run = m_new;
+        if (__any_sync(kFull, need)) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float a = G == 1 ? alpha : __shfl_sync(kFull, alpha, h);  // lane h: head h
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o[h][i] *= a;
+            }
+        }
         __syncwarp();
 
-        // ---- o = alpha * o + p V for this lane's head and dims
-        if (__any_sync(kFull, alpha != 1.f)) {
-#pragma unroll
-            for (int i = 0; i < DPL; ++i) o[i] *= alpha;
-        }
-        const uint4 pa = *reinterpret_cast<const uint4*>(ps + g_lane * kPage);
-        const uint4 pb = *reinterpret_cast<const uint4*>(ps + g_lane * kPage + 8);
-        const uint32_t pw[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+        // ---- o += p V: head h, dims [4*lane, 4*lane + 4)
         auto pv_token = [&](int t) {
-            const uint8_t* vrow = Vs + t * (kD * 2);
+            uint32_t pw[(G + 1) / 2];
             if constexpr (G == 1) {
-                const uint2 vv = *reinterpret_cast<const uint2*>(vrow + 8 * lane);
-                if (t & 1) {
-                    axpy2_h<BF, true>(pw[t >> 1], vv.x, o[0], o[1]);
-                    axpy2_h<BF, true>(pw[t >> 1], vv.y, o[2], o[3]);
-                } else {
-                    axpy2_h<BF, false>(pw[t >> 1], vv.x, o[0], o[1]);
-                    axpy2_h<BF, false>(pw[t >> 1], vv.y, o[2], o[3]);
-                }
+                pw[0] = ps[t];
+            } else if constexpr (G == 2) {
+                pw[0] = *reinterpret_cast<const uint32_t*>(ps + t * G);
+            } else if constexpr (G == 4) {
+                const uint2 a = *reinterpret_cast<const uint2*>(ps + t * G);
+                pw[0] = a.x; pw[1] = a.y;
             } else {
+                const uint4 a = *reinterpret_cast<const uint4*>(ps + t * G);
+                pw[0] = a.x; pw[1] = a.y; pw[2] = a.z; pw[3] = a.w;
+            }
+            const uint2 vv = *reinterpret_cast<const uint2*>(Vs + t * (kD * 2) + 8 * lane);
 #pragma unroll
-                for (int j = 0; j < CPL; ++j) {
-                    const uint4 vv = *reinterpret_cast<const uint4*>(vrow + (x_lane + j * TGN) * 16);
-                    const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        if (t & 1)
-                            axpy2_h<BF, true>(pw[t >> 1], w4[i], o[8 * j + 2 * i], o[8 * j + 2 * i + 1]);
-                        else
-                            axpy2_h<BF, false>(pw[t >> 1], w4[i], o[8 * j + 2 * i], o[8 * j + 2 * i + 1]);
-                    }
+            for (int h = 0; h < G; ++h) {
+                if (h & 1) {
+                    axpy2_h<BF, true>(pw[h >> 1], vv.x, o[h][0], o[h][1]);
+                    axpy2_h<BF, true>(pw[h >> 1], vv.y, o[h][2], o[h][3]);
+                } else {
+                    axpy2_h<BF, false>(pw[h >> 1], vv.x, o[h][0], o[h][1]);
+                    axpy2_h<BF, false>(pw[h >> 1], vv.y, o[h][2], o[h][3]);
                 }
             }
         };
@@ -391,33 +468,22 @@ splitkv_decode_kernel(const DecodeParams p) {
 
     // This warp's per-head totals: l over the lanes of the head.
 #pragma unroll
-    for (int mm = 1; mm < (G == 1 ? 16 : TGN); mm <<= 1) l_run += __shfl_xor_sync(kFull, l_run, mm);
+    for (int mm = (G == 1 ? 1 : G); mm < (G == 1 ? 16 : 32); mm <<= 1)
+        l_run += __shfl_xor_sync(kFull, l_run, mm);
 
     __syncthreads();  // every warp is done with its ring: reuse it
     float* wo = reinterpret_cast<float*>(ring);  // [W][G][kD]
     float* wm = wo + W * G * kD;                 // [W][G]
     float* wl = wm + W * G;                      // [W][G]
-    if constexpr (G == 1) {
-        *reinterpret_cast<float4*>(wo + warp * kD + 4 * lane) = make_float4(o[0], o[1], o[2], o[3]);
-        if (lane == 0) {
-            wm[warp] = m_run;
-            wl[warp] = l_run;
-        }
-    } else {
-        float* dst = wo + (warp * G + g_lane) * kD;
 #pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            float4* d4 = reinterpret_cast<float4*>(dst + 8 * (x_lane + j * TGN));
-            d4[0] = make_float4(o[8 * j + 0], o[8 * j + 1], o[8 * j + 2], o[8 * j + 3]);
-            d4[1] = make_float4(o[8 * j + 4], o[8 * j + 5], o[8 * j + 6], o[8 * j + 7]);
-        }
-        if (x_lane == 0) {
-            wm[warp * G + g_lane] = m_run;
-            wl[warp * G + g_lane] = l_run;
-        }
+    for (int h = 0; h < G; ++h)
+        *reinterpret_cast<float4*>(wo + (warp * G + h) * kD + 4 * lane) =
+            make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+    if (lane < G) {  // lane h holds head h's m and l
+        wm[warp * G + lane] = m_run;
+        wl[warp * G + lane] = l_run;
     }
     __syncthreads();
-
     // Merge the W warp states of each head ([F2] §③ over W states) and write
     // the split state; an empty split ends as o = 0, lse = -inf ([L3] §④).
     for (int idx = threadIdx.x; idx < G * (kD / 4); idx += W * 32) {
@@ -470,7 +536,10 @@ cudaError_t launch_g(const DecodeParams& p, int B, int Hkv, int NS,
     // Measured on the cascade suffixes (<= 8 pages per split, B=64, NS=16):
     // pass 1 takes 53 us with 1 warp and a 2-page ring (about 13 CTAs per
     // SM), 64 us with 2 warps, 72 us with 3; a 4-page ring for the 1-warp
-    // CTA (fewer CTAs per SM) takes 74 us.  Long splits (32 pages) keep 3.
+    // CTA (fewer CTAs per SM) takes 74 us.  On long splits (32 pages, B=1,
+    // NS=64) 3 warps with a 6-page ring, 2 with 6 and 2 with 4 are level
+    // (27.6-28.0 us): the pages in flight per SM, not the warps, set the
+    // pace there; 1 warp with 4 takes 33 us.
     const int pps = (max_pages + NS - 1) / NS;
     if (pps <= 8) return launch_gwr<G, 1, 2, BF>(p, B, Hkv, NS, st);
     if (pps <= 16) return launch_gwr<G, 2, 4, BF>(p, B, Hkv, NS, st);
