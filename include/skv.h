@@ -257,7 +257,11 @@ size_t skv_cascade_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
  * prefix_len = 0 gives an empty prefix state (o = 0, s = -inf); ctx[b] = 0 an
  * empty suffix; both empty give out = 0, lse_out = -inf.
  * workspace: at least skv_cascade_workspace_size(B, Hq, Hkv, D, prefix_len, 0)
- *   bytes, 16-byte aligned; no initial contents are needed.
+ *   bytes, 16-byte aligned; no initial contents are needed.  Calls that
+ *   share a workspace must not overlap on the GPU.
+ * All three steps are queued on `stream`, chained by programmatic dependent
+ * launch: the suffix pass starts while the prefix pass runs (each sized to
+ * share the GPU), and the combine waits for both.
  * Supported: dtype SKV_F16 or SKV_BF16 (the tensor-core products in the
  *   same type), D = 128, page = 16, G = Hq/Hkv in {1, 2, 4, 8},
  *   1 <= num_splits <= 256.  Device-side checks as for skv_splitkv_decode

@@ -24,18 +24,6 @@ constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
-// The cascade's shared-prefix passes run on library-owned streams beside the
-// caller's, forked from and joined back into it with events, so that they
-// overlap the suffix pass and each other (the groups of a level).  kSides
-// streams and their events per device, created on first use; the fork/join
-// sequence is serialised per device.
-constexpr int kSides = 8;
-struct SideStream {
-    cudaStream_t stream[kSides] = {};
-    cudaEvent_t fork = nullptr, join[kSides] = {};
-    std::mutex mu;
-};
-SideStream g_side[kMaxDevices];
 
 // Share of the SMs the prefix pass is sized for (its CTAs hold a whole SM
 // each); the suffix pass fills the rest of the GPU meanwhile.
@@ -289,29 +277,6 @@ static skv_status cascade_chunks(int32_t B, int32_t Hq, int32_t Hkv, int32_t pre
     return SKV_OK;
 }
 
-// The device's side stream (highest priority) and fork/join events.
-static skv_status side_stream(int device, SideStream** out) {
-    if (device < 0 || device >= kMaxDevices) return SKV_ERR_CUDA;
-    SideStream& s = g_side[device];
-    std::lock_guard<std::mutex> lk(s.mu);
-    if (s.stream[kSides - 1] == nullptr) {
-        int lo = 0, hi = 0;
-        if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return SKV_ERR_CUDA;
-        if (s.fork == nullptr && cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess)
-            return SKV_ERR_CUDA;
-        for (int i = 0; i < kSides; ++i) {
-            if (s.stream[i] != nullptr) continue;
-            cudaStream_t st = nullptr;
-            if (cudaEventCreateWithFlags(&s.join[i], cudaEventDisableTiming) != cudaSuccess ||
-                cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, hi) != cudaSuccess)
-                return SKV_ERR_CUDA;
-            s.stream[i] = st;
-        }
-    }
-    *out = &s;
-    return SKV_OK;
-}
-
 }  // extern "C"
 
 namespace {
@@ -362,6 +327,8 @@ skv_status cascade_plan(const CascadeLevels& levels, int32_t Hq, int32_t Hkv, in
     return SKV_OK;
 }
 
+// Workspace: chunk states [rows, slots, D] fp32, their lse [rows, slots],
+// then 256 bytes holding the suffix pass's completion counter.
 size_t cascade_ws_bytes(size_t rows, int slots, int32_t D) {
     return align256(rows * slots * D * 4) + align256(rows * slots * 4) + 256;
 }
@@ -389,7 +356,7 @@ skv_status read_levels(int32_t num_levels, const skv_cascade_level* levels, int3
 
 // The cascade for any number of shared levels ([F2] §⑥ and the multi-level
 // wrapper it names): each group's prefix pass writes its chunk states into
-// its level's slots of every row it covers (on the side stream), the
+// its level's slots of every row it covers (beside the suffix pass), the
 // suffixes run through the split-KV decode, and one combine merges all
 // slots into the prefix state and that with the suffix splits.
 skv_status cascade_run(const void* q, const void* k_cache, const void* v_cache,
@@ -432,30 +399,35 @@ skv_status cascade_run(const void* q, const void* k_cache, const void* v_cache,
     float* pre_part = static_cast<float*>(workspace);
     float* pre_lse =
         reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * slots * D * 4));
+    // Completion counter of the suffix pass (the workspace's last 256 bytes).
+    unsigned int* done_ctr = reinterpret_cast<unsigned int*>(
+        static_cast<char*>(workspace) + align256(rows * slots * D * 4) + align256(rows * slots * 4));
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    SideStream* side = nullptr;
-    if (slots > 0 && (st = side_stream(dev->device, &side)) != SKV_OK) return st;
-    std::unique_lock<std::mutex> side_lk;
-    int nsides = 0;  // side streams used by this call
-    // 1. Shared prefixes on the tensor cores, one state per prefix chunk, on
-    // the side stream: forked after everything the caller queued before this
-    // call, joined back before the combine.
+    // 1. Shared prefixes on the tensor cores, one state per prefix chunk.
+    // Every kernel of the cascade goes into the caller's stream, chained by
+    // programmatic dependent launch: each prefix pass lets the next kernel
+    // start at once, so the prefix passes and the suffix pass run side by
+    // side (a prefix pass takes about a quarter of the SMs), and each
+    // completes only after the kernel before it, so that the combine, which
+    // waits for the suffix pass, sees every prefix state.  The first prefix
+    // pass zeroes the suffix pass's completion counter.
+    // A chained pass that ends before the pass launched ahead of it holds
+    // its SMs until that one completes, so the passes go in order of their
+    // work per CTA (prefix blocks per chunk), shortest first.
+    int launched = 0;
     if (slots > 0) {
-        int ngroups = 0;
-        for (size_t l = 0; l < levels.size(); ++l)
-            if (plan[l].slots > 0) ngroups += (int)levels[l].size();
-        nsides = std::min(ngroups, kSides);
-        side_lk = std::unique_lock<std::mutex>(side->mu);
-        if (cudaEventRecord(side->fork, cs) != cudaSuccess) return SKV_ERR_CUDA;
-        for (int i = 0; i < nsides; ++i)
-            if (cudaStreamWaitEvent(side->stream[i], side->fork, 0) != cudaSuccess)
-                return SKV_ERR_CUDA;
         const size_t elt = 2;  // fp16 / bf16
-        int launched = 0;  // group launches, spread over the side streams in turn
-        for (size_t l = 0; l < levels.size(); ++l) {
+        std::vector<std::pair<int, std::pair<size_t, size_t>>> order;  // (bpc, (level, group))
+        for (size_t l = 0; l < levels.size(); ++l)
+            if (plan[l].slots > 0)
+                for (size_t gi = 0; gi < levels[l].size(); ++gi)
+                    order.push_back({plan[l].bpc[gi], {l, gi}});
+        std::stable_sort(order.begin(), order.end(),
+                         [](const auto& x, const auto& y) { return x.first < y.first; });
+        for (const auto& o : order) {
+            const size_t l = o.second.first, gi = o.second.second;
             const LevelPlan& lp = plan[l];
-            if (lp.slots == 0) continue;
-            for (size_t gi = 0; gi < levels[l].size(); ++gi) {
+            {
                 const CascadeGroup& g = levels[l][gi];
                 CascadeArgs ca;
                 ca.q = static_cast<const char*>(q) + (size_t)g.r0 * Hq * D * elt;
@@ -469,16 +441,16 @@ skv_status cascade_run(const void* q, const void* k_cache, const void* v_cache,
                 ca.Hkv = Hkv;
                 ca.bf16 = dtype == SKV_BF16;
                 ca.sm_scale = sm_scale;
+                ca.zero_ctr = launched == 0 ? done_ctr : nullptr;
+                ca.chained = launched > 0;
                 const size_t row0 = (size_t)g.r0 * Hq;
                 if (launch_cascade_prefix(ca, *dev, pre_part + row0 * slots * D, pre_lse + row0 * slots,
                                           lp.slots, lp.bpc[gi], lp.mt[gi], slots, lp.offset,
-                                          side->stream[launched % nsides]) != cudaSuccess)
+                                          cs) != cudaSuccess)
                     return SKV_ERR_CUDA;
                 ++launched;
             }
         }
-        for (int i = 0; i < nsides; ++i)
-            if (cudaEventRecord(side->join[i], side->stream[i]) != cudaSuccess) return SKV_ERR_CUDA;
     }
     // 2. Each request's own suffix through the split-KV decode.
     DecodeArgs a;
@@ -500,11 +472,10 @@ skv_status cascade_run(const void* q, const void* k_cache, const void* v_cache,
     a.lse_part = lse_part;
     a.ranges_dbg = nullptr;
     a.bf16 = dtype == SKV_BF16;
+    a.done_ctr = launched > 0 ? done_ctr : nullptr;  // chained after the prefix passes
     if ((use_tc_decode() ? launch_splitkv_decode_tc(a, *dev, cs) : launch_splitkv_decode(a, *dev, cs)) !=
         cudaSuccess)
         return SKV_ERR_CUDA;
-    for (int i = 0; i < nsides; ++i)
-        if (cudaStreamWaitEvent(cs, side->join[i], 0) != cudaSuccess) return SKV_ERR_CUDA;
     // 3. Prefix chunks of every level -> prefix state; merge_state(prefix,
     // suffix) -> out.
     CombineArgs c = {};
@@ -521,9 +492,9 @@ skv_status cascade_run(const void* q, const void* k_cache, const void* v_cache,
     c.C = slots;
     c.o_pre = o_pre;
     c.s_pre = s_pre;
-    // Without a prefix the combine follows pass 1 directly (programmatic
-    // dependent launch); after the join it waits for both in stream order.
-    if (launch_combine(c, slots == 0, *dev, cs) != cudaSuccess) return SKV_ERR_CUDA;
+    // The combine follows pass 1 directly (programmatic dependent launch) and
+    // waits for it to complete (hence for the prefix passes too).
+    if (launch_combine(c, true, *dev, cs) != cudaSuccess) return SKV_ERR_CUDA;
     return SKV_OK;
 }
 

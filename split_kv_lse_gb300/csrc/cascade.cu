@@ -74,6 +74,8 @@ struct PrefixParams {
     float* pre_part;          // [B*Hq, chunk_stride, D] split-normalised chunk states
     float* pre_lse;           // [B*Hq, chunk_stride] base 2
     unsigned long long* err;
+    unsigned int* zero_ctr;   // CascadeArgs::zero_ctr or nullptr
+    int32_t chained;          // CascadeArgs::chained
 };
 
 constexpr size_t kSmemQ = 0;                                   // Q_0, Q_1
@@ -122,6 +124,18 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chunk = blockIdx.x, mpair = blockIdx.y, hkv = blockIdx.z;
+    // Chaining in one stream: CTA 0 of a cascade's first prefix pass zeroes
+    // the completion counter of the suffix pass before any dependent kernel
+    // can start; then every CTA lets the next kernel start at once (nothing
+    // launched after this pass reads what it writes before it completes).
+    if (p.zero_ctr != nullptr && chunk == 0 && mpair == 0 && hkv == 0) {
+        if (tid == 0) {
+            *p.zero_ctr = 0u;
+            __threadfence();
+        }
+        __syncthreads();
+    }
+    pdl_launch_dependents();
     const int nblocks_total = (p.prefix_len + kBlockKeys - 1) / kBlockKeys;
     const int blk0 = chunk * p.blocks_per_chunk;
     const int nb = min(p.blocks_per_chunk, nblocks_total - blk0);
@@ -137,6 +151,7 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                 p.pre_lse[((int64_t)req * p.Hq + hkv * p.G + g) * p.chunk_stride + p.chunk_offset +
                           chunk] = -INFINITY;
         }
+        if (p.chained) pdl_wait_primary();  // complete after the previous prefix pass
         return;
     }
 
@@ -441,6 +456,7 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         tc::fence_after_sync();
         tc::tmem_free(tmem, kTmemCols);
     }
+    if (p.chained) pdl_wait_primary();  // complete after the previous prefix pass
 }
 
 }  // namespace
@@ -491,13 +507,24 @@ cudaError_t launch_cascade_prefix(const CascadeArgs& a, const DeviceInfo& dev, f
     p.pre_part = pre_part;
     p.pre_lse = pre_lse;
     p.err = dev.err;
+    p.zero_ctr = a.zero_ctr;
+    p.chained = a.chained ? 1 : 0;
     const size_t smem = prefix_smem_bytes(blocks_per_chunk);
     if (smem > dev.max_smem_optin) return cudaErrorInvalidValue;
     auto kern = a.bf16 ? cascade_prefix_kernel<true> : cascade_prefix_kernel<false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(nchunks, (mtiles + 1) / 2, a.Hkv), kThreads, smem, st>>>(tq, tk, tv, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nchunks, (mtiles + 1) / 2, a.Hkv);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.chained ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p);
 }
 
 }  // namespace skv

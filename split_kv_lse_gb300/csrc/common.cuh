@@ -169,6 +169,21 @@ SKV_DEVINL void pdl_launch_dependents() {
 SKV_DEVINL void pdl_wait_primary() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
+// Completion chaining for a grid launched as a programmatic dependent of
+// the preceding grid in its stream without reading anything that grid
+// writes: every CTA counts itself on *ctr (zeroed before this grid
+// started) at its very end, and the last one to do so waits for the
+// preceding grid to complete, so that this grid completes after it and a
+// kernel that waits for this grid also sees the preceding grid's writes.
+// Every CTA of the grid must call this exactly once; ctr == nullptr: no-op.
+SKV_DEVINL void last_cta_waits_primary(unsigned int* ctr) {
+    if (ctr == nullptr) return;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned total = gridDim.x * gridDim.y * gridDim.z;
+        if (atomicAdd(ctr, 1u) == total - 1u) pdl_wait_primary();
+    }
+}
 
 // ------------------------------------------------------------------ mbarrier / bulk copy
 SKV_DEVINL uint32_t smem_addr(const void* p) {

@@ -54,6 +54,7 @@ struct DecodeParams {
     float* lse_part;
     int32_t* ranges_dbg;
     unsigned long long* err;
+    unsigned int* done_ctr;  // cascade chaining (DecodeArgs::done_ctr) or nullptr
     int32_t num_pool_pages, max_pages, Hq, Hkv, NS;
     float scale_log2;  // sm_scale * log2(e)
 };
@@ -507,6 +508,7 @@ splitkv_decode_kernel(const DecodeParams p) {
             make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
         if (d4 == 0) p.lse_part[row] = L > 0.f ? M + log2f(L) : -INFINITY;
     }
+    last_cta_waits_primary(p.done_ctr);
 }
 
 template <int G, int W, int R, bool BF>
@@ -522,8 +524,17 @@ cudaError_t launch_gwr(const DecodeParams& p, int B, int Hkv, int NS,
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    kern<<<dim3(NS, Hkv, B), W * 32, smem, st>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(NS, Hkv, B);
+    cfg.blockDim = dim3(W * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.done_ctr != nullptr ? 1 : 0;  // chained after a prefix pass
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 // Warps per CTA follow the longest possible split (the page table's width
@@ -803,6 +814,7 @@ cudaError_t launch_splitkv_decode(const DecodeArgs& a, const DeviceInfo& dev, cu
     p.lse_part = a.lse_part;
     p.ranges_dbg = a.ranges_dbg;
     p.err = dev.err;
+    p.done_ctr = a.done_ctr;
     p.num_pool_pages = a.num_pool_pages;
     p.max_pages = a.max_pages;
     p.Hq = a.Hq;

@@ -127,6 +127,7 @@ struct TcParams {
     float* lse_part;
     int32_t* ranges_dbg;
     unsigned long long* err;
+    unsigned int* done_ctr;  // cascade chaining (DecodeArgs::done_ctr) or nullptr
     int32_t num_pool_pages, max_pages, B, Hq, Hkv, NS;
     int32_t units;  // B * Hkv * NS; unit u = ((b * NS) + split) * Hkv + hkv
     float scale_log2;
@@ -543,7 +544,7 @@ splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
         for (int g = 0; g < G; ++g) m[g] = l[g] = 0.f;
         int gcount = 0;
         for (int i = 0;; ++i) {
-            const int s = i % kStages, sb = i & 1, pb = i & 1;
+            const int sb = i & 1, pb = i & 1;
             if (!wait_or_abort(&desc_full[i % kDescs], (uint32_t)((i / kDescs) & 1), abort_flag, p.err, 47))
                 break;
             const TileDesc* d = descs + i % kDescs;
@@ -771,6 +772,7 @@ splitkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tk,
         tc::fence_after_sync();
         tc::tmem_free(tmem, kTmemCols);
     }
+    last_cta_waits_primary(p.done_ctr);
 }
 
 template <int G, bool BF>
@@ -784,8 +786,17 @@ cudaError_t launch_tc_g(const CUtensorMap& tk, const CUtensorMap& tv, const TcPa
         if (e != cudaSuccess) return e;
         attr_set[dev.device] = true;
     }
-    kern<<<grid, kThreads, kSmemBytes, st>>>(tk, tv, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.done_ctr != nullptr ? 1 : 0;  // chained after a prefix pass
+    return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
 }  // namespace
@@ -806,6 +817,7 @@ cudaError_t launch_splitkv_decode_tc(const DecodeArgs& a, const DeviceInfo& dev,
     p.lse_part = a.lse_part;
     p.ranges_dbg = a.ranges_dbg;
     p.err = dev.err;
+    p.done_ctr = a.done_ctr;
     p.num_pool_pages = a.num_pool_pages;
     p.max_pages = a.max_pages;
     p.B = a.B;

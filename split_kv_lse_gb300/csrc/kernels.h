@@ -81,6 +81,12 @@ struct DecodeArgs {
     float* lse_part;
     int32_t* ranges_dbg;
     bool bf16;  // q, K, V are bf16 (else fp16)
+    // Cascade chaining (programmatic dependent launch): when set, the pass
+    // is launched as a dependent of the preceding shared-prefix pass in the
+    // same stream, so that the two run side by side, and the pass's last CTA
+    // (counted on *done_ctr, zeroed by that prefix pass) waits for the
+    // prefix pass to complete, so that the pass completes after it.
+    unsigned int* done_ctr = nullptr;
 };
 cudaError_t launch_splitkv_decode(const DecodeArgs& a, const DeviceInfo& dev, cudaStream_t st);
 // The same pass on the tensor cores (persistent CTAs, packed short splits).
@@ -97,6 +103,13 @@ struct CascadeArgs {
     int32_t B, Hq, Hkv;
     float sm_scale;
     bool bf16;  // q, K, V are bf16 (else fp16)
+    // Chaining in one stream (programmatic dependent launch): every launch
+    // lets the next kernel start at once.  zero_ctr (first launch of a
+    // cascade): CTA 0 zeroes this counter before that.  chained (later
+    // launches): launched as a dependent of the previous prefix pass, and
+    // each CTA waits for that pass to complete before it exits.
+    unsigned int* zero_ctr = nullptr;
+    bool chained = false;
 };
 // Grid of the shared-prefix pass: M tiles of 128 query rows, prefix blocks
 // of 128 keys per chunk, number of chunks.
