@@ -26,8 +26,11 @@ std::mutex g_dev_mu;
 
 
 // Share of the SMs the prefix pass is sized for (its CTAs hold a whole SM
-// each); the suffix pass fills the rest of the GPU meanwhile.
-constexpr int kPrefixSmNum = 1, kPrefixSmDen = 4;
+// each); the suffix pass fills the rest of the GPU meanwhile.  Measured on
+// B=64 requests sharing 8192 tokens with suffixes of 1..2048 (NS=16): 1/5
+// and 1/6 (24 prefix CTAs) 64 us, 1/4 and 1/3 (32) 66-67 us, 1/7 (16) 83 us,
+// where the prefix pass outlasts the suffix pass.
+constexpr int kPrefixSmNum = 1, kPrefixSmDen = 5;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -407,7 +410,7 @@ skv_status cascade_run(const void* q, const void* k_cache, const void* v_cache,
     // Every kernel of the cascade goes into the caller's stream, chained by
     // programmatic dependent launch: each prefix pass lets the next kernel
     // start at once, so the prefix passes and the suffix pass run side by
-    // side (a prefix pass takes about a quarter of the SMs), and each
+    // side (a prefix pass takes about a fifth of the SMs), and each
     // completes only after the kernel before it, so that the combine, which
     // waits for the suffix pass, sees every prefix state.  The first prefix
     // pass zeroes the suffix pass's completion counter.
