@@ -157,10 +157,13 @@ constexpr int kRowWarps = SKV_ROW_WARPS;
 constexpr int kRowBatch = SKV_ROW_BATCH;
 constexpr int kBulkMaxN = 256;
 
-SKV_HOSTDEV_CONST size_t rows_smem_bytes(int row_bytes) {
+// Entries per warp of the compacted state list: N rounded up to a warp.
+SKV_HOSTDEV_CONST int rows_list_len(int N) { return (N + 31) & ~31; }
+
+SKV_HOSTDEV_CONST size_t rows_smem_bytes(int row_bytes, int N) {
     return (size_t)kRowWarps * 2 * kRowBatch * row_bytes +        // double-buffered batches
            (size_t)kRowWarps * 2 * sizeof(uint64_t) +               // one mbarrier per buffer
-           (size_t)kRowWarps * kBulkMaxN * (sizeof(float) + sizeof(int));  // compacted list
+           (size_t)kRowWarps * rows_list_len(N) * (sizeof(float) + sizeof(int));  // compacted list
 }
 
 template <typename T>
@@ -176,8 +179,8 @@ merge_states_bulk_kernel(const T* __restrict__ v, const float* __restrict__ s,
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kRowWarps * 2 * kRowBatch * row_bytes) +
                      warp * 2;
     float* cw = reinterpret_cast<float*>(smem + (size_t)kRowWarps * 2 * kRowBatch * row_bytes +
-                                         (size_t)kRowWarps * 2 * sizeof(uint64_t)) + warp * kBulkMaxN;
-    int* cidx = reinterpret_cast<int*>(cw + (kRowWarps - warp) * kBulkMaxN) + warp * kBulkMaxN;
+                                         (size_t)kRowWarps * 2 * sizeof(uint64_t)) + warp * rows_list_len(N);
+    int* cidx = reinterpret_cast<int*>(cw + (kRowWarps - warp) * rows_list_len(N)) + warp * rows_list_len(N);
 
     const int64_t r = (int64_t)blockIdx.x * kRowWarps + warp;
     if (r >= rows) return;  // whole warp; no block-wide barrier follows
@@ -550,10 +553,14 @@ template <typename T>
 cudaError_t launch_rows(const T* v, const float* s, T* vo, float* so, int64_t rows, int N, int64_t H,
                         int chunks, unsigned blocks, size_t smem, const DeviceInfo& dev,
                         cudaStream_t st) {
+    // The limit is set once per device, to the largest size any call can
+    // ask for (rows of up to 128 fp32 values, up to kBulkMaxN states).
+    constexpr size_t kMaxSmem = rows_smem_bytes(128 * 4, kBulkMaxN);
+    if (smem > kMaxSmem) return cudaErrorInvalidValue;
     static bool attr_set[64] = {};
     if (dev.device >= 0 && dev.device < 64 && !attr_set[dev.device]) {
         cudaError_t e = cudaFuncSetAttribute(merge_states_bulk_kernel<T>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
         if (e != cudaSuccess) return e;
         attr_set[dev.device] = true;
     }
@@ -570,7 +577,7 @@ cudaError_t launch_merge_states(const void* v, const float* s, void* vo, float* 
     const MergeStatesPlan pl = plan_merge_states(rows, N, D, chunks, dev.sm_count, ws ? ws_bytes : 0);
     if (pl.team_kernel) {
         const int row_bytes = chunks * 16;
-        const size_t smem = rows_smem_bytes(row_bytes);
+        const size_t smem = rows_smem_bytes(row_bytes, (int)N);
         const unsigned blocks = (unsigned)((rows + kRowWarps - 1) / kRowWarps);
 #define SKV_ROWS(T_)                                                                           \
     launch_rows<T_>(static_cast<const T_*>(v), s, static_cast<T_*>(vo), so, rows, (int)N, H,   \
