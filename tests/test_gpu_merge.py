@@ -186,3 +186,36 @@ def test_merge_states_two_equals_merge_state(lib):
                               torch.stack([d["s_a"], d["s_b"]], 1).contiguous())
     torch.testing.assert_close(vn, v2, rtol=1e-6, atol=1e-7)
     torch.testing.assert_close(sn, s2, rtol=0, atol=1e-6)
+
+
+_ROW_SIZES_SCRIPT = r"""
+import sys, torch
+sys.path.insert(0, sys.argv[1]); sys.path.insert(0, sys.argv[1] + "/tests")
+import oracle
+from gpu_helpers import assert_states, skv
+from split_kv_lse_gb300 import workloads as W
+lib = skv()
+# Short rows and few states first (a small shared-memory need of the
+# many-rows kernel, 4096 rows), then long rows with more states.
+for (S, N, H, D, dt) in ((128, 2, 32, 64, torch.float16), (128, 32, 32, 128, torch.float32)):
+    d = W.merge_states_inputs(S, N, H, D, dt, seed=N)
+    v, s = lib.merge_states(d["v"].to("cuda:0"), d["s"].to("cuda:0"))
+    torch.cuda.synchronize()
+    vr, sr = oracle.merge_states(d["v"], d["s"])
+    assert_states(v, s, vr, sr, dt)
+print("ok")
+"""
+
+
+def test_merge_states_row_sizes_in_a_fresh_process(lib):
+    """The many-rows N-state kernel takes more shared memory for longer rows
+    and more states: a first call with the smallest need must not cap a
+    later call with the largest (run in a fresh process, where the first
+    call is known)."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _ROW_SIZES_SCRIPT, root], capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
