@@ -238,3 +238,32 @@ def test_cascade_multilevel_full_size(lib):
     levels = [[(0, 64, 8192)], [(8 * i, 8 * i + 8, 512) for i in range(8)]]
     d = W.cascade_multilevel_inputs(64, 32, 8, 128, 16, levels, suffix, seed=45)
     run_multilevel(lib, d, 16, poison=False)
+
+
+def test_cascade_back_to_back_on_a_side_stream_sharing_a_workspace(lib):
+    """The cascade's kernels are chained in the caller's stream (the suffix
+    pass's last CTA waits for the prefix pass, counted on a word of the
+    workspace that the prefix pass zeroes): two calls of different sizes
+    queued back to back on a non-default stream, sharing one workspace, each
+    match the oracle."""
+    cases = [W.cascade_inputs(6, 32, 8, 128, 16, 1000, [40, 1, 300, 0, 17, 129], seed=61),
+             W.cascade_inputs(20, 16, 4, 128, 16, 333, [5 * i + 3 for i in range(20)], seed=62)]
+    need = max(lib.cascade_workspace_size(d["q"].shape[0], d["q"].shape[1], d["k_cache"].shape[1],
+                                          128, d["prefix_len"]) for d in cases)
+    st = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(st):
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=DEV)
+        for d in cases:
+            g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+            outs.append(lib.cascade_decode(g["q"], g["k_cache"], g["v_cache"], g["prefix_pages"],
+                                           d["prefix_len"], g["block_table"], g["ctx"], 4,
+                                           d["sm_scale"], workspace=ws)[:2])
+    st.synchronize()
+    assert lib.get_device_error() == (0, 0)
+    for d, (out, lse) in zip(cases, outs):
+        o_r, s_r, _, _ = oracle.cascade(d["q"], d["k_cache"], d["v_cache"], d["prefix_pages"],
+                                        d["prefix_len"], d["block_table"], d["ctx"], d["sm_scale"])
+        atol, _, rtol_out = DEC_O_TOL[d["q"].dtype]
+        assert_s_close(lse, s_r, DEC_LSE_ATOL, "lse_out")
+        assert_v_close(out, o_r, atol, rtol_out, "out", empty_rows=(s_r == -math.inf))
