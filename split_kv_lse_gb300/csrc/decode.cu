@@ -592,36 +592,36 @@ struct WarpState {
 // lse and computes its weight, the batch max and weight sum go through
 // shuffles, and every lane then accumulates its 4 dims of the batch's v rows
 // with the weights broadcast from their lanes.
-template <int WPR>
+template <int WPR, int BATCH = kCombBatch>
 SKV_DEVINL WarpState warp_merge(const float* o, const float* lse, int N, int D, int64_t row,
                                 int sub) {
-    static_assert(kCombBatch == 16, "two lanes per state in a batch");
+    static_assert(BATCH == 8 || BATCH == 16, "lanes k, k + BATCH, ... read state k of a batch");
     const int lane = threadIdx.x & 31;
     const bool has = 4 * lane < D;
     WarpState st{-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
-    for (int n0 = sub; n0 < N; n0 += WPR * kCombBatch) {
-        const int nk = n0 + (lane & 15) * WPR;
+    for (int n0 = sub; n0 < N; n0 += WPR * BATCH) {
+        const int nk = n0 + (lane & (BATCH - 1)) * WPR;
         const float lk = nk < N ? sanitize_lse(__ldcg(lse + row * N + nk)) : -INFINITY;
-        float4 x[kCombBatch];
+        float4 x[BATCH];
 #pragma unroll
-        for (int k = 0; k < kCombBatch; ++k) {
+        for (int k = 0; k < BATCH; ++k) {
             const int n = n0 + k * WPR;
             x[k] = (n < N && has) ? __ldcg(reinterpret_cast<const float4*>(o + (row * N + n) * D) + lane)
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         float mb = lk;
 #pragma unroll
-        for (int mm = 1; mm < 16; mm <<= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, mm));
+        for (int mm = 1; mm < BATCH; mm <<= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, mm));
         mb = fmaxf(mb, st.m);
         const float wk = merge_weight(lk, mb);
         float ws = wk;
 #pragma unroll
-        for (int mm = 1; mm < 16; mm <<= 1) ws += __shfl_xor_sync(kFull, ws, mm);
+        for (int mm = 1; mm < BATCH; mm <<= 1) ws += __shfl_xor_sync(kFull, ws, mm);
         const float sc = merge_weight(st.m, mb);  // rescale of the running state
         st.W = fmaf(st.W, sc, ws);
         st.acc.x *= sc; st.acc.y *= sc; st.acc.z *= sc; st.acc.w *= sc;
 #pragma unroll
-        for (int k = 0; k < kCombBatch; ++k) {
+        for (int k = 0; k < BATCH; ++k) {
             const float w = __shfl_sync(kFull, wk, k);
             if (w > 0.f) {  // a zero-weight state is not read into the result
                 st.acc.x = fmaf(w, x[k].x, st.acc.x); st.acc.y = fmaf(w, x[k].y, st.acc.y);
@@ -640,10 +640,10 @@ struct CombSmem {
 
 // Merged state of `row` over N states: v (this lane's 4 dims) and s.  With
 // WPR > 1 every thread of the CTA must call this (block barriers).
-template <int WPR>
+template <int WPR, int BATCH = kCombBatch>
 SKV_DEVINL void merge_row(const float* o, const float* lse, int N, int D, int64_t row, int sub,
                           CombSmem& sm, float (&v)[4], float& s_out) {
-    WarpState st = warp_merge<WPR>(o, lse, N, D, row, sub);
+    WarpState st = warp_merge<WPR, BATCH>(o, lse, N, D, row, sub);
     if constexpr (WPR > 1) {
         const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
         __syncthreads();  // the buffers may still be read from a previous merge
@@ -734,12 +734,16 @@ combine_kernel(const CombineParams p) {
     }
 }
 
+// States a warp of the cascade combine requests per L2 round trip: 8 keeps
+// the kernel under 64 registers, so that all of its CTAs are resident at once.
+constexpr int kCascadeBatch = 8;
+
 // Cascade combine with many rows: two warps per row, so that the row's two
 // lists are read at once -- warp 0 merges the suffix's split states, warp 1
 // the prefix chunks' states into the prefix state (written to o_pre/s_pre)
 // -- and they meet in shared memory for the two-state merge, prefix first.
 template <typename Tout>
-__global__ void __launch_bounds__(kCombWarps * 32)
+__global__ void __launch_bounds__(kCombWarps * 32, 8)
 cascade_combine_kernel(const CombineParams p) {
     pdl_wait_primary();  // the states are written by the preceding grids
     __shared__ CombSmem sm;  // unused by merge_row<1>
@@ -753,9 +757,9 @@ cascade_combine_kernel(const CombineParams p) {
     const bool has = 4 * lane < p.D;
     float v[4] = {0.f, 0.f, 0.f, 0.f}, s = -INFINITY;
     if (sub == 0) {
-        merge_row<1>(p.o_part, p.lse_part, p.NS, p.D, row, 0, sm, v, s);
+        merge_row<1, kCascadeBatch>(p.o_part, p.lse_part, p.NS, p.D, row, 0, sm, v, s);
     } else {
-        if (p.C > 0) merge_row<1>(p.pre_part, p.pre_lse, p.C, p.D, row, 0, sm, v, s);
+        if (p.C > 0) merge_row<1, kCascadeBatch>(p.pre_part, p.pre_lse, p.C, p.D, row, 0, sm, v, s);
         if (row_ok) {
             if (p.o_pre != nullptr && has)
                 *reinterpret_cast<float4*>(p.o_pre + row * p.D + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
