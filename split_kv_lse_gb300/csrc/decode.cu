@@ -278,7 +278,7 @@ splitkv_decode_kernel(const DecodeParams p) {
     // quarter-warp then read 8 different 16-byte bank groups.
     const int rot = G == 1 ? (lane & 7) : (lane / (G / 2)) % P;
     uint32_t qh[QW];
-    {
+    if (npages > 0) {  // an empty split reads no q
         const uint16_t* qbase = p.q + ((int64_t)b * p.Hq + hkv * G) * kD;
 #pragma unroll
         for (int h = 0; h < G; ++h)
@@ -472,41 +472,57 @@ splitkv_decode_kernel(const DecodeParams p) {
     for (int mm = (G == 1 ? 1 : G); mm < (G == 1 ? 16 : 32); mm <<= 1)
         l_run += __shfl_xor_sync(kFull, l_run, mm);
 
-    __syncthreads();  // every warp is done with its ring: reuse it
-    float* wo = reinterpret_cast<float*>(ring);  // [W][G][kD]
-    float* wm = wo + W * G * kD;                 // [W][G]
-    float* wl = wm + W * G;                      // [W][G]
+    if constexpr (W == 1) {
+        // One warp: its state is the split's.  Lane h holds head h's m and
+        // l; lane l writes dims [4l, 4l + 4) of every head (an empty split
+        // ends as o = 0, lse = -inf, [L3] §④).
 #pragma unroll
-    for (int h = 0; h < G; ++h)
-        *reinterpret_cast<float4*>(wo + (warp * G + h) * kD + 4 * lane) =
-            make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
-    if (lane < G) {  // lane h holds head h's m and l
-        wm[warp * G + lane] = m_run;
-        wl[warp * G + lane] = l_run;
-    }
-    __syncthreads();
-    // Merge the W warp states of each head ([F2] §③ over W states) and write
-    // the split state; an empty split ends as o = 0, lse = -inf ([L3] §④).
-    for (int idx = threadIdx.x; idx < G * (kD / 4); idx += W * 32) {
-        const int g = idx / (kD / 4), d4 = idx % (kD / 4);
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < W; ++w) M = fmaxf(M, wm[w * G + g]);
-        float L = 0.f;
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int w = 0; w < W; ++w) {
-            const float sc = merge_weight(wm[w * G + g], M);
-            L = fmaf(sc, wl[w * G + g], L);
-            const float4 t4 = *reinterpret_cast<const float4*>(wo + (w * G + g) * kD + 4 * d4);
-            a.x = fmaf(sc, t4.x, a.x); a.y = fmaf(sc, t4.y, a.y);
-            a.z = fmaf(sc, t4.z, a.z); a.w = fmaf(sc, t4.w, a.w);
+        for (int h = 0; h < G; ++h) {
+            const float M = __shfl_sync(kFull, m_run, G == 1 ? 0 : h);
+            const float L = __shfl_sync(kFull, l_run, G == 1 ? 0 : h);
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            const int64_t row = ((int64_t)b * p.Hq + hkv * G + h) * p.NS + split;
+            *reinterpret_cast<float4*>(p.o_part + row * kD + 4 * lane) =
+                make_float4(o[h][0] * inv, o[h][1] * inv, o[h][2] * inv, o[h][3] * inv);
+            if (lane == 0) p.lse_part[row] = L > 0.f ? M + log2f(L) : -INFINITY;
         }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        const int64_t row = ((int64_t)b * p.Hq + hkv * G + g) * p.NS + split;
-        *reinterpret_cast<float4*>(p.o_part + row * kD + 4 * d4) =
-            make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
-        if (d4 == 0) p.lse_part[row] = L > 0.f ? M + log2f(L) : -INFINITY;
+    } else {
+        __syncthreads();  // every warp is done with its ring: reuse it
+        float* wo = reinterpret_cast<float*>(ring);  // [W][G][kD]
+        float* wm = wo + W * G * kD;                 // [W][G]
+        float* wl = wm + W * G;                      // [W][G]
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+            *reinterpret_cast<float4*>(wo + (warp * G + h) * kD + 4 * lane) =
+                make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+        if (lane < G) {  // lane h holds head h's m and l
+            wm[warp * G + lane] = m_run;
+            wl[warp * G + lane] = l_run;
+        }
+        __syncthreads();
+        // Merge the W warp states of each head ([F2] §③ over W states) and write
+        // the split state; an empty split ends as o = 0, lse = -inf ([L3] §④).
+        for (int idx = threadIdx.x; idx < G * (kD / 4); idx += W * 32) {
+            const int g = idx / (kD / 4), d4 = idx % (kD / 4);
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < W; ++w) M = fmaxf(M, wm[w * G + g]);
+            float L = 0.f;
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                const float sc = merge_weight(wm[w * G + g], M);
+                L = fmaf(sc, wl[w * G + g], L);
+                const float4 t4 = *reinterpret_cast<const float4*>(wo + (w * G + g) * kD + 4 * d4);
+                a.x = fmaf(sc, t4.x, a.x); a.y = fmaf(sc, t4.y, a.y);
+                a.z = fmaf(sc, t4.z, a.z); a.w = fmaf(sc, t4.w, a.w);
+            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            const int64_t row = ((int64_t)b * p.Hq + hkv * G + g) * p.NS + split;
+            *reinterpret_cast<float4*>(p.o_part + row * kD + 4 * d4) =
+                make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+            if (d4 == 0) p.lse_part[row] = L > 0.f ? M + log2f(L) : -INFINITY;
+        }
     }
     last_cta_waits_primary(p.done_ctr);
 }
