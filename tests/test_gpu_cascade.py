@@ -267,3 +267,21 @@ def test_cascade_back_to_back_on_a_side_stream_sharing_a_workspace(lib):
         atol, _, rtol_out = DEC_O_TOL[d["q"].dtype]
         assert_s_close(lse, s_r, DEC_LSE_ATOL, "lse_out")
         assert_v_close(out, o_r, atol, rtol_out, "out", empty_rows=(s_r == -math.inf))
+
+
+def test_cascade_bad_prefix_page_id_is_flagged_not_faulted(lib):
+    """A prefix page id outside the pool is replaced by page 0 and reported
+    in the device error word (detail 2 << 20 | the entry); the call
+    completes and the context stays usable."""
+    lib.get_device_error()  # clear
+    d = W.cascade_inputs(4, 16, 4, 128, 16, 300, [20, 1, 0, 77], seed=63)
+    d["prefix_pages"][2] = 10_000_000
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    lib.cascade_decode(g["q"], g["k_cache"], g["v_cache"], g["prefix_pages"], d["prefix_len"],
+                       g["block_table"], g["ctx"], 4, d["sm_scale"])
+    torch.cuda.synchronize()
+    code, detail = lib.get_device_error()
+    assert code == 1 and detail == (2 << 20 | 2)  # SKV_ERR_INVALID_ARG, prefix entry 2
+    assert lib.get_device_error() == (0, 0)
+    # The next call on clean inputs is correct.
+    run_and_check(lib, W.cascade_inputs(4, 16, 4, 128, 16, 300, [20, 1, 0, 77], seed=63), 4)
