@@ -12,7 +12,12 @@
 // GB300 design of pass 1 (not the page's Triton program):
 //   * One CTA per (b, hkv, split) serves all G = Hq/Hkv query heads of that
 //     KV head, so each K/V byte fetched from HBM feeds G heads.
-//   * W warps; warp w owns the split's pages w, w + W, ... and R/W ring slots.
+//   * W warps, each with R/W ring slots.  Warp w takes the split's pages w,
+//     w + W, ...; for splits of 17..64 pages (3 warps) the warps instead
+//     claim the next page from a counter in shared memory whenever a slot
+//     is free, so a warp whose copies land late does not hold the split
+//     back (the fp32 sums are then grouped by arrival order, which can vary
+//     in the last bits from run to run).
 //     A slot holds one (page, kv-head) tile: K and V, each one contiguous
 //     4 KB run of its cache, copied by two bulk copies (TMA engine) that two
 //     lanes issue in one instruction, completion counted on the slot's
@@ -148,13 +153,17 @@ constexpr size_t bars_bytes() {
     return ((size_t)R * sizeof(uint64_t) + 15) / 16 * 16;
 }
 
-template <int G, int W, int R>
+// Page ids of a split held in shared memory when its warps claim pages
+// dynamically (at most kDynMaxPages pages per split), then the claim counter.
+constexpr int kDynMaxPages = 64;
+
+template <int G, int W, int R, bool DYN>
 constexpr size_t smem_bytes() {
     return 128 /* alignment slack */ + (size_t)R * kStageBytes + bars_bytes<R>() +
-           (size_t)W * G * kPage * sizeof(uint16_t);
+           (size_t)W * G * kPage * sizeof(uint16_t) + (DYN ? (kDynMaxPages + 4) * sizeof(int) : 0);
 }
 
-template <int G, int W, int R, bool BF>
+template <int G, int W, int R, bool BF, bool DYN>
 __global__ void __launch_bounds__(W * 32)
 splitkv_decode_kernel(const DecodeParams p) {
     using Ro = Roles<G>;
@@ -170,6 +179,8 @@ splitkv_decode_kernel(const DecodeParams p) {
     uint8_t* ring = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring + R * kStageBytes);
     uint16_t* ps_all = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(bars) + bars_bytes<R>());
+    int* dyn_ids = reinterpret_cast<int*>(ps_all + W * kPage * G);  // DYN: [kDynMaxPages], then the counter
+    int* dyn_next = dyn_ids + kDynMaxPages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
@@ -189,10 +200,17 @@ splitkv_decode_kernel(const DecodeParams p) {
     const int ulo = split, uhi = min((split + 1) * pps_max, p.max_pages);
     const bool spec_union = uhi - ulo <= 32 * kSpecRegs;
     int spec[kSpecRegs];
+    if constexpr (DYN) {
+        // The split's pages are claimed by whichever warp is free: thread t
+        // loads entry t of a full table's split (pps_max <= kDynMaxPages).
+        const int e = split * pps_max + (int)threadIdx.x;
+        spec[0] = ((int)threadIdx.x < pps_max && e < p.max_pages) ? bt[e] : 0;
+    } else {
 #pragma unroll
-    for (int i = 0; i < kSpecRegs; ++i) {
-        const int e = spec_union ? ulo + lane + 32 * i : (i == 0 ? split * pps_max + warp + lane * W : -1);
-        spec[i] = (e >= 0 && e < uhi) ? bt[e] : 0;
+        for (int i = 0; i < kSpecRegs; ++i) {
+            const int e = spec_union ? ulo + lane + 32 * i : (i == 0 ? split * pps_max + warp + lane * W : -1);
+            spec[i] = (e >= 0 && e < uhi) ? bt[e] : 0;
+        }
     }
 
     int ctx = p.ctx[b];
@@ -210,6 +228,12 @@ splitkv_decode_kernel(const DecodeParams p) {
     const int npages = p1 > p0 ? p1 - p0 : 0;
     const int nw = npages > warp ? (npages - warp + W - 1) / W : 0;  // this warp's pages
 
+    if constexpr (DYN) {
+        static_assert(W * 32 >= kDynMaxPages, "one page id per thread");
+        const int t = threadIdx.x;
+        if (t < kDynMaxPages) dyn_ids[t] = t < npages ? (p0 == split * pps_max ? spec[0] : bt[p0 + t]) : 0;
+        if (t == 0) *dyn_next = 0;
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < R; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
@@ -224,7 +248,7 @@ splitkv_decode_kernel(const DecodeParams p) {
     // they hold it.
     int kb = 0;
     int my_id = 0;
-    {
+    if constexpr (!DYN) {
         const int e = p0 + warp + lane * W;
         if (spec_union) {
             // e lies in [ulo, uhi) for lane < nw (p0 >= split, e < p1).
@@ -240,12 +264,31 @@ splitkv_decode_kernel(const DecodeParams p) {
             my_id = bt[e];
         }
     }
-    auto issue = [&](int k) {  // warp-uniform call; lanes 0 and 1 issue the copies
-        if (k - kb >= 32) {
-            kb += 32;
-            my_id = (kb + lane < nw) ? bt[p0 + warp + (kb + lane) * W] : 0;
+    // DYN: page index of each of the warp's ring slots (claimed dynamically).
+    int claimed[SPW];
+#pragma unroll
+    for (int i = 0; i < SPW; ++i) claimed[i] = 0;
+    // Issues the copies of the warp's k-th page into slot k % SPW; with DYN
+    // the page is first claimed from the split's counter, and false is
+    // returned (nothing issued) once every page is taken.
+    auto issue = [&](int k) -> bool {  // warp-uniform call; lanes 0 and 1 issue the copies
+        int pid;
+        if constexpr (DYN) {
+            int j = 0;
+            if (lane == 0) j = atomicAdd(dyn_next, 1);
+            j = __shfl_sync(kFull, j, 0);
+            if (j >= npages) return false;
+#pragma unroll
+            for (int i = 0; i < SPW; ++i)
+                if (i == k % SPW) claimed[i] = j;
+            pid = dyn_ids[j];
+        } else {
+            if (k - kb >= 32) {
+                kb += 32;
+                my_id = (kb + lane < nw) ? bt[p0 + warp + (kb + lane) * W] : 0;
+            }
+            pid = __shfl_sync(kFull, my_id, k - kb);
         }
-        int pid = __shfl_sync(kFull, my_id, k - kb);
         if ((unsigned)pid >= (unsigned)p.num_pool_pages) {
             if (lane == 0) record_error(p.err, SKV_ERR_INVALID_ARG, 1 << 20 | b);
             pid = 0;
@@ -262,9 +305,13 @@ splitkv_decode_kernel(const DecodeParams p) {
         if (lane < 2)
             bulk_g2s(dst + lane * kTileBytes, (lane == 0 ? p.k_cache : p.v_cache) + row * kD,
                      kTileBytes, bar, pol);
+        return true;
     };
+    // Pages of this warp issued so far: static, pages warp, warp + W, ...
+    // (nw of them); DYN, as many as it has claimed.
+    int nseq = 0;
 #pragma unroll 1
-    for (int k = 0; k < SPW && k < nw; ++k) issue(k);
+    while (nseq < SPW && (DYN || nseq < nw) && issue(nseq)) ++nseq;
 
     // q pinned in registers for the whole split, as 16-bit pairs, loaded
     // while the first pages are in flight.  G == 1: the 64 dims of the
@@ -301,18 +348,24 @@ splitkv_decode_kernel(const DecodeParams p) {
     uint16_t* ps = ps_all + warp * (kPage * G);  // p[token][head], 16-bit
 
 #pragma unroll 1
-    for (int k = 0; k < nw; ++k) {
+    for (int k = 0; k < nseq; ++k) {
         const int slot = k % SPW;
         const bool ok = mbar_wait(&my_bars[slot], (uint32_t)((k / SPW) & 1), p.err, 2);
         if (!__all_sync(kFull, ok)) {
             // A bounded wait gave up (error recorded).  Give the copies this
             // warp still has in flight one more bounded wait each before the
             // ring is reused, then stop.
-            for (int kk = k + 1; kk < nw && kk < k + SPW; ++kk)
+            for (int kk = k + 1; kk < nseq; ++kk)
                 mbar_wait(&my_bars[kk % SPW], (uint32_t)((kk / SPW) & 1), p.err, 3);
             break;
         }
-        const int nvalid = min(kPage, ctx - (p0 + warp + k * W) * kPage);  // >= 1
+        int pj = warp + k * W;  // index of the page in the split
+        if constexpr (DYN) {
+#pragma unroll
+            for (int i = 0; i < SPW; ++i)
+                if (i == slot) pj = claimed[i];
+        }
+        const int nvalid = min(kPage, ctx - (p0 + pj) * kPage);  // >= 1
         const uint8_t* Kb = my_ring + slot * kStageBytes;
         const uint8_t* Vs = Kb + kTileBytes;
 
@@ -464,7 +517,7 @@ splitkv_decode_kernel(const DecodeParams p) {
                 if (t < nvalid) pv_token(t);
         }
         __syncwarp();  // slot and p buffer fully read
-        if (k + SPW < nw) issue(k + SPW);
+        if ((DYN || k + SPW < nw) && issue(k + SPW)) ++nseq;  // refills this slot (nseq == k + SPW)
     }
 
     // This warp's per-head totals: l over the lanes of the head.
@@ -527,11 +580,11 @@ splitkv_decode_kernel(const DecodeParams p) {
     last_cta_waits_primary(p.done_ctr);
 }
 
-template <int G, int W, int R, bool BF>
+template <int G, int W, int R, bool BF, bool DYN = false>
 cudaError_t launch_gwr(const DecodeParams& p, int B, int Hkv, int NS,
                        cudaStream_t st) {
-    constexpr size_t smem = smem_bytes<G, W, R>();
-    auto kern = splitkv_decode_kernel<G, W, R, BF>;
+    constexpr size_t smem = smem_bytes<G, W, R, DYN>();
+    auto kern = splitkv_decode_kernel<G, W, R, BF, DYN>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -570,6 +623,10 @@ cudaError_t launch_g(const DecodeParams& p, int B, int Hkv, int NS,
     const int pps = (max_pages + NS - 1) / NS;
     if (pps <= 8) return launch_gwr<G, 1, 2, BF>(p, B, Hkv, NS, st);
     if (pps <= 16) return launch_gwr<G, 2, 4, BF>(p, B, Hkv, NS, st);
+    // Splits of up to kDynMaxPages pages: the warps claim pages one at a
+    // time from the split's counter, so that a warp whose copies land late
+    // does not hold the split back while its neighbours idle.
+    if (pps <= kDynMaxPages) return launch_gwr<G, 3, 6, BF, true>(p, B, Hkv, NS, st);
     return launch_gwr<G, 3, 6, BF>(p, B, Hkv, NS, st);
 }
 
