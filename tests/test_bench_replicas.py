@@ -77,3 +77,29 @@ def test_recorded_traffic_only_for_unchanged_sources(tmp_path):
     stale.write_text(json.dumps({kern: {"sources_sha": "0" * 16, "dram_bytes_per_launch": 123}}))
     assert bench.recorded_traffic(str(stale))[0] is None
     assert bench.recorded_traffic(str(tmp_path / "missing.json"))[0] is None
+
+
+def test_reference_arm_prints_one_complete_json_line():
+    """On rank 0 the reference arm (the fp64 oracle on the host cores) prints
+    exactly one JSON line with the contract's keys, its own cpu_baseline and
+    an e2e entry without host-device copies."""
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 1
+    assert d["value"] > 0 and d["higher_is_better"] is True
+    assert "workload" in d["config"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
