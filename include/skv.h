@@ -218,7 +218,7 @@ skv_status skv_splitkv_decode_plan(int32_t B, const int32_t* ctx_host, int32_t H
  *   G in {1, 2, 4, 8}, 1 <= num_splits <= 256.  B = 0 is a no-op.
  * Device-side checks: a ctx outside [0, max_pages*page] or a page id outside
  *   [0, num_pool_pages) is clamped into range and flagged in the error word.
- * Rounding: when the longest split has 17..64 pages (max_pages / num_splits
+ * Rounding: when the longest split has 9..64 pages (max_pages / num_splits
  *   rounded up), the warps of a split's CTA take its pages in the order
  *   their copies land, so o_part and lse_part may differ between runs in
  *   the last bits (fp32 sums grouped differently); otherwise results are

@@ -13,7 +13,7 @@
 //   * One CTA per (b, hkv, split) serves all G = Hq/Hkv query heads of that
 //     KV head, so each K/V byte fetched from HBM feeds G heads.
 //   * W warps, each with R/W ring slots.  Warp w takes the split's pages w,
-//     w + W, ...; for splits of 17..64 pages (3 warps) the warps instead
+//     w + W, ...; for splits of 9..64 pages (2 or 3 warps) the warps instead
 //     claim the next page from a counter in shared memory whenever a slot
 //     is free, so a warp whose copies land late does not hold the split
 //     back (the fp32 sums are then grouped by arrival order, which can vary
@@ -620,12 +620,13 @@ cudaError_t launch_g(const DecodeParams& p, int B, int Hkv, int NS,
     // NS=64) 3 warps with a 6-page ring, 2 with 6 and 2 with 4 are level
     // (27.6-28.0 us): the pages in flight per SM, not the warps, set the
     // pace there; 1 warp with 4 takes 33 us.
+    // Splits of 9..kDynMaxPages pages: the warps claim pages one at a time
+    // from the split's counter (DYN), so that a warp whose copies land late
+    // does not hold the split back while its neighbours idle (long context,
+    // 32 pages: 30.5-30.9 -> 29.5-29.7 us for the decode).
     const int pps = (max_pages + NS - 1) / NS;
     if (pps <= 8) return launch_gwr<G, 1, 2, BF>(p, B, Hkv, NS, st);
-    if (pps <= 16) return launch_gwr<G, 2, 4, BF>(p, B, Hkv, NS, st);
-    // Splits of up to kDynMaxPages pages: the warps claim pages one at a
-    // time from the split's counter, so that a warp whose copies land late
-    // does not hold the split back while its neighbours idle.
+    if (pps <= 16) return launch_gwr<G, 2, 4, BF, true>(p, B, Hkv, NS, st);
     if (pps <= kDynMaxPages) return launch_gwr<G, 3, 6, BF, true>(p, B, Hkv, NS, st);
     return launch_gwr<G, 3, 6, BF>(p, B, Hkv, NS, st);
 }
