@@ -22,7 +22,7 @@
  *     default stream) and returns as soon as its kernels are enqueued.
  *   - Arguments are checked on the host before anything is launched; a failed
  *     check returns SKV_ERR_INVALID_ARG (bad pointer, size, alignment) or
- *     SKV_ERR_UNSUPPORTED (a valid shape this build has no kernel for) and
+ *     SKV_ERR_UNSUPPORTED (a valid shape this library has no kernel for) and
  *     enqueues nothing.  A launch failure returns SKV_ERR_CUDA.  Errors that
  *     only the device can see (a page id outside the pool, a ctx larger than
  *     the page table, a bounded wait that gave up) are recorded in a per-device
@@ -50,7 +50,7 @@ typedef struct CUstream_st* skv_stream_t;
 typedef enum {
     SKV_OK = 0,
     SKV_ERR_INVALID_ARG = 1, /* a pointer, size or alignment check failed         */
-    SKV_ERR_UNSUPPORTED = 2, /* a valid shape or dtype this build has no kernel for */
+    SKV_ERR_UNSUPPORTED = 2, /* a valid shape or dtype this library has no kernel for */
     SKV_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed         */
     SKV_ERR_TIMEOUT = 4      /* a bounded device wait gave up (device error word)   */
 } skv_status;
