@@ -184,7 +184,8 @@ def nbytes(t):
 STAGE_NAMES = ("merge_state", "merge_state_in_place", "merge_states", "splitkv_decode",
                "cascade_decode")
 # Diagnostic stages, selectable with --only (not part of the default step).
-EXTRA_STAGES = ("splitkv_decode_pass1", "cascade_suffix_pass1", "cascade_multilevel")
+EXTRA_STAGES = ("splitkv_decode_pass1", "cascade_suffix_pass1", "cascade_multilevel",
+                "merge_states_sweep")
 
 
 def build_stages(torch, skv, W, dev, only=None):
@@ -207,6 +208,8 @@ def build_stages(torch, skv, W, dev, only=None):
         _cascade_stage(torch, skv, W, dev, to_dev, stages, hostside, want)
     if "cascade_multilevel" in want:
         _multilevel_stage(torch, skv, W, dev, to_dev, stages)
+    if "merge_states_sweep" in want:
+        _merge_states_sweep_stages(torch, skv, W, dev, to_dev, stages)
     return stages, hostside
 
 
@@ -240,6 +243,24 @@ def _merge_states_stage(torch, skv, W, dev, to_dev, stages, hostside):
     stages.append(Stage("merge_states", lambda: skv.merge_states(g3["v"], g3["s"], None, vo3, so3),
                         mss_bytes, 1))
     hostside["merge_states"] = d3
+
+
+def _merge_states_sweep_stages(torch, skv, W, dev, to_dev, stages):
+    # The large-N sweep: S=16 H=8 D=128 fp32, N in {1, 2, 3, 128, 1024} (few
+    # rows: the two-level path through a zero-filled workspace).
+    for N in (1, 2, 3, 128, 1024):
+        d = W.merge_states_sweep(N)
+        g = to_dev(d)
+        S, _, H, D = d["v"].shape
+        vo = torch.empty(S, H, D, device=dev)
+        so = torch.empty(S, H, device=dev)
+        ws = torch.zeros(max(256, skv.merge_states_workspace_size(S, N, H, D)), dtype=torch.uint8,
+                         device=dev)
+        nonempty = int((d["s"] != -math.inf).sum())
+        nb = nonempty * D * 4 + nbytes(d["s"]) + nbytes(vo) + nbytes(so)
+        stages.append(Stage(f"merge_states_N{N}",
+                            lambda g=g, ws=ws, vo=vo, so=so: skv.merge_states(g["v"], g["s"], ws, vo, so),
+                            nb, 1))
 
 
 def _decode_stage(torch, skv, W, dev, to_dev, stages, hostside, want):
