@@ -10,7 +10,9 @@ split_kv_lse_gb300/workloads.py), inputs resident in HBM:
   splitkv_decode        B=1, ctx=32768, Hq=32, Hkv=8, D=128, page 16, NS=64,
                         pass 1 + PDL-chained combine to fp16
   cascade_decode        B=64, shared 8192-token prefix + 1..2048-token suffixes
-                        (when the library exports it)
+Diagnostic stages (--only, not in the step): splitkv_decode_pass1 and
+cascade_suffix_pass1 (pass 1 alone), cascade_multilevel (three levels) and
+merge_states_sweep (S=16, H=8, N in 1, 2, 3, 128, 1024).
 value = algorithmic HBM bytes of the step / step time (GB/s).  Each stage is
 timed with CUDA events on the launching stream; L2 is flushed (a 512 MB
 write, then a 512 MB read, so it holds clean lines) before every stage,
