@@ -215,3 +215,18 @@ def test_product_path_never_imports_the_oracle():
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert not re.search(r"\bimport\s+oracle\b|\bfrom\s+oracle\b|oracle\.c\b|liboracle",
                                      text), f
+
+
+def test_cascade_prefix_sizing_on_the_cascade_workload(lib):
+    """The shared-prefix pass is sized for about a fifth of the SMs so that it
+    runs beside the suffix pass: for B=64 requests sharing 8192 tokens
+    (Hq=32, Hkv=8) on 152 SMs that is 3 prefix chunks x 8 kv heads = 24 CTAs,
+    i.e. 3 chunk-state slots per row in the workspace ([rows, slots, D] fp32
+    states, [rows, slots] LSEs, then 256 bytes of counters)."""
+    def align256(x):
+        return (x + 255) // 256 * 256
+    rows, D = 64 * 32, 128
+    want = lambda slots: align256(rows * slots * D * 4) + align256(rows * slots * 4) + 256
+    assert lib.skv_cascade_workspace_size(64, 32, 8, D, 8192, 152) == want(3)
+    # No prefix: no slots.
+    assert lib.skv_cascade_workspace_size(64, 32, 8, D, 0, 152) == want(0)
