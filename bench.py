@@ -145,10 +145,6 @@ DOMINANT_STAGE = "cascade_suffix_pass1"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dominant_kernel_traffic.json")
 
 
-def decode_kernel_name():
-    return "tensor_cores" if os.environ.get("SKV_DECODE_TC") == "1" else "cuda_cores"
-
-
 def kernel_sources_sha():
     """Digest of every kernel source: a recorded ncu traffic figure only
     stands while none of them has changed since the capture."""
@@ -171,7 +167,7 @@ def recorded_traffic(path=TRAFFIC_FILE):
             rec = json.load(f)
     except (OSError, ValueError):
         return None, "no recorded capture"
-    entry = rec.get(decode_kernel_name())
+    entry = rec.get("dominant_kernel")
     if not entry:
         return None, "no capture of this kernel"
     if entry.get("sources_sha") != kernel_sources_sha():
@@ -641,7 +637,7 @@ def run_ours(args):
         dk, dms = dom_rep
         traffic, traffic_src = recorded_traffic()
         roofline = {"bound": "hbm",
-                    "kernel": f"splitkv_decode pass 1 ({decode_kernel_name()}) on the cascade "
+                    "kernel": "splitkv_decode pass 1 on the cascade "
                               "suffixes: B=64 Hq=32 Hkv=8 D=128, 1..2048 tokens, NS=16",
                     "achieved": round(dk.bytes / (dms * 1e-3) / 1e9, 1), "peak": None,
                     "unit": "GB/s", "frac": None, "traffic": traffic,

@@ -60,7 +60,7 @@ typedef enum { SKV_F32 = 0, SKV_F16 = 1, SKV_BF16 = 2 } skv_dtype;
 /* Human-readable name of a status code (static string, never NULL). */
 const char* skv_status_string(skv_status status);
 
-/* ABI version of this header; bumped on any signature change. */
+/* ABI version of this header (2); bumped on any signature change. */
 int32_t skv_abi_version(void);
 
 /*
@@ -75,7 +75,10 @@ int32_t skv_abi_version(void);
  * `dtype` (round to nearest even).  The formula is symmetric, so swapping the
  * two inputs gives bit-identical outputs.  Outputs must not overlap inputs
  * (use skv_merge_state_in_place for in-place merging).
- * Limits: S, H >= 0 (S*H == 0 is a no-op), 1 <= D, D*sizeof(dtype) % 16 == 0.
+ * Limits: S, H >= 0 (S*H == 0 is a no-op), 1 <= D, D*sizeof(dtype) % 16 == 0
+ * (else SKV_ERR_INVALID_ARG), and a row of at most 512 bytes, D*sizeof(dtype)
+ * <= 512 (D <= 128 in fp32, D <= 256 in fp16/bf16; a longer row returns
+ * SKV_ERR_UNSUPPORTED).
  */
 skv_status skv_merge_state(const void* v_a, const float* s_a,
                            const void* v_b, const float* s_b,
@@ -122,7 +125,8 @@ size_t skv_merge_states_workspace_size(int64_t S, int64_t N, int64_t H, int64_t 
  *   returns to zero, so one buffer serves consecutive calls on one stream
  *   without re-zeroing (zero it again after a call that did not complete).
  *   Calls that share a workspace must not overlap on the GPU.
- * Limits: S, H >= 0, N >= 1, D as for skv_merge_state.
+ * Limits: S, H >= 0, N >= 1, D as for skv_merge_state (rows of at most 512
+ * bytes).
  */
 skv_status skv_merge_states(const void* v, const float* s,
                             void* v_out, float* s_out,
@@ -149,10 +153,14 @@ skv_status skv_merge_states(const void* v, const float* s,
  * states live in a file-scope device array of
  * SKV_MERGE_STATES_NOALLOC_SCRATCH_BYTES bytes inside the library.
  *   - Sizes whose two-level merge would need more scratch than that are
- *     rejected with SKV_ERR_UNSUPPORTED (nothing is enqueued).  The two-level
- *     path is only taken for at most SM-count rows, with at most about
- *     3 * SM-count partial rows of D fp32 values, so on a GPU with up to 300
- *     SMs (a GB300 has 152) every supported shape fits.
+ *     rejected with SKV_ERR_UNSUPPORTED (nothing is enqueued);
+ *     skv_merge_states_noalloc_scratch_size gives the need in advance.  The
+ *     two-level path is only taken for fewer than 2 * SM-count rows (S*H),
+ *     which it gives about 2 * SM-count CTAs, so at most about 4 * SM-count
+ *     partial rows of D fp32 values (1 KB each at D = 256) plus 12 bytes per
+ *     row.  On a GPU with up to about 250 SMs (a GB300 has 152) every
+ *     supported shape fits; on larger GPUs the few-row, many-state shapes
+ *     with D = 256 can be rejected.
  *   - The first call on a device looks up the array's device address with
  *     cudaGetSymbolAddress (with that device current) and caches it; make that
  *     first call before any stream capture on the device.
@@ -166,6 +174,16 @@ skv_status skv_merge_states_noalloc(const void* v, const float* s,
                                     void* v_out, float* s_out,
                                     int64_t S, int64_t N, int64_t H, int64_t D,
                                     skv_dtype dtype, skv_stream_t stream);
+
+/*
+ * Bytes of the fixed scratch array that skv_merge_states_noalloc would use
+ * for these sizes on a GPU with sm_count SMs (0 = the current device's);
+ * 0 when the call needs none, or for invalid sizes.  A call whose need
+ * exceeds SKV_MERGE_STATES_NOALLOC_SCRATCH_BYTES returns SKV_ERR_UNSUPPORTED.
+ * Host only when sm_count > 0.
+ */
+size_t skv_merge_states_noalloc_scratch_size(int64_t S, int64_t N, int64_t H, int64_t D,
+                                             skv_dtype dtype, int32_t sm_count);
 
 /*
  * Page range of one split ([L3] §②), computed on the host with exactly the
@@ -343,6 +361,38 @@ skv_status skv_cascade_decode_multilevel(const void* q, const void* k_cache, con
  * an index that identifies it (0 if none).  Synchronises the device.
  */
 skv_status skv_get_device_error(int32_t* code, int32_t* detail);
+
+/*
+ * As skv_get_device_error, but waits only for the work queued on `stream`
+ * (NULL: the legacy default stream, which waits for every blocking stream):
+ * the word then holds every error of that work.  Kernels still running on
+ * other streams may record an error later, which the next poll reports.
+ * The first error since the word was last cleared wins; later ones are not
+ * kept.
+ */
+skv_status skv_poll_device_error(int32_t* code, int32_t* detail, skv_stream_t stream);
+
+/*
+ * Self-test of the bounded device waits (the pages have no counterpart: it
+ * checks this library's failure reporting without any fault).  Every
+ * shared-memory barrier wait in the library's kernels gives up after a
+ * limit (2 s), records SKV_ERR_TIMEOUT in the error word and returns, so a
+ * lost copy can neither hang the GPU nor pass silently.  This call launches
+ * one small kernel on `stream` that runs those same wait routines, with a
+ * limit of limit_ns nanoseconds, on barriers that nothing ever completes (no
+ * copy is issued, so nothing is left in flight):
+ *   mode 0: the wait of the decode and merge kernels gives up and records
+ *           SKV_ERR_TIMEOUT with detail 100;
+ *   mode 1: the abort-aware wait of the warp-specialised kernels: one warp's
+ *           limit runs out (SKV_ERR_TIMEOUT, detail 101) and raises the
+ *           block's abort flag; a second warp, waiting on another barrier
+ *           with a limit 100 times longer, sees the flag and returns without
+ *           recording anything.
+ * The kernel then returns normally and the context stays usable; read the
+ * outcome with skv_get_device_error or skv_poll_device_error.
+ * Limits: mode 0 or 1; 1000 <= limit_ns <= 10000000 (else SKV_ERR_INVALID_ARG).
+ */
+skv_status skv_selftest_bounded_wait(int32_t mode, int64_t limit_ns, skv_stream_t stream);
 
 #ifdef __cplusplus
 }

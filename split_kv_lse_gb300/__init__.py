@@ -23,7 +23,7 @@ __all__ = [
     "SkvError", "merge_state", "merge_state_in_place", "merge_states",
     "merge_states_workspace_size", "split_page_range", "splitkv_decode_plan",
     "splitkv_decode", "cascade_workspace_size", "cascade_decode", "get_device_error",
-    "abi_version", "library_path",
+    "poll_device_error", "selftest_bounded_wait", "abi_version", "library_path",
 ]
 
 _DT = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
@@ -320,3 +320,23 @@ def get_device_error():
     _ffi.check("skv_get_device_error", _ffi.lib().skv_get_device_error(
         ctypes.byref(code), ctypes.byref(detail)))
     return code.value, detail.value
+
+
+def poll_device_error(stream=None):
+    """As get_device_error, waiting only for the work queued on `stream`
+    (default: the current stream)."""
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    code, detail = ctypes.c_int32(), ctypes.c_int32()
+    _ffi.check("skv_poll_device_error", _ffi.lib().skv_poll_device_error(
+        ctypes.byref(code), ctypes.byref(detail), stream.cuda_stream))
+    return code.value, detail.value
+
+
+def selftest_bounded_wait(mode: int, limit_ns: int, stream=None):
+    """Runs the library's bounded barrier waits on barriers nothing completes
+    (see skv_selftest_bounded_wait); the outcome is read from the error word."""
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    _ffi.check("skv_selftest_bounded_wait", _ffi.lib().skv_selftest_bounded_wait(
+        int(mode), int(limit_ns), stream.cuda_stream))

@@ -53,7 +53,10 @@ SIGNATURES = {
                                             c_void_p, i32, c_void_p, i32, i32, i32, i32, i32, i32,
                                             f32, i32, c_void_p, c_void_p, c_void_p, c_void_p,
                                             c_void_p, c_void_p, c_void_p, size_t, c_void_p]),
+    "skv_merge_states_noalloc_scratch_size": (size_t, [i64, i64, i64, i64, i32, i32]),
     "skv_get_device_error": (i32, [c_int32_p, c_int32_p]),
+    "skv_poll_device_error": (i32, [c_int32_p, c_int32_p, c_void_p]),
+    "skv_selftest_bounded_wait": (i32, [i32, i64, c_void_p]),
 }
 
 

@@ -47,16 +47,10 @@ def _stale(target: str, sources: list[str]) -> bool:
     return any(os.path.getmtime(s) > t for s in sources)
 
 
-def _extra_flags() -> list[str]:
-    """Extra nvcc flags from SKV_NVCC_EXTRA (whitespace separated), e.g. a -D
-    selecting a kernel variant; empty by default."""
-    return os.environ.get("SKV_NVCC_EXTRA", "").split()
-
-
 def _compile(src: str) -> tuple[str, str]:
     obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
     if _stale(obj, [src] + _deps()):
-        cmd = [nvcc(), *NVCC_FLAGS, *_extra_flags(), "-c", src, "-o", obj + ".tmp"]
+        cmd = [nvcc(), *NVCC_FLAGS, "-c", src, "-o", obj + ".tmp"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")

@@ -12,7 +12,6 @@
 
 #include "common.cuh"
 #include "kernels.h"
-#include <stdlib.h>
 #include "split_range.h"
 
 namespace skv {
@@ -88,7 +87,7 @@ const char* skv_status_string(skv_status status) {
     return "SKV_UNKNOWN_STATUS";
 }
 
-int32_t skv_abi_version(void) { return 1; }
+int32_t skv_abi_version(void) { return 2; }
 
 skv_status skv_merge_state(const void* v_a, const float* s_a, const void* v_b, const float* s_b,
                            void* v_out, float* s_out, int64_t S, int64_t H, int64_t D,
@@ -189,13 +188,6 @@ skv_status skv_splitkv_decode_plan(int32_t B, const int32_t* ctx_host, int32_t H
     return SKV_OK;
 }
 
-// Pass 1 runs on CUDA cores unless SKV_DECODE_TC=1 selects the tensor-core
-// kernel (decode_tc.cu), which is still being tuned for these shapes.
-static bool use_tc_decode() {
-    const char* v = getenv("SKV_DECODE_TC");
-    return v != nullptr && v[0] == '1';
-}
-
 skv_status skv_splitkv_decode(const void* q, const void* k_cache, const void* v_cache,
                               int32_t num_pool_pages, const int32_t* block_table,
                               int32_t max_pages, const int32_t* ctx, int32_t B, int32_t Hq,
@@ -245,8 +237,7 @@ skv_status skv_splitkv_decode(const void* q, const void* k_cache, const void* v_
     a.lse_part = lse_part;
     a.ranges_dbg = ranges_dbg;
     a.bf16 = dtype == SKV_BF16;
-    cudaError_t e = use_tc_decode() ? launch_splitkv_decode_tc(a, *dev, cs)
-                                    : launch_splitkv_decode(a, *dev, cs);
+    cudaError_t e = launch_splitkv_decode(a, *dev, cs);
     if (e != cudaSuccess) return SKV_ERR_CUDA;
     if (out != nullptr) {
         CombineArgs c = {};
@@ -476,9 +467,7 @@ skv_status cascade_run(const void* q, const void* k_cache, const void* v_cache,
     a.ranges_dbg = nullptr;
     a.bf16 = dtype == SKV_BF16;
     a.done_ctr = launched > 0 ? done_ctr : nullptr;  // chained after the prefix passes
-    if ((use_tc_decode() ? launch_splitkv_decode_tc(a, *dev, cs) : launch_splitkv_decode(a, *dev, cs)) !=
-        cudaSuccess)
-        return SKV_ERR_CUDA;
+    if (launch_splitkv_decode(a, *dev, cs) != cudaSuccess) return SKV_ERR_CUDA;
     // 3. Prefix chunks of every level -> prefix state; merge_state(prefix,
     // suffix) -> out.
     CombineArgs c = {};
@@ -579,6 +568,29 @@ skv_status skv_get_device_error(int32_t* code, int32_t* detail) {
         return SKV_ERR_CUDA;
     if (cudaMemcpy(dev->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
         return SKV_ERR_CUDA;
+    *code = (int32_t)(w & 0xffu);
+    *detail = (int32_t)(w >> 8);
+    return SKV_OK;
+}
+
+skv_status skv_poll_device_error(int32_t* code, int32_t* detail, skv_stream_t stream) {
+    if (!code || !detail) return SKV_ERR_INVALID_ARG;
+    const DeviceInfo* dev = nullptr;
+    skv_status st = current_device(&dev);
+    if (st != SKV_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    // The copy to pageable host memory returns once it has run, i.e. after
+    // the work queued on `stream` before it.  A non-zero word is never
+    // overwritten (the first error wins), so clearing it after reading it
+    // loses nothing.
+    unsigned long long w = 0;
+    if (cudaMemcpyAsync(&w, dev->err, sizeof(w), cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        return SKV_ERR_CUDA;
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return SKV_ERR_CUDA;
+    if (w != 0) {
+        if (cudaMemsetAsync(dev->err, 0, sizeof(w), cs) != cudaSuccess) return SKV_ERR_CUDA;
+        if (cudaStreamSynchronize(cs) != cudaSuccess) return SKV_ERR_CUDA;
+    }
     *code = (int32_t)(w & 0xffu);
     *detail = (int32_t)(w >> 8);
     return SKV_OK;

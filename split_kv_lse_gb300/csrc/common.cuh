@@ -229,31 +229,26 @@ SKV_DEVINL uint64_t globaltimer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// Bounded wait: gives up after `limit_ns` of wall time, records
-// SKV_ERR_TIMEOUT with `where` as detail and returns false.
+// Bounded wait: gives up after `limit_ns` of wall time (%globaltimer),
+// records SKV_ERR_TIMEOUT with `where` as detail and returns false.  The
+// kernels use kWaitLimitNs; skv_selftest_bounded_wait passes a short limit.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
-                                                    unsigned long long* err, int where) {
+                                                    unsigned long long* err, int where,
+                                                    uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             record_error(err, SKV_ERR_TIMEOUT, where);
             return false;
         }
     }
 }
-SKV_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned long long* err, int where) {
+SKV_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned long long* err, int where,
+                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_slow(bar, parity, err, where);
-}
-// Bounded wait that records nothing: used after an abort, to let copies
-// still in flight land before the CTA ends.
-SKV_DEVINL bool mbar_wait_quiet(uint64_t* bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-    return true;
+    return mbar_wait_slow(bar, parity, err, where, limit_ns);
 }
 // Bounded wait that also gives up as soon as another role of the CTA has
 // raised the shared abort flag; a wait that runs out raises it.  The first
@@ -262,12 +257,13 @@ SKV_DEVINL bool mbar_wait_quiet(uint64_t* bar, uint32_t parity) {
 // and share the instruction cache).
 static __device__ __noinline__ bool wait_or_abort_slow(uint64_t* bar, uint32_t parity,
                                                  volatile int* abort_flag,
-                                                 unsigned long long* err, int where) {
+                                                 unsigned long long* err, int where,
+                                                 uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             record_error(err, SKV_ERR_TIMEOUT, where);
             *abort_flag = 1;
             return false;
@@ -275,9 +271,10 @@ static __device__ __noinline__ bool wait_or_abort_slow(uint64_t* bar, uint32_t p
     }
 }
 SKV_DEVINL bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                              unsigned long long* err, int where) {
+                              unsigned long long* err, int where,
+                              uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
-    return wait_or_abort_slow(bar, parity, abort_flag, err, where);
+    return wait_or_abort_slow(bar, parity, abort_flag, err, where, limit_ns);
 }
 // 16-byte asynchronous global -> shared copy (cp.async, bypassing L1), and
 // an arrive on `bar` once every cp.async of this thread so far has landed

@@ -89,8 +89,6 @@ struct DecodeArgs {
     unsigned int* done_ctr = nullptr;
 };
 cudaError_t launch_splitkv_decode(const DecodeArgs& a, const DeviceInfo& dev, cudaStream_t st);
-// The same pass on the tensor cores (persistent CTAs, packed short splits).
-cudaError_t launch_splitkv_decode_tc(const DecodeArgs& a, const DeviceInfo& dev, cudaStream_t st);
 
 // ---------------------------------------------------------------- cascade
 struct CascadeArgs {

@@ -147,16 +147,10 @@ merge_state_kernel(const T* va, const float* sa, const T* __restrict__ vb,
 // kRowBatch rows: a batch is kRowBatch TMA bulk copies issued by kRowBatch
 // lanes at once and completed on one mbarrier, so the ring bookkeeping is
 // paid once per batch, not once per state.
-#ifndef SKV_ROW_WARPS
-#define SKV_ROW_WARPS 4
-#endif
-#ifndef SKV_ROW_BATCH
+constexpr int kRowWarps = 4;
 // Rows per batch, measured on S=256 N=64 H=32 D=128 fp32 (us, 30 steps, L2
 // flushed): 3: 49.5, 4: 45.8-46.3, 5: 45.0, 6: 44.5-44.8, 7: 45.0, 8: 46.3.
-#define SKV_ROW_BATCH 6
-#endif
-constexpr int kRowWarps = SKV_ROW_WARPS;
-constexpr int kRowBatch = SKV_ROW_BATCH;
+constexpr int kRowBatch = 6;
 constexpr int kBulkMaxN = 256;
 
 // Entries per warp of the compacted state list: N rounded up to a warp.

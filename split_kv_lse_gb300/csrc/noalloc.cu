@@ -48,6 +48,21 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 
 using namespace skv;
 
+extern "C" size_t skv_merge_states_noalloc_scratch_size(int64_t S, int64_t N, int64_t H,
+                                                        int64_t D, skv_dtype dtype,
+                                                        int32_t sm_count) {
+    if (S <= 0 || H <= 0 || N < 1 || D < 1 || sm_count < 0) return 0;
+    if (!(dtype == SKV_F32 || dtype == SKV_F16 || dtype == SKV_BF16)) return 0;
+    const int64_t row_bytes = D * (int64_t)dtype_size(dtype);
+    if (row_bytes % 16 != 0 || row_bytes > 512) return 0;
+    if (sm_count == 0) {
+        const DeviceInfo* dev = nullptr;
+        if (current_device(&dev) != SKV_OK) return 0;
+        sm_count = dev->sm_count;
+    }
+    return plan_merge_states(S * H, N, D, (int)(row_bytes / 16), sm_count, SIZE_MAX).ws_bytes;
+}
+
 extern "C" skv_status skv_merge_states_noalloc(const void* v, const float* s, void* v_out,
                                                float* s_out, int64_t S, int64_t N, int64_t H,
                                                int64_t D, skv_dtype dtype, skv_stream_t stream) {

@@ -81,17 +81,3 @@ def assert_states(v_gpu, s_gpu, v_ref, s_ref, dtype):
     r = np.asarray(s_ref)
     assert_s_close(s_gpu, r, S_ATOL)
     assert_v_close(v_gpu, v_ref, atol, rtol, empty_rows=(r == -math.inf))
-
-
-# Pass 1 of the split-KV decode has two kernels: CUDA cores (the default) and
-# tcgen05 tensor cores (selected by SKV_DECODE_TC=1, read at every call).
-DECODE_KERNELS = ("cuda_cores", "tensor_cores")
-
-
-def select_decode_kernel(which):
-    """Set the environment so that the next decode calls use `which`."""
-    import os
-    if which == "tensor_cores":
-        os.environ["SKV_DECODE_TC"] = "1"
-    else:
-        os.environ.pop("SKV_DECODE_TC", None)

@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.skv_abi_version() == 1
+    assert lib.skv_abi_version() == 2
     for code, name in ((0, b"SKV_OK"), (1, b"SKV_ERR_INVALID_ARG"), (2, b"SKV_ERR_UNSUPPORTED"),
                        (3, b"SKV_ERR_CUDA"), (4, b"SKV_ERR_TIMEOUT")):
         assert lib.skv_status_string(code) == name
@@ -160,6 +160,11 @@ def test_device_entry_points_reject_bad_arguments_before_any_cuda_call(lib):
     assert d(lo=fake) == 1        # lse_out without out
     code = ctypes.c_int32()
     assert lib.skv_get_device_error(None, ctypes.byref(code)) == 1
+    assert lib.skv_poll_device_error(None, ctypes.byref(code), None) == 1
+    st = lib.skv_selftest_bounded_wait
+    assert st(2, 1_000_000, None) == 1           # unknown mode
+    assert st(0, 999, None) == 1                 # limit below 1 us
+    assert st(1, 10_000_001, None) == 1          # limit above 10 ms
 
 
 def test_merge_states_workspace_size(lib):
@@ -230,3 +235,25 @@ def test_cascade_prefix_sizing_on_the_cascade_workload(lib):
     assert lib.skv_cascade_workspace_size(64, 32, 8, D, 8192, 152) == want(3)
     # No prefix: no slots.
     assert lib.skv_cascade_workspace_size(64, 32, 8, D, 0, 152) == want(0)
+
+
+def test_noalloc_scratch_fits_every_shape_on_gb300(lib):
+    """skv_merge_states_noalloc keeps its two-level partials in a fixed 1 MiB
+    array.  The heaviest shape is fp16 D=256 (1 KB fp32 partial rows) with
+    S*H = 2*SM - 1 rows, just below the count at which every row gets one CTA:
+    on a GB300 (152 SMs) it needs about 612 KB, which fits, and a few-row
+    shape needs less.  On a GPU with 300 SMs the same kind of shape no longer
+    fits, so there the call returns SKV_ERR_UNSUPPORTED."""
+    cap = 1 << 20
+    f = lib.skv_merge_states_noalloc_scratch_size
+    F16 = 1
+    sm = 152
+    worst = max(f(rows, 1024, 1, 256, F16, sm) for rows in range(1, 2 * sm + 1))
+    assert worst == f(2 * sm - 1, 1024, 1, 256, F16, sm)
+    assert 600_000 < worst < cap
+    assert f(2 * sm, 1024, 1, 256, F16, sm) == 0      # one CTA per row: no scratch
+    assert f(16, 1024, 8, 128, 0, sm) > 0             # the large-N sweep shape (fp32, D=128)
+    assert f(8, 1, 4, 128, 0, sm) == 0                # N = 1: one CTA per row
+    big = 300
+    assert f(2 * big - 1, 1024, 1, 256, F16, big) > cap
+    assert f(0, 4, 4, 64, 0, sm) == 0 and f(4, 4, 4, 3, 0, sm) == 0   # invalid sizes

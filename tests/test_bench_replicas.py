@@ -68,7 +68,7 @@ def test_recorded_traffic_only_for_unchanged_sources(tmp_path):
     """The roofline's DRAM traffic comes from a committed ncu capture and is
     reported only while the kernel sources are those that were captured."""
     import bench
-    kern = bench.decode_kernel_name()
+    kern = "dominant_kernel"
     good = tmp_path / "good.json"
     good.write_text(json.dumps({kern: {"sources_sha": bench.kernel_sources_sha(),
                                        "dram_bytes_per_launch": 123, "profile": "p.md"}}))

@@ -12,20 +12,12 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import (DECODE_KERNELS, select_decode_kernel, DEC_LSE_ATOL, DEC_O_TOL, assert_s_close, assert_v_close,
+from gpu_helpers import (DEC_LSE_ATOL, DEC_O_TOL, assert_s_close, assert_v_close,
                          require_gpu, skv)
 from split_kv_lse_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
-
-
-@pytest.fixture(params=DECODE_KERNELS, autouse=True)
-def decode_kernel(request):
-    """Every test runs once per pass-1 kernel."""
-    select_decode_kernel(request.param)
-    yield request.param
-    select_decode_kernel("cuda_cores")
 
 
 @pytest.fixture(scope="module")

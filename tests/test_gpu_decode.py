@@ -11,20 +11,12 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import (DECODE_KERNELS, select_decode_kernel, DEC_LSE_ATOL, DEC_O_TOL, assert_s_close, assert_v_close, np64,
+from gpu_helpers import (DEC_LSE_ATOL, DEC_O_TOL, assert_s_close, assert_v_close, np64,
                          require_gpu, skv)
 from split_kv_lse_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
-
-
-@pytest.fixture(params=DECODE_KERNELS, autouse=True)
-def decode_kernel(request):
-    """Every test runs once per pass-1 kernel."""
-    select_decode_kernel(request.param)
-    yield request.param
-    select_decode_kernel("cuda_cores")
 
 
 @pytest.fixture(scope="module")
@@ -186,3 +178,49 @@ def test_decode_bf16_long_context(lib):
     """The long-context workload (B=1, ctx=32768, Hq=32, Hkv=8, NS=64) in bf16."""
     d = W.decode_inputs(1, 32, 8, 128, 16, [32768], seed=0, dtype=torch.bfloat16)
     check_decode(lib, d, 64)
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("ns", [1, 2])
+def test_decode_long_splits(lib, G, ns):
+    """Splits of more than 64 pages (the CTA shape whose warps take fixed
+    pages w, w+3, ...): the unsplit decode ([L3] §⑥, no split) and a two-way
+    split.  ctx 4096 is 256 pages: unsplit, each of the 3 warps owns about 86
+    pages, so its page ids are reloaded past 32 and 64; ctx 2500 and 1100
+    (157 and 69 pages) end on partial pages whose tails hold NaN, as does
+    every pool page no sequence uses."""
+    ctx = [4096, 2500, 1100]
+    Hkv = 2
+    d = W.decode_inputs(len(ctx), Hkv * G, Hkv, 128, 16, ctx, seed=300 + 10 * G + ns,
+                        pool_extra=3)
+    check_decode(lib, d, ns, nan_tail=True)
+
+
+def test_decode_plan_unsplit_batch(lib):
+    """The plan chooses no split when B*Hkv already fills the GPU ([L3] §⑥):
+    B=64, Hkv=8 (512 programs) with 1100..1900-token contexts on this GPU's
+    SMs gives NS=1 (the oracle's plan agrees), and the unsplit decode of that
+    batch (69..119 pages per split) matches the oracle."""
+    rng = np.random.default_rng(13)
+    ctx = [int(c) for c in rng.integers(1100, 1901, size=64)]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ns = lib.splitkv_decode_plan(ctx, 8, 16, 0)
+    assert ns == oracle.plan(ctx, 8, 16, sms)
+    assert ns == 1 or 64 * 8 < 3 * sms
+    d = W.decode_inputs(len(ctx), 32, 8, 128, 16, ctx, seed=13)
+    check_decode(lib, d, ns, nan_tail=True)
+
+
+@pytest.mark.parametrize("mode,detail", [(0, 100), (1, 101)])
+def test_bounded_wait_gives_up_and_reports(lib, mode, detail):
+    """A barrier wait that nothing completes gives up after its limit (1 ms
+    here), records SKV_ERR_TIMEOUT with the wait's detail code and returns:
+    the kernel completes, the error is read on the host, and the GPU goes on
+    working (a decode right after is exact)."""
+    lib.get_device_error()  # clear
+    lib.selftest_bounded_wait(mode, 1_000_000)
+    assert lib.poll_device_error() == (4, detail)
+    assert lib.poll_device_error() == (0, 0)
+    d = W.decode_inputs(2, 8, 2, 128, 16, [100, 37], seed=14)
+    check_decode(lib, d, 4)
+    assert lib.get_device_error() == (0, 0)
