@@ -95,6 +95,11 @@ class Oracle:
         lib.oracle_attend_splits.argtypes = common + [_ip, _i32, _ip, ctypes.c_double, _i32,
                                                       _dp, _dp]
         lib.oracle_attend_splits.restype = None
+        lib.oracle_plan_varlen.argtypes = [_i32, _ip, _i32, _i32, _i32, _ip]
+        lib.oracle_plan_varlen.restype = None
+        lib.oracle_attend_splits_varlen.argtypes = common + [_ip, _i32, _ip, ctypes.c_double,
+                                                             _ip, _i32, _dp, _dp]
+        lib.oracle_attend_splits_varlen.restype = None
         lib.oracle_cascade.argtypes = common + [_ip, _i32, _ip, _i32, _ip, ctypes.c_double,
                                                 _dp, _dp, _dp, _dp]
         lib.oracle_cascade.restype = None
@@ -173,6 +178,29 @@ class Oracle:
         self.lib.oracle_attend_splits(B, Hq, Hkv, D, page, _p(q), _p(kc), _p(vc), _pi(bt),
                                       bt.shape[1], _pi(cx), float(sm_scale), num_splits,
                                       _p(o), _p(lse))
+        return o, lse
+
+    def plan_varlen(self, ctx, page: int, max_splits: int, pages_per_split: int):
+        """Split count of each sequence ([L3] §⑥, per-sequence reading) -> int32 [B]."""
+        c = _i32a(ctx).reshape(-1)
+        ns = np.zeros(c.size, dtype=np.int32)
+        self.lib.oracle_plan_varlen(c.size, _pi(c), page, max_splits, pages_per_split, _pi(ns))
+        return ns
+
+    def attend_splits_varlen(self, q, k_cache, v_cache, block_table, ctx, sm_scale: float,
+                             num_splits, max_splits: int):
+        """Per-split states with num_splits[b] splits for sequence b ->
+        (o_part [B,Hq,max_splits,D], lse_part [B,Hq,max_splits]); entries past a
+        sequence's count are empty states."""
+        q, kc, vc, bt, cx, B, Hq, Hkv, D, page = self._decode_args(
+            q, k_cache, v_cache, block_table, ctx)
+        ns = _i32a(num_splits).reshape(-1)
+        assert ns.size == B and np.all(ns >= 1) and np.all(ns <= max_splits)
+        o = np.empty((B, Hq, max_splits, D))
+        lse = np.empty((B, Hq, max_splits))
+        self.lib.oracle_attend_splits_varlen(B, Hq, Hkv, D, page, _p(q), _p(kc), _p(vc),
+                                             _pi(bt), bt.shape[1], _pi(cx), float(sm_scale),
+                                             _pi(ns), max_splits, _p(o), _p(lse))
         return o, lse
 
     def cascade(self, q, k_cache, v_cache, prefix_pages, prefix_len: int, block_table, ctx,
@@ -256,6 +284,14 @@ def attend_full(*a, **k):
 
 def attend_splits(*a, **k):
     return default().attend_splits(*a, **k)
+
+
+def plan_varlen(*a, **k):
+    return default().plan_varlen(*a, **k)
+
+
+def attend_splits_varlen(*a, **k):
+    return default().attend_splits_varlen(*a, **k)
 
 
 def cascade(*a, **k):

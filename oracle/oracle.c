@@ -287,6 +287,76 @@ void oracle_attend_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t
 }
 
 /*
+ * Per-sequence split counts ([L3] §⑥: a real planner decides the splits from
+ * B, each sequence's ctx and the SM count, and can give sequences of
+ * different lengths different split counts).  The page fixes no rule for
+ * the per-sequence count; the reading taken keeps its other rule, every
+ * split holds several pages: sequence b's n_b = ceil(ctx_b / page) pages
+ * get ns_b = ceil(n_b / pages_per_split) splits, so that no split holds
+ * more than pages_per_split pages, clamped to [1, max_splits] (a sequence
+ * with no pages has one, empty, split; at the clamp a split holds
+ * ceil(n_b / max_splits) pages).
+ */
+void oracle_plan_varlen(int32_t B, const int32_t* ctx, int32_t page, int32_t max_splits,
+                        int32_t pages_per_split, int32_t* num_splits) {
+    for (int32_t b = 0; b < B; ++b) {
+        int32_t n = (ctx[b] + page - 1) / page;
+        int32_t ns = (n + pages_per_split - 1) / pages_per_split;
+        if (ns < 1) ns = 1;
+        if (ns > max_splits) ns = max_splits;
+        num_splits[b] = ns;
+    }
+}
+
+/*
+ * Per-split partial states with a split count per sequence: as
+ * oracle_attend_splits, but sequence b is cut into num_splits[b] splits by
+ * the [L3] §② formula with NS = num_splits[b].  Outputs keep the split axis
+ * max_splits long: o_part [B, Hq, max_splits, D], lse_part [B, Hq,
+ * max_splits]; entries sp >= num_splits[b] are not splits of the sequence
+ * and are written as empty states (o = 0, s = -inf).
+ */
+void oracle_attend_splits_varlen(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page,
+                                 const double* q, const double* k_cache, const double* v_cache,
+                                 const int32_t* block_table, int32_t max_pages,
+                                 const int32_t* ctx, double sm_scale,
+                                 const int32_t* num_splits, int32_t max_splits,
+                                 double* o_part, double* lse_part) {
+    int32_t G = Hq / Hkv;
+    int32_t maxn = 0;
+    for (int32_t b = 0; b < B; ++b) if (ctx[b] > maxn) maxn = ctx[b];
+    const double** kr = (const double**)malloc(sizeof(double*) * (size_t)(maxn > 0 ? maxn : 1));
+    const double** vr = (const double**)malloc(sizeof(double*) * (size_t)(maxn > 0 ? maxn : 1));
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t* pages = block_table + (int64_t)b * max_pages;
+        int32_t ns = num_splits[b];
+        for (int32_t hq = 0; hq < Hq; ++hq) {
+            int32_t hk = hq / G;
+            for (int32_t sp = 0; sp < max_splits; ++sp) {
+                int32_t n = 0, t0 = 0;
+                if (sp < ns) {
+                    int32_t p0, p1;
+                    oracle_split_range(ctx[b], page, ns, sp, &p0, &p1);
+                    int32_t t1 = p1 * page;
+                    t0 = p0 * page;
+                    if (t1 > ctx[b]) t1 = ctx[b];
+                    n = (p1 > p0 && t1 > t0) ? t1 - t0 : 0;
+                }
+                for (int32_t j = 0; j < n; ++j) {
+                    kr[j] = token_row(k_cache, pages, t0 + j, Hkv, hk, page, D);
+                    vr[j] = token_row(v_cache, pages, t0 + j, Hkv, hk, page, D);
+                }
+                int64_t row = ((int64_t)b * Hq + hq) * max_splits + sp;
+                attend_rows(D, q + ((int64_t)b * Hq + hq) * D, n, kr, vr, sm_scale,
+                            o_part + row * D, lse_part + row);
+            }
+        }
+    }
+    free(kr);
+    free(vr);
+}
+
+/*
  * Two-level cascade ([F2] §⑥): every request b attends to a shared prefix
  * of prefix_len tokens (pool pages prefix_pages[0..]) followed by its own
  * suffix of ctx[b] tokens (pool pages block_table[b][..]).  The plain

@@ -542,4 +542,76 @@ def pin_cascade_multilevel(orc):
         assert np.allclose(mv.reshape(out.shape), out, rtol=1e-12, atol=1e-13)
 
 
+# ---------------------------------------------------------------- per-sequence split counts
+def pin_plan_varlen(orc):
+    """[L3] §⑥ per-sequence split counts, read as: n pages get ceil(n / P)
+    splits of at most P pages, clamped to [1, max_splits].  Values worked by
+    hand for page 16: ctx 0, 1, 128, 129, 1000, 2048, 4096 are 0, 1, 8, 9, 63,
+    128, 256 pages."""
+    ctx = [0, 1, 128, 129, 1000, 2048, 4096]
+    assert orc.plan_varlen(ctx, 16, 16, 8).tolist() == [1, 1, 1, 2, 8, 16, 16]
+    assert orc.plan_varlen(ctx, 16, 4, 8).tolist() == [1, 1, 1, 2, 4, 4, 4]
+    assert orc.plan_varlen(ctx, 16, 64, 8).tolist() == [1, 1, 1, 2, 8, 16, 32]
+    assert orc.plan_varlen(ctx, 16, 16, 1).tolist() == [1, 1, 8, 9, 16, 16, 16]
+    assert orc.plan_varlen(ctx, 16, 256, 64).tolist() == [1, 1, 1, 1, 1, 2, 4]
+
+
+def pin_varlen_splits_printed_ranges(orc):
+    """Per-sequence split counts reuse the [L3] §② ranges with each sequence's
+    own count: a batch of ctx 100, 37, 1000 (page 16) with 4, 1 and 4 splits.
+    Sequence 0 is §⑧ 自测 1 (pages [0,2), [2,4), [4,6), [6,7)), sequence 2 the
+    §② ctx = 1000 example (split 3 is pages 48-62), sequence 1 is not split, so
+    its one state is the whole sequence's; the slots past a sequence's count
+    hold empty states.  Every state is checked by brute force over the tokens
+    of the printed page ranges."""
+    from scipy.special import logsumexp, softmax
+    rows = read_golden_table("split_ranges.txt")
+    printed = {}
+    for ctx, page, ns, _, _, split, p0, p1, _ in rows:
+        printed[(ctx, split)] = (p0, p1)
+    rng = np.random.default_rng(31)
+    ctx = [100, 37, 1000]
+    ns = np.array([4, 1, 4], np.int32)
+    q, kc, vc, bt, cx = _rand_decode(rng, 3, 4, 2, 8, 16, ctx)
+    scale = 0.3
+    op, sp = orc.attend_splits_varlen(q, kc, vc, bt, cx, scale, ns, 4)
+    for b, c in enumerate(ctx):
+        for hq in range(4):
+            K = np.stack([kc[bt[b, t // 16], hq // 2, t % 16] for t in range(c)])
+            V = np.stack([vc[bt[b, t // 16], hq // 2, t % 16] for t in range(c)])
+            x = scale * (K @ q[b, hq])
+            for spl in range(4):
+                if spl >= ns[b]:
+                    assert sp[b, hq, spl] == NEG and np.all(op[b, hq, spl] == 0.0)
+                    continue
+                p0, p1 = printed[(c, spl)] if ns[b] == 4 else (0, -(-c // 16))
+                t0, t1 = p0 * 16, min(p1 * 16, c)
+                assert abs(sp[b, hq, spl] - logsumexp(x[t0:t1]) / LN2) < 1e-12
+                assert np.allclose(op[b, hq, spl], softmax(x[t0:t1]) @ V[t0:t1], rtol=1e-12,
+                                   atol=1e-13)
+    # With the same count for every sequence it is the uniform split.
+    op4, sp4 = orc.attend_splits(q, kc, vc, bt, cx, scale, 4)
+    o4, s4 = orc.attend_splits_varlen(q, kc, vc, bt, cx, scale, np.full(3, 4, np.int32), 4)
+    assert np.array_equal(op4, o4) and np.array_equal(sp4, s4)
+
+
+def pin_varlen_split_merge_identity(orc):
+    """Merging the first ns_b states of each sequence gives unsplit attention
+    ([FA] §0.2), whatever the per-sequence counts."""
+    rng = np.random.default_rng(32)
+    ctx = [0, 5, 37, 300, 1000, 16, 17]
+    q, kc, vc, bt, cx = _rand_decode(rng, len(ctx), 4, 2, 8, 16, ctx)
+    ns = orc.plan_varlen(ctx, 16, 8, 2)
+    assert ns.tolist() == [1, 1, 2, 8, 8, 1, 1]
+    op, sp = orc.attend_splits_varlen(q, kc, vc, bt, cx, 0.25, ns, 8)
+    o, s = orc.attend_full(q, kc, vc, bt, cx, 0.25)
+    for b in range(len(ctx)):
+        n = int(ns[b])
+        vo, so = orc.merge_states(op[b, :, :n].transpose(1, 0, 2)[None], sp[b, :, :n].T[None])
+        fin = np.isfinite(s[b])
+        assert np.array_equal(fin, np.isfinite(so[0]))
+        assert np.allclose(vo[0], o[b], rtol=1e-12, atol=1e-13)
+        assert np.allclose(so[0][fin], s[b][fin], rtol=0, atol=1e-12)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -64,6 +64,13 @@ MUTANTS = [
      "                vr[n] = token_row(v_cache, sfx, t, Hkv, hk, page, D);\n"
      "            }\n"
      "            attend_rows(D, q + row * D, n, kr, vr, sm_scale, o_pre + row * D, s_pre + row);\n"),
+    # per-sequence split counts: the largest count used for every sequence;
+    # floor instead of ceil; no clamp to the caller's largest count
+    ("varlen_uses_max_splits", "oracle_split_range(ctx[b], page, ns, sp, &p0, &p1);",
+     "oracle_split_range(ctx[b], page, max_splits, sp, &p0, &p1);"),
+    ("plan_varlen_floor", "int32_t ns = (n + pages_per_split - 1) / pages_per_split;",
+     "int32_t ns = n / pages_per_split;"),
+    ("plan_varlen_no_clamp", "if (ns > max_splits) ns = max_splits;", ""),
     ("multilevel_suffix_from_shared_pages",
      "kr[n] = token_row(k_cache, sfx, t, Hkv, hk, page, D);",
      "kr[n] = token_row(k_cache, seg_pages, t, Hkv, hk, page, D);"),
