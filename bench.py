@@ -9,10 +9,14 @@ split_kv_lse_gb300/workloads.py), inputs resident in HBM:
   merge_states          S=256, N=64, H=32, D=128 fp32, 5% empty
   splitkv_decode        B=1, ctx=32768, Hq=32, Hkv=8, D=128, page 16, NS=64,
                         pass 1 + PDL-chained combine to fp16
-  cascade_decode        B=64, shared 8192-token prefix + 1..2048-token suffixes
+  cascade_decode        B=64, shared 8192-token prefix + 1..2048-token suffixes,
+                        NS=16 for every suffix
+  cascade_decode_varlen the same with per-sequence suffix split counts (at
+                        most 16 splits of at most 8 pages each)
+Reported beside the step (timed in every step, not counted in value):
+merge_states_N1..N1024, the large-N sweep (S=16, H=8, D=128 fp32).
 Diagnostic stages (--only, not in the step): splitkv_decode_pass1 and
-cascade_suffix_pass1 (pass 1 alone), cascade_multilevel (three levels) and
-merge_states_sweep (S=16, H=8, N in 1, 2, 3, 128, 1024).
+cascade_suffix_pass1 (pass 1 alone) and cascade_multilevel (three levels).
 value = algorithmic HBM bytes of the step / step time (GB/s).  Each stage is
 timed with CUDA events on the launching stream; L2 is flushed (a 512 MB
 write, then a 512 MB read, so it holds clean lines) before every stage,
@@ -46,7 +50,9 @@ FALLBACK_HBM_GBS = 6800.0
 WORKLOAD = ("split-KV hot path step: merge_state + merge_state_in_place S=8192 H=32 D=128 fp16; "
             "merge_states S=256 N=64 H=32 D=128 fp32; splitkv_decode B=1 ctx=32768 Hq=32 Hkv=8 "
             "D=128 page=16 NS=64 fp16; cascade_decode B=64 Hq=32 Hkv=8 shared prefix 8192 + "
-            "suffixes 1..2048 NS=16 fp16")
+            "suffixes 1..2048 NS=16 fp16, and the same cascade with per-sequence suffix splits "
+            "(at most 16 of at most 8 pages); reported beside the step: merge_states S=16 H=8 "
+            "D=128 fp32, N in 1, 2, 3, 128, 1024")
 
 
 def parse_args():
@@ -129,8 +135,13 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- stages
+# Pages per split of the per-sequence suffix plan (the plan's "several pages").
+VARLEN_PAGES_PER_SPLIT = 8
+
+
 class Stage:
     def __init__(self, name, fn, algo_bytes, launches, e2e=None):
+        self.in_step = True
         self.name = name
         self.fn = fn
         self.bytes = int(algo_bytes)
@@ -180,17 +191,20 @@ def nbytes(t):
 
 
 STAGE_NAMES = ("merge_state", "merge_state_in_place", "merge_states", "splitkv_decode",
-               "cascade_decode")
+               "cascade_decode", "cascade_decode_varlen")
+# Timed in every step and reported beside the step's stages, but not counted
+# in value or ms_per_step: the large-N merge sweep (S=16, H=8, D=128 fp32,
+# N in 1, 2, 3, 128, 1024), whose small N are launch-latency bound.
+REPORTED_STAGES = ("merge_states_sweep",)
 # Diagnostic stages, selectable with --only (not part of the default step).
-EXTRA_STAGES = ("splitkv_decode_pass1", "cascade_suffix_pass1", "cascade_multilevel",
-                "merge_states_sweep")
+EXTRA_STAGES = ("splitkv_decode_pass1", "cascade_suffix_pass1", "cascade_multilevel")
 
 
 def build_stages(torch, skv, W, dev, only=None):
     """Create the GPU stages; inputs are generated on the host and copied once."""
     stages = []
     hostside = {}
-    want = set(only) if only else set(STAGE_NAMES)
+    want = set(only) if only else set(STAGE_NAMES) | set(REPORTED_STAGES)
 
     def to_dev(d):
         return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
@@ -202,7 +216,7 @@ def build_stages(torch, skv, W, dev, only=None):
         _merge_states_stage(torch, skv, W, dev, to_dev, stages, hostside)
     if want & {"splitkv_decode", "splitkv_decode_pass1"}:
         _decode_stage(torch, skv, W, dev, to_dev, stages, hostside, want)
-    if want & {"cascade_decode", "cascade_suffix_pass1"}:
+    if want & {"cascade_decode", "cascade_suffix_pass1", "cascade_decode_varlen"}:
         _cascade_stage(torch, skv, W, dev, to_dev, stages, hostside, want)
     if "cascade_multilevel" in want:
         _multilevel_stage(torch, skv, W, dev, to_dev, stages)
@@ -256,9 +270,11 @@ def _merge_states_sweep_stages(torch, skv, W, dev, to_dev, stages):
                          device=dev)
         nonempty = int((d["s"] != -math.inf).sum())
         nb = nonempty * D * 4 + nbytes(d["s"]) + nbytes(vo) + nbytes(so)
-        stages.append(Stage(f"merge_states_N{N}",
-                            lambda g=g, ws=ws, vo=vo, so=so: skv.merge_states(g["v"], g["s"], ws, vo, so),
-                            nb, 1))
+        st = Stage(f"merge_states_N{N}",
+                   lambda g=g, ws=ws, vo=vo, so=so: skv.merge_states(g["v"], g["s"], ws, vo, so),
+                   nb, 1)
+        st.in_step = False
+        stages.append(st)
 
 
 def _decode_stage(torch, skv, W, dev, to_dev, stages, hostside, want):
@@ -317,6 +333,20 @@ def _cascade_stage(torch, skv, W, dev, to_dev, stages, hostside, want):
                                                        g5["block_table"], g5["ctx"], ns,
                                                        d5["sm_scale"], workspace=ws, **bufs),
                             cas_bytes, 3))
+    if "cascade_decode_varlen" in want:
+        # The same workload with per-sequence suffix split counts ([L3] §⑥
+        # F1): at most 16 splits of at most 8 pages, planned on the host once.
+        plan = skv.splitkv_plan_varlen(d5["ctx"], 16, ns, VARLEN_PAGES_PER_SPLIT)
+        plan.device(dev)
+        vbufs = dict(bufs)
+        stages.append(Stage("cascade_decode_varlen",
+                            lambda: skv.cascade_decode_varlen(g5["q"], g5["k_cache"], g5["v_cache"],
+                                                              g5["prefix_pages"], d5["prefix_len"],
+                                                              g5["block_table"], g5["ctx"], plan,
+                                                              d5["sm_scale"], workspace=ws,
+                                                              **vbufs),
+                            cas_bytes, 3))
+        hostside["cascade_varlen_plan"] = plan
     if "cascade_suffix_pass1" in want:
         # The kernel that dominates the step: pass 1 of the split-KV decode on
         # the cascade's suffixes, launched exactly as cascade_decode launches it.
@@ -398,6 +428,12 @@ def e2e_step(torch, skv, host, dev):
                                                 g5["block_table"], g5["ctx"], d5["num_splits"],
                                                 d5["sm_scale"])
     outs += [out5, lse5]
+    plan = host.get("cascade_varlen_plan")
+    if plan is not None:
+        out6, lse6, _, _, _, _ = skv.cascade_decode_varlen(
+            g5["q"], g5["k_cache"], g5["v_cache"], g5["prefix_pages"], d5["prefix_len"],
+            g5["block_table"], g5["ctx"], plan, d5["sm_scale"])
+        outs += [out6, lse6]
     key = tuple((tuple(o.shape), o.dtype) for o in outs)
     if key not in _PINNED_OUT:
         _PINNED_OUT[key] = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
@@ -596,8 +632,9 @@ def run_ours(args):
     for evs in all_evs:
         for st, e0, e1 in evs:
             st.times_ms.append(e0.elapsed_time(e1))
-    step_ms = max_over_ranks(sum(statistics.mean(st.times_ms) for st in stages), dist, dev)
-    step_bytes = sum(st.bytes for st in stages)
+    in_step = [st for st in stages if st.in_step]
+    step_ms = max_over_ranks(sum(statistics.mean(st.times_ms) for st in in_step), dist, dev)
+    step_bytes = sum(st.bytes for st in in_step)
     value = job_value(world, step_bytes, step_ms)
     launches = args.steps * sum(st.launches for st in stages)
     assert skv.get_device_error() == (0, 0), "device-side error during the benchmark"
@@ -633,6 +670,8 @@ def run_ours(args):
                               "algo_bytes": st.bytes, "GB_s": round(gbs, 1),
                               "frac_of_measured_hbm": round(gbs / peak, 4),
                               "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4)}
+        if not st.in_step:
+            stage_rep[st.name]["in_step"] = False
     if dom_rep is not None:
         dk, dms = dom_rep
         traffic, traffic_src = recorded_traffic()

@@ -253,6 +253,59 @@ skv_status skv_splitkv_decode(const void* q, const void* k_cache, const void* v_
                               int32_t* ranges_dbg, skv_stream_t stream);
 
 /*
+ * Per-sequence split counts ([L3] §⑥: a planner decides the splits before
+ * each decode step from B, every sequence's ctx and the GPU, and may give
+ * sequences of different lengths different split counts).  The page fixes
+ * no rule for the per-sequence count; the rule taken keeps its "several
+ * pages per split": sequence b, of n_b = ceil(ctx_host[b] / page) pages,
+ * gets ns_b = ceil(n_b / pages_per_split) splits, clamped to
+ * [1, max_splits], cut by the [L3] §② ranges with NUM_SPLITS = ns_b.
+ * Host only; needs no GPU.
+ * plan_host: host int32 buffer of plan_capacity >= 2 * sum_b ns_b + B
+ *   elements (2 * B * max_splits + B always suffices).  It receives
+ *   [*num_units][2] work units (b, split | ns_b << 16), one per split of
+ *   every sequence, the longest splits first, followed by [B] the split
+ *   counts ns_b.  Copy it as is into a 16-byte aligned device buffer for
+ *   skv_splitkv_decode_varlen / skv_cascade_decode_varlen.
+ * *num_units receives sum_b ns_b; *max_split_pages the most pages any one
+ *   split holds (it sets the decode kernel's shape).
+ * Limits: B >= 0, page >= 1, 1 <= max_splits <= 256, pages_per_split >= 1,
+ *   ctx_host[b] >= 0.
+ */
+skv_status skv_splitkv_plan_varlen(int32_t B, const int32_t* ctx_host, int32_t page,
+                                   int32_t max_splits, int32_t pages_per_split,
+                                   int32_t* plan_host, int64_t plan_capacity,
+                                   int32_t* num_units, int32_t* max_split_pages);
+
+/*
+ * Split-KV paged decode with a split count per sequence: as
+ * skv_splitkv_decode, but sequence b is cut into ns_b splits (the plan's
+ * counts) and pass 1 runs one CTA per (unit, kv head) of the plan's work list
+ * only.  o_part [B, Hq, max_splits, D] and lse_part [B, Hq, max_splits] keep
+ * the split axis max_splits long: split sp < ns_b of sequence b is written
+ * there, slots sp >= ns_b are not written.  The combine (out != NULL) merges
+ * the ns_b states of each (b, hq).  ranges_dbg [B, max_splits, 2] as for
+ * skv_splitkv_decode, for sp < ns_b.
+ * plan: device copy of skv_splitkv_plan_varlen's buffer (16-byte aligned),
+ *   num_units and max_split_pages as that call returned them; the contexts
+ *   in `ctx` (device) must be those the plan was made for (a longer one can
+ *   make a split longer than max_split_pages, which is flagged in the error
+ *   word and cut).  A unit naming a sequence outside [0, B) or a split count
+ *   outside [1, max_splits] is flagged and skipped.
+ * Other arguments, layouts, support and device-side checks as for
+ * skv_splitkv_decode (with max_splits <= 256 in place of num_splits).
+ */
+skv_status skv_splitkv_decode_varlen(const void* q, const void* k_cache, const void* v_cache,
+                                     int32_t num_pool_pages, const int32_t* block_table,
+                                     int32_t max_pages, const int32_t* ctx, int32_t B,
+                                     int32_t Hq, int32_t Hkv, int32_t D, int32_t page,
+                                     int32_t max_splits, const int32_t* plan,
+                                     int32_t num_units, int32_t max_split_pages,
+                                     float sm_scale, skv_dtype dtype, float* o_part,
+                                     float* lse_part, void* out, float* lse_out,
+                                     int32_t* ranges_dbg, skv_stream_t stream);
+
+/*
  * Device workspace, in bytes, that skv_cascade_decode needs for these sizes
  * (the per-chunk states of the shared-prefix pass).  sm_count > 0 is used as
  * given; 0 means the current device's SM count (the chunking depends on it).
@@ -301,6 +354,25 @@ skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_
                               float* o_part, float* lse_part,
                               void* out, float* lse_out,
                               void* workspace, size_t workspace_bytes, skv_stream_t stream);
+
+/*
+ * Two-level cascade decode whose suffixes have a split count per sequence:
+ * as skv_cascade_decode, with the suffix pass and its merge as in
+ * skv_splitkv_decode_varlen (plan, num_units, max_split_pages from
+ * skv_splitkv_plan_varlen over the suffix contexts; o_part / lse_part with a
+ * split axis max_splits long).  Workspace as for skv_cascade_decode.
+ */
+skv_status skv_cascade_decode_varlen(const void* q, const void* k_cache, const void* v_cache,
+                                     int32_t num_pool_pages, const int32_t* prefix_pages,
+                                     int32_t prefix_len, const int32_t* block_table,
+                                     int32_t max_pages, const int32_t* ctx, int32_t B,
+                                     int32_t Hq, int32_t Hkv, int32_t D, int32_t page,
+                                     int32_t max_splits, const int32_t* plan,
+                                     int32_t num_units, int32_t max_split_pages,
+                                     float sm_scale, skv_dtype dtype, float* o_pre,
+                                     float* s_pre, float* o_part, float* lse_part, void* out,
+                                     float* lse_out, void* workspace, size_t workspace_bytes,
+                                     skv_stream_t stream);
 
 /*
  * One shared level of a multi-level cascade: the requests are cut into

@@ -22,7 +22,8 @@ from ._ffi import SkvError
 __all__ = [
     "SkvError", "merge_state", "merge_state_in_place", "merge_states",
     "merge_states_workspace_size", "split_page_range", "splitkv_decode_plan",
-    "splitkv_decode", "cascade_workspace_size", "cascade_decode", "get_device_error",
+    "splitkv_decode", "SplitPlan", "splitkv_plan_varlen", "splitkv_decode_varlen",
+    "cascade_workspace_size", "cascade_decode", "cascade_decode_varlen", "get_device_error",
     "poll_device_error", "selftest_bounded_wait", "abi_version", "library_path",
 ]
 
@@ -134,6 +135,104 @@ def splitkv_decode_plan(ctx, Hkv: int, page: int = 16, sm_count: int = 0) -> int
     return ns.value
 
 
+class SplitPlan:
+    """A per-sequence split plan from skv_splitkv_plan_varlen: the host int32
+    buffer ([num_units][2] work units, longest first, then [B] split counts),
+    its unit count, longest split and split-axis length, and a cached device
+    copy per device."""
+
+    def __init__(self, host: torch.Tensor, num_units: int, max_split_pages: int,
+                 max_splits: int, B: int):
+        self.host = host
+        self.num_units = num_units
+        self.max_split_pages = max_split_pages
+        self.max_splits = max_splits
+        self.B = B
+        self._dev = {}
+
+    @property
+    def num_splits(self) -> torch.Tensor:
+        """Split count of each sequence (host int32 [B])."""
+        return self.host[2 * self.num_units:2 * self.num_units + self.B]
+
+    def device(self, dev) -> torch.Tensor:
+        dev = torch.device(dev)
+        if dev not in self._dev:
+            t = torch.empty(max(4, self.host.numel()), dtype=torch.int32, device=dev)
+            t[:self.host.numel()].copy_(self.host)
+            self._dev[dev] = t
+        return self._dev[dev]
+
+
+def splitkv_plan_varlen(ctx, page: int = 16, max_splits: int = 16,
+                        pages_per_split: int = 8) -> SplitPlan:
+    """Per-sequence split counts and work list (host; see skv_splitkv_plan_varlen)."""
+    vals = [int(x) for x in (ctx.tolist() if hasattr(ctx, "tolist") else ctx)]
+    B = len(vals)
+    arr = (ctypes.c_int32 * max(1, B))(*vals)
+    cap = 2 * B * max_splits + B
+    host = torch.zeros(max(1, cap), dtype=torch.int32)
+    nu, msp = ctypes.c_int32(), ctypes.c_int32()
+    _ffi.check("skv_splitkv_plan_varlen", _ffi.lib().skv_splitkv_plan_varlen(
+        B, arr, page, max_splits, pages_per_split,
+        ctypes.cast(host.data_ptr(), ctypes.POINTER(ctypes.c_int32)), cap, ctypes.byref(nu),
+        ctypes.byref(msp)))
+    used = 2 * nu.value + B
+    return SplitPlan(host[:used].clone(), nu.value, msp.value, max_splits, B)
+
+
+def _decode_bufs(q, k_cache, v_cache, block_table, ctx, ns, o_part, lse_part, out, lse_out,
+                 combine, ranges_dbg):
+    B, Hq, D = q.shape
+    _need(q, "q")
+    _need(k_cache, "k_cache", q.dtype)
+    _need(v_cache, "v_cache", q.dtype, tuple(k_cache.shape))
+    _need(block_table, "block_table", torch.int32)
+    _need(ctx, "ctx", torch.int32, (B,))
+    if k_cache.shape[3] != D or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("inconsistent decode shapes")
+    dev = q.device
+    if o_part is None:
+        o_part = torch.empty((B, Hq, ns, D), dtype=torch.float32, device=dev)
+    if lse_part is None:
+        lse_part = torch.empty((B, Hq, ns), dtype=torch.float32, device=dev)
+    _need(o_part, "o_part", torch.float32, (B, Hq, ns, D))
+    _need(lse_part, "lse_part", torch.float32, (B, Hq, ns))
+    if combine:
+        out = torch.empty((B, Hq, D), dtype=q.dtype, device=dev) if out is None else out
+        lse_out = torch.empty((B, Hq), dtype=torch.float32, device=dev) if lse_out is None else lse_out
+        _need(out, "out", q.dtype, (B, Hq, D))
+        _need(lse_out, "lse_out", torch.float32, (B, Hq))
+    else:
+        out = lse_out = None
+    if ranges_dbg is not None:
+        _need(ranges_dbg, "ranges_dbg", torch.int32, (B, ns, 2))
+    return o_part, lse_part, out, lse_out
+
+
+def splitkv_decode_varlen(q, k_cache, v_cache, block_table, ctx, plan: SplitPlan,
+                          sm_scale: float, o_part=None, lse_part=None, out=None, lse_out=None,
+                          combine: bool = True, ranges_dbg=None):
+    """Split-KV paged decode with the per-sequence split counts of `plan`.
+    Returns (out, lse_out, o_part, lse_part); o_part has plan.max_splits slots
+    per (b, hq), of which the first plan.num_splits[b] are written."""
+    B, Hq, D = q.shape
+    P, Hkv, page, _ = k_cache.shape
+    if plan.B != B:
+        raise ValueError("the plan was made for another batch size")
+    o_part, lse_part, out, lse_out = _decode_bufs(q, k_cache, v_cache, block_table, ctx,
+                                                  plan.max_splits, o_part, lse_part, out,
+                                                  lse_out, combine, ranges_dbg)
+    dplan = plan.device(q.device)
+    _ffi.check("skv_splitkv_decode_varlen", _ffi.lib().skv_splitkv_decode_varlen(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), P, block_table.data_ptr(),
+        block_table.shape[1], ctx.data_ptr(), B, Hq, Hkv, D, page, plan.max_splits,
+        dplan.data_ptr(), plan.num_units, plan.max_split_pages, float(sm_scale), _DT[q.dtype],
+        o_part.data_ptr(), lse_part.data_ptr(), _ptr(out), _ptr(lse_out), _ptr(ranges_dbg),
+        _stream(q)))
+    return out, lse_out, o_part, lse_part
+
+
 def splitkv_decode(q, k_cache, v_cache, block_table, ctx, num_splits: int, sm_scale: float,
                    o_part=None, lse_part=None, out=None, lse_out=None, combine: bool = True,
                    ranges_dbg=None):
@@ -225,6 +324,42 @@ def cascade_decode(q, k_cache, v_cache, prefix_pages, prefix_len: int, block_tab
         Hkv, D, page, num_splits, float(sm_scale), _DT[q.dtype], o_pre.data_ptr(),
         s_pre.data_ptr(), o_part.data_ptr(), lse_part.data_ptr(), out.data_ptr(),
         lse_out.data_ptr(), workspace.data_ptr(), ws_bytes, _stream(q)))
+    return out, lse_out, o_pre, s_pre, o_part, lse_part
+
+
+def cascade_decode_varlen(q, k_cache, v_cache, prefix_pages, prefix_len: int, block_table, ctx,
+                          plan: SplitPlan, sm_scale: float, out=None, lse_out=None, o_pre=None,
+                          s_pre=None, o_part=None, lse_part=None, workspace=None):
+    """Two-level cascade whose suffixes use the per-sequence split counts of
+    `plan` (made over the suffix contexts).  Returns
+    (out, lse_out, o_pre, s_pre, o_part, lse_part)."""
+    B, Hq, D = q.shape
+    P, Hkv, page, D2 = k_cache.shape
+    if plan.B != B:
+        raise ValueError("the plan was made for another batch size")
+    _need(prefix_pages, "prefix_pages", torch.int32)
+    ns = plan.max_splits
+    o_part, lse_part, out, lse_out = _decode_bufs(q, k_cache, v_cache, block_table, ctx, ns,
+                                                  o_part, lse_part, out, lse_out, True, None)
+    dev = q.device
+    f32 = torch.float32
+    o_pre = torch.empty((B, Hq, D), dtype=f32, device=dev) if o_pre is None else o_pre
+    s_pre = torch.empty((B, Hq), dtype=f32, device=dev) if s_pre is None else s_pre
+    _need(o_pre, "o_pre", f32, (B, Hq, D))
+    _need(s_pre, "s_pre", f32, (B, Hq))
+    need = cascade_workspace_size(B, Hq, Hkv, D, prefix_len)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    dplan = plan.device(dev)
+    _ffi.check("skv_cascade_decode_varlen", _ffi.lib().skv_cascade_decode_varlen(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), P, prefix_pages.data_ptr(),
+        int(prefix_len), block_table.data_ptr(), block_table.shape[1], ctx.data_ptr(), B, Hq,
+        Hkv, D, page, ns, dplan.data_ptr(), plan.num_units, plan.max_split_pages,
+        float(sm_scale), _DT[q.dtype], o_pre.data_ptr(), s_pre.data_ptr(), o_part.data_ptr(),
+        lse_part.data_ptr(), out.data_ptr(), lse_out.data_ptr(), workspace.data_ptr(), ws_bytes,
+        _stream(q)))
     return out, lse_out, o_pre, s_pre, o_part, lse_part
 
 

@@ -43,6 +43,17 @@ SIGNATURES = {
     "skv_splitkv_decode": (i32, [c_void_p, c_void_p, c_void_p, i32, c_void_p, i32, c_void_p,
                                  i32, i32, i32, i32, i32, i32, f32, i32, c_void_p, c_void_p,
                                  c_void_p, c_void_p, c_void_p, c_void_p]),
+    "skv_splitkv_plan_varlen": (i32, [i32, c_int32_p, i32, i32, i32, c_int32_p, i64, c_int32_p,
+                                      c_int32_p]),
+    "skv_splitkv_decode_varlen": (i32, [c_void_p, c_void_p, c_void_p, i32, c_void_p, i32,
+                                        c_void_p, i32, i32, i32, i32, i32, i32, c_void_p, i32,
+                                        i32, f32, i32, c_void_p, c_void_p, c_void_p, c_void_p,
+                                        c_void_p, c_void_p]),
+    "skv_cascade_decode_varlen": (i32, [c_void_p, c_void_p, c_void_p, i32, c_void_p, i32,
+                                        c_void_p, i32, c_void_p, i32, i32, i32, i32, i32, i32,
+                                        c_void_p, i32, i32, f32, i32, c_void_p, c_void_p,
+                                        c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                        size_t, c_void_p]),
     "skv_cascade_workspace_size": (size_t, [i32, i32, i32, i32, i32, i32]),
     "skv_cascade_decode": (i32, [c_void_p, c_void_p, c_void_p, i32, c_void_p, i32, c_void_p, i32,
                                  c_void_p, i32, i32, i32, i32, i32, i32, f32, i32, c_void_p,

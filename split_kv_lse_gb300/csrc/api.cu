@@ -188,13 +188,48 @@ skv_status skv_splitkv_decode_plan(int32_t B, const int32_t* ctx_host, int32_t H
     return SKV_OK;
 }
 
-skv_status skv_splitkv_decode(const void* q, const void* k_cache, const void* v_cache,
-                              int32_t num_pool_pages, const int32_t* block_table,
-                              int32_t max_pages, const int32_t* ctx, int32_t B, int32_t Hq,
-                              int32_t Hkv, int32_t D, int32_t page, int32_t num_splits,
-                              float sm_scale, skv_dtype dtype, float* o_part, float* lse_part,
-                              void* out, float* lse_out, int32_t* ranges_dbg,
-                              skv_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// A per-sequence split plan as the decode kernels take it: the device copy
+// of skv_splitkv_plan_varlen's buffer ([num_units][2] units, then [B] split
+// counts), its unit count and its longest split.
+struct VarlenPlan {
+    const int32_t* plan = nullptr;
+    int32_t num_units = 0;
+    int32_t max_split_pages = 0;
+};
+
+skv_status check_varlen(const VarlenPlan* vl, int32_t B) {
+    if (vl == nullptr) return SKV_OK;
+    if (!vl->plan || !aligned16(vl->plan) || vl->num_units < B || vl->num_units < 1 ||
+        vl->max_split_pages < 0)
+        return SKV_ERR_INVALID_ARG;
+    if ((int64_t)vl->num_units > (int64_t)INT32_MAX / 256) return SKV_ERR_UNSUPPORTED;
+    return SKV_OK;
+}
+
+void apply_varlen(const VarlenPlan* vl, DecodeArgs* a) {
+    if (vl == nullptr) return;
+    a->units = vl->plan;
+    a->num_units = vl->num_units;
+    a->max_split_pages = vl->max_split_pages;
+}
+
+const int32_t* varlen_counts(const VarlenPlan* vl) {
+    return vl == nullptr ? nullptr : vl->plan + 2 * (size_t)vl->num_units;
+}
+
+// Split-KV decode ([L3] §①-⑤): pass 1 over every (sequence, split) of the
+// uniform count num_splits or of the per-sequence plan `vl`, then (out !=
+// NULL) the combine, chained by programmatic dependent launch.
+skv_status decode_run(const void* q, const void* k_cache, const void* v_cache,
+                      int32_t num_pool_pages, const int32_t* block_table, int32_t max_pages,
+                      const int32_t* ctx, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                      int32_t page, int32_t num_splits, const VarlenPlan* vl, float sm_scale,
+                      skv_dtype dtype, float* o_part, float* lse_part, void* out,
+                      float* lse_out, int32_t* ranges_dbg, skv_stream_t stream) {
     if (B < 0 || Hq < 1 || Hkv < 1 || D < 1 || page < 1 || num_splits < 1 || max_pages < 1 ||
         num_pool_pages < 1 || !valid_dtype(dtype))
         return SKV_ERR_INVALID_ARG;
@@ -214,9 +249,11 @@ skv_status skv_splitkv_decode(const void* q, const void* k_cache, const void* v_
     if (lse_out && !aligned4(lse_out)) return SKV_ERR_INVALID_ARG;
     if (lse_out && !out) return SKV_ERR_INVALID_ARG;
     if (ranges_dbg && !aligned4(ranges_dbg)) return SKV_ERR_INVALID_ARG;
-    const DeviceInfo* dev = nullptr;
-    skv_status st = current_device(&dev);
+    skv_status st = check_varlen(vl, B);
     if (st != SKV_OK) return st;
+    if (vl && (int64_t)vl->num_units * Hkv > INT32_MAX) return SKV_ERR_UNSUPPORTED;
+    const DeviceInfo* dev = nullptr;
+    if ((st = current_device(&dev)) != SKV_OK) return st;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     DecodeArgs a;
     a.q = q;
@@ -237,6 +274,7 @@ skv_status skv_splitkv_decode(const void* q, const void* k_cache, const void* v_
     a.lse_part = lse_part;
     a.ranges_dbg = ranges_dbg;
     a.bf16 = dtype == SKV_BF16;
+    apply_varlen(vl, &a);
     cudaError_t e = launch_splitkv_decode(a, *dev, cs);
     if (e != cudaSuccess) return SKV_ERR_CUDA;
     if (out != nullptr) {
@@ -245,6 +283,8 @@ skv_status skv_splitkv_decode(const void* q, const void* k_cache, const void* v_
         c.lse_part = lse_part;
         c.rows = (int64_t)B * Hq;
         c.NS = num_splits;
+        c.seq_splits = varlen_counts(vl);
+        c.Hq = Hq;
         c.D = D;
         c.out = out;
         c.out_dt = dtype;
@@ -252,6 +292,89 @@ skv_status skv_splitkv_decode(const void* q, const void* k_cache, const void* v_
         e = launch_combine(c, true, *dev, cs);
         if (e != cudaSuccess) return SKV_ERR_CUDA;
     }
+    return SKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+skv_status skv_splitkv_decode(const void* q, const void* k_cache, const void* v_cache,
+                              int32_t num_pool_pages, const int32_t* block_table,
+                              int32_t max_pages, const int32_t* ctx, int32_t B, int32_t Hq,
+                              int32_t Hkv, int32_t D, int32_t page, int32_t num_splits,
+                              float sm_scale, skv_dtype dtype, float* o_part, float* lse_part,
+                              void* out, float* lse_out, int32_t* ranges_dbg,
+                              skv_stream_t stream) {
+    return decode_run(q, k_cache, v_cache, num_pool_pages, block_table, max_pages, ctx, B, Hq,
+                      Hkv, D, page, num_splits, nullptr, sm_scale, dtype, o_part, lse_part, out,
+                      lse_out, ranges_dbg, stream);
+}
+
+skv_status skv_splitkv_decode_varlen(const void* q, const void* k_cache, const void* v_cache,
+                                     int32_t num_pool_pages, const int32_t* block_table,
+                                     int32_t max_pages, const int32_t* ctx, int32_t B,
+                                     int32_t Hq, int32_t Hkv, int32_t D, int32_t page,
+                                     int32_t max_splits, const int32_t* plan,
+                                     int32_t num_units, int32_t max_split_pages,
+                                     float sm_scale, skv_dtype dtype, float* o_part,
+                                     float* lse_part, void* out, float* lse_out,
+                                     int32_t* ranges_dbg, skv_stream_t stream) {
+    VarlenPlan vl;
+    vl.plan = plan;
+    vl.num_units = num_units;
+    vl.max_split_pages = max_split_pages;
+    return decode_run(q, k_cache, v_cache, num_pool_pages, block_table, max_pages, ctx, B, Hq,
+                      Hkv, D, page, max_splits, &vl, sm_scale, dtype, o_part, lse_part, out,
+                      lse_out, ranges_dbg, stream);
+}
+
+skv_status skv_splitkv_plan_varlen(int32_t B, const int32_t* ctx_host, int32_t page,
+                                   int32_t max_splits, int32_t pages_per_split,
+                                   int32_t* plan_host, int64_t plan_capacity,
+                                   int32_t* num_units, int32_t* max_split_pages) {
+    if (B < 0 || page < 1 || max_splits < 1 || max_splits > 256 || pages_per_split < 1 ||
+        !num_units || !max_split_pages || (B > 0 && (!ctx_host || !plan_host)))
+        return SKV_ERR_INVALID_ARG;
+    // [L3] §⑥ (a planner may give sequences of different lengths different
+    // split counts), with the page's "several pages per split": sequence b
+    // gets ceil(pages_b / pages_per_split) splits, clamped to [1, max_splits].
+    std::vector<int32_t> ns((size_t)B);
+    int64_t units = 0;
+    for (int32_t b = 0; b < B; ++b) {
+        if (ctx_host[b] < 0) return SKV_ERR_INVALID_ARG;
+        const int32_t np = (int32_t)(((int64_t)ctx_host[b] + page - 1) / page);
+        const int32_t want = (int32_t)(((int64_t)np + pages_per_split - 1) / pages_per_split);
+        ns[b] = std::min(max_splits, std::max(1, want));
+        units += ns[b];
+    }
+    if (plan_capacity < 2 * units + B) return SKV_ERR_INVALID_ARG;
+    if (units > (int64_t)INT32_MAX / 256) return SKV_ERR_UNSUPPORTED;
+    // Units, longest first (a unit's pages from the [L3] §② range), so that
+    // the short ones fill the end of the launch; ties keep (b, split) order.
+    struct Unit {
+        int32_t pages, b, split;
+    };
+    std::vector<Unit> list;
+    list.reserve((size_t)units);
+    int32_t longest = 0;
+    for (int32_t b = 0; b < B; ++b)
+        for (int32_t sp = 0; sp < ns[b]; ++sp) {
+            int p0 = 0, p1 = 0;
+            split_page_range(ctx_host[b], page, ns[b], sp, &p0, &p1);
+            const int32_t n = p1 > p0 ? p1 - p0 : 0;
+            longest = std::max(longest, n);
+            list.push_back(Unit{n, b, sp});
+        }
+    std::stable_sort(list.begin(), list.end(),
+                     [](const Unit& x, const Unit& y) { return x.pages > y.pages; });
+    for (size_t i = 0; i < list.size(); ++i) {
+        plan_host[2 * i] = list[i].b;
+        plan_host[2 * i + 1] = list[i].split | (ns[list[i].b] << 16);
+    }
+    for (int32_t b = 0; b < B; ++b) plan_host[2 * units + b] = ns[b];
+    *num_units = (int32_t)units;
+    *max_split_pages = longest;
     return SKV_OK;
 }
 
@@ -357,9 +480,10 @@ skv_status cascade_run(const void* q, const void* k_cache, const void* v_cache,
                        int32_t num_pool_pages, const CascadeLevels& levels,
                        const int32_t* block_table, int32_t max_pages, const int32_t* ctx,
                        int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page,
-                       int32_t num_splits, float sm_scale, skv_dtype dtype, float* o_pre,
-                       float* s_pre, float* o_part, float* lse_part, void* out, float* lse_out,
-                       void* workspace, size_t workspace_bytes, skv_stream_t stream) {
+                       int32_t num_splits, const VarlenPlan* vl, float sm_scale,
+                       skv_dtype dtype, float* o_pre, float* s_pre, float* o_part,
+                       float* lse_part, void* out, float* lse_out, void* workspace,
+                       size_t workspace_bytes, skv_stream_t stream) {
     if (B < 0 || Hq < 1 || Hkv < 1 || D < 1 || page < 1 || num_splits < 1 || max_pages < 1 ||
         num_pool_pages < 1 || !valid_dtype(dtype))
         return SKV_ERR_INVALID_ARG;
@@ -382,9 +506,11 @@ skv_status cascade_run(const void* q, const void* k_cache, const void* v_cache,
     if ((o_pre && !aligned16(o_pre)) || (s_pre && !aligned4(s_pre)) ||
         (lse_out && !aligned4(lse_out)))
         return SKV_ERR_INVALID_ARG;
-    const DeviceInfo* dev = nullptr;
-    skv_status st = current_device(&dev);
+    skv_status st = check_varlen(vl, B);
     if (st != SKV_OK) return st;
+    if (vl && (int64_t)vl->num_units * Hkv > INT32_MAX) return SKV_ERR_UNSUPPORTED;
+    const DeviceInfo* dev = nullptr;
+    if ((st = current_device(&dev)) != SKV_OK) return st;
     std::vector<LevelPlan> plan;
     int slots = 0;
     if ((st = cascade_plan(levels, Hq, Hkv, dev->sm_count, &plan, &slots)) != SKV_OK) return st;
@@ -467,6 +593,7 @@ skv_status cascade_run(const void* q, const void* k_cache, const void* v_cache,
     a.ranges_dbg = nullptr;
     a.bf16 = dtype == SKV_BF16;
     a.done_ctr = launched > 0 ? done_ctr : nullptr;  // chained after the prefix passes
+    apply_varlen(vl, &a);
     if (launch_splitkv_decode(a, *dev, cs) != cudaSuccess) return SKV_ERR_CUDA;
     // 3. Prefix chunks of every level -> prefix state; merge_state(prefix,
     // suffix) -> out.
@@ -475,6 +602,8 @@ skv_status cascade_run(const void* q, const void* k_cache, const void* v_cache,
     c.lse_part = lse_part;
     c.rows = (int64_t)rows;
     c.NS = num_splits;
+    c.seq_splits = varlen_counts(vl);
+    c.Hq = Hq;
     c.D = D;
     c.out = out;
     c.out_dt = dtype;
@@ -522,9 +651,32 @@ skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_
     if (prefix_len < 0) return SKV_ERR_INVALID_ARG;
     if (prefix_len > 0 && (!prefix_pages || !aligned4(prefix_pages))) return SKV_ERR_INVALID_ARG;
     return cascade_run(q, k_cache, v_cache, num_pool_pages, two_level(B, prefix_pages, prefix_len),
-                       block_table, max_pages, ctx, B, Hq, Hkv, D, page, num_splits, sm_scale, dtype,
-                       o_pre, s_pre, o_part, lse_part, out, lse_out, workspace, workspace_bytes,
-                       stream);
+                       block_table, max_pages, ctx, B, Hq, Hkv, D, page, num_splits, nullptr,
+                       sm_scale, dtype, o_pre, s_pre, o_part, lse_part, out, lse_out, workspace,
+                       workspace_bytes, stream);
+}
+
+skv_status skv_cascade_decode_varlen(const void* q, const void* k_cache, const void* v_cache,
+                                     int32_t num_pool_pages, const int32_t* prefix_pages,
+                                     int32_t prefix_len, const int32_t* block_table,
+                                     int32_t max_pages, const int32_t* ctx, int32_t B,
+                                     int32_t Hq, int32_t Hkv, int32_t D, int32_t page,
+                                     int32_t max_splits, const int32_t* plan,
+                                     int32_t num_units, int32_t max_split_pages,
+                                     float sm_scale, skv_dtype dtype, float* o_pre,
+                                     float* s_pre, float* o_part, float* lse_part, void* out,
+                                     float* lse_out, void* workspace, size_t workspace_bytes,
+                                     skv_stream_t stream) {
+    if (prefix_len < 0) return SKV_ERR_INVALID_ARG;
+    if (prefix_len > 0 && (!prefix_pages || !aligned4(prefix_pages))) return SKV_ERR_INVALID_ARG;
+    VarlenPlan vl;
+    vl.plan = plan;
+    vl.num_units = num_units;
+    vl.max_split_pages = max_split_pages;
+    return cascade_run(q, k_cache, v_cache, num_pool_pages, two_level(B, prefix_pages, prefix_len),
+                       block_table, max_pages, ctx, B, Hq, Hkv, D, page, max_splits, &vl,
+                       sm_scale, dtype, o_pre, s_pre, o_part, lse_part, out, lse_out, workspace,
+                       workspace_bytes, stream);
 }
 
 size_t skv_cascade_multilevel_workspace_size(int32_t num_levels, const skv_cascade_level* levels,
@@ -553,8 +705,8 @@ skv_status skv_cascade_decode_multilevel(const void* q, const void* k_cache, con
     skv_status st = read_levels(num_levels, levels, B, &lv);
     if (st != SKV_OK) return st;
     return cascade_run(q, k_cache, v_cache, num_pool_pages, lv, block_table, max_pages, ctx, B, Hq,
-                       Hkv, D, page, num_splits, sm_scale, dtype, o_pre, s_pre, o_part, lse_part,
-                       out, lse_out, workspace, workspace_bytes, stream);
+                       Hkv, D, page, num_splits, nullptr, sm_scale, dtype, o_pre, s_pre, o_part,
+                       lse_part, out, lse_out, workspace, workspace_bytes, stream);
 }
 
 skv_status skv_get_device_error(int32_t* code, int32_t* detail) {

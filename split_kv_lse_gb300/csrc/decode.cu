@@ -60,7 +60,8 @@ struct DecodeParams {
     int32_t* ranges_dbg;
     unsigned long long* err;
     unsigned int* done_ctr;  // cascade chaining (DecodeArgs::done_ctr) or nullptr
-    int32_t num_pool_pages, max_pages, Hq, Hkv, NS;
+    const int2* units;       // per-sequence split counts: the (sequence, split) list, or nullptr
+    int32_t num_pool_pages, max_pages, B, Hq, Hkv, NS;  // NS: split-axis length of o_part
     float scale_log2;  // sm_scale * log2(e)
 };
 
@@ -183,7 +184,28 @@ splitkv_decode_kernel(const DecodeParams p) {
     int* dyn_next = dyn_ids + kDynMaxPages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
+    // Uniform splits: CTA (split, hkv, b).  Per-sequence splits: CTA u*Hkv +
+    // hkv takes unit u of the list, sequence b's split `split` of ns.
+    int split, hkv, b, ns;
+    if (p.units != nullptr) {
+        const int u = blockIdx.x / p.Hkv;
+        hkv = blockIdx.x - u * p.Hkv;
+        const int2 wi = __ldg(p.units + u);
+        b = wi.x;
+        split = wi.y & 0xffff;
+        ns = wi.y >> 16;
+        if (b < 0 || b >= p.B || ns < 1 || ns > p.NS || split >= ns) {
+            if (threadIdx.x == 0 && hkv == 0) record_error(p.err, SKV_ERR_INVALID_ARG, 2 << 20 | u);
+            pdl_launch_dependents();
+            last_cta_waits_primary(p.done_ctr);
+            return;
+        }
+    } else {
+        split = blockIdx.x;
+        hkv = blockIdx.y;
+        b = blockIdx.z;
+        ns = p.NS;
+    }
 
     // The combine grid may be scheduled now; it waits for this grid to finish.
     pdl_launch_dependents();
@@ -196,7 +218,7 @@ splitkv_decode_kernel(const DecodeParams p) {
     // otherwise the ids of a full table's split are, and reloaded if ctx
     // turns out shorter.
     const int32_t* bt = p.block_table + (int64_t)b * p.max_pages;
-    const int pps_max = (p.max_pages + p.NS - 1) / p.NS;
+    const int pps_max = (p.max_pages + ns - 1) / ns;
     const int ulo = split, uhi = min((split + 1) * pps_max, p.max_pages);
     const bool spec_union = uhi - ulo <= 32 * kSpecRegs;
     int spec[kSpecRegs];
@@ -220,12 +242,22 @@ splitkv_decode_kernel(const DecodeParams p) {
         ctx = ctx < 0 ? 0 : cap;
     }
     int p0, p1;
-    split_page_range(ctx, kPage, p.NS, split, &p0, &p1);
+    split_page_range(ctx, kPage, ns, split, &p0, &p1);
     if (p.ranges_dbg != nullptr && hkv == 0 && threadIdx.x == 0) {
         p.ranges_dbg[((int64_t)b * p.NS + split) * 2 + 0] = p0;
         p.ranges_dbg[((int64_t)b * p.NS + split) * 2 + 1] = p1;
     }
-    const int npages = p1 > p0 ? p1 - p0 : 0;
+    int npages = p1 > p0 ? p1 - p0 : 0;
+    if constexpr (DYN) {
+        // The shape was chosen for splits of at most kDynMaxPages pages; a
+        // longer one (a split list planned for shorter contexts than ctx
+        // holds) is flagged and cut, so no page id is read past the
+        // shared-memory list.
+        if (npages > kDynMaxPages) {
+            if (threadIdx.x == 0) record_error(p.err, SKV_ERR_INVALID_ARG, 3 << 20 | b);
+            npages = kDynMaxPages;
+        }
+    }
     const int nw = npages > warp ? (npages - warp + W - 1) / W : 0;  // this warp's pages
 
     if constexpr (DYN) {
@@ -581,7 +613,7 @@ splitkv_decode_kernel(const DecodeParams p) {
 }
 
 template <int G, int W, int R, bool BF, bool DYN = false>
-cudaError_t launch_gwr(const DecodeParams& p, int B, int Hkv, int NS,
+cudaError_t launch_gwr(const DecodeParams& p, int B, int Hkv, int NS, int num_units,
                        cudaStream_t st) {
     constexpr size_t smem = smem_bytes<G, W, R, DYN>();
     auto kern = splitkv_decode_kernel<G, W, R, BF, DYN>;
@@ -594,7 +626,8 @@ cudaError_t launch_gwr(const DecodeParams& p, int B, int Hkv, int NS,
         attr_set[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(NS, Hkv, B);
+    cfg.gridDim = p.units != nullptr ? dim3((unsigned)num_units * (unsigned)Hkv, 1, 1)
+                                     : dim3(NS, Hkv, B);
     cfg.blockDim = dim3(W * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -611,8 +644,8 @@ cudaError_t launch_gwr(const DecodeParams& p, int B, int Hkv, int NS,
 // short splits smaller CTAs, so that many more of them are resident per SM
 // and their fixed latencies (q, page table, first copies) overlap.
 template <int G, bool BF>
-cudaError_t launch_g(const DecodeParams& p, int B, int Hkv, int NS,
-                     int max_pages, cudaStream_t st) {
+cudaError_t launch_g(const DecodeParams& p, int B, int Hkv, int NS, int num_units,
+                     int pps, cudaStream_t st) {
     // Measured on the cascade suffixes (<= 8 pages per split, B=64, NS=16):
     // pass 1 takes 53 us with 1 warp and a 2-page ring (about 13 CTAs per
     // SM), 64 us with 2 warps, 72 us with 3; a 4-page ring for the 1-warp
@@ -624,11 +657,10 @@ cudaError_t launch_g(const DecodeParams& p, int B, int Hkv, int NS,
     // from the split's counter (DYN), so that a warp whose copies land late
     // does not hold the split back while its neighbours idle (long context,
     // 32 pages: 30.5-30.9 -> 29.5-29.7 us for the decode).
-    const int pps = (max_pages + NS - 1) / NS;
-    if (pps <= 8) return launch_gwr<G, 1, 2, BF>(p, B, Hkv, NS, st);
-    if (pps <= 16) return launch_gwr<G, 2, 4, BF, true>(p, B, Hkv, NS, st);
-    if (pps <= kDynMaxPages) return launch_gwr<G, 3, 6, BF, true>(p, B, Hkv, NS, st);
-    return launch_gwr<G, 3, 6, BF>(p, B, Hkv, NS, st);
+    if (pps <= 8) return launch_gwr<G, 1, 2, BF>(p, B, Hkv, NS, num_units, st);
+    if (pps <= 16) return launch_gwr<G, 2, 4, BF, true>(p, B, Hkv, NS, num_units, st);
+    if (pps <= kDynMaxPages) return launch_gwr<G, 3, 6, BF, true>(p, B, Hkv, NS, num_units, st);
+    return launch_gwr<G, 3, 6, BF>(p, B, Hkv, NS, num_units, st);
 }
 
 // ---------------------------------------------------------------- combine (pass 2)
@@ -646,6 +678,8 @@ constexpr int kCombBatch = 16;
 struct CombineParams {
     const float* o_part;   // [rows, NS, D]
     const float* lse_part; // [rows, NS]
+    const int32_t* seq_splits;  // [rows / Hq] states per row, or nullptr (NS each)
+    unsigned long long* err;
     void* out;             // [rows, D] Tout
     float* lse_out;        // [rows] or nullptr
     const float* pre_part; // [rows, C, D] prefix-chunk states or nullptr
@@ -653,34 +687,47 @@ struct CombineParams {
     float* o_pre;          // [rows, D] merged prefix state or nullptr
     float* s_pre;          // [rows]
     int64_t rows;
-    int NS, C, D;
+    int NS, C, D, Hq;
 };
+
+// States of `row` (at most NS): its sequence's split count with per-sequence
+// splits (a count outside [1, NS] is flagged and clamped), else NS.
+SKV_DEVINL int row_splits(const CombineParams& p, int64_t row) {
+    if (p.seq_splits == nullptr) return p.NS;
+    const int n = __ldg(p.seq_splits + row / p.Hq);
+    if (n < 1 || n > p.NS) {
+        if ((threadIdx.x & 31) == 0) record_error(p.err, SKV_ERR_INVALID_ARG, 4 << 20 | (int)(row / p.Hq));
+        return n < 1 ? 1 : p.NS;
+    }
+    return n;
+}
 
 struct WarpState {
     float m, W;
     float4 acc;
 };
 
-// This warp's share (states sub, sub + WPR, ...) of the N states of `row`.
+// This warp's share (states sub, sub + WPR, ...) of the first N of the
+// `stride` states of `row`.
 // Per batch of kCombBatch states: lane k (and lane k + 16) reads state k's
 // lse and computes its weight, the batch max and weight sum go through
 // shuffles, and every lane then accumulates its 4 dims of the batch's v rows
 // with the weights broadcast from their lanes.
 template <int WPR, int BATCH = kCombBatch>
-SKV_DEVINL WarpState warp_merge(const float* o, const float* lse, int N, int D, int64_t row,
-                                int sub) {
+SKV_DEVINL WarpState warp_merge(const float* o, const float* lse, int stride, int N, int D,
+                                int64_t row, int sub) {
     static_assert(BATCH == 8 || BATCH == 16, "lanes k, k + BATCH, ... read state k of a batch");
     const int lane = threadIdx.x & 31;
     const bool has = 4 * lane < D;
     WarpState st{-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
     for (int n0 = sub; n0 < N; n0 += WPR * BATCH) {
         const int nk = n0 + (lane & (BATCH - 1)) * WPR;
-        const float lk = nk < N ? sanitize_lse(__ldcg(lse + row * N + nk)) : -INFINITY;
+        const float lk = nk < N ? sanitize_lse(__ldcg(lse + row * stride + nk)) : -INFINITY;
         float4 x[BATCH];
 #pragma unroll
         for (int k = 0; k < BATCH; ++k) {
             const int n = n0 + k * WPR;
-            x[k] = (n < N && has) ? __ldcg(reinterpret_cast<const float4*>(o + (row * N + n) * D) + lane)
+            x[k] = (n < N && has) ? __ldcg(reinterpret_cast<const float4*>(o + (row * stride + n) * D) + lane)
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         float mb = lk;
@@ -712,12 +759,13 @@ struct CombSmem {
     __align__(16) float wacc[kCombWarps][kD];
 };
 
-// Merged state of `row` over N states: v (this lane's 4 dims) and s.  With
-// WPR > 1 every thread of the CTA must call this (block barriers).
+// Merged state of `row` over the first N of its `stride` states: v (this
+// lane's 4 dims) and s.  With WPR > 1 every thread of the CTA must call this
+// (block barriers).
 template <int WPR, int BATCH = kCombBatch>
-SKV_DEVINL void merge_row(const float* o, const float* lse, int N, int D, int64_t row, int sub,
-                          CombSmem& sm, float (&v)[4], float& s_out) {
-    WarpState st = warp_merge<WPR, BATCH>(o, lse, N, D, row, sub);
+SKV_DEVINL void merge_row(const float* o, const float* lse, int stride, int N, int D,
+                          int64_t row, int sub, CombSmem& sm, float (&v)[4], float& s_out) {
+    WarpState st = warp_merge<WPR, BATCH>(o, lse, stride, N, D, row, sub);
     if constexpr (WPR > 1) {
         const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
         __syncthreads();  // the buffers may still be read from a previous merge
@@ -764,10 +812,10 @@ combine_kernel(const CombineParams p) {
     const int sub = w % WPR;
     const bool has = 4 * lane < p.D;
     float vd[4], sd;
-    merge_row<WPR>(p.o_part, p.lse_part, p.NS, p.D, row, sub, sm, vd, sd);
+    merge_row<WPR>(p.o_part, p.lse_part, p.NS, row_splits(p, row), p.D, row, sub, sm, vd, sd);
     if (p.pre_part != nullptr) {
         float vp[4] = {0.f, 0.f, 0.f, 0.f}, sp = -INFINITY;  // empty prefix when C == 0
-        if (p.C > 0) merge_row<WPR>(p.pre_part, p.pre_lse, p.C, p.D, row, sub, sm, vp, sp);
+        if (p.C > 0) merge_row<WPR>(p.pre_part, p.pre_lse, p.C, p.C, p.D, row, sub, sm, vp, sp);
         if (sub == 0 && row_ok) {
             if (p.o_pre != nullptr && has)
                 *reinterpret_cast<float4*>(p.o_pre + row * p.D + 4 * lane) =
@@ -831,9 +879,11 @@ cascade_combine_kernel(const CombineParams p) {
     const bool has = 4 * lane < p.D;
     float v[4] = {0.f, 0.f, 0.f, 0.f}, s = -INFINITY;
     if (sub == 0) {
-        merge_row<1, kCascadeBatch>(p.o_part, p.lse_part, p.NS, p.D, row, 0, sm, v, s);
+        merge_row<1, kCascadeBatch>(p.o_part, p.lse_part, p.NS, row_splits(p, row), p.D, row, 0,
+                                    sm, v, s);
     } else {
-        if (p.C > 0) merge_row<1, kCascadeBatch>(p.pre_part, p.pre_lse, p.C, p.D, row, 0, sm, v, s);
+        if (p.C > 0)
+            merge_row<1, kCascadeBatch>(p.pre_part, p.pre_lse, p.C, p.C, p.D, row, 0, sm, v, s);
         if (row_ok) {
             if (p.o_pre != nullptr && has)
                 *reinterpret_cast<float4*>(p.o_pre + row * p.D + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
@@ -893,18 +943,25 @@ cudaError_t launch_splitkv_decode(const DecodeArgs& a, const DeviceInfo& dev, cu
     p.ranges_dbg = a.ranges_dbg;
     p.err = dev.err;
     p.done_ctr = a.done_ctr;
+    p.units = reinterpret_cast<const int2*>(a.units);
     p.num_pool_pages = a.num_pool_pages;
     p.max_pages = a.max_pages;
+    p.B = a.B;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
     p.NS = a.num_splits;
     p.scale_log2 = a.sm_scale * 1.4426950408889634f;
+    // The CTA shape follows the longest split: the page table's width over
+    // the split count, or the longest split of the per-sequence list.
+    if (a.units != nullptr && a.num_units < 1) return cudaErrorInvalidValue;
+    const int pps = a.units != nullptr ? a.max_split_pages
+                                       : (a.max_pages + a.num_splits - 1) / a.num_splits;
 #define SKV_LAUNCH_G(BF_)                                                             \
     switch (a.Hq / a.Hkv) {                                                           \
-        case 1: return launch_g<1, BF_>(p, a.B, a.Hkv, a.num_splits, a.max_pages, st); \
-        case 2: return launch_g<2, BF_>(p, a.B, a.Hkv, a.num_splits, a.max_pages, st); \
-        case 4: return launch_g<4, BF_>(p, a.B, a.Hkv, a.num_splits, a.max_pages, st); \
-        case 8: return launch_g<8, BF_>(p, a.B, a.Hkv, a.num_splits, a.max_pages, st); \
+        case 1: return launch_g<1, BF_>(p, a.B, a.Hkv, a.num_splits, a.num_units, pps, st); \
+        case 2: return launch_g<2, BF_>(p, a.B, a.Hkv, a.num_splits, a.num_units, pps, st); \
+        case 4: return launch_g<4, BF_>(p, a.B, a.Hkv, a.num_splits, a.num_units, pps, st); \
+        case 8: return launch_g<8, BF_>(p, a.B, a.Hkv, a.num_splits, a.num_units, pps, st); \
     }
     if (a.bf16) SKV_LAUNCH_G(true) else SKV_LAUNCH_G(false)
 #undef SKV_LAUNCH_G
@@ -920,6 +977,9 @@ cudaError_t launch_combine(const CombineArgs& a, bool pdl, const DeviceInfo& dev
     CombineParams p;
     p.o_part = a.o_part;
     p.lse_part = a.lse_part;
+    p.seq_splits = a.seq_splits;
+    p.err = dev.err;
+    p.Hq = a.Hq > 0 ? a.Hq : 1;
     p.out = a.out;
     p.lse_out = a.lse_out;
     p.pre_part = a.pre_part;

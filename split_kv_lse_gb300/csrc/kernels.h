@@ -53,7 +53,11 @@ struct CombineArgs {
     const float* o_part;
     const float* lse_part;
     int64_t rows;
-    int NS;
+    int NS;  // split-axis length of o_part / lse_part
+    // Per-sequence split counts ([B], row r reads seq_splits[r / Hq] states)
+    // or nullptr (every row reads NS states).
+    const int32_t* seq_splits;
+    int Hq;
     int64_t D;
     void* out;
     skv_dtype out_dt;
@@ -81,6 +85,14 @@ struct DecodeArgs {
     float* lse_part;
     int32_t* ranges_dbg;
     bool bf16;  // q, K, V are bf16 (else fp16)
+    // Per-sequence split counts: `units` lists num_units (sequence, split)
+    // pairs as int32 [b, split | splits_b << 16], one CTA per pair and kv
+    // head, and num_splits is then the split-axis length of o_part;
+    // max_split_pages is the longest split of the list (sets the CTA shape).
+    // units == nullptr: every sequence has num_splits splits.
+    const int32_t* units = nullptr;
+    int32_t num_units = 0;
+    int32_t max_split_pages = 0;
     // Cascade chaining (programmatic dependent launch): when set, the pass
     // is launched as a dependent of the preceding shared-prefix pass in the
     // same stream, so that the two run side by side, and the pass's last CTA

@@ -257,3 +257,56 @@ def test_noalloc_scratch_fits_every_shape_on_gb300(lib):
     big = 300
     assert f(2 * big - 1, 1024, 1, 256, F16, big) > cap
     assert f(0, 4, 4, 64, 0, sm) == 0 and f(4, 4, 4, 3, 0, sm) == 0   # invalid sizes
+
+
+def _plan_varlen(ctx, page, max_splits, pps):
+    import split_kv_lse_gb300 as m
+    return m.splitkv_plan_varlen(ctx, page, max_splits, pps)
+
+
+def test_plan_varlen_matches_oracle_and_lists_every_split(lib, orc):
+    """skv_splitkv_plan_varlen: the split counts bit-exact against the
+    oracle's per-sequence reading ([L3] §⑥); the work list holds every
+    (sequence, split < ns_b) exactly once, longest splits first, each unit
+    carrying its sequence's count; max_split_pages is the longest split."""
+    import numpy as np
+    rng = np.random.default_rng(5)
+    cases = [([0, 1, 128, 129, 1000, 2048, 4096], 16, 16, 8), ([37], 16, 4, 1),
+             ([0, 0], 16, 3, 2), ([32768], 16, 64, 8)]
+    for _ in range(200):
+        B = int(rng.integers(1, 70))
+        cases.append(([int(x) for x in rng.integers(0, 5000, B)], 16,
+                      int(rng.integers(1, 257)), int(rng.integers(1, 20))))
+    for ctx, page, ms, pps in cases:
+        plan = _plan_varlen(ctx, page, ms, pps)
+        ns = plan.num_splits.numpy()
+        assert np.array_equal(ns, orc.plan_varlen(ctx, page, ms, pps)), (ctx, ms, pps)
+        assert plan.num_units == int(ns.sum())
+        units = plan.host[:2 * plan.num_units].view(-1, 2).numpy()
+        b, word = units[:, 0], units[:, 1]
+        split, cnt = word & 0xFFFF, word >> 16
+        assert np.array_equal(cnt, ns[b])
+        assert sorted(zip(b.tolist(), split.tolist())) == [
+            (i, s) for i in range(len(ctx)) for s in range(int(ns[i]))]
+        pages = []
+        for bi, sp in zip(b.tolist(), split.tolist()):
+            a, e = orc.split_range(ctx[bi], page, int(ns[bi]), sp)
+            pages.append(max(0, e - a))
+        assert pages == sorted(pages, reverse=True)
+        assert plan.max_split_pages == max(pages)
+
+
+def test_plan_varlen_argument_checks(lib):
+    f = lib.skv_splitkv_plan_varlen
+    c = ctypes.c_int32
+    ctx = (c * 2)(10, 20)
+    buf = (c * 64)()
+    nu, mp = c(), c()
+    ok = f(2, ctx, 16, 4, 8, buf, 64, ctypes.byref(nu), ctypes.byref(mp))
+    assert ok == 0 and nu.value == 2 and mp.value == 2
+    assert f(2, ctx, 16, 0, 8, buf, 64, ctypes.byref(nu), ctypes.byref(mp)) == 1    # max_splits 0
+    assert f(2, ctx, 16, 257, 8, buf, 64, ctypes.byref(nu), ctypes.byref(mp)) == 1  # > 256
+    assert f(2, ctx, 16, 4, 0, buf, 64, ctypes.byref(nu), ctypes.byref(mp)) == 1    # pps 0
+    assert f(2, ctx, 16, 4, 8, buf, 5, ctypes.byref(nu), ctypes.byref(mp)) == 1     # too small
+    neg = (c * 2)(10, -1)
+    assert f(2, neg, 16, 4, 8, buf, 64, ctypes.byref(nu), ctypes.byref(mp)) == 1

@@ -277,3 +277,63 @@ def test_cascade_bad_prefix_page_id_is_flagged_not_faulted(lib):
     assert lib.get_device_error() == (0, 0)
     # The next call on clean inputs is correct.
     run_and_check(lib, W.cascade_inputs(4, 16, 4, 128, 16, 300, [20, 1, 0, 77], seed=63), 4)
+
+
+# ---------------------------------------------------------------- per-sequence split counts
+def run_and_check_varlen(lib, d, max_splits, pps, poison=True):
+    """skv_cascade_decode_varlen: prefix state, the written suffix split
+    states (per-sequence counts) and the merged output against the oracle."""
+    if poison:
+        poison_unused(d)
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    pp = g["prefix_pages"] if g["prefix_pages"].numel() else torch.zeros(1, dtype=torch.int32,
+                                                                       device=DEV)
+    plan = lib.splitkv_plan_varlen(d["ctx"], 16, max_splits, pps)
+    ns = plan.num_splits.numpy()
+    out, lse, o_pre, s_pre, o_part, lse_part = lib.cascade_decode_varlen(
+        g["q"], g["k_cache"], g["v_cache"], pp, d["prefix_len"], g["block_table"], g["ctx"],
+        plan, d["sm_scale"])
+    torch.cuda.synchronize()
+    assert lib.get_device_error() == (0, 0)
+    o_r, s_r, op_r, sp_r = oracle.cascade(d["q"], d["k_cache"], d["v_cache"], d["prefix_pages"],
+                                          d["prefix_len"], d["block_table"], d["ctx"],
+                                          d["sm_scale"])
+    atol, rtol_part, rtol_out = DEC_O_TOL[d["q"].dtype]
+    assert_s_close(s_pre, sp_r, DEC_LSE_ATOL, "s_pre")
+    assert_v_close(o_pre, op_r, atol, rtol_part, "o_pre", empty_rows=(sp_r == -math.inf))
+    opr, lpr = oracle.attend_splits_varlen(d["q"], d["k_cache"], d["v_cache"], d["block_table"],
+                                           d["ctx"], d["sm_scale"], ns, max_splits)
+    B, Hq = d["q"].shape[:2]
+    w = np.broadcast_to((np.arange(max_splits)[None, :] < ns[:, None])[:, None, :],
+                        (B, Hq, max_splits))
+    lp = lse_part.cpu().double().numpy()
+    assert_s_close(lp[w], lpr[w], DEC_LSE_ATOL, "lse_part")
+    assert_v_close(o_part.cpu().double().numpy()[w], opr[w], atol, rtol_part, "o_part",
+                   empty_rows=(lpr[w] == -math.inf))
+    assert_s_close(lse, s_r, DEC_LSE_ATOL, "lse_out")
+    assert_v_close(out, o_r, atol, rtol_out, "out", empty_rows=(s_r == -math.inf))
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+def test_cascade_varlen_small(lib, G):
+    """Per-sequence suffix splits ([L3] §⑥ F1) under a 777-token shared prefix,
+    ragged suffixes including empty ones."""
+    B = (160 + G - 1) // G
+    ctx = [int(x) for x in np.random.default_rng(50 + G).integers(0, 700, B)]
+    ctx[0], ctx[1] = 0, 1
+    d = W.cascade_inputs(B, 2 * G, 2, 128, 16, 777, ctx, seed=50 + G)
+    run_and_check_varlen(lib, d, 16, 8)
+
+
+def test_cascade_varlen_full_workload(lib):
+    """The B=64 cascade workload (8192 shared tokens, suffixes of 1..2048
+    tokens) with at most 16 suffix splits of at most 8 pages each."""
+    d = W.cascade_mixed()
+    run_and_check_varlen(lib, d, 16, 8, poison=False)
+
+
+def test_cascade_varlen_bf16(lib):
+    B = 40
+    ctx = [int(x) for x in np.random.default_rng(60).integers(0, 900, B)]
+    d = W.cascade_inputs(B, 8, 2, 128, 16, 300, ctx, seed=60, dtype=torch.bfloat16)
+    run_and_check_varlen(lib, d, 8, 4)

@@ -25,7 +25,7 @@ def lib():
     return skv()
 
 
-def run_decode(lib, d, ns, nan_tail=False):
+def to_dev(d, nan_tail=False):
     g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
     if nan_tail:
         # Poison every cache slot past each sequence's end (inside its last
@@ -43,6 +43,11 @@ def run_decode(lib, d, ns, nan_tail=False):
             if pid not in used:
                 kc[pid] = float("nan")
                 vc[pid] = float("nan")
+    return g
+
+
+def run_decode(lib, d, ns, nan_tail=False):
+    g = to_dev(d, nan_tail)
     B = d["q"].shape[0]
     rd = torch.full((B, ns, 2), -7, dtype=torch.int32, device=DEV)
     out, lse, o_part, lse_part = lib.splitkv_decode(
@@ -223,4 +228,94 @@ def test_bounded_wait_gives_up_and_reports(lib, mode, detail):
     assert lib.poll_device_error() == (0, 0)
     d = W.decode_inputs(2, 8, 2, 128, 16, [100, 37], seed=14)
     check_decode(lib, d, 4)
+    assert lib.get_device_error() == (0, 0)
+
+
+# ---------------------------------------------------------------- per-sequence split counts
+def check_decode_varlen(lib, d, max_splits, pps, nan_tail=False):
+    """skv_splitkv_decode_varlen against the oracle's per-sequence split
+    states (the written slots), the unsplit attention (merged output) and the
+    per-sequence page ranges (bit-exact; unwritten slots keep their fill)."""
+    g = to_dev(d, nan_tail)
+    B, Hq = d["q"].shape[:2]
+    plan = lib.splitkv_plan_varlen(d["ctx"], 16, max_splits, pps)
+    ns = plan.num_splits.numpy()
+    assert np.array_equal(ns, oracle.plan_varlen(d["ctx"], 16, max_splits, pps))
+    rd = torch.full((B, max_splits, 2), -7, dtype=torch.int32, device=DEV)
+    op = torch.full((B, Hq, max_splits, 128), 5.0, device=DEV)
+    out, lse, o_part, lse_part = lib.splitkv_decode_varlen(
+        g["q"], g["k_cache"], g["v_cache"], g["block_table"], g["ctx"], plan, d["sm_scale"],
+        o_part=op, ranges_dbg=rd)
+    torch.cuda.synchronize()
+    args = (d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["ctx"], d["sm_scale"])
+    op_r, lp_r = oracle.attend_splits_varlen(*args, ns, max_splits)
+    o_r, s_r = oracle.attend_full(*args)
+    atol, rtol_part, rtol_out = DEC_O_TOL[d["q"].dtype]
+    written = np.arange(max_splits)[None, :] < ns[:, None]            # [B, max_splits]
+    wmask = np.broadcast_to(written[:, None, :], (B, Hq, max_splits))
+    lp = np64(lse_part)
+    assert_s_close(lp[wmask], lp_r[wmask], DEC_LSE_ATOL, "lse_part")
+    assert_v_close(np64(o_part)[wmask], op_r[wmask], atol, rtol_part, "o_part",
+                   empty_rows=(lp_r[wmask] == -math.inf))
+    assert np.all(np64(o_part)[~wmask] == 5.0), "a slot past a sequence's split count was written"
+    assert_s_close(lse, s_r, DEC_LSE_ATOL, "lse_out")
+    assert_v_close(out, o_r, atol, rtol_out, "out", empty_rows=(s_r == -math.inf))
+    ranges = rd.cpu().numpy()
+    for b, c in enumerate(d["ctx"].tolist()):
+        for sp in range(max_splits):
+            want = oracle.split_range(int(c), 16, int(ns[b]), sp) if sp < ns[b] else (-7, -7)
+            assert tuple(ranges[b, sp]) == want, (b, sp)
+    return plan
+
+
+VARLEN_CTX = [0, 1, 15, 16, 17, 100, 129, 1000, 2500, 4096]
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("max_splits,pps", [(16, 8), (4, 2), (64, 1), (2, 64)])
+def test_decode_varlen_ragged(lib, G, max_splits, pps):
+    """Per-sequence split counts ([L3] §⑥ F1) on a ragged batch: ctx 0..4096
+    with NaN in every slot that must not be read.  The four plans give splits
+    of at most 16, 64, 4 and 128 pages (each CTA shape of pass 1)."""
+    Hkv = 2
+    d = W.decode_inputs(len(VARLEN_CTX), Hkv * G, Hkv, 128, 16, VARLEN_CTX,
+                        seed=400 + G + max_splits + pps, pool_extra=3)
+    plan = check_decode_varlen(lib, d, max_splits, pps, nan_tail=True)
+    assert plan.max_split_pages == {(16, 8): 16, (4, 2): 64, (64, 1): 4, (2, 64): 128}[
+        (max_splits, pps)]
+
+
+def test_decode_varlen_cascade_suffix_mix(lib):
+    """The cascade workload's suffixes (B=64, Hq=32, Hkv=8, 1..2048 tokens) with
+    at most 16 splits of at most 8 pages each: every written partial, range
+    and output at full size."""
+    d5 = W.cascade_mixed()
+    ctx = d5["ctx"].tolist()
+    d = W.decode_inputs(64, 32, 8, 128, 16, ctx, seed=41)
+    check_decode_varlen(lib, d, 16, 8)
+
+
+@pytest.mark.parametrize("G", [1, 8])
+def test_decode_varlen_bf16(lib, G):
+    d = W.decode_inputs(len(VARLEN_CTX), 2 * G, 2, 128, 16, VARLEN_CTX, seed=430 + G,
+                        dtype=torch.bfloat16, pool_extra=2)
+    check_decode_varlen(lib, d, 16, 8, nan_tail=True)
+
+
+def test_decode_varlen_plan_for_shorter_contexts_is_flagged(lib):
+    """A plan made for 200 tokens (one split of 13 pages: the two-warp CTA
+    shape, which holds at most 64 page ids) run on a 2000-token context: the
+    125-page split is flagged in the error word and cut, nothing faults, and
+    the GPU goes on working."""
+    lib.get_device_error()
+    plan = lib.splitkv_plan_varlen([200], 16, 16, 16)
+    assert plan.max_split_pages == 13
+    d = W.decode_inputs(1, 8, 2, 128, 16, [2000], seed=44)
+    g = to_dev(d)
+    lib.splitkv_decode_varlen(g["q"], g["k_cache"], g["v_cache"], g["block_table"], g["ctx"],
+                              plan, d["sm_scale"])
+    code, detail = lib.get_device_error()
+    assert code == 1 and detail == (3 << 20)
+    d2 = W.decode_inputs(2, 8, 2, 128, 16, [100, 37], seed=45)
+    check_decode_varlen(lib, d2, 4, 2)
     assert lib.get_device_error() == (0, 0)
