@@ -528,15 +528,17 @@ size_t merge_states_ws_upper_bound(int64_t rows, int64_t N, int64_t D) {
 }
 
 MergeStatesPlan plan_merge_states(int64_t rows, int64_t N, int64_t D, int chunks, int sm_count,
-                                  size_t ws_available) {
+                                  size_t ws_available, int ctas_per_sm) {
     (void)chunks;
     MergeStatesPlan pl;
     if (rows >= kTeamRows && N <= kBulkMaxN) {
         pl.team_kernel = true;
         return pl;
     }
-    // Enough CTAs to give every SM about two.
-    int64_t want = (2LL * sm_count + rows - 1) / (rows > 0 ? rows : 1);
+    // Enough CTAs to give every SM about ctas_per_sm: with few rows and many
+    // states, the loads in flight per SM (and so the stream rate) grow with
+    // the CTAs resident on it.
+    int64_t want = ((int64_t)ctas_per_sm * sm_count + rows - 1) / (rows > 0 ? rows : 1);
     int nsplit = (int)(want < 1 ? 1 : (want > max_split_for(N) ? max_split_for(N) : want));
     if (nsplit > 1 && ws_bytes_for(rows, nsplit, D) > ws_available) nsplit = 1;
     pl.nsplit = nsplit;
@@ -567,10 +569,12 @@ cudaError_t launch_rows(const T* v, const float* s, T* vo, float* so, int64_t ro
 
 cudaError_t launch_merge_states(const void* v, const float* s, void* vo, float* so, int64_t S,
                                 int64_t N, int64_t H, int64_t D, skv_dtype dt, void* ws,
-                                size_t ws_bytes, const DeviceInfo& dev, cudaStream_t st) {
+                                size_t ws_bytes, int ctas_per_sm, const DeviceInfo& dev,
+                                cudaStream_t st) {
     const int64_t rows = S * H;
     const int chunks = (int)(D * (int64_t)dtype_size(dt) / 16);
-    const MergeStatesPlan pl = plan_merge_states(rows, N, D, chunks, dev.sm_count, ws ? ws_bytes : 0);
+    const MergeStatesPlan pl =
+        plan_merge_states(rows, N, D, chunks, dev.sm_count, ws ? ws_bytes : 0, ctas_per_sm);
     if (pl.team_kernel) {
         const int row_bytes = chunks * 16;
         const size_t smem = rows_smem_bytes(row_bytes, (int)N);

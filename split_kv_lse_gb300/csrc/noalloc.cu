@@ -60,7 +60,8 @@ extern "C" size_t skv_merge_states_noalloc_scratch_size(int64_t S, int64_t N, in
         if (current_device(&dev) != SKV_OK) return 0;
         sm_count = dev->sm_count;
     }
-    return plan_merge_states(S * H, N, D, (int)(row_bytes / 16), sm_count, SIZE_MAX).ws_bytes;
+    return plan_merge_states(S * H, N, D, (int)(row_bytes / 16), sm_count, SIZE_MAX,
+                             kNoallocCtasPerSm).ws_bytes;
 }
 
 extern "C" skv_status skv_merge_states_noalloc(const void* v, const float* s, void* v_out,
@@ -83,7 +84,8 @@ extern "C" skv_status skv_merge_states_noalloc(const void* v, const float* s, vo
     // The scratch this call would use with no size limit; reject what does
     // not fit in the fixed array rather than silently taking another path.
     const int chunks = (int)(row_bytes / 16);
-    const MergeStatesPlan want = plan_merge_states(S * H, N, D, chunks, dev->sm_count, SIZE_MAX);
+    const MergeStatesPlan want =
+        plan_merge_states(S * H, N, D, chunks, dev->sm_count, SIZE_MAX, kNoallocCtasPerSm);
     if (want.ws_bytes > kScratchBytes) return SKV_ERR_UNSUPPORTED;
     void* scratch = nullptr;
     if ((st = scratch_address(dev->device, &scratch)) != SKV_OK) return st;
@@ -93,6 +95,6 @@ extern "C" skv_status skv_merge_states_noalloc(const void* v, const float* s, vo
     if (want.ws_bytes > 0 && cudaMemsetAsync(scratch, 0, want.ws_bytes, cs) != cudaSuccess)
         return SKV_ERR_CUDA;
     cudaError_t e = launch_merge_states(v, s, v_out, s_out, S, N, H, D, dtype, scratch,
-                                        kScratchBytes, *dev, cs);
+                                        kScratchBytes, kNoallocCtasPerSm, *dev, cs);
     return e == cudaSuccess ? SKV_OK : SKV_ERR_CUDA;
 }
