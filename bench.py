@@ -695,6 +695,8 @@ def run_ours(args):
     if not args.no_e2e and only is None:
         # Same step through the public API with the inputs in pinned host memory.
         for d in host.values():
+            if not isinstance(d, dict):
+                continue
             for k, v in list(d.items()):
                 if isinstance(v, torch.Tensor):
                     d[k] = v.pin_memory()
