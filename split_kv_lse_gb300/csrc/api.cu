@@ -141,7 +141,7 @@ skv_status skv_merge_states(const void* v, const float* s, void* v_out, float* s
     const DeviceInfo* dev = nullptr;
     if ((st = current_device(&dev)) != SKV_OK) return st;
     return from_cuda(launch_merge_states(v, s, v_out, s_out, S, N, H, D, dtype, workspace,
-                                         workspace_bytes, kMergeCtasPerSm, *dev,
+                                         workspace_bytes, kMergeCtasPerSm, true, *dev,
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -29,24 +29,24 @@ cudaError_t launch_merge_state(const void* va, const float* sa, const void* vb, 
 // Which N-state merge path a call takes (host logic, shared with the
 // workspace-size query so the two always agree).
 struct MergeStatesPlan {
-    bool team_kernel = false;  // one lane team per row
+    bool team_kernel = false;  // warp-per-row bulk kernel (nsplit warps per row if > 1)
     int nsplit = 1;            // CTAs per row on the CTA path (>1 needs workspace)
     int per_split = 0;         // states per CTA on the CTA path
     size_t ws_bytes = 0;       // workspace the plan needs
 };
-// ctas_per_sm: CTAs the few-row path aims for per SM (the chunks of a row
-// spread over that many); the workspace path uses kMergeCtasPerSm, the
-// fixed-scratch entry point kNoallocCtasPerSm.
-constexpr int kMergeCtasPerSm = 8;
-constexpr int kNoallocCtasPerSm = 2;
+// ctas_per_sm: CTAs the one-CTA-per-row path aims for per SM (the chunks of
+// a row spread over that many).  allow_bulk_split: few rows with many states
+// may instead take the two-level warp-per-row path (bulk copies), given the
+// workspace; the fixed-scratch entry point keeps the CTA path.
+constexpr int kMergeCtasPerSm = 2;
 MergeStatesPlan plan_merge_states(int64_t rows, int64_t N, int64_t D, int chunks, int sm_count,
-                                  size_t ws_available, int ctas_per_sm);
+                                  size_t ws_available, int ctas_per_sm, bool allow_bulk_split);
 size_t merge_states_ws_upper_bound(int64_t rows, int64_t N, int64_t D);
 
 cudaError_t launch_merge_states(const void* v, const float* s, void* vo, float* so, int64_t S,
                                 int64_t N, int64_t H, int64_t D, skv_dtype dt, void* ws,
-                                size_t ws_bytes, int ctas_per_sm, const DeviceInfo& dev,
-                                cudaStream_t st);
+                                size_t ws_bytes, int ctas_per_sm, bool allow_bulk_split,
+                                const DeviceInfo& dev, cudaStream_t st);
 
 // Combine pass of the split-KV decode: merges NS fp32 partial states per row
 // (rows = B*Hq) into `out` (out_dt) and optional lse_out.  For the cascade,

@@ -18,6 +18,8 @@
 //                             chunks of a row meet in a workspace and the
 //                             last-arriving CTA merges them (associativity,
 //                             [F2] §①) -- never a spin-wait.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -162,38 +164,56 @@ SKV_HOSTDEV_CONST size_t rows_smem_bytes(int row_bytes, int N) {
            (size_t)kRowWarps * rows_list_len(N) * (sizeof(float) + sizeof(int));  // compacted list
 }
 
+// Two-level split of the warp-per-row merge (few rows, many states): warp
+// (row, split) merges states [split * per, min(N, (split + 1) * per)) of its
+// row into an unnormalised partial (m, W, sum w v) in the workspace, then
+// takes a ticket; the row's last warp merges the nsplit partials
+// (associativity, [F2] §①) and writes the row -- never a spin-wait.
+struct BulkSplit {
+    int nsplit = 1;       // warps per row; 1: no workspace, each warp writes its row
+    int per = 0;          // states per warp (<= kBulkMaxN)
+    float* ws_v = nullptr;       // [rows, nsplit, D] fp32 unnormalised sums
+    float* ws_s = nullptr;       // [rows, nsplit, 2]: chunk max m, weight sum W
+    unsigned* ws_cnt = nullptr;  // [rows] arrival tickets, zero between calls
+};
+
 template <typename T>
 __global__ void __launch_bounds__(kRowWarps * 32)
 merge_states_bulk_kernel(const T* __restrict__ v, const float* __restrict__ s,
                          T* __restrict__ vo, float* __restrict__ so, int64_t rows, int N,
-                         int64_t H, int chunks, unsigned long long* err) {
+                         int64_t H, int chunks, unsigned long long* err, const BulkSplit bs) {
     constexpr int E = Vec<T>::N;
     extern __shared__ __align__(128) uint8_t smem[];
     const int row_bytes = chunks * 16;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int per = bs.nsplit > 1 ? bs.per : N;  // states this warp may own (<= kBulkMaxN)
     uint8_t* ring = smem + (size_t)warp * 2 * kRowBatch * row_bytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kRowWarps * 2 * kRowBatch * row_bytes) +
                      warp * 2;
     float* cw = reinterpret_cast<float*>(smem + (size_t)kRowWarps * 2 * kRowBatch * row_bytes +
-                                         (size_t)kRowWarps * 2 * sizeof(uint64_t)) + warp * rows_list_len(N);
-    int* cidx = reinterpret_cast<int*>(cw + (kRowWarps - warp) * rows_list_len(N)) + warp * rows_list_len(N);
+                                         (size_t)kRowWarps * 2 * sizeof(uint64_t)) + warp * rows_list_len(per);
+    int* cidx = reinterpret_cast<int*>(cw + (kRowWarps - warp) * rows_list_len(per)) + warp * rows_list_len(per);
 
-    const int64_t r = (int64_t)blockIdx.x * kRowWarps + warp;
+    const int64_t wg = (int64_t)blockIdx.x * kRowWarps + warp;
+    const int64_t r = wg / bs.nsplit;
+    const int split = (int)(wg - r * bs.nsplit);
     if (r >= rows) return;  // whole warp; no block-wide barrier follows
     if (lane == 0) {
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
         fence_mbar_init();
     }
+    const int n_begin = split * per;
+    const int n_cnt = min(per, N - n_begin);  // >= 1
     const int64_t pos = r / H, h = r % H;
     // s[pos, n, h] at (pos*N + n)*H + h ([F2] §④).
-    const float* srow = s + (pos * N) * H + h;
+    const float* srow = s + (pos * N + n_begin) * H + h;
     float sv[kBulkMaxN / 32];
     float m = -INFINITY;
 #pragma unroll
     for (int k = 0; k < kBulkMaxN / 32; ++k) {
         const int n = lane + 32 * k;
-        sv[k] = n < N ? sanitize_lse(__ldg(srow + (int64_t)n * H)) : -INFINITY;
+        sv[k] = n < n_cnt ? sanitize_lse(__ldg(srow + (int64_t)n * H)) : -INFINITY;
         m = fmaxf(m, sv[k]);
     }
     m = warp_max(m);
@@ -214,7 +234,7 @@ merge_states_bulk_kernel(const T* __restrict__ v, const float* __restrict__ s,
     W = warp_sum(W);
     __syncwarp();
 
-    const char* vrow = reinterpret_cast<const char*>(v) + ((pos * N) * H + h) * (int64_t)row_bytes;
+    const char* vrow = reinterpret_cast<const char*>(v) + ((pos * N + n_begin) * H + h) * (int64_t)row_bytes;
     const int64_t nstride = H * (int64_t)row_bytes;
     const uint64_t pol = policy_evict_first();
     const int nbatch = (nnz + kRowBatch - 1) / kRowBatch;
@@ -256,6 +276,66 @@ merge_states_bulk_kernel(const T* __restrict__ v, const float* __restrict__ s,
         }
         __syncwarp();  // buffer fully read
         if (j + 2 < nbatch) issue(j + 2);
+    }
+    if (bs.nsplit > 1) {
+        // Publish this warp's partial unnormalised (an fp32 s = m + log2 W of
+        // magnitude ~40 would carry ~1e-6 relative weight error), then take a
+        // ticket; the warp that draws the row's last one merges.
+        const int64_t slot = r * bs.nsplit + split;
+        const int D = chunks * E;
+        if (lane < chunks) {
+            float* dst = bs.ws_v + slot * D + lane * E;
+#pragma unroll
+            for (int e = 0; e < E; e += 4)
+                *reinterpret_cast<float4*>(dst + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+        }
+        if (lane == 0) {
+            bs.ws_s[slot * 2 + 0] = m;
+            bs.ws_s[slot * 2 + 1] = W;
+        }
+        __threadfence();  // every lane's partial is visible device-wide ...
+        __syncwarp();     // ... before lane 0 takes the ticket
+        unsigned last = 0;
+        if (lane == 0) {
+            const unsigned ticket = atomicAdd(&bs.ws_cnt[r], 1u);
+            last = ticket == (unsigned)bs.nsplit - 1u;
+            if (last) bs.ws_cnt[r] = 0u;  // every warp of the row has arrived
+        }
+        if (!__shfl_sync(0xffffffffu, last, 0)) return;
+        __threadfence();
+        // The row's partials: lane k holds partial k's (m, W) (nsplit <= 64).
+        const float* ps = bs.ws_s + r * bs.nsplit * 2;
+        float mk[2], wk[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int k = lane + 32 * i;
+            mk[i] = k < bs.nsplit ? ld_cg_f32(ps + 2 * k) : -INFINITY;
+            wk[i] = k < bs.nsplit ? ld_cg_f32(ps + 2 * k + 1) : 0.f;
+        }
+        const float M = warp_max(fmaxf(mk[0], mk[1]));
+        float sc[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) sc[i] = merge_weight(mk[i], M);
+        const float WW = warp_sum(sc[0] * wk[0] + sc[1] * wk[1]);
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = 0.f;
+        const float* pv = bs.ws_v + r * bs.nsplit * (int64_t)D + lane * E;
+#pragma unroll 4
+        for (int k = 0; k < bs.nsplit; ++k) {
+            const float c = __shfl_sync(0xffffffffu, k < 32 ? sc[0] : sc[1], k & 31);
+            if (c > 0.f && lane < chunks) {  // a zero-weight partial is not read
+#pragma unroll
+                for (int e = 0; e < E; e += 4) {
+                    const uint4 raw = ld_cg(pv + (int64_t)k * D + e);
+                    acc[e] = fmaf(c, __uint_as_float(raw.x), acc[e]);
+                    acc[e + 1] = fmaf(c, __uint_as_float(raw.y), acc[e + 1]);
+                    acc[e + 2] = fmaf(c, __uint_as_float(raw.z), acc[e + 2]);
+                    acc[e + 3] = fmaf(c, __uint_as_float(raw.w), acc[e + 3]);
+                }
+            }
+        }
+        m = M;
+        W = WW;
     }
     const float inv = W > 0.f ? 1.f / W : 0.f;
     if (lane < chunks) {
@@ -507,6 +587,12 @@ cudaError_t launch_merge_state(const void* va, const float* sa, const void* vb, 
 
 static constexpr int64_t kTeamRows = 4096;  // rows at or above which the team kernel is used
 static constexpr int kMaxSplit = 16;
+// Two-level warp-per-row merge: at most kMaxBulkSplit warps per row, each
+// with between kMinBulkPer and kBulkMaxN states, and about kBulkWarpsPerSm
+// warps per SM in all (the bulk copies in flight per SM grow with them).
+static constexpr int kMaxBulkSplit = 64;
+static constexpr int kMinBulkPer = 16;
+static constexpr int kBulkWarpsPerSm = 32;
 
 static int max_split_for(int64_t N) {
     int64_t m = (N + 7) / 8;  // at least 8 states per CTA
@@ -522,18 +608,48 @@ static size_t ws_bytes_for(int64_t rows, int nsplit, int64_t D) {
            align256((size_t)rows * 4);
 }
 
+// The two-level warp-per-row split for these sizes (nsplit 1: none).
+static void bulk_split_for(int64_t rows, int64_t N, int sm_count, int* nsplit, int* per) {
+    const int64_t target = (int64_t)kBulkWarpsPerSm * (sm_count > 0 ? sm_count : 1);
+    int64_t p = (N * rows + target - 1) / target;
+    p = (p + kMinBulkPer - 1) / kMinBulkPer * kMinBulkPer;
+    p = std::max<int64_t>(p, (N + kMaxBulkSplit - 1) / kMaxBulkSplit);
+    p = std::min<int64_t>(std::max<int64_t>(p, kMinBulkPer), kBulkMaxN);
+    const int64_t ns = (N + p - 1) / p;
+    *nsplit = (int)ns;
+    *per = (int)((N + ns - 1) / ns);  // the states spread evenly over the warps
+}
+
+static bool bulk_split_fits(int64_t N) { return N <= (int64_t)kBulkMaxN * kMaxBulkSplit; }
+
 size_t merge_states_ws_upper_bound(int64_t rows, int64_t N, int64_t D) {
-    if (rows <= 0 || rows >= kTeamRows) return 0;
-    return ws_bytes_for(rows, max_split_for(N), D);
+    if (rows <= 0) return 0;
+    if (rows >= kTeamRows && N <= kBulkMaxN) return 0;
+    size_t cta = rows < kTeamRows ? ws_bytes_for(rows, max_split_for(N), D) : 0;
+    if (!bulk_split_fits(N)) return cta;
+    // The most warps per row any SM count gives: kMinBulkPer states each.
+    const int64_t most = std::min<int64_t>(kMaxBulkSplit, (N + kMinBulkPer - 1) / kMinBulkPer);
+    return std::max(cta, ws_bytes_for(rows, (int)most, D));
 }
 
 MergeStatesPlan plan_merge_states(int64_t rows, int64_t N, int64_t D, int chunks, int sm_count,
-                                  size_t ws_available, int ctas_per_sm) {
+                                  size_t ws_available, int ctas_per_sm, bool allow_bulk_split) {
     (void)chunks;
     MergeStatesPlan pl;
     if (rows >= kTeamRows && N <= kBulkMaxN) {
         pl.team_kernel = true;
         return pl;
+    }
+    if (allow_bulk_split && bulk_split_fits(N)) {
+        int nsplit = 1, per = 0;
+        bulk_split_for(rows, N, sm_count, &nsplit, &per);
+        if (nsplit > 1 && ws_bytes_for(rows, nsplit, D) <= ws_available) {
+            pl.team_kernel = true;
+            pl.nsplit = nsplit;
+            pl.per_split = per;
+            pl.ws_bytes = ws_bytes_for(rows, nsplit, D);
+            return pl;
+        }
     }
     // Enough CTAs to give every SM about ctas_per_sm: with few rows and many
     // states, the loads in flight per SM (and so the stream rate) grow with
@@ -549,8 +665,8 @@ MergeStatesPlan plan_merge_states(int64_t rows, int64_t N, int64_t D, int chunks
 
 template <typename T>
 cudaError_t launch_rows(const T* v, const float* s, T* vo, float* so, int64_t rows, int N, int64_t H,
-                        int chunks, unsigned blocks, size_t smem, const DeviceInfo& dev,
-                        cudaStream_t st) {
+                        int chunks, unsigned blocks, size_t smem, const BulkSplit& bs,
+                        const DeviceInfo& dev, cudaStream_t st) {
     // The limit is set once per device, to the largest size any call can
     // ask for (rows of up to 128 fp32 values, up to kBulkMaxN states).
     constexpr size_t kMaxSmem = rows_smem_bytes(128 * 4, kBulkMaxN);
@@ -563,25 +679,37 @@ cudaError_t launch_rows(const T* v, const float* s, T* vo, float* so, int64_t ro
         attr_set[dev.device] = true;
     }
     merge_states_bulk_kernel<T><<<blocks, kRowWarps * 32, smem, st>>>(v, s, vo, so, rows, N, H, chunks,
-                                                                       dev.err);
+                                                                       dev.err, bs);
     return cudaGetLastError();
 }
 
 cudaError_t launch_merge_states(const void* v, const float* s, void* vo, float* so, int64_t S,
                                 int64_t N, int64_t H, int64_t D, skv_dtype dt, void* ws,
-                                size_t ws_bytes, int ctas_per_sm, const DeviceInfo& dev,
-                                cudaStream_t st) {
+                                size_t ws_bytes, int ctas_per_sm, bool allow_bulk_split,
+                                const DeviceInfo& dev, cudaStream_t st) {
     const int64_t rows = S * H;
     const int chunks = (int)(D * (int64_t)dtype_size(dt) / 16);
-    const MergeStatesPlan pl =
-        plan_merge_states(rows, N, D, chunks, dev.sm_count, ws ? ws_bytes : 0, ctas_per_sm);
+    const MergeStatesPlan pl = plan_merge_states(rows, N, D, chunks, dev.sm_count,
+                                                 ws ? ws_bytes : 0, ctas_per_sm, allow_bulk_split);
     if (pl.team_kernel) {
         const int row_bytes = chunks * 16;
-        const size_t smem = rows_smem_bytes(row_bytes, (int)N);
-        const unsigned blocks = (unsigned)((rows + kRowWarps - 1) / kRowWarps);
+        BulkSplit bs;
+        if (pl.nsplit > 1) {
+            bs.nsplit = pl.nsplit;
+            bs.per = pl.per_split;
+            char* w = static_cast<char*>(ws);
+            bs.ws_v = reinterpret_cast<float*>(w);
+            w += align256((size_t)rows * pl.nsplit * D * 4);
+            bs.ws_s = reinterpret_cast<float*>(w);
+            w += align256((size_t)rows * pl.nsplit * 8);
+            bs.ws_cnt = reinterpret_cast<unsigned*>(w);
+        }
+        const size_t smem = rows_smem_bytes(row_bytes, pl.nsplit > 1 ? pl.per_split : (int)N);
+        const int64_t warps = rows * pl.nsplit;
+        const unsigned blocks = (unsigned)((warps + kRowWarps - 1) / kRowWarps);
 #define SKV_ROWS(T_)                                                                           \
     launch_rows<T_>(static_cast<const T_*>(v), s, static_cast<T_*>(vo), so, rows, (int)N, H,   \
-                    chunks, blocks, smem, dev, st)
+                    chunks, blocks, smem, bs, dev, st)
         switch (dt) {
             case SKV_F32: return SKV_ROWS(float);
             case SKV_F16: return SKV_ROWS(__half);

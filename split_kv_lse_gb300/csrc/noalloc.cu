@@ -61,7 +61,7 @@ extern "C" size_t skv_merge_states_noalloc_scratch_size(int64_t S, int64_t N, in
         sm_count = dev->sm_count;
     }
     return plan_merge_states(S * H, N, D, (int)(row_bytes / 16), sm_count, SIZE_MAX,
-                             kNoallocCtasPerSm).ws_bytes;
+                             kMergeCtasPerSm, false).ws_bytes;
 }
 
 extern "C" skv_status skv_merge_states_noalloc(const void* v, const float* s, void* v_out,
@@ -85,7 +85,7 @@ extern "C" skv_status skv_merge_states_noalloc(const void* v, const float* s, vo
     // not fit in the fixed array rather than silently taking another path.
     const int chunks = (int)(row_bytes / 16);
     const MergeStatesPlan want =
-        plan_merge_states(S * H, N, D, chunks, dev->sm_count, SIZE_MAX, kNoallocCtasPerSm);
+        plan_merge_states(S * H, N, D, chunks, dev->sm_count, SIZE_MAX, kMergeCtasPerSm, false);
     if (want.ws_bytes > kScratchBytes) return SKV_ERR_UNSUPPORTED;
     void* scratch = nullptr;
     if ((st = scratch_address(dev->device, &scratch)) != SKV_OK) return st;
@@ -95,6 +95,6 @@ extern "C" skv_status skv_merge_states_noalloc(const void* v, const float* s, vo
     if (want.ws_bytes > 0 && cudaMemsetAsync(scratch, 0, want.ws_bytes, cs) != cudaSuccess)
         return SKV_ERR_CUDA;
     cudaError_t e = launch_merge_states(v, s, v_out, s_out, S, N, H, D, dtype, scratch,
-                                        kScratchBytes, kNoallocCtasPerSm, *dev, cs);
+                                        kScratchBytes, kMergeCtasPerSm, false, *dev, cs);
     return e == cudaSuccess ? SKV_OK : SKV_ERR_CUDA;
 }

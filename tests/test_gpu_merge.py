@@ -219,3 +219,46 @@ def test_merge_states_row_sizes_in_a_fresh_process(lib):
     r = subprocess.run([sys.executable, "-c", _ROW_SIZES_SCRIPT, root], capture_output=True,
                        text=True, timeout=600)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("S,N,H,D", [(16, 1024, 8, 128), (2, 5000, 3, 64), (32, 260, 128, 64),
+                                     (1, 16384, 1, 64), (1, 16385, 1, 64), (3, 40, 1, 128)])
+def test_merge_states_two_level_warp_split(lib, dtype, S, N, H, D):
+    """Few rows with many states through a workspace: each row's states are
+    cut over up to 64 warps, whose unnormalised partials the row's last warp
+    merges ([F2] §① associativity, §⑦ the large-N kernel).  Shapes cover the
+    large-N sweep's N = 1024, 4096 rows with N > 256, the largest N the warp
+    split takes (16384) and one past it (the CTA path), and few states.  The
+    workspace is reused without re-zeroing for a second call, which must give
+    the same bits."""
+    if dtype == torch.float32 and D * 4 > 512:
+        pytest.skip("fp32 rows of more than 512 bytes are not supported")
+    d = W.merge_states_inputs(S, N, H, D, dtype, seed=S * 31 + N + D, empty_p=0.05)
+    ws, need = _ws(lib, S, N, H, D)
+    assert need > 0
+    v1, s1 = _check_merge_states(lib, d, dtype, ws)
+    v2, s2 = lib.merge_states(d["v"].to(DEV), d["s"].to(DEV), workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(v1, v2) and torch.equal(s1, s2)
+    assert lib.get_device_error() == (0, 0)
+
+
+def test_merge_states_two_level_empty_chunks_and_poison(lib):
+    """Rows whose states are all empty, all poisoned (+inf or NaN s), or empty
+    except for one state in one chunk: every warp's partial of such a row may
+    be empty, and the row's merge must still be exact (v = 0, s = -inf when
+    nothing is left)."""
+    S, N, H, D = 8, 2048, 2, 128
+    g = torch.Generator().manual_seed(77)
+    v = torch.randn(S, N, H, D, generator=g)
+    s = 30 + 8 * torch.randn(S, N, H, generator=g)
+    s[0] = -math.inf                   # all empty
+    s[1, :, 0] = math.inf              # all +inf (read as empty)
+    s[1, :, 1] = math.nan              # all NaN
+    s[2] = -math.inf
+    s[2, 1999, 1] = 4.0                # one state, in the last chunk
+    v[2, :, 0] = math.nan              # empty states' v are never read
+    s[3, ::3, :] = math.nan            # a third poisoned
+    ws, _ = _ws(lib, S, N, H, D)
+    _check_merge_states(lib, {"v": v, "s": s}, torch.float32, ws)
