@@ -164,7 +164,7 @@ constexpr size_t smem_bytes() {
            (size_t)W * G * kPage * sizeof(uint16_t) + (DYN ? (kDynMaxPages + 4) * sizeof(int) : 0);
 }
 
-template <int G, int W, int R, bool BF, bool DYN>
+template <int G, int W, int R, bool BF, bool DYN, bool VAR>
 __global__ void __launch_bounds__(W * 32)
 splitkv_decode_kernel(const DecodeParams p) {
     using Ro = Roles<G>;
@@ -184,10 +184,11 @@ splitkv_decode_kernel(const DecodeParams p) {
     int* dyn_next = dyn_ids + kDynMaxPages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Uniform splits: CTA (split, hkv, b).  Per-sequence splits: CTA u*Hkv +
-    // hkv takes unit u of the list, sequence b's split `split` of ns.
+    // Uniform splits: CTA (split, hkv, b).  Per-sequence splits (VAR): CTA
+    // u*Hkv + hkv takes unit u of the list, sequence b's split `split` of ns.
+    // (Separate instantiations: the uniform kernel keeps its registers.)
     int split, hkv, b, ns;
-    if (p.units != nullptr) {
+    if constexpr (VAR) {
         const int u = blockIdx.x / p.Hkv;
         hkv = blockIdx.x - u * p.Hkv;
         const int2 wi = __ldg(p.units + u);
@@ -612,11 +613,11 @@ splitkv_decode_kernel(const DecodeParams p) {
     last_cta_waits_primary(p.done_ctr);
 }
 
-template <int G, int W, int R, bool BF, bool DYN = false>
-cudaError_t launch_gwr(const DecodeParams& p, int B, int Hkv, int NS, int num_units,
-                       cudaStream_t st) {
+template <int G, int W, int R, bool BF, bool DYN, bool VAR>
+cudaError_t launch_gwr_t(const DecodeParams& p, int B, int Hkv, int NS, int num_units,
+                         cudaStream_t st) {
     constexpr size_t smem = smem_bytes<G, W, R, DYN>();
-    auto kern = splitkv_decode_kernel<G, W, R, BF, DYN>;
+    auto kern = splitkv_decode_kernel<G, W, R, BF, DYN, VAR>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -626,8 +627,7 @@ cudaError_t launch_gwr(const DecodeParams& p, int B, int Hkv, int NS, int num_un
         attr_set[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = p.units != nullptr ? dim3((unsigned)num_units * (unsigned)Hkv, 1, 1)
-                                     : dim3(NS, Hkv, B);
+    cfg.gridDim = VAR ? dim3((unsigned)num_units * (unsigned)Hkv, 1, 1) : dim3(NS, Hkv, B);
     cfg.blockDim = dim3(W * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -637,6 +637,13 @@ cudaError_t launch_gwr(const DecodeParams& p, int B, int Hkv, int NS, int num_un
     cfg.attrs = attr;
     cfg.numAttrs = p.done_ctr != nullptr ? 1 : 0;  // chained after a prefix pass
     return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int G, int W, int R, bool BF, bool DYN = false>
+cudaError_t launch_gwr(const DecodeParams& p, int B, int Hkv, int NS, int num_units,
+                       cudaStream_t st) {
+    return p.units != nullptr ? launch_gwr_t<G, W, R, BF, DYN, true>(p, B, Hkv, NS, num_units, st)
+                              : launch_gwr_t<G, W, R, BF, DYN, false>(p, B, Hkv, NS, num_units, st);
 }
 
 // Warps per CTA follow the longest possible split (the page table's width
@@ -692,11 +699,13 @@ struct CombineParams {
 
 // States of `row` (at most NS): its sequence's split count with per-sequence
 // splits (a count outside [1, NS] is flagged and clamped), else NS.
+template <bool VAR>
 SKV_DEVINL int row_splits(const CombineParams& p, int64_t row) {
-    if (p.seq_splits == nullptr) return p.NS;
-    const int n = __ldg(p.seq_splits + row / p.Hq);
+    if (!VAR) return p.NS;
+    const int b = (int)row / p.Hq;  // rows = B * Hq < 2^31
+    const int n = __ldg(p.seq_splits + b);
     if (n < 1 || n > p.NS) {
-        if ((threadIdx.x & 31) == 0) record_error(p.err, SKV_ERR_INVALID_ARG, 4 << 20 | (int)(row / p.Hq));
+        if ((threadIdx.x & 31) == 0) record_error(p.err, SKV_ERR_INVALID_ARG, 4 << 20 | b);
         return n < 1 ? 1 : p.NS;
     }
     return n;
@@ -799,7 +808,7 @@ SKV_DEVINL void merge_row(const float* o, const float* lse, int stride, int N, i
     s_out = st.m + log2f(st.W);  // -inf when every state is empty
 }
 
-template <typename Tout, int WPR>
+template <typename Tout, int WPR, bool VAR>
 __global__ void __launch_bounds__(kCombWarps * 32)
 combine_kernel(const CombineParams p) {
     pdl_wait_primary();  // the states are written by the preceding grids
@@ -812,7 +821,7 @@ combine_kernel(const CombineParams p) {
     const int sub = w % WPR;
     const bool has = 4 * lane < p.D;
     float vd[4], sd;
-    merge_row<WPR>(p.o_part, p.lse_part, p.NS, row_splits(p, row), p.D, row, sub, sm, vd, sd);
+    merge_row<WPR>(p.o_part, p.lse_part, p.NS, row_splits<VAR>(p, row), p.D, row, sub, sm, vd, sd);
     if (p.pre_part != nullptr) {
         float vp[4] = {0.f, 0.f, 0.f, 0.f}, sp = -INFINITY;  // empty prefix when C == 0
         if (p.C > 0) merge_row<WPR>(p.pre_part, p.pre_lse, p.C, p.C, p.D, row, sub, sm, vp, sp);
@@ -864,7 +873,7 @@ constexpr int kCascadeBatch = 8;
 // lists are read at once -- warp 0 merges the suffix's split states, warp 1
 // the prefix chunks' states into the prefix state (written to o_pre/s_pre)
 // -- and they meet in shared memory for the two-state merge, prefix first.
-template <typename Tout>
+template <typename Tout, bool VAR>
 __global__ void __launch_bounds__(kCombWarps * 32, 8)
 cascade_combine_kernel(const CombineParams p) {
     pdl_wait_primary();  // the states are written by the preceding grids
@@ -879,7 +888,7 @@ cascade_combine_kernel(const CombineParams p) {
     const bool has = 4 * lane < p.D;
     float v[4] = {0.f, 0.f, 0.f, 0.f}, s = -INFINITY;
     if (sub == 0) {
-        merge_row<1, kCascadeBatch>(p.o_part, p.lse_part, p.NS, row_splits(p, row), p.D, row, 0,
+        merge_row<1, kCascadeBatch>(p.o_part, p.lse_part, p.NS, row_splits<VAR>(p, row), p.D, row, 0,
                                     sm, v, s);
     } else {
         if (p.C > 0)
@@ -1004,14 +1013,17 @@ cudaError_t launch_combine(const CombineArgs& a, bool pdl, const DeviceInfo& dev
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-#define SKV_COMB(T_) \
-    (cascade ? cudaLaunchKernelEx(&cfg, cascade_combine_kernel<T_>, p) \
-             : (wide ? cudaLaunchKernelEx(&cfg, combine_kernel<T_, 1>, p) \
-                     : cudaLaunchKernelEx(&cfg, combine_kernel<T_, kCombWarps>, p)))
+#define SKV_COMB(T_, V_) \
+    (cascade ? cudaLaunchKernelEx(&cfg, cascade_combine_kernel<T_, V_>, p) \
+             : (wide ? cudaLaunchKernelEx(&cfg, combine_kernel<T_, 1, V_>, p) \
+                     : cudaLaunchKernelEx(&cfg, combine_kernel<T_, kCombWarps, V_>, p)))
+    // Per-sequence split counts are separate instantiations: a count that
+    // varies by row costs the uniform kernels registers.
+    const bool var = a.seq_splits != nullptr;
     switch (a.out_dt) {
-        case SKV_F32: return SKV_COMB(float);
-        case SKV_F16: return SKV_COMB(__half);
-        case SKV_BF16: return SKV_COMB(__nv_bfloat16);
+        case SKV_F32: return var ? SKV_COMB(float, true) : SKV_COMB(float, false);
+        case SKV_F16: return var ? SKV_COMB(__half, true) : SKV_COMB(__half, false);
+        case SKV_BF16: return var ? SKV_COMB(__nv_bfloat16, true) : SKV_COMB(__nv_bfloat16, false);
     }
 #undef SKV_COMB
     return cudaErrorInvalidValue;
