@@ -30,6 +30,7 @@ cudaError_t launch_merge_state(const void* va, const float* sa, const void* vb, 
 // workspace-size query so the two always agree).
 struct MergeStatesPlan {
     bool team_kernel = false;  // warp-per-row bulk kernel (nsplit warps per row if > 1)
+    bool row_cta = false;      // bulk CTA per row (per_split states per warp), no workspace
     int nsplit = 1;            // CTAs per row on the CTA path (>1 needs workspace)
     int per_split = 0;         // states per CTA on the CTA path
     size_t ws_bytes = 0;       // workspace the plan needs

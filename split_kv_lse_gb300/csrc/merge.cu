@@ -158,9 +158,16 @@ constexpr int kBulkMaxN = 256;
 // Entries per warp of the compacted state list: N rounded up to a warp.
 SKV_HOSTDEV_CONST int rows_list_len(int N) { return (N + 31) & ~31; }
 
+// Ring of NBUF batches of BATCH rows per warp: the many-rows path keeps
+// (kRowBatch, 2); the two-level split, whose warps each stream only a chunk
+// of a row, keeps more in flight per warp: (kSplitBatch, kSplitBufs).
+constexpr int kSplitBatch = 8;
+constexpr int kSplitBufs = 3;
+
+template <int BATCH, int NBUF>
 SKV_HOSTDEV_CONST size_t rows_smem_bytes(int row_bytes, int N) {
-    return (size_t)kRowWarps * 2 * kRowBatch * row_bytes +        // double-buffered batches
-           (size_t)kRowWarps * 2 * sizeof(uint64_t) +               // one mbarrier per buffer
+    return (size_t)kRowWarps * NBUF * BATCH * row_bytes +           // the batch ring
+           (size_t)kRowWarps * NBUF * sizeof(uint64_t) +            // one mbarrier per buffer
            (size_t)kRowWarps * rows_list_len(N) * (sizeof(float) + sizeof(int));  // compacted list
 }
 
@@ -177,35 +184,28 @@ struct BulkSplit {
     unsigned* ws_cnt = nullptr;  // [rows] arrival tickets, zero between calls
 };
 
-template <typename T>
-__global__ void __launch_bounds__(kRowWarps * 32)
-merge_states_bulk_kernel(const T* __restrict__ v, const float* __restrict__ s,
-                         T* __restrict__ vo, float* __restrict__ so, int64_t rows, int N,
-                         int64_t H, int chunks, unsigned long long* err, const BulkSplit bs) {
+// One warp streams states [n_begin, n_begin + n_cnt) of row (pos, h): their
+// LSEs are read once (lane n holds states n, n + 32, ...), the non-empty
+// ones are compacted (ballot) into a list of (index, weight) in shared
+// memory -- a zero-weight state is never read, so its v cannot poison the
+// sum -- and their v rows stream through the warp's ring of NBUF batches of
+// BATCH rows (one TMA bulk copy per row, issued by BATCH lanes at once,
+// completed on one mbarrier per batch).  Returns the chunk max m (log2
+// units), W = sum 2^(s - m) and acc = sum 2^(s - m) v (this lane's 16-byte
+// chunk of D).  The ring's barriers must be initialised.  Returns false if
+// a bounded wait gave up (error recorded; every copy of the warp has landed
+// or been waited for once more).
+template <typename T, int BATCH, int NBUF>
+SKV_DEVINL bool warp_stream_states(const T* __restrict__ v, const float* __restrict__ s,
+                                   int64_t pos, int64_t h, int64_t H, int N, int n_begin,
+                                   int n_cnt, int chunks, uint8_t* ring, uint64_t* bars,
+                                   float* cw, int* cidx, unsigned long long* err, float& m_out,
+                                   float& W_out, float (&acc)[Vec<T>::N]) {
     constexpr int E = Vec<T>::N;
-    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31;
     const int row_bytes = chunks * 16;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int per = bs.nsplit > 1 ? bs.per : N;  // states this warp may own (<= kBulkMaxN)
-    uint8_t* ring = smem + (size_t)warp * 2 * kRowBatch * row_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kRowWarps * 2 * kRowBatch * row_bytes) +
-                     warp * 2;
-    float* cw = reinterpret_cast<float*>(smem + (size_t)kRowWarps * 2 * kRowBatch * row_bytes +
-                                         (size_t)kRowWarps * 2 * sizeof(uint64_t)) + warp * rows_list_len(per);
-    int* cidx = reinterpret_cast<int*>(cw + (kRowWarps - warp) * rows_list_len(per)) + warp * rows_list_len(per);
-
-    const int64_t wg = (int64_t)blockIdx.x * kRowWarps + warp;
-    const int64_t r = wg / bs.nsplit;
-    const int split = (int)(wg - r * bs.nsplit);
-    if (r >= rows) return;  // whole warp; no block-wide barrier follows
-    if (lane == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        fence_mbar_init();
-    }
-    const int n_begin = split * per;
-    const int n_cnt = min(per, N - n_begin);  // >= 1
-    const int64_t pos = r / H, h = r % H;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
     // s[pos, n, h] at (pos*N + n)*H + h ([F2] §④).
     const float* srow = s + (pos * N + n_begin) * H + h;
     float sv[kBulkMaxN / 32];
@@ -221,7 +221,7 @@ merge_states_bulk_kernel(const T* __restrict__ v, const float* __restrict__ s,
     int nnz = 0;  // non-empty states, in state order
 #pragma unroll
     for (int k = 0; k < kBulkMaxN / 32; ++k) {
-        const float w = merge_weight(sv[k], m);  // 0 for empty states and n >= N
+        const float w = merge_weight(sv[k], m);  // 0 for empty states and n >= n_cnt
         W += w;
         const unsigned live = __ballot_sync(0xffffffffu, w > 0.f);
         if (w > 0.f) {
@@ -231,42 +231,40 @@ merge_states_bulk_kernel(const T* __restrict__ v, const float* __restrict__ s,
         }
         nnz += __popc(live);
     }
-    W = warp_sum(W);
+    m_out = m;
+    W_out = warp_sum(W);
     __syncwarp();
 
     const char* vrow = reinterpret_cast<const char*>(v) + ((pos * N + n_begin) * H + h) * (int64_t)row_bytes;
     const int64_t nstride = H * (int64_t)row_bytes;
     const uint64_t pol = policy_evict_first();
-    const int nbatch = (nnz + kRowBatch - 1) / kRowBatch;
-    auto issue = [&](int j) {  // batch j into buffer j & 1
-        const int cnt = min(kRowBatch, nnz - j * kRowBatch);
-        uint64_t* bar = &bars[j & 1];
+    const int nbatch = (nnz + BATCH - 1) / BATCH;
+    auto issue = [&](int j) {  // batch j into buffer j % NBUF
+        const int cnt = min(BATCH, nnz - j * BATCH);
+        uint64_t* bar = &bars[j % NBUF];
         if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(cnt * row_bytes));
         __syncwarp();
         if (lane < cnt)
-            bulk_g2s(ring + ((j & 1) * kRowBatch + lane) * row_bytes,
-                     vrow + (int64_t)cidx[j * kRowBatch + lane] * nstride, row_bytes, bar, pol);
+            bulk_g2s(ring + ((j % NBUF) * BATCH + lane) * row_bytes,
+                     vrow + (int64_t)cidx[j * BATCH + lane] * nstride, row_bytes, bar, pol);
     };
-    if (nbatch > 0) issue(0);
-    if (nbatch > 1) issue(1);
-    float acc[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    for (int j = 0; j < NBUF && j < nbatch; ++j) issue(j);
     for (int j = 0; j < nbatch; ++j) {
-        const bool ok = mbar_wait(&bars[j & 1], (uint32_t)((j >> 1) & 1), err, 6);
+        const bool ok = mbar_wait(&bars[j % NBUF], (uint32_t)((j / NBUF) & 1), err, 6);
         if (!__all_sync(0xffffffffu, ok)) {
             // A bounded wait gave up (error recorded): one more bounded wait
-            // for the other batch in flight, then stop.
-            if (j + 1 < nbatch) mbar_wait(&bars[(j + 1) & 1], (uint32_t)(((j + 1) >> 1) & 1), err, 7);
-            return;
+            // for each other batch in flight, then stop.
+            for (int jj = j + 1; jj < nbatch && jj < j + NBUF; ++jj)
+                mbar_wait(&bars[jj % NBUF], (uint32_t)((jj / NBUF) & 1), err, 7);
+            return false;
         }
-        const int cnt = min(kRowBatch, nnz - j * kRowBatch);
+        const int cnt = min(BATCH, nnz - j * BATCH);
         if (lane < chunks) {
-            const uint8_t* buf = ring + (j & 1) * kRowBatch * row_bytes + lane * 16;
+            const uint8_t* buf = ring + (j % NBUF) * BATCH * row_bytes + lane * 16;
 #pragma unroll
-            for (int b = 0; b < kRowBatch; ++b) {
+            for (int b = 0; b < BATCH; ++b) {
                 if (b < cnt) {
-                    const float w = cw[j * kRowBatch + b];
+                    const float w = cw[j * BATCH + b];
                     float f[E];
                     to_float<T>(*reinterpret_cast<const uint4*>(buf + b * row_bytes), f);
 #pragma unroll
@@ -275,8 +273,52 @@ merge_states_bulk_kernel(const T* __restrict__ v, const float* __restrict__ s,
             }
         }
         __syncwarp();  // buffer fully read
-        if (j + 2 < nbatch) issue(j + 2);
+        if (j + NBUF < nbatch) issue(j + NBUF);
     }
+    return true;
+}
+
+template <typename T, int BATCH, int NBUF>
+__global__ void __launch_bounds__(kRowWarps * 32)
+merge_states_bulk_kernel(const T* __restrict__ v, const float* __restrict__ s,
+                         T* __restrict__ vo, float* __restrict__ so, int64_t rows, int N,
+                         int64_t H, int chunks, unsigned long long* err, const BulkSplit bs) {
+    constexpr int E = Vec<T>::N;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int row_bytes = chunks * 16;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int per = bs.nsplit > 1 ? bs.per : N;  // states this warp may own (<= kBulkMaxN)
+    uint8_t* ring = smem + (size_t)warp * NBUF * BATCH * row_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kRowWarps * NBUF * BATCH * row_bytes) +
+                     warp * NBUF;
+    float* cw = reinterpret_cast<float*>(smem + (size_t)kRowWarps * NBUF * BATCH * row_bytes +
+                                         (size_t)kRowWarps * NBUF * sizeof(uint64_t)) + warp * rows_list_len(per);
+    int* cidx = reinterpret_cast<int*>(cw + (kRowWarps - warp) * rows_list_len(per)) + warp * rows_list_len(per);
+
+    // Warp wg: row wg (one warp per row), or with the split the warps of one
+    // (pos, split) over consecutive heads h, so that a CTA's warps read
+    // adjacent rows of each state (one contiguous run of the [S, N, H, D]
+    // layout) as the many-rows path does.
+    const int64_t wg = (int64_t)blockIdx.x * kRowWarps + warp;
+    int64_t r = wg;
+    int split = 0;
+    if (bs.nsplit > 1) {
+        const int64_t hh = wg % H, t = wg / H;
+        split = (int)(t % bs.nsplit);
+        r = (t / bs.nsplit) * H + hh;
+    }
+    if (r >= rows) return;  // whole warp; no block-wide barrier follows
+    if (lane == 0) {
+        for (int i = 0; i < NBUF; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const int n_begin = split * per;
+    const int n_cnt = min(per, N - n_begin);  // >= 1
+    float m, W, acc[E];
+    if (!warp_stream_states<T, BATCH, NBUF>(v, s, r / H, r % H, H, N, n_begin, n_cnt, chunks, ring,
+                                            bars, cw, cidx, err, m, W, acc))
+        return;
     if (bs.nsplit > 1) {
         // Publish this warp's partial unnormalised (an fp32 s = m + log2 W of
         // magnitude ~40 would carry ~1e-6 relative weight error), then take a
@@ -320,17 +362,32 @@ merge_states_bulk_kernel(const T* __restrict__ v, const float* __restrict__ s,
 #pragma unroll
         for (int e = 0; e < E; ++e) acc[e] = 0.f;
         const float* pv = bs.ws_v + r * bs.nsplit * (int64_t)D + lane * E;
-#pragma unroll 4
-        for (int k = 0; k < bs.nsplit; ++k) {
-            const float c = __shfl_sync(0xffffffffu, k < 32 ? sc[0] : sc[1], k & 31);
-            if (c > 0.f && lane < chunks) {  // a zero-weight partial is not read
+        // kFinalBatch partials per L2 round trip: every load of a batch is
+        // issued before any is used.
+        constexpr int kFinalBatch = 16 * 4 / E;
+        for (int k0 = 0; k0 < bs.nsplit; k0 += kFinalBatch) {
+            float4 raw[kFinalBatch][E / 4];
+            float c[kFinalBatch];
+#pragma unroll
+            for (int i = 0; i < kFinalBatch; ++i) {
+                const int k = k0 + i;
+                c[i] = __shfl_sync(0xffffffffu, k < 32 ? sc[0] : sc[1], k & 31);
+                if (k >= bs.nsplit) c[i] = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; e += 4)  // a zero-weight partial is not read
+                    raw[i][e / 4] = (c[i] > 0.f && lane < chunks)
+                                        ? __ldcg(reinterpret_cast<const float4*>(pv + (int64_t)k * D + e))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int i = 0; i < kFinalBatch; ++i) {
+                if (!(c[i] > 0.f)) continue;
 #pragma unroll
                 for (int e = 0; e < E; e += 4) {
-                    const uint4 raw = ld_cg(pv + (int64_t)k * D + e);
-                    acc[e] = fmaf(c, __uint_as_float(raw.x), acc[e]);
-                    acc[e + 1] = fmaf(c, __uint_as_float(raw.y), acc[e + 1]);
-                    acc[e + 2] = fmaf(c, __uint_as_float(raw.z), acc[e + 2]);
-                    acc[e + 3] = fmaf(c, __uint_as_float(raw.w), acc[e + 3]);
+                    acc[e] = fmaf(c[i], raw[i][e / 4].x, acc[e]);
+                    acc[e + 1] = fmaf(c[i], raw[i][e / 4].y, acc[e + 1]);
+                    acc[e + 2] = fmaf(c[i], raw[i][e / 4].z, acc[e + 2]);
+                    acc[e + 3] = fmaf(c[i], raw[i][e / 4].w, acc[e + 3]);
                 }
             }
         }
@@ -345,6 +402,101 @@ merge_states_bulk_kernel(const T* __restrict__ v, const float* __restrict__ s,
         st_stream(reinterpret_cast<char*>(vo) + r * row_bytes + lane * 16, from_float<T>(f));
     }
     if (lane == 0) so[r] = m + log2f(W);
+}
+
+// ---------------------------------------------------------------- N-state, bulk CTA per row
+// Few rows, many states: one CTA of kRowCtaWarps warps per row, warp w
+// streaming states [w * per, (w + 1) * per) through its own ring (as the
+// warp-per-row kernel does), the warps' unnormalised partial states then
+// merged in shared memory by warp 0 -- no workspace, no second pass through
+// global memory ([F2] §① associativity; the large-N kernel of §⑦).
+constexpr int kRowCtaWarps = 16;
+constexpr int kRowCtaBatch = 8;
+constexpr int kRowCtaBufs = 3;
+
+SKV_HOSTDEV_CONST size_t rowcta_smem_bytes(int row_bytes, int per) {
+    return (size_t)kRowCtaWarps * kRowCtaBufs * kRowCtaBatch * row_bytes +  // rings
+           (size_t)kRowCtaWarps * kRowCtaBufs * sizeof(uint64_t) +          // barriers
+           (size_t)kRowCtaWarps * rows_list_len(per) * (sizeof(float) + sizeof(int)) +
+           (size_t)kRowCtaWarps * 2 * sizeof(float);                        // partial m, W
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRowCtaWarps * 32, 1)
+merge_states_rowcta_kernel(const T* __restrict__ v, const float* __restrict__ s,
+                           T* __restrict__ vo, float* __restrict__ so, int N, int64_t H,
+                           int chunks, int per, unsigned long long* err) {
+    constexpr int E = Vec<T>::N;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int row_bytes = chunks * 16;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr size_t kRing = (size_t)kRowCtaBufs * kRowCtaBatch;
+    uint8_t* rings = smem;
+    uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + kRowCtaWarps * kRing * row_bytes);
+    float* cw_all = reinterpret_cast<float*>(bars_all + kRowCtaWarps * kRowCtaBufs);
+    int* cidx_all = reinterpret_cast<int*>(cw_all + kRowCtaWarps * rows_list_len(per));
+    float* pm = reinterpret_cast<float*>(cidx_all + kRowCtaWarps * rows_list_len(per));
+    float* pW = pm + kRowCtaWarps;
+
+    const int64_t r = blockIdx.x;
+    uint64_t* bars = bars_all + warp * kRowCtaBufs;
+    if (lane == 0) {
+        for (int i = 0; i < kRowCtaBufs; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const int n_begin = warp * per;
+    const int n_cnt = min(per, N - n_begin);
+    float m = -INFINITY, W = 0.f, acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    bool ok = true;
+    if (n_cnt > 0)
+        ok = warp_stream_states<T, kRowCtaBatch, kRowCtaBufs>(
+            v, s, r / H, r % H, H, N, n_begin, n_cnt, chunks, rings + warp * kRing * row_bytes, bars,
+            cw_all + warp * rows_list_len(per), cidx_all + warp * rows_list_len(per), err, m, W, acc);
+    if (!ok) {  // a wait gave up (recorded): this warp adds nothing, the CTA still meets
+        m = -INFINITY;
+        W = 0.f;
+    }
+    __syncthreads();  // every ring is drained: reuse the first as [warps][D] partial sums
+    float* pacc = reinterpret_cast<float*>(rings);
+    const int D = chunks * E;
+    if (lane < chunks) {
+#pragma unroll
+        for (int e = 0; e < E; e += 4)
+            *reinterpret_cast<float4*>(pacc + warp * D + lane * E + e) =
+                make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+    }
+    if (lane == 0) {
+        pm[warp] = m;
+        pW[warp] = W;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    // Warp 0 merges the kRowCtaWarps partial states and writes the row.
+    const float mk = lane < kRowCtaWarps ? pm[lane] : -INFINITY;
+    const float M = warp_max(mk);
+    const float sc = merge_weight(mk, M);  // 0 for an empty partial
+    const float WW = warp_sum(lane < kRowCtaWarps ? sc * pW[lane] : 0.f);
+    float o[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[e] = 0.f;
+#pragma unroll
+    for (int k = 0; k < kRowCtaWarps; ++k) {
+        const float c = __shfl_sync(0xffffffffu, sc, k);
+        if (c > 0.f && lane < chunks) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[e] = fmaf(c, pacc[k * D + lane * E + e], o[e]);
+        }
+    }
+    const float inv = WW > 0.f ? 1.f / WW : 0.f;
+    if (lane < chunks) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] *= inv;
+        st_stream(reinterpret_cast<char*>(vo) + r * row_bytes + lane * 16, from_float<T>(o));
+    }
+    if (lane == 0) so[r] = M + log2f(WW);
 }
 
 // ---------------------------------------------------------------- N-state, CTA per row
@@ -592,7 +744,7 @@ static constexpr int kMaxSplit = 16;
 // warps per SM in all (the bulk copies in flight per SM grow with them).
 static constexpr int kMaxBulkSplit = 64;
 static constexpr int kMinBulkPer = 16;
-static constexpr int kBulkWarpsPerSm = 32;
+static constexpr int kBulkWarpsPerSm = 16;
 
 static int max_split_for(int64_t N) {
     int64_t m = (N + 7) / 8;  // at least 8 states per CTA
@@ -640,6 +792,13 @@ MergeStatesPlan plan_merge_states(int64_t rows, int64_t N, int64_t D, int chunks
         pl.team_kernel = true;
         return pl;
     }
+    if (allow_bulk_split && rows < kTeamRows && 2 * rows >= sm_count &&
+        N <= (int64_t)kRowCtaWarps * kBulkMaxN) {
+        // Enough rows for every SM to stream about one: a CTA per row.
+        pl.row_cta = true;
+        pl.per_split = (int)((N + kRowCtaWarps - 1) / kRowCtaWarps);
+        return pl;
+    }
     if (allow_bulk_split && bulk_split_fits(N)) {
         int nsplit = 1, per = 0;
         bulk_split_for(rows, N, sm_count, &nsplit, &per);
@@ -663,24 +822,56 @@ MergeStatesPlan plan_merge_states(int64_t rows, int64_t N, int64_t D, int chunks
     return pl;
 }
 
-template <typename T>
-cudaError_t launch_rows(const T* v, const float* s, T* vo, float* so, int64_t rows, int N, int64_t H,
-                        int chunks, unsigned blocks, size_t smem, const BulkSplit& bs,
-                        const DeviceInfo& dev, cudaStream_t st) {
+template <typename T, int BATCH, int NBUF>
+cudaError_t launch_rows_t(const T* v, const float* s, T* vo, float* so, int64_t rows, int N,
+                          int64_t H, int chunks, int list_len, const BulkSplit& bs,
+                          const DeviceInfo& dev, cudaStream_t st) {
     // The limit is set once per device, to the largest size any call can
     // ask for (rows of up to 128 fp32 values, up to kBulkMaxN states).
-    constexpr size_t kMaxSmem = rows_smem_bytes(128 * 4, kBulkMaxN);
+    constexpr size_t kMaxSmem = rows_smem_bytes<BATCH, NBUF>(128 * 4, kBulkMaxN);
+    const size_t smem = rows_smem_bytes<BATCH, NBUF>(chunks * 16, list_len);
     if (smem > kMaxSmem) return cudaErrorInvalidValue;
     static bool attr_set[64] = {};
     if (dev.device >= 0 && dev.device < 64 && !attr_set[dev.device]) {
-        cudaError_t e = cudaFuncSetAttribute(merge_states_bulk_kernel<T>,
+        cudaError_t e = cudaFuncSetAttribute(merge_states_bulk_kernel<T, BATCH, NBUF>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
         if (e != cudaSuccess) return e;
         attr_set[dev.device] = true;
     }
-    merge_states_bulk_kernel<T><<<blocks, kRowWarps * 32, smem, st>>>(v, s, vo, so, rows, N, H, chunks,
-                                                                       dev.err, bs);
+    const int64_t warps = rows * bs.nsplit;
+    const unsigned blocks = (unsigned)((warps + kRowWarps - 1) / kRowWarps);
+    merge_states_bulk_kernel<T, BATCH, NBUF><<<blocks, kRowWarps * 32, smem, st>>>(
+        v, s, vo, so, rows, N, H, chunks, dev.err, bs);
     return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_rowcta(const T* v, const float* s, T* vo, float* so, int64_t rows, int N,
+                          int64_t H, int chunks, int per, size_t smem, const DeviceInfo& dev,
+                          cudaStream_t st) {
+    // The limit is set once per device, to the largest size any call can ask
+    // for (rows of up to 512 bytes, kBulkMaxN states per warp).
+    constexpr size_t kMaxSmem = rowcta_smem_bytes(512, kBulkMaxN);
+    if (smem > kMaxSmem || kMaxSmem > dev.max_smem_optin) return cudaErrorInvalidValue;
+    static bool attr_set[64] = {};
+    if (dev.device >= 0 && dev.device < 64 && !attr_set[dev.device]) {
+        cudaError_t e = cudaFuncSetAttribute(merge_states_rowcta_kernel<T>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev.device] = true;
+    }
+    merge_states_rowcta_kernel<T><<<(unsigned)rows, kRowCtaWarps * 32, smem, st>>>(
+        v, s, vo, so, N, H, chunks, per, dev.err);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_rows(const T* v, const float* s, T* vo, float* so, int64_t rows, int N, int64_t H,
+                        int chunks, const BulkSplit& bs, const DeviceInfo& dev, cudaStream_t st) {
+    if (bs.nsplit > 1)
+        return launch_rows_t<T, kSplitBatch, kSplitBufs>(v, s, vo, so, rows, N, H, chunks, bs.per, bs,
+                                                         dev, st);
+    return launch_rows_t<T, kRowBatch, 2>(v, s, vo, so, rows, N, H, chunks, N, bs, dev, st);
 }
 
 cudaError_t launch_merge_states(const void* v, const float* s, void* vo, float* so, int64_t S,
@@ -691,8 +882,20 @@ cudaError_t launch_merge_states(const void* v, const float* s, void* vo, float* 
     const int chunks = (int)(D * (int64_t)dtype_size(dt) / 16);
     const MergeStatesPlan pl = plan_merge_states(rows, N, D, chunks, dev.sm_count,
                                                  ws ? ws_bytes : 0, ctas_per_sm, allow_bulk_split);
+    if (pl.row_cta) {
+        const size_t smem = rowcta_smem_bytes(chunks * 16, pl.per_split);
+#define SKV_ROWCTA(T_)                                                                        \
+    launch_rowcta<T_>(static_cast<const T_*>(v), s, static_cast<T_*>(vo), so, rows, (int)N, H, \
+                      chunks, pl.per_split, smem, dev, st)
+        switch (dt) {
+            case SKV_F32: return SKV_ROWCTA(float);
+            case SKV_F16: return SKV_ROWCTA(__half);
+            case SKV_BF16: return SKV_ROWCTA(__nv_bfloat16);
+        }
+#undef SKV_ROWCTA
+        return cudaErrorInvalidValue;
+    }
     if (pl.team_kernel) {
-        const int row_bytes = chunks * 16;
         BulkSplit bs;
         if (pl.nsplit > 1) {
             bs.nsplit = pl.nsplit;
@@ -704,12 +907,9 @@ cudaError_t launch_merge_states(const void* v, const float* s, void* vo, float* 
             w += align256((size_t)rows * pl.nsplit * 8);
             bs.ws_cnt = reinterpret_cast<unsigned*>(w);
         }
-        const size_t smem = rows_smem_bytes(row_bytes, pl.nsplit > 1 ? pl.per_split : (int)N);
-        const int64_t warps = rows * pl.nsplit;
-        const unsigned blocks = (unsigned)((warps + kRowWarps - 1) / kRowWarps);
 #define SKV_ROWS(T_)                                                                           \
     launch_rows<T_>(static_cast<const T_*>(v), s, static_cast<T_*>(vo), so, rows, (int)N, H,   \
-                    chunks, blocks, smem, bs, dev, st)
+                    chunks, bs, dev, st)
         switch (dt) {
             case SKV_F32: return SKV_ROWS(float);
             case SKV_F16: return SKV_ROWS(__half);

@@ -262,3 +262,18 @@ def test_merge_states_two_level_empty_chunks_and_poison(lib):
     s[3, ::3, :] = math.nan            # a third poisoned
     ws, _ = _ws(lib, S, N, H, D)
     _check_merge_states(lib, {"v": v, "s": s}, torch.float32, ws)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("S,N,H,D", [(100, 3, 1, 128), (80, 33, 1, 64), (10, 4096, 9, 64),
+                                     (90, 4097, 1, 64), (16, 17, 8, 128)])
+@pytest.mark.parametrize("use_ws", [False, True])
+def test_merge_states_row_per_cta(lib, dtype, S, N, H, D, use_ws):
+    """Enough rows for about one per SM and up to 16 x 256 states: one CTA per
+    row, 16 warps each streaming a chunk of the states, their partials merged
+    in shared memory (warps past N hold nothing); N = 4097 and above takes the
+    other paths.  Same result with or without a workspace."""
+    d = W.merge_states_inputs(S, N, H, D, dtype, seed=S + 3 * N + D, empty_p=0.1)
+    ws = _ws(lib, S, N, H, D)[0] if use_ws else None
+    _check_merge_states(lib, d, dtype, ws)
+    assert lib.get_device_error() == (0, 0)
