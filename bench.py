@@ -632,7 +632,8 @@ def run_ours(args):
     for evs in all_evs:
         for st, e0, e1 in evs:
             st.times_ms.append(e0.elapsed_time(e1))
-    in_step = [st for st in stages if st.in_step]
+    # With --only, every selected stage counts (a profiling run of reported stages).
+    in_step = [st for st in stages if st.in_step or only is not None]
     step_ms = max_over_ranks(sum(statistics.mean(st.times_ms) for st in in_step), dist, dev)
     step_bytes = sum(st.bytes for st in in_step)
     value = job_value(world, step_bytes, step_ms)
