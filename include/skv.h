@@ -306,9 +306,11 @@ skv_status skv_splitkv_decode_varlen(const void* q, const void* k_cache, const v
                                      int32_t* ranges_dbg, skv_stream_t stream);
 
 /*
- * Device workspace, in bytes, that skv_cascade_decode needs for these sizes
- * (the per-chunk states of the shared-prefix pass).  sm_count > 0 is used as
- * given; 0 means the current device's SM count (the chunking depends on it).
+ * Device workspace, in bytes, that skv_cascade_decode and
+ * skv_cascade_decode_varlen need for these sizes (the per-chunk states of the
+ * shared-prefix pass; the two size that pass for different shares of the
+ * SMs, and this is enough for either).  sm_count > 0 is used as given; 0
+ * means the current device's SM count (the chunking depends on it).
  * Returns 0 for invalid sizes.
  */
 size_t skv_cascade_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,

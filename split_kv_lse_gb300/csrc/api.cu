@@ -25,11 +25,17 @@ std::mutex g_dev_mu;
 
 
 // Share of the SMs the prefix pass is sized for (its CTAs hold a whole SM
-// each); the suffix pass fills the rest of the GPU meanwhile.  Measured on
-// B=64 requests sharing 8192 tokens with suffixes of 1..2048 (NS=16): 1/5
-// and 1/6 (24 prefix CTAs) 64 us, 1/4 and 1/3 (32) 66-67 us, 1/7 (16) 83 us,
-// where the prefix pass outlasts the suffix pass.
+// each); the suffix pass fills the rest of the GPU meanwhile.  Both passes
+// are bound by how fast each SM takes in K/V (the prefix pass's tensor
+// loads accept about 2 KB per 100 cycles), so the share balances their
+// ends.  Measured on B=64 requests sharing 8192 tokens with suffixes of
+// 1..2048 (median of 40): with 16 splits for every suffix, 1/5 (24 prefix
+// CTAs) 62.5 us, 1/4 (32) 66.6 us, 1/3 (48) 66.6 us, 1/7 (16) 80.9 us;
+// with per-sequence split counts (a faster suffix pass, which slows the
+// prefix pass more beside it), 1/5 68.6-70.7 us, 1/4 60.4-62.5 us, 1/3
+// 64.5 us.
 constexpr int kPrefixSmNum = 1, kPrefixSmDen = 5;
+constexpr int kPrefixSmDenVarlen = 4;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -381,14 +387,15 @@ skv_status skv_splitkv_plan_varlen(int32_t B, const int32_t* ctx_host, int32_t p
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 static skv_status cascade_chunks(int32_t B, int32_t Hq, int32_t Hkv, int32_t prefix_len,
-                                 int32_t sm_count, int* mtiles, int* bpc, int* nchunks) {
+                                 int32_t sm_count, int prefix_den, int* mtiles, int* bpc,
+                                 int* nchunks) {
     if (sm_count == 0) {
         const DeviceInfo* dev = nullptr;
         skv_status st = current_device(&dev);
         if (st != SKV_OK) return st;
         sm_count = dev->sm_count;
     }
-    const int budget = sm_count * kPrefixSmNum / kPrefixSmDen;
+    const int budget = sm_count * kPrefixSmNum / prefix_den;
     cascade_prefix_geometry(B, Hq / Hkv, Hkv, prefix_len, budget > 0 ? budget : 1, mtiles, bpc,
                             nchunks);
     return SKV_OK;
@@ -415,7 +422,7 @@ struct LevelPlan {
 };
 
 skv_status cascade_plan(const CascadeLevels& levels, int32_t Hq, int32_t Hkv, int32_t sm_count,
-                        std::vector<LevelPlan>* plan, int* total_slots) {
+                        int prefix_den, std::vector<LevelPlan>* plan, int* total_slots) {
     plan->assign(levels.size(), LevelPlan());
     if (sm_count == 0) {  // the current device's
         const DeviceInfo* dev = nullptr;
@@ -431,7 +438,8 @@ skv_status cascade_plan(const CascadeLevels& levels, int32_t Hq, int32_t Hkv, in
         const int share = std::max(1, sm_count / std::max(1, (int)levels[l].size()));
         for (const CascadeGroup& g : levels[l]) {
             int mt = 0, bpc = 0, nc = 0;
-            skv_status st = cascade_chunks(g.r1 - g.r0, Hq, Hkv, g.len, share, &mt, &bpc, &nc);
+            skv_status st =
+                cascade_chunks(g.r1 - g.r0, Hq, Hkv, g.len, share, prefix_den, &mt, &bpc, &nc);
             if (st != SKV_OK) return st;
             lp.mt.push_back(mt);
             lp.bpc.push_back(bpc);
@@ -513,7 +521,8 @@ skv_status cascade_run(const void* q, const void* k_cache, const void* v_cache,
     if ((st = current_device(&dev)) != SKV_OK) return st;
     std::vector<LevelPlan> plan;
     int slots = 0;
-    if ((st = cascade_plan(levels, Hq, Hkv, dev->sm_count, &plan, &slots)) != SKV_OK) return st;
+    const int den = vl != nullptr ? kPrefixSmDenVarlen : kPrefixSmDen;
+    if ((st = cascade_plan(levels, Hq, Hkv, dev->sm_count, den, &plan, &slots)) != SKV_OK) return st;
     const size_t rows = (size_t)B * Hq;
     if (workspace_bytes < cascade_ws_bytes(rows, slots, D)) return SKV_ERR_INVALID_ARG;
     float* pre_part = static_cast<float*>(workspace);
@@ -633,11 +642,18 @@ size_t skv_cascade_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
                                   int32_t prefix_len, int32_t sm_count) {
     if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 1 || prefix_len < 0 || sm_count < 0)
         return 0;
-    std::vector<LevelPlan> plan;
-    int slots = 0;
-    if (cascade_plan(two_level(B, nullptr, prefix_len), Hq, Hkv, sm_count, &plan, &slots) != SKV_OK)
-        return 0;
-    return cascade_ws_bytes((size_t)B * Hq, slots, D);
+    // Enough for the uniform and the per-sequence suffix plans (whose
+    // prefix passes are sized for different shares of the SMs).
+    size_t most = 0;
+    for (int den : {kPrefixSmDen, kPrefixSmDenVarlen}) {
+        std::vector<LevelPlan> plan;
+        int slots = 0;
+        if (cascade_plan(two_level(B, nullptr, prefix_len), Hq, Hkv, sm_count, den, &plan,
+                         &slots) != SKV_OK)
+            return 0;
+        most = std::max(most, cascade_ws_bytes((size_t)B * Hq, slots, D));
+    }
+    return most;
 }
 
 skv_status skv_cascade_decode(const void* q, const void* k_cache, const void* v_cache,
@@ -687,7 +703,7 @@ size_t skv_cascade_multilevel_workspace_size(int32_t num_levels, const skv_casca
     if (read_levels(num_levels, levels, B, &lv) != SKV_OK) return 0;
     std::vector<LevelPlan> plan;
     int slots = 0;
-    if (cascade_plan(lv, Hq, Hkv, sm_count, &plan, &slots) != SKV_OK) return 0;
+    if (cascade_plan(lv, Hq, Hkv, sm_count, kPrefixSmDen, &plan, &slots) != SKV_OK) return 0;
     return cascade_ws_bytes((size_t)B * Hq, slots, D);
 }
 

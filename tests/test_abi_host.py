@@ -188,14 +188,15 @@ def _level(starts, lens):
 
 
 def test_cascade_multilevel_workspace_size(lib):
-    """One level of one group needs what the two-level cascade needs; more
-    levels add their chunk-state slots; a level that does not cover 0..B in
-    order is rejected (size 0)."""
+    """One level of one group needs no more than the two-level cascade's size
+    query gives (which also covers per-sequence suffix splits); more levels
+    add their chunk-state slots; a level that does not cover 0..B in order is
+    rejected (size 0)."""
     from split_kv_lse_gb300 import _ffi
-    two = lib.skv_cascade_workspace_size(64, 32, 8, 128, 8192, 152)
     lv, keep = _level([0, 64], [8192])
     arr = (_ffi.CascadeLevel * 1)(lv)
-    assert lib.skv_cascade_multilevel_workspace_size(1, arr, 64, 32, 8, 128, 152) == two
+    two = lib.skv_cascade_multilevel_workspace_size(1, arr, 64, 32, 8, 128, 152)
+    assert 0 < two <= lib.skv_cascade_workspace_size(64, 32, 8, 128, 8192, 152)
     lv1, k1 = _level([0, 30, 64], [1000, 0])
     arr2 = (_ffi.CascadeLevel * 2)(lv, lv1)
     assert lib.skv_cascade_multilevel_workspace_size(2, arr2, 64, 32, 8, 128, 152) > two
@@ -223,16 +224,22 @@ def test_product_path_never_imports_the_oracle():
 
 
 def test_cascade_prefix_sizing_on_the_cascade_workload(lib):
-    """The shared-prefix pass is sized for about a fifth of the SMs so that it
-    runs beside the suffix pass: for B=64 requests sharing 8192 tokens
-    (Hq=32, Hkv=8) on 152 SMs that is 3 prefix chunks x 8 kv heads = 24 CTAs,
-    i.e. 3 chunk-state slots per row in the workspace ([rows, slots, D] fp32
-    states, [rows, slots] LSEs, then 256 bytes of counters)."""
+    """The shared-prefix pass is sized for about a fifth of the SMs (a quarter
+    when the suffixes have per-sequence split counts) so that it runs beside
+    the suffix pass: for B=64 requests sharing 8192 tokens (Hq=32, Hkv=8) on
+    152 SMs that is 3 (4) prefix chunks x 8 kv heads = 24 (32) CTAs, i.e. 3
+    (4) chunk-state slots per row in the workspace ([rows, slots, D] fp32
+    states, [rows, slots] LSEs, then 256 bytes of counters); the size query
+    covers both.  A one-level multi-level cascade takes the uniform sizing."""
+    from split_kv_lse_gb300 import _ffi
     def align256(x):
         return (x + 255) // 256 * 256
     rows, D = 64 * 32, 128
     want = lambda slots: align256(rows * slots * D * 4) + align256(rows * slots * 4) + 256
-    assert lib.skv_cascade_workspace_size(64, 32, 8, D, 8192, 152) == want(3)
+    assert lib.skv_cascade_workspace_size(64, 32, 8, D, 8192, 152) == want(4)
+    lv, keep = _level([0, 64], [8192])
+    assert lib.skv_cascade_multilevel_workspace_size(1, (_ffi.CascadeLevel * 1)(lv), 64, 32, 8, D,
+                                                     152) == want(3)
     # No prefix: no slots.
     assert lib.skv_cascade_workspace_size(64, 32, 8, D, 0, 152) == want(0)
 
