@@ -156,16 +156,19 @@ DOMINANT_STAGE = "cascade_suffix_pass1"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dominant_kernel_traffic.json")
 
 
+# The dominant kernel's translation unit and the headers it includes.
+DOMINANT_SOURCES = ("decode.cu", "common.cuh", "kernels.h", "split_range.h")
+
+
 def kernel_sources_sha():
-    """Digest of every kernel source: a recorded ncu traffic figure only
-    stands while none of them has changed since the capture."""
+    """Digest of the dominant kernel's sources: a recorded ncu traffic figure
+    only stands while none of them has changed since the capture."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "split_kv_lse_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(DOMINANT_SOURCES):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
