@@ -261,8 +261,10 @@ skv_status skv_splitkv_decode(const void* q, const void* k_cache, const void* v_
  * gets ns_b = ceil(n_b / pages_per_split) splits, clamped to
  * [1, max_splits], cut by the [L3] §② ranges with NUM_SPLITS = ns_b.
  * Host only; needs no GPU.
- * plan_host: host int32 buffer of plan_capacity >= 2 * sum_b ns_b + B
- *   elements (2 * B * max_splits + B always suffices).  It receives
+ * plan_host: NULL to query only *num_units and *max_split_pages (so that the
+ *   buffer can be sized exactly), or a host int32 buffer of plan_capacity >=
+ *   2 * sum_b ns_b + B elements (2 * B * max_splits + B always suffices).  It
+ *   receives
  *   [*num_units][2] work units (b, split | ns_b << 16), one per split of
  *   every sequence, the longest splits first, followed by [B] the split
  *   counts ns_b.  Copy it as is into a 16-byte aligned device buffer for

@@ -170,15 +170,17 @@ def splitkv_plan_varlen(ctx, page: int = 16, max_splits: int = 16,
     vals = [int(x) for x in (ctx.tolist() if hasattr(ctx, "tolist") else ctx)]
     B = len(vals)
     arr = (ctypes.c_int32 * max(1, B))(*vals)
-    cap = 2 * B * max_splits + B
-    host = torch.zeros(max(1, cap), dtype=torch.int32)
     nu, msp = ctypes.c_int32(), ctypes.c_int32()
-    _ffi.check("skv_splitkv_plan_varlen", _ffi.lib().skv_splitkv_plan_varlen(
+    f = _ffi.lib().skv_splitkv_plan_varlen
+    _ffi.check("skv_splitkv_plan_varlen", f(B, arr, page, max_splits, pages_per_split, None, 0,
+                                            ctypes.byref(nu), ctypes.byref(msp)))
+    cap = 2 * nu.value + B
+    host = torch.zeros(max(1, cap), dtype=torch.int32)
+    _ffi.check("skv_splitkv_plan_varlen", f(
         B, arr, page, max_splits, pages_per_split,
         ctypes.cast(host.data_ptr(), ctypes.POINTER(ctypes.c_int32)), cap, ctypes.byref(nu),
         ctypes.byref(msp)))
-    used = 2 * nu.value + B
-    return SplitPlan(host[:used].clone(), nu.value, msp.value, max_splits, B)
+    return SplitPlan(host[:cap], nu.value, msp.value, max_splits, B)
 
 
 def _decode_bufs(q, k_cache, v_cache, block_table, ctx, ns, o_part, lse_part, out, lse_out,

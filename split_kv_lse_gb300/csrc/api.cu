@@ -340,7 +340,7 @@ skv_status skv_splitkv_plan_varlen(int32_t B, const int32_t* ctx_host, int32_t p
                                    int32_t* plan_host, int64_t plan_capacity,
                                    int32_t* num_units, int32_t* max_split_pages) {
     if (B < 0 || page < 1 || max_splits < 1 || max_splits > 256 || pages_per_split < 1 ||
-        !num_units || !max_split_pages || (B > 0 && (!ctx_host || !plan_host)))
+        !num_units || !max_split_pages || (B > 0 && !ctx_host))
         return SKV_ERR_INVALID_ARG;
     // [L3] §⑥ (a planner may give sequences of different lengths different
     // split counts), with the page's "several pages per split": sequence b
@@ -354,8 +354,19 @@ skv_status skv_splitkv_plan_varlen(int32_t B, const int32_t* ctx_host, int32_t p
         ns[b] = std::min(max_splits, std::max(1, want));
         units += ns[b];
     }
-    if (plan_capacity < 2 * units + B) return SKV_ERR_INVALID_ARG;
     if (units > (int64_t)INT32_MAX / 256) return SKV_ERR_UNSUPPORTED;
+    if (plan_host == nullptr) {  // size query: the counts only
+        int32_t longest = 0;
+        for (int32_t b = 0; b < B; ++b) {
+            int p0 = 0, p1 = 0;
+            split_page_range(ctx_host[b], page, ns[b], 0, &p0, &p1);  // split 0 is the longest
+            longest = std::max(longest, p1 > p0 ? p1 - p0 : 0);
+        }
+        *num_units = (int32_t)units;
+        *max_split_pages = longest;
+        return SKV_OK;
+    }
+    if (plan_capacity < 2 * units + B) return SKV_ERR_INVALID_ARG;
     // Units, longest first (a unit's pages from the [L3] §② range), so that
     // the short ones fill the end of the launch; ties keep (b, split) order.
     struct Unit {

@@ -315,5 +315,8 @@ def test_plan_varlen_argument_checks(lib):
     assert f(2, ctx, 16, 257, 8, buf, 64, ctypes.byref(nu), ctypes.byref(mp)) == 1  # > 256
     assert f(2, ctx, 16, 4, 0, buf, 64, ctypes.byref(nu), ctypes.byref(mp)) == 1    # pps 0
     assert f(2, ctx, 16, 4, 8, buf, 5, ctypes.byref(nu), ctypes.byref(mp)) == 1     # too small
+    nu.value = mp.value = -1
+    assert f(2, ctx, 16, 4, 8, None, 0, ctypes.byref(nu), ctypes.byref(mp)) == 0    # size query
+    assert nu.value == 2 and mp.value == 2
     neg = (c * 2)(10, -1)
     assert f(2, neg, 16, 4, 8, buf, 64, ctypes.byref(nu), ctypes.byref(mp)) == 1
