@@ -337,3 +337,13 @@ def test_cascade_varlen_bf16(lib):
     ctx = [int(x) for x in np.random.default_rng(60).integers(0, 900, B)]
     d = W.cascade_inputs(B, 8, 2, 128, 16, 300, ctx, seed=60, dtype=torch.bfloat16)
     run_and_check_varlen(lib, d, 8, 4)
+
+
+def test_cascade_varlen_empty_prefix_and_empty_suffixes(lib):
+    """Per-sequence suffix splits with no shared prefix (no prefix pass is
+    launched: the suffix pass is not chained), and with a prefix but every
+    suffix empty (one empty split each)."""
+    d = W.cascade_inputs(6, 16, 4, 128, 16, 0, [40, 0, 3, 300, 17, 129], seed=61)
+    run_and_check_varlen(lib, d, 8, 2)
+    d = W.cascade_inputs(5, 8, 2, 128, 16, 500, [0] * 5, seed=62)
+    run_and_check_varlen(lib, d, 4, 8)
