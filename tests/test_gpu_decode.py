@@ -168,6 +168,21 @@ def test_decode_short_splits_many_requests(lib):
     check_decode(lib, d, 4)
 
 
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("ns,ctx", [
+    (2, [0, 1, 16, 130, 255, 256]),
+    (6, [0, 1, 17, 100, 129, 500, 767, 768]),
+    (7, [0, 3, 100, 700]),
+])
+def test_decode_short_split_boundaries(lib, G, ns, ctx):
+    """One-warp CTAs (splits of at most 8 pages) at split counts that are not
+    powers of two: split boundaries on page edges, a last split that is empty
+    or ends in a partial page, whole sequences empty."""
+    d = W.decode_inputs(len(ctx), 2 * G, 2, 128, 16, ctx, seed=40 + G * 7 + ns, pool_extra=2)
+    assert -(-d["block_table"].shape[1] // ns) <= 8
+    check_decode(lib, d, ns, nan_tail=True)
+
+
 @pytest.mark.parametrize("G", [1, 4, 8])
 @pytest.mark.parametrize("ns", [3, 64])
 def test_decode_bf16_small(lib, G, ns):
