@@ -21,8 +21,13 @@ value = algorithmic HBM bytes of the step / step time (GB/s).  Each stage is
 timed with CUDA events on the launching stream; L2 is flushed (a 512 MB
 write, then a 512 MB read, so it holds clean lines) before every stage,
 outside the stage events, so each stage starts cold and is not charged for
-the write-back of the previous stage's output.  --impl reference times
-the fp64 CPU oracle on a bounded sample of the same stages instead.
+the write-back of the previous stage's output.  Beside each stage of at
+least 4 MB the line also reports it run back to back: 2n calls captured in
+one CUDA graph and replayed between one pair of events, rotating over n
+copies of the inputs (more than twice the L2 size read between two uses of a
+copy); that figure leaves out the per-call event and launch latency and is
+not part of value.  --impl reference times the fp64 CPU oracle on a bounded
+sample of the same stages instead.
 
 Prints ONE JSON line (rank 0).
 """
@@ -65,10 +70,69 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--only", default=None,
                     help="comma-separated stage names to run (profiling); default all")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the back-to-back timing of each stage from a CUDA graph")
     ap.add_argument("--soak-s", type=float, default=1.5,
                     help="seconds of untimed steps before the timed region, during which "
                          "(and during the timed region) SM clocks are sampled")
     return ap.parse_args()
+
+
+# Back-to-back timing: stages that read less than this are launch-latency
+# bound and skipped.
+GRAPH_MIN_BYTES = 4 << 20
+GRAPH_REPS = 10
+
+
+def graph_copies(stage_bytes, l2_bytes):
+    """Input copies for the back-to-back timing: the n - 1 other copies read
+    between two uses of one copy hold more than twice the L2 size (n >= 3)."""
+    return max(3, 2 * int(l2_bytes) // int(stage_bytes) + 2)
+
+
+def graph_back_to_back(torch, st, flush, flush_rd, l2_bytes):
+    """Per-call time of a stage run back to back: K calls captured in one CUDA
+    graph and replayed between one pair of events (after the usual flush),
+    the calls rotating over n copies of the stage's inputs, with n chosen so
+    that more than twice the L2 size is read between two uses of a copy (no
+    call finds its inputs in L2).  Returns (us per call, n, K) or None."""
+    if st.make_fn is None or st.bytes < GRAPH_MIN_BYTES:
+        return None
+    n = graph_copies(st.bytes, l2_bytes)
+    K = 2 * n
+    copies = [st.inputs] + [{k: v.clone() for k, v in st.inputs.items()} for _ in range(n - 1)]
+    fns = [st.make_fn(c) for c in copies]
+
+    def body():
+        for i in range(K):
+            fns[i % n]()
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        body()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        body()
+    stream = torch.cuda.current_stream()
+    graph.replay()
+    evs = []
+    for _ in range(GRAPH_REPS):
+        flush.zero_()
+        flush_rd.sum()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    us = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3 / K
+    del graph, fns, copies
+    torch.cuda.empty_cache()
+    return us, n, K
 
 
 def measured_peaks():
@@ -140,7 +204,7 @@ VARLEN_PAGES_PER_SPLIT = 8
 
 
 class Stage:
-    def __init__(self, name, fn, algo_bytes, launches, e2e=None):
+    def __init__(self, name, fn, algo_bytes, launches, e2e=None, inputs=None, make_fn=None):
         self.in_step = True
         self.name = name
         self.fn = fn
@@ -148,6 +212,10 @@ class Stage:
         self.launches = launches
         self.e2e = e2e          # (h2d_fn, run_fn, d2h_fn, h2d_bytes, d2h_bytes)
         self.times_ms = []
+        # For the back-to-back timing: the device tensors the stage reads and
+        # a factory make_fn(inputs) of the same call over another copy of them.
+        self.inputs = inputs
+        self.make_fn = make_fn
 
 
 # The kernel that dominates the step (largest share of the GPU time in the
@@ -235,14 +303,13 @@ def _merge_state_stages(torch, skv, W, dev, to_dev, want, stages, hostside):
     so = torch.empty_like(g["s_a"])
     ms_bytes = 3 * nbytes(g["v_a"]) + 3 * nbytes(g["s_a"])
     if "merge_state" in want:
-        stages.append(Stage("merge_state",
-                            lambda: skv.merge_state(g["v_a"], g["s_a"], g["v_b"], g["s_b"], vo, so),
-                            ms_bytes, 1))
+        mk = lambda c: (lambda: skv.merge_state(c["v_a"], c["s_a"], c["v_b"], c["s_b"], vo, so))
+        ins = {k: g[k] for k in ("v_a", "s_a", "v_b", "s_b")}
+        stages.append(Stage("merge_state", mk(ins), ms_bytes, 1, inputs=ins, make_fn=mk))
     if "merge_state_in_place" in want:
-        v_ip, s_ip = g["v_a"].clone(), g["s_a"].clone()
-        stages.append(Stage("merge_state_in_place",
-                            lambda: skv.merge_state_in_place(v_ip, s_ip, g["v_b"], g["s_b"]),
-                            ms_bytes, 1))
+        ins = {"v": g["v_a"].clone(), "s": g["s_a"].clone(), "v_b": g["v_b"], "s_b": g["s_b"]}
+        mk = lambda c: (lambda: skv.merge_state_in_place(c["v"], c["s"], c["v_b"], c["s_b"]))
+        stages.append(Stage("merge_state_in_place", mk(ins), ms_bytes, 1, inputs=ins, make_fn=mk))
     hostside["merge_state"] = d
 
 
@@ -255,8 +322,9 @@ def _merge_states_stage(torch, skv, W, dev, to_dev, stages, hostside):
     so3 = torch.empty(S, H, device=dev)
     nonempty = int((d3["s"] != -math.inf).sum())
     mss_bytes = nonempty * D * 4 + nbytes(d3["s"]) + nbytes(vo3) + nbytes(so3)
-    stages.append(Stage("merge_states", lambda: skv.merge_states(g3["v"], g3["s"], None, vo3, so3),
-                        mss_bytes, 1))
+    mk = lambda c: (lambda: skv.merge_states(c["v"], c["s"], None, vo3, so3))
+    ins = {"v": g3["v"], "s": g3["s"]}
+    stages.append(Stage("merge_states", mk(ins), mss_bytes, 1, inputs=ins, make_fn=mk))
     hostside["merge_states"] = d3
 
 
@@ -273,9 +341,9 @@ def _merge_states_sweep_stages(torch, skv, W, dev, to_dev, stages):
                          device=dev)
         nonempty = int((d["s"] != -math.inf).sum())
         nb = nonempty * D * 4 + nbytes(d["s"]) + nbytes(vo) + nbytes(so)
-        st = Stage(f"merge_states_N{N}",
-                   lambda g=g, ws=ws, vo=vo, so=so: skv.merge_states(g["v"], g["s"], ws, vo, so),
-                   nb, 1)
+        mk = lambda c, ws=ws, vo=vo, so=so: (lambda: skv.merge_states(c["v"], c["s"], ws, vo, so))
+        ins = {"v": g["v"], "s": g["s"]}
+        st = Stage(f"merge_states_N{N}", mk(ins), nb, 1, inputs=ins, make_fn=mk)
         st.in_step = False
         stages.append(st)
 
@@ -296,11 +364,11 @@ def _decode_stage(torch, skv, W, dev, to_dev, stages, hostside, want):
                  sum(-(-int(c) // 16) for c in d4["ctx"]) * 4 + nbytes(d4["ctx"]) +
                  nbytes(out4) + nbytes(lo4))
     if "splitkv_decode" in want:
-        stages.append(Stage("splitkv_decode",
-                            lambda: skv.splitkv_decode(g4["q"], g4["k_cache"], g4["v_cache"],
-                                                       g4["block_table"], g4["ctx"], ns,
-                                                       d4["sm_scale"], op, lp, out4, lo4),
-                            dec_bytes, 2))
+        mk = lambda c: (lambda: skv.splitkv_decode(c["q"], c["k_cache"], c["v_cache"],
+                                                   c["block_table"], c["ctx"], ns, d4["sm_scale"],
+                                                   op, lp, out4, lo4))
+        ins = {k: g4[k] for k in ("q", "k_cache", "v_cache", "block_table", "ctx")}
+        stages.append(Stage("splitkv_decode", mk(ins), dec_bytes, 2, inputs=ins, make_fn=mk))
     if "splitkv_decode_pass1" in want:
         stages.append(Stage("splitkv_decode_pass1",
                             lambda: skv.splitkv_decode(g4["q"], g4["k_cache"], g4["v_cache"],
@@ -329,38 +397,37 @@ def _cascade_stage(torch, skv, W, dev, to_dev, stages, hostside, want):
     npages = -(-d5["prefix_len"] // 16) + sum(-(-int(c) // 16) for c in d5["ctx"])
     cas_bytes = (kv_tokens * Hkv * D * 2 * 2 + nbytes(d5["q"]) + npages * 4 + nbytes(d5["ctx"]) +
                  nbytes(bufs["out"]) + nbytes(bufs["lse_out"]))
+    cas_in = {k: g5[k] for k in ("q", "k_cache", "v_cache", "prefix_pages", "block_table", "ctx")}
     if "cascade_decode" in want:
-        stages.append(Stage("cascade_decode",
-                            lambda: skv.cascade_decode(g5["q"], g5["k_cache"], g5["v_cache"],
-                                                       g5["prefix_pages"], d5["prefix_len"],
-                                                       g5["block_table"], g5["ctx"], ns,
-                                                       d5["sm_scale"], workspace=ws, **bufs),
-                            cas_bytes, 3))
+        mk = lambda c: (lambda: skv.cascade_decode(c["q"], c["k_cache"], c["v_cache"],
+                                                   c["prefix_pages"], d5["prefix_len"],
+                                                   c["block_table"], c["ctx"], ns, d5["sm_scale"],
+                                                   workspace=ws, **bufs))
+        stages.append(Stage("cascade_decode", mk(cas_in), cas_bytes, 3, inputs=cas_in, make_fn=mk))
     if "cascade_decode_varlen" in want:
         # The same workload with per-sequence suffix split counts ([L3] §⑥
         # F1): at most 16 splits of at most 8 pages, planned on the host once.
         plan = skv.splitkv_plan_varlen(d5["ctx"], 16, ns, VARLEN_PAGES_PER_SPLIT)
         plan.device(dev)
         vbufs = dict(bufs)
-        stages.append(Stage("cascade_decode_varlen",
-                            lambda: skv.cascade_decode_varlen(g5["q"], g5["k_cache"], g5["v_cache"],
-                                                              g5["prefix_pages"], d5["prefix_len"],
-                                                              g5["block_table"], g5["ctx"], plan,
-                                                              d5["sm_scale"], workspace=ws,
-                                                              **vbufs),
-                            cas_bytes, 3))
+        mk = lambda c: (lambda: skv.cascade_decode_varlen(c["q"], c["k_cache"], c["v_cache"],
+                                                          c["prefix_pages"], d5["prefix_len"],
+                                                          c["block_table"], c["ctx"], plan,
+                                                          d5["sm_scale"], workspace=ws, **vbufs))
+        stages.append(Stage("cascade_decode_varlen", mk(cas_in), cas_bytes, 3, inputs=cas_in,
+                            make_fn=mk))
         hostside["cascade_varlen_plan"] = plan
     if "cascade_suffix_pass1" in want:
         # The kernel that dominates the step: pass 1 of the split-KV decode on
         # the cascade's suffixes, launched exactly as cascade_decode launches it.
         suf_bytes = (int(d5["ctx"].sum()) * Hkv * D * 2 * 2 + nbytes(d5["q"]) +
                      sum(-(-int(c) // 16) for c in d5["ctx"]) * 4 + nbytes(d5["ctx"]))
-        stages.append(Stage("cascade_suffix_pass1",
-                            lambda: skv.splitkv_decode(g5["q"], g5["k_cache"], g5["v_cache"],
-                                                       g5["block_table"], g5["ctx"], ns,
-                                                       d5["sm_scale"], bufs["o_part"],
-                                                       bufs["lse_part"], combine=False),
-                            suf_bytes, 1))
+        mk = lambda c: (lambda: skv.splitkv_decode(c["q"], c["k_cache"], c["v_cache"],
+                                                   c["block_table"], c["ctx"], ns, d5["sm_scale"],
+                                                   bufs["o_part"], bufs["lse_part"],
+                                                   combine=False))
+        stages.append(Stage("cascade_suffix_pass1", mk(cas_in), suf_bytes, 1, inputs=cas_in,
+                            make_fn=mk))
     hostside["cascade"] = d5
 
 
@@ -665,6 +732,17 @@ def run_ours(args):
         dom_rep = (dk, ms)
         assert skv.get_device_error() == (0, 0), "device-side error in the dominant kernel"
 
+    # Each stage again, back to back from a CUDA graph over rotating input
+    # copies (reported beside the step; not part of value or ms_per_step).
+    graph_rep = {}
+    if not args.no_graph and only is None:
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        for st in stages + ([dom_rep[0]] if dom_rep is not None else []):
+            r = graph_back_to_back(torch, st, flush, flush_rd, l2)
+            if r is not None:
+                graph_rep[st.name] = r
+        assert skv.get_device_error() == (0, 0), "device-side error in the back-to-back timing"
+
     peak, peak_kind = measured_peaks()
     stage_rep = {}
     for st in stages:
@@ -676,6 +754,12 @@ def run_ours(args):
                               "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4)}
         if not st.in_step:
             stage_rep[st.name]["in_step"] = False
+        if st.name in graph_rep:
+            gus, n, K = graph_rep[st.name]
+            ggbs = st.bytes / (gus * 1e-6) / 1e9
+            stage_rep[st.name]["back_to_back"] = {
+                "us": round(gus, 2), "frac_of_measured_hbm": round(ggbs / peak, 4),
+                "input_copies": n, "calls_per_graph": K}
     if dom_rep is not None:
         dk, dms = dom_rep
         traffic, traffic_src = recorded_traffic()
@@ -694,6 +778,11 @@ def run_ours(args):
     roofline["peak"] = peak
     roofline["peak_kind"] = peak_kind
     roofline["frac"] = round(roofline["achieved"] / peak, 4)
+    if dom_rep is not None and dom_rep[0].name in graph_rep:
+        gus, n, K = graph_rep[dom_rep[0].name]
+        ach = dom_rep[0].bytes / (gus * 1e-6) / 1e9
+        roofline["back_to_back"] = {"us_per_launch": round(gus, 2), "achieved": round(ach, 1),
+                                    "frac": round(ach / peak, 4)}
 
     e2e = None
     if not args.no_e2e and only is None:
@@ -737,6 +826,13 @@ def run_ours(args):
                        "l2_flush": "512 MB write + 512 MB read before every stage of every step (outside the stage events)",
                        "clock_window": f"{args.soak_s} s untimed soak of the same steps, then the timed region",
                        "parallelism": "replicas" if world > 1 else "single GPU",
+                       "back_to_back": ("beside each stage of at least 4 MB: K calls captured "
+                                        "in one CUDA graph, replayed between one pair of "
+                                        "events after the same flush, rotating over n copies "
+                                        "of the inputs so that more than twice the L2 size "
+                                        "is read between two uses of a copy; us = elapsed / K "
+                                        "(the flushed single-call figure excludes nothing "
+                                        "and is the one in value)") if graph_rep else None,
                        "stages": stage_rep, "wall_s": round(wall, 3)},
             "roofline": roofline,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,

@@ -103,3 +103,15 @@ def test_reference_arm_prints_one_complete_json_line():
     e = d["e2e"]
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+def test_back_to_back_copies_exceed_twice_l2():
+    """The back-to-back timing rotates over enough input copies that the
+    other copies read between two uses of one copy exceed twice the L2 size."""
+    import bench
+    l2 = 126 * 2**20
+    for nbytes in (4 << 20, 8_135_168, 64_322_048, 134_242_436, 291_030_672, 10**9):
+        n = bench.graph_copies(nbytes, l2)
+        assert n >= 3
+        assert (n - 1) * nbytes > 2 * l2
+        assert n == 3 or (n - 2) * nbytes <= 2 * l2  # no more copies than needed
