@@ -359,21 +359,25 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                 }
                 sc = 1.f;
             }
-            if (mx > m_ref + kRescaleThreshold) {  // also the first block (m_ref = -inf)
-                if (j > 0) {
-                    const float alpha = exp2f(m_ref - mx);
-                    l_run *= alpha;
+            // Lazy rescale, also the first block (m_ref = -inf).  The TMEM
+            // loads and stores are warp-wide (.sync.aligned), so the warp
+            // rescales O when any of its rows needs it, with alpha = 1 for
+            // the rows that do not.
+            const bool need = mx > m_ref + kRescaleThreshold;
+            const float m_new = need ? mx : m_ref;
+            if (j > 0 && __any_sync(kFull, need)) {
+                const float alpha = need ? exp2f(m_ref - m_new) : 1.f;
+                l_run *= alpha;
 #pragma unroll 1
-                    for (int c = 0; c < kD / 32; ++c) {  // 32 columns at a time: x[] stays live
-                        float ob[32];
-                        tc::tmem_ld32(tO + 32 * c, ob);
+                for (int c = 0; c < kD / 32; ++c) {  // 32 columns at a time: x[] stays live
+                    float ob[32];
+                    tc::tmem_ld32(tO + 32 * c, ob);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) ob[i] *= alpha;
-                        tc::tmem_st32(tO + 32 * c, ob);
-                    }
+                    for (int i = 0; i < 32; ++i) ob[i] *= alpha;
+                    tc::tmem_st32(tO + 32 * c, ob);
                 }
-                m_ref = mx;
             }
+            m_ref = m_new;
             // P as fp16 pairs, key 2c in the low half of column c, written
             // over S (this thread's own TMEM lane, already read).
             float ps4[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums

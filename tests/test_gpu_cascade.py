@@ -109,6 +109,22 @@ def test_cascade_everything_empty(lib):
     assert torch.all(lse.cpu() == -math.inf) and torch.all(out.cpu() == 0)
 
 
+def test_cascade_prefix_rescale_in_some_rows_only(lib):
+    """Scores that rise along the prefix for the even query heads only: their
+    rows pass the running max by more than the lazy-rescale threshold in
+    block after block while the odd heads' rows, in the same warps, never
+    do (the rescale of O in TMEM is warp-wide)."""
+    B, G, Hkv, plen = 40, 4, 2, 1000
+    ctx = [int(x) for x in np.random.default_rng(31).integers(0, 200, B)]
+    d = W.cascade_inputs(B, G * Hkv, Hkv, 128, 16, plen, ctx, seed=31)
+    pages = d["prefix_pages"].tolist()
+    for t in range(plen):
+        d["k_cache"][pages[t // 16], :, t % 16, 0] = t / 16.0  # exact in fp16 and bf16
+    d["q"][:, 0::2, 0] = 8.0
+    d["q"][:, 1::2, 0] = 0.0
+    run_and_check(lib, d, 4)
+
+
 def test_cascade_full_workload(lib):
     """B=64, Hq=32, Hkv=8, an 8192-token shared prefix, suffixes of 1..2048 tokens, NS=16."""
     d = W.cascade_mixed()
