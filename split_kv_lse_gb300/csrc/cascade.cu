@@ -243,27 +243,35 @@ cascade_prefix_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
             constexpr uint32_t idS = tc::idesc_f16_f32(kM, kBlockKeys, false, false, BF);
             // A (P) from TMEM, B (V) MN-major
             constexpr uint32_t idPV = tc::idesc_f16_f32(kM, kD, true, false, BF);
+            // The descriptors differ only in their start address (bits 0-13,
+            // the byte address >> 4; shared addresses stay below 256 KB, so
+            // an offset added there never carries out): built once, then
+            // offset by constants, so that this thread -- which shares its
+            // scheduler with two softmax warps -- spends few instructions
+            // per MMA.
+            const uint64_t q_desc = tc::sdesc_sw128(smem_addr(Qs), 16, 1024);
+            const uint64_t k_desc = tc::sdesc_sw128(smem_addr(Ks), 16, 1024);
+            const uint64_t v_desc = tc::sdesc_sw128(smem_addr(Vs), kHalf, 1024);
             auto qk = [&](int j, int w) {  // S_w = Q_w K_j^T
-                const int st = j % kStages;
-                const uint8_t* Qw = Qs + w * kTile;
+                const uint64_t ab = q_desc + (uint64_t)((w * kTile) >> 4);
+                const uint64_t bb = k_desc + (uint64_t)(((j % kStages) * kTile) >> 4);
 #pragma unroll
                 for (int k = 0; k < kD / 16; ++k) {
-                    const int h = k >> 2, kk = k & 3;
-                    const uint64_t ad = tc::sdesc_sw128(smem_addr(Qw + h * kHalf) + kk * 32, 16, 1024);
-                    const uint64_t bd = tc::sdesc_sw128(smem_addr(Ks + st * kTile + h * kHalf) + kk * 32, 16, 1024);
-                    tc::mma_f16_ss(tmem + 256 * w, ad, bd, idS, k > 0);
+                    // K step k: head-dim half k / 4 (a swizzled half tile),
+                    // 32 bytes (16 elements) k % 4 into its 128-byte rows.
+                    const uint64_t off = (uint64_t)(((k >> 2) * kHalf + (k & 3) * 32) >> 4);
+                    tc::mma_f16_ss(tmem + 256 * w, ab + off, bb + off, idS, k > 0);
                 }
                 tc::mma_commit(&s_full[w]);
             };
             auto pv = [&](int j, int w) -> bool {  // O_w += P_w V_j
                 if (!wait_or_abort(&p_full[w], (uint32_t)(j & 1), abort_flag, p.err, 22)) return false;
                 tc::fence_after_sync();
-                const int st = j % kStages;
+                const uint64_t vb = v_desc + (uint64_t)(((j % kStages) * kTile) >> 4);
 #pragma unroll
-                for (int k = 0; k < kBlockKeys / 16; ++k) {
-                    const uint64_t bd = tc::sdesc_sw128(smem_addr(Vs + st * kTile) + k * 2048, kHalf, 1024);
-                    mma_f16_ts(tmem + 256 * w + 128, tmem + 256 * w + 8 * k, bd, idPV, j > 0 || k > 0);
-                }
+                for (int k = 0; k < kBlockKeys / 16; ++k)  // 16 keys (rows of 128 bytes) a step
+                    mma_f16_ts(tmem + 256 * w + 128, tmem + 256 * w + 8 * k, vb + (uint64_t)((k * 2048) >> 4),
+                               idPV, j > 0 || k > 0);
                 tc::mma_commit(&pv_done[w]);
                 return true;
             };
