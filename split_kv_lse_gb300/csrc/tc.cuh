@@ -49,18 +49,6 @@ SKV_DEVINL uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo
     return d;
 }
 
-// Descriptor of an operand without swizzle (K-major core matrices of 8 rows
-// x 16 bytes): LBO = distance between core matrices along K, SBO = along
-// M/N.  Used only for a constant operand whose every element is equal, so
-// the reads stay inside a region of (M/8) * SBO bytes.
-SKV_DEVINL uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;
-    return d;
-}
 
 // Instruction descriptor for kind::f16: fp16 or bf16 A and B, fp32
 // accumulator, M x N tile, A and B each K-major or MN-major.
@@ -103,9 +91,6 @@ SKV_DEVINL void fence_after_sync() {
 // tensor cores).
 SKV_DEVINL void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-SKV_DEVINL void named_bar_sync(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
 }
 
 // ---------------------------------------------------------------- TMEM loads
@@ -154,35 +139,6 @@ SKV_DEVINL void tmem_st32(uint32_t taddr, const float (&v)[32]) {
         : "memory");
 }
 
-// 16 consecutive 32-bit columns of this thread's lane (load + wait; store +
-// wait).
-SKV_DEVINL void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-SKV_DEVINL void tmem_st16(uint32_t taddr, const float (&v)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
-        "tcgen05.wait::st.sync.aligned;"
-        :: "r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
-           "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])),
-           "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
-           "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
-           "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
-           "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
-        : "memory");
-}
 
 // The 128 consecutive 32-bit columns of this thread's lane in one load (and
 // its wait), as used for a whole S or O row.
@@ -196,13 +152,6 @@ SKV_DEVINL void tmem_ld128(uint32_t taddr, float (&v)[128]) {
         : "memory");
 #pragma unroll
     for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
-}
-SKV_DEVINL void tmem_st128(uint32_t taddr, const float (&v)[128]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x128.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127,%128};\n\t"
-        "tcgen05.wait::st.sync.aligned;"
-        :: "r"(taddr), "r"(__float_as_uint(v[0])),"r"(__float_as_uint(v[1])),"r"(__float_as_uint(v[2])),"r"(__float_as_uint(v[3])),"r"(__float_as_uint(v[4])),"r"(__float_as_uint(v[5])),"r"(__float_as_uint(v[6])),"r"(__float_as_uint(v[7])),"r"(__float_as_uint(v[8])),"r"(__float_as_uint(v[9])),"r"(__float_as_uint(v[10])),"r"(__float_as_uint(v[11])),"r"(__float_as_uint(v[12])),"r"(__float_as_uint(v[13])),"r"(__float_as_uint(v[14])),"r"(__float_as_uint(v[15])),"r"(__float_as_uint(v[16])),"r"(__float_as_uint(v[17])),"r"(__float_as_uint(v[18])),"r"(__float_as_uint(v[19])),"r"(__float_as_uint(v[20])),"r"(__float_as_uint(v[21])),"r"(__float_as_uint(v[22])),"r"(__float_as_uint(v[23])),"r"(__float_as_uint(v[24])),"r"(__float_as_uint(v[25])),"r"(__float_as_uint(v[26])),"r"(__float_as_uint(v[27])),"r"(__float_as_uint(v[28])),"r"(__float_as_uint(v[29])),"r"(__float_as_uint(v[30])),"r"(__float_as_uint(v[31])),"r"(__float_as_uint(v[32])),"r"(__float_as_uint(v[33])),"r"(__float_as_uint(v[34])),"r"(__float_as_uint(v[35])),"r"(__float_as_uint(v[36])),"r"(__float_as_uint(v[37])),"r"(__float_as_uint(v[38])),"r"(__float_as_uint(v[39])),"r"(__float_as_uint(v[40])),"r"(__float_as_uint(v[41])),"r"(__float_as_uint(v[42])),"r"(__float_as_uint(v[43])),"r"(__float_as_uint(v[44])),"r"(__float_as_uint(v[45])),"r"(__float_as_uint(v[46])),"r"(__float_as_uint(v[47])),"r"(__float_as_uint(v[48])),"r"(__float_as_uint(v[49])),"r"(__float_as_uint(v[50])),"r"(__float_as_uint(v[51])),"r"(__float_as_uint(v[52])),"r"(__float_as_uint(v[53])),"r"(__float_as_uint(v[54])),"r"(__float_as_uint(v[55])),"r"(__float_as_uint(v[56])),"r"(__float_as_uint(v[57])),"r"(__float_as_uint(v[58])),"r"(__float_as_uint(v[59])),"r"(__float_as_uint(v[60])),"r"(__float_as_uint(v[61])),"r"(__float_as_uint(v[62])),"r"(__float_as_uint(v[63])),"r"(__float_as_uint(v[64])),"r"(__float_as_uint(v[65])),"r"(__float_as_uint(v[66])),"r"(__float_as_uint(v[67])),"r"(__float_as_uint(v[68])),"r"(__float_as_uint(v[69])),"r"(__float_as_uint(v[70])),"r"(__float_as_uint(v[71])),"r"(__float_as_uint(v[72])),"r"(__float_as_uint(v[73])),"r"(__float_as_uint(v[74])),"r"(__float_as_uint(v[75])),"r"(__float_as_uint(v[76])),"r"(__float_as_uint(v[77])),"r"(__float_as_uint(v[78])),"r"(__float_as_uint(v[79])),"r"(__float_as_uint(v[80])),"r"(__float_as_uint(v[81])),"r"(__float_as_uint(v[82])),"r"(__float_as_uint(v[83])),"r"(__float_as_uint(v[84])),"r"(__float_as_uint(v[85])),"r"(__float_as_uint(v[86])),"r"(__float_as_uint(v[87])),"r"(__float_as_uint(v[88])),"r"(__float_as_uint(v[89])),"r"(__float_as_uint(v[90])),"r"(__float_as_uint(v[91])),"r"(__float_as_uint(v[92])),"r"(__float_as_uint(v[93])),"r"(__float_as_uint(v[94])),"r"(__float_as_uint(v[95])),"r"(__float_as_uint(v[96])),"r"(__float_as_uint(v[97])),"r"(__float_as_uint(v[98])),"r"(__float_as_uint(v[99])),"r"(__float_as_uint(v[100])),"r"(__float_as_uint(v[101])),"r"(__float_as_uint(v[102])),"r"(__float_as_uint(v[103])),"r"(__float_as_uint(v[104])),"r"(__float_as_uint(v[105])),"r"(__float_as_uint(v[106])),"r"(__float_as_uint(v[107])),"r"(__float_as_uint(v[108])),"r"(__float_as_uint(v[109])),"r"(__float_as_uint(v[110])),"r"(__float_as_uint(v[111])),"r"(__float_as_uint(v[112])),"r"(__float_as_uint(v[113])),"r"(__float_as_uint(v[114])),"r"(__float_as_uint(v[115])),"r"(__float_as_uint(v[116])),"r"(__float_as_uint(v[117])),"r"(__float_as_uint(v[118])),"r"(__float_as_uint(v[119])),"r"(__float_as_uint(v[120])),"r"(__float_as_uint(v[121])),"r"(__float_as_uint(v[122])),"r"(__float_as_uint(v[123])),"r"(__float_as_uint(v[124])),"r"(__float_as_uint(v[125])),"r"(__float_as_uint(v[126])),"r"(__float_as_uint(v[127]))
-        : "memory");
 }
 
 }  // namespace tc
