@@ -1,5 +1,5 @@
 // tc.cuh -- 5th-generation tensor core (tcgen05) helpers for sm_103a:
-// tensor-memory allocation, the UMMA shared-memory and instruction
+// tensor-memory allocation, the tcgen05.mma shared-memory and instruction
 // descriptors, MMA issue/commit, tensor-memory loads and the fences between
 // the generic, async and tensor-core proxies.  Inline PTX only.
 #pragma once
