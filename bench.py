@@ -465,52 +465,107 @@ def _multilevel_stage(torch, skv, W, dev, to_dev, stages):
                         nbytes_, launches))
 
 
-_PINNED_OUT = {}
+class E2EPipe:
+    """The step through the public API from pinned host buffers, as a serving
+    loop would run it: device buffers for every stage's inputs and outputs
+    and pinned host buffers for the results are allocated once; every step
+    copies all inputs in (copy-in stream, one event per stage), runs each
+    stage on the current stream once its inputs are in, and copies each
+    stage's results out (copy-out stream) as soon as the stage is done, so
+    the link carries inputs and results at the same time and the kernels run
+    under the copies."""
 
+    def __init__(self, torch, skv, host, dev):
+        self.torch, self.skv, self.host, self.dev = torch, skv, host, dev
+        self.cin = torch.cuda.Stream(device=dev)
+        self.cout = torch.cuda.Stream(device=dev)
+        self.names = [n for n in ("merge_state", "merge_states", "decode", "cascade") if n in host]
+        self.dbuf = {n: {k: torch.empty_like(v, device=dev) for k, v in host[n].items()
+                         if isinstance(v, torch.Tensor)} for n in self.names}
+        self.h2d = sum(nbytes(v) for n in self.names for v in host[n].values()
+                       if isinstance(v, torch.Tensor))
+        f32 = torch.float32
+        e = lambda *shape, dtype=f32: torch.empty(*shape, dtype=dtype, device=dev)
+        ms = self.dbuf["merge_state"]
+        self.ms_out = (torch.empty_like(ms["v_a"]), torch.empty_like(ms["s_a"]))
+        S, N, H, D = host["merge_states"]["v"].shape
+        self.mss_out = (e(S, H, D, dtype=host["merge_states"]["v"].dtype), e(S, H))
+        d4 = host["decode"]
+        B, Hq, D = d4["q"].shape
+        ns = d4["num_splits"]
+        self.dec_bufs = dict(o_part=e(B, Hq, ns, D), lse_part=e(B, Hq, ns),
+                             out=e(B, Hq, D, dtype=d4["q"].dtype), lse_out=e(B, Hq))
+        d5 = host["cascade"]
+        B, Hq, D = d5["q"].shape
+        Hkv = d5["k_cache"].shape[1]
+        ns = d5["num_splits"]
+        cas = lambda: dict(out=e(B, Hq, D, dtype=d5["q"].dtype), lse_out=e(B, Hq),
+                           o_pre=e(B, Hq, D), s_pre=e(B, Hq), o_part=e(B, Hq, ns, D),
+                           lse_part=e(B, Hq, ns))
+        self.cas_bufs, self.var_bufs = cas(), cas()
+        self.ws = torch.empty(max(256, skv.cascade_workspace_size(B, Hq, Hkv, D, d5["prefix_len"])),
+                              dtype=torch.uint8, device=dev)
+        self.results = {}  # stage -> (device tensors, pinned host copies)
 
-def e2e_step(torch, skv, host, dev):
-    """One step through the public API from pinned host buffers: copy every
-    stage's inputs in, run, copy every stage's outputs back."""
-    h2d = d2h = 0
-    d = host["merge_state"]
-    ga = {k: v.to(dev, non_blocking=True) for k, v in d.items()}
-    h2d += sum(nbytes(v) for v in d.values())
-    v, s = skv.merge_state(ga["v_a"], ga["s_a"], ga["v_b"], ga["s_b"])
-    skv.merge_state_in_place(ga["v_a"], ga["s_a"], ga["v_b"], ga["s_b"])
-    outs = [v, s, ga["v_a"], ga["s_a"]]
-    d3 = host["merge_states"]
-    g3 = {k: v.to(dev, non_blocking=True) for k, v in d3.items()}
-    h2d += sum(nbytes(v) for v in d3.values())
-    outs += list(skv.merge_states(g3["v"], g3["s"]))
-    d4 = host["decode"]
-    g4 = {k: (v.to(dev, non_blocking=True) if isinstance(v, torch.Tensor) else v)
-          for k, v in d4.items()}
-    h2d += sum(nbytes(v) for v in d4.values() if isinstance(v, torch.Tensor))
-    out, lse, _, _ = skv.splitkv_decode(g4["q"], g4["k_cache"], g4["v_cache"], g4["block_table"],
-                                        g4["ctx"], d4["num_splits"], d4["sm_scale"])
-    outs += [out, lse]
-    d5 = host["cascade"]
-    g5 = {k: (v.to(dev, non_blocking=True) if isinstance(v, torch.Tensor) else v)
-          for k, v in d5.items()}
-    h2d += sum(nbytes(v) for v in d5.values() if isinstance(v, torch.Tensor))
-    out5, lse5, _, _, _, _ = skv.cascade_decode(g5["q"], g5["k_cache"], g5["v_cache"],
-                                                g5["prefix_pages"], d5["prefix_len"],
-                                                g5["block_table"], g5["ctx"], d5["num_splits"],
-                                                d5["sm_scale"])
-    outs += [out5, lse5]
-    plan = host.get("cascade_varlen_plan")
-    if plan is not None:
-        out6, lse6, _, _, _, _ = skv.cascade_decode_varlen(
-            g5["q"], g5["k_cache"], g5["v_cache"], g5["prefix_pages"], d5["prefix_len"],
-            g5["block_table"], g5["ctx"], plan, d5["sm_scale"])
-        outs += [out6, lse6]
-    key = tuple((tuple(o.shape), o.dtype) for o in outs)
-    if key not in _PINNED_OUT:
-        _PINNED_OUT[key] = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-    for h, o in zip(_PINNED_OUT[key], outs):
-        h.copy_(o, non_blocking=True)
-        d2h += nbytes(o)
-    return h2d, d2h
+    def _send(self, tag, tensors):
+        # The stage's results leave once the kernels that wrote them are done.
+        torch = self.torch
+        ev = torch.cuda.Event()
+        ev.record(torch.cuda.current_stream())
+        self.cout.wait_event(ev)
+        if tag not in self.results:
+            self.results[tag] = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in tensors]
+        with torch.cuda.stream(self.cout):
+            for h, t in zip(self.results[tag], tensors):
+                h.copy_(t, non_blocking=True)
+        return sum(nbytes(t) for t in tensors)
+
+    def step(self):
+        torch, skv, host = self.torch, self.skv, self.host
+        main = torch.cuda.current_stream()
+        # The input buffers are reused: the previous step's kernels must be
+        # done with them, and its results out, before they are overwritten.
+        self.cin.wait_stream(main)
+        self.cin.wait_stream(self.cout)
+        ready = {}
+        with torch.cuda.stream(self.cin):
+            for n in self.names:
+                for k, dst in self.dbuf[n].items():
+                    dst.copy_(host[n][k], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(self.cin)
+                ready[n] = ev
+        d2h = 0
+        main.wait_event(ready["merge_state"])
+        g = self.dbuf["merge_state"]
+        d2h += self._send("merge_state", skv.merge_state(g["v_a"], g["s_a"], g["v_b"], g["s_b"],
+                                                         *self.ms_out))
+        skv.merge_state_in_place(g["v_a"], g["s_a"], g["v_b"], g["s_b"])
+        d2h += self._send("merge_state_in_place", (g["v_a"], g["s_a"]))
+        main.wait_event(ready["merge_states"])
+        g = self.dbuf["merge_states"]
+        d2h += self._send("merge_states", skv.merge_states(g["v"], g["s"], None, *self.mss_out))
+        main.wait_event(ready["decode"])
+        g, d4 = self.dbuf["decode"], host["decode"]
+        b = self.dec_bufs
+        skv.splitkv_decode(g["q"], g["k_cache"], g["v_cache"], g["block_table"], g["ctx"],
+                           d4["num_splits"], d4["sm_scale"], b["o_part"], b["lse_part"], b["out"],
+                           b["lse_out"])
+        d2h += self._send("decode", (b["out"], b["lse_out"]))
+        main.wait_event(ready["cascade"])
+        g, d5 = self.dbuf["cascade"], host["cascade"]
+        args = (g["q"], g["k_cache"], g["v_cache"], g["prefix_pages"], d5["prefix_len"],
+                g["block_table"], g["ctx"])
+        b = self.cas_bufs
+        skv.cascade_decode(*args, d5["num_splits"], d5["sm_scale"], workspace=self.ws, **b)
+        d2h += self._send("cascade", (b["out"], b["lse_out"]))
+        plan = host.get("cascade_varlen_plan")
+        if plan is not None:
+            b = self.var_bufs
+            skv.cascade_decode_varlen(*args, plan, d5["sm_scale"], workspace=self.ws, **b)
+            d2h += self._send("cascade_varlen", (b["out"], b["lse_out"]))
+        main.wait_stream(self.cout)
+        return self.h2d, d2h
 
 
 # ---------------------------------------------------------------- oracle (CPU) stages
@@ -793,13 +848,14 @@ def run_ours(args):
             for k, v in list(d.items()):
                 if isinstance(v, torch.Tensor):
                     d[k] = v.pin_memory()
-        e2e_step(torch, skv, host, dev)
+        pipe = E2EPipe(torch, skv, host, dev)
+        pipe.step()
         torch.cuda.synchronize()
         barrier()
         t0 = time.perf_counter()
         nsteps = max(1, min(args.steps, 5))
         for _ in range(nsteps):
-            h2d, d2h = e2e_step(torch, skv, host, dev)
+            h2d, d2h = pipe.step()
         torch.cuda.synchronize()
         barrier()
         e2e_s = (time.perf_counter() - t0) / nsteps
