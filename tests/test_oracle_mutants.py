@@ -74,6 +74,14 @@ MUTANTS = [
     ("multilevel_suffix_from_shared_pages",
      "kr[n] = token_row(k_cache, sfx, t, Hkv, hk, page, D);",
      "kr[n] = token_row(k_cache, seg_pages, t, Hkv, hk, page, D);"),
+    ("range_floor_num_pages", "int32_t num_pages = (ctx + page - 1) / page;",
+     "int32_t num_pages = ctx / page;"),
+    ("merge_states_no_all_empty_guard", "            if (m == -INFINITY) {",
+     "            if (0) {"),
+    ("empty_split_s_zero", "        *s_out = -INFINITY;", "        *s_out = 0.0;"),
+    ("plan_varlen_zero_splits", "if (ns < 1) ns = 1;", ""),
+    ("page_index_modulo", "int64_t pid = pages[t / page];", "int64_t pid = pages[t % page];"),
+    ("softmax_max_not_subtracted", "z += exp(score[j] - mx);", "z += exp(score[j]);"),
 ]
 
 
