@@ -82,6 +82,10 @@ MUTANTS = [
     ("plan_varlen_zero_splits", "if (ns < 1) ns = 1;", ""),
     ("page_index_modulo", "int64_t pid = pages[t / page];", "int64_t pid = pages[t % page];"),
     ("softmax_max_not_subtracted", "z += exp(score[j] - mx);", "z += exp(score[j]);"),
+    ("weight_b_from_a", "double wb = (b == -INFINITY) ? 0.0 : exp2(b - m);",
+     "double wb = (b == -INFINITY) ? 0.0 : exp2(a - m);"),
+    ("cascade_prefix_drops_first_token", "for (int32_t t = 0; t < prefix_len; ++t, ++n) {",
+     "for (int32_t t = 1; t < prefix_len; ++t, ++n) {"),
 ]
 
 
