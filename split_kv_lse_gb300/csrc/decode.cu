@@ -184,8 +184,10 @@ splitkv_decode_kernel(const DecodeParams p) {
     int* dyn_next = dyn_ids + kDynMaxPages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Uniform splits: CTA (split, hkv, b).  Per-sequence splits (VAR): CTA
-    // u*Hkv + hkv takes unit u of the list, sequence b's split `split` of ns.
+    // Uniform splits: CTA (hkv, split, b), the kv head fastest, so that the
+    // CTAs reading the Hkv tiles of one page (one contiguous run of the
+    // cache) start together.  Per-sequence splits (VAR): CTA u*Hkv + hkv
+    // takes unit u of the list, sequence b's split `split` of ns.
     // (Separate instantiations: the uniform kernel keeps its registers.)
     int split, hkv, b, ns;
     if constexpr (VAR) {
@@ -202,8 +204,8 @@ splitkv_decode_kernel(const DecodeParams p) {
             return;
         }
     } else {
-        split = blockIdx.x;
-        hkv = blockIdx.y;
+        hkv = blockIdx.x;
+        split = blockIdx.y;
         b = blockIdx.z;
         ns = p.NS;
     }
@@ -627,7 +629,7 @@ cudaError_t launch_gwr_t(const DecodeParams& p, int B, int Hkv, int NS, int num_
         attr_set[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = VAR ? dim3((unsigned)num_units * (unsigned)Hkv, 1, 1) : dim3(NS, Hkv, B);
+    cfg.gridDim = VAR ? dim3((unsigned)num_units * (unsigned)Hkv, 1, 1) : dim3(Hkv, NS, B);
     cfg.blockDim = dim3(W * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
