@@ -135,6 +135,31 @@ def graph_back_to_back(torch, st, flush, flush_rd, l2_bytes):
     return us, n, K
 
 
+def host_cpu():
+    """The host the oracle runs on: logical CPUs and model name (lscpu, else
+    /proc/cpuinfo)."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu part")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"nproc": os.cpu_count(), "model": model or "unknown", "arch": platform.machine()}
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -663,7 +688,7 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD + " (bounded oracle sample)", "sample": desc},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
-                             "kind": "oracle", "sample": desc},
+                             "kind": "oracle", "sample": desc, "host": host_cpu()},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -870,7 +895,8 @@ def run_ours(args):
         samples, desc = oracle_sample(W)
         v, t, passes = time_oracle_for(samples, CPU_BASELINE_SECONDS)
         cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{passes} passes over: {desc}", "seconds": round(t, 2)}
+               "sample": f"{passes} passes over: {desc}", "seconds": round(t, 2),
+               "host": host_cpu()}
 
     if rank == 0:
         line = {
