@@ -50,11 +50,14 @@ def _stale(target: str, sources: list[str]) -> bool:
 def _compile(src: str) -> tuple[str, str]:
     obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
     if _stale(obj, [src] + _deps()):
-        cmd = [nvcc(), *NVCC_FLAGS, "-c", src, "-o", obj + ".tmp"]
+        # A per-process temporary: processes building at once (one per rank)
+        # each write their own, and the rename is atomic.
+        tmp = obj + f".tmp{os.getpid()}"
+        cmd = [nvcc(), *NVCC_FLAGS, "-c", src, "-o", tmp]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
-        os.replace(obj + ".tmp", obj)
+        os.replace(tmp, obj)
         return obj, r.stderr
     return obj, ""
 
