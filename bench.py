@@ -16,7 +16,8 @@ split_kv_lse_gb300/workloads.py), inputs resident in HBM:
 Reported beside the step (timed in every step, not counted in value):
 merge_states_N1..N1024, the large-N sweep (S=16, H=8, D=128 fp32).
 Diagnostic stages (--only, not in the step): splitkv_decode_pass1 and
-cascade_suffix_pass1 (pass 1 alone) and cascade_multilevel (three levels).
+cascade_suffix_pass1 (pass 1 alone), cascade_multilevel (three levels), and
+splitkv_decode_bf16 / cascade_decode_bf16 (the same workloads in bf16).
 value = algorithmic HBM bytes of the step / step time (GB/s).  Each stage is
 timed with CUDA events on the launching stream; L2 is flushed (a 512 MB
 write, then a 512 MB read, so it holds clean lines) before every stage,
@@ -293,7 +294,8 @@ STAGE_NAMES = ("merge_state", "merge_state_in_place", "merge_states", "splitkv_d
 # N in 1, 2, 3, 128, 1024), whose small N are launch-latency bound.
 REPORTED_STAGES = ("merge_states_sweep",)
 # Diagnostic stages, selectable with --only (not part of the default step).
-EXTRA_STAGES = ("splitkv_decode_pass1", "cascade_suffix_pass1", "cascade_multilevel")
+EXTRA_STAGES = ("splitkv_decode_pass1", "cascade_suffix_pass1", "cascade_multilevel",
+                "splitkv_decode_bf16", "cascade_decode_bf16")
 
 
 def build_stages(torch, skv, W, dev, only=None):
@@ -316,6 +318,8 @@ def build_stages(torch, skv, W, dev, only=None):
         _cascade_stage(torch, skv, W, dev, to_dev, stages, hostside, want)
     if "cascade_multilevel" in want:
         _multilevel_stage(torch, skv, W, dev, to_dev, stages)
+    if want & {"splitkv_decode_bf16", "cascade_decode_bf16"}:
+        _bf16_stages(torch, skv, W, dev, to_dev, stages, want)
     if "merge_states_sweep" in want:
         _merge_states_sweep_stages(torch, skv, W, dev, to_dev, stages)
     return stages, hostside
@@ -454,6 +458,50 @@ def _cascade_stage(torch, skv, W, dev, to_dev, stages, hostside, want):
         stages.append(Stage("cascade_suffix_pass1", mk(cas_in), suf_bytes, 1, inputs=cas_in,
                             make_fn=mk))
     hostside["cascade"] = d5
+
+
+def _bf16_stages(torch, skv, W, dev, to_dev, stages, want):
+    # The long-context decode and the uniform cascade with bf16 q/K/V (same
+    # shapes, seeds and algorithmic bytes as the fp16 stages).
+    bf16 = torch.bfloat16
+    if "splitkv_decode_bf16" in want:
+        d = W.decode_long(dtype=bf16)
+        g = to_dev(d)
+        B, Hq, D = d["q"].shape
+        Hkv = d["k_cache"].shape[1]
+        ns4 = d["num_splits"]
+        op, lp = torch.empty(B, Hq, ns4, D, device=dev), torch.empty(B, Hq, ns4, device=dev)
+        out, lo = torch.empty(B, Hq, D, dtype=bf16, device=dev), torch.empty(B, Hq, device=dev)
+        nb = (int(d["ctx"].sum()) * Hkv * D * 2 * 2 + nbytes(d["q"]) +
+              sum(-(-int(c) // 16) for c in d["ctx"]) * 4 + nbytes(d["ctx"]) + nbytes(out) + nbytes(lo))
+        stages.append(Stage("splitkv_decode_bf16",
+                            lambda: skv.splitkv_decode(g["q"], g["k_cache"], g["v_cache"],
+                                                       g["block_table"], g["ctx"], ns4,
+                                                       d["sm_scale"], op, lp, out, lo), nb, 2))
+    if "cascade_decode_bf16" in want:
+        d5 = W.cascade_mixed(dtype=bf16)
+        g5 = to_dev(d5)
+        B, Hq, D = d5["q"].shape
+        Hkv = d5["k_cache"].shape[1]
+        ns5 = d5["num_splits"]
+        f32 = torch.float32
+        bufs = dict(out=torch.empty(B, Hq, D, dtype=bf16, device=dev),
+                    lse_out=torch.empty(B, Hq, device=dev), o_pre=torch.empty(B, Hq, D, device=dev),
+                    s_pre=torch.empty(B, Hq, device=dev),
+                    o_part=torch.empty(B, Hq, ns5, D, dtype=f32, device=dev),
+                    lse_part=torch.empty(B, Hq, ns5, dtype=f32, device=dev))
+        ws = torch.empty(max(256, skv.cascade_workspace_size(B, Hq, Hkv, D, d5["prefix_len"])),
+                         dtype=torch.uint8, device=dev)
+        kv_tokens = d5["prefix_len"] + int(d5["ctx"].sum())
+        npages = -(-d5["prefix_len"] // 16) + sum(-(-int(c) // 16) for c in d5["ctx"])
+        nb = (kv_tokens * Hkv * D * 2 * 2 + nbytes(d5["q"]) + npages * 4 + nbytes(d5["ctx"]) +
+              nbytes(bufs["out"]) + nbytes(bufs["lse_out"]))
+        stages.append(Stage("cascade_decode_bf16",
+                            lambda: skv.cascade_decode(g5["q"], g5["k_cache"], g5["v_cache"],
+                                                       g5["prefix_pages"], d5["prefix_len"],
+                                                       g5["block_table"], g5["ctx"], ns5,
+                                                       d5["sm_scale"], workspace=ws, **bufs),
+                            nb, 3))
 
 
 def _multilevel_stage(torch, skv, W, dev, to_dev, stages):

@@ -140,9 +140,9 @@ def decode_inputs(B, Hq, Hkv, D, page, ctx, seed=0, dtype=torch.float16, pool_ex
             "page": page}
 
 
-def decode_long(seed=0):
+def decode_long(seed=0, dtype=torch.float16):
     """B=1, ctx=32768 (2048 pages = the whole pool, randomly permuted), NS=64."""
-    d = decode_inputs(1, 32, 8, 128, 16, [32768], seed)
+    d = decode_inputs(1, 32, 8, 128, 16, [32768], seed, dtype=dtype)
     d["num_splits"] = 64
     return d
 
@@ -208,12 +208,12 @@ def cascade_multilevel_inputs(B, Hq, Hkv, D, page, levels, suffix_ctx, seed=0,
             "page": page}
 
 
-def cascade_mixed(seed=0):
+def cascade_mixed(seed=0, dtype=torch.float16):
     """B=64 requests sharing an 8192-token prefix; suffix lengths uniform in
     [1, 2048] (so some have fewer tokens than page*NS and get empty splits);
     NS=16 for the suffix."""
     g = _gen(seed + 1000)
     suffix = torch.randint(1, 2049, (64,), generator=g).tolist()
-    d = cascade_inputs(64, 32, 8, 128, 16, 8192, suffix, seed)
+    d = cascade_inputs(64, 32, 8, 128, 16, 8192, suffix, seed, dtype=dtype)
     d["num_splits"] = 16
     return d
